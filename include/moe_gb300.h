@@ -1,0 +1,215 @@
+/*
+ * moe_gb300.h - C ABI of the GB300 (sm_103a) 4-bit quantized Mixture-of-Experts layer forward.
+ *
+ * The layer (page "Perplexity's Lily beats MLX-LM on MacBook M5 because it only runs one model",
+ * agentnative.dev):
+ *   - section "Why Qwen3.6-35B-A3B is a weird workload": a router scores E experts, each token
+ *     picks top_k of them, and one shared expert sees every token;
+ *   - section "Prefill and decode are different problems": prefill runs the expert projections
+ *     as matrix-matrix products, batch-1 decode as a bandwidth-bound matrix-vector product;
+ *   - section "Prefill: keep routing on the GPU, dequantize in flight": weights are groupwise
+ *     affine 4-bit (group 64, one bf16 scale and one bf16 bias per group), dequantized tile by
+ *     tile on chip with fp32 accumulation and bf16 output; routing after top-k is histogram,
+ *     prefix scan, scatter and block map, all on the GPU with no host round trip;
+ *   - section "Decode: minimize bytes per token" (fusion): the expert input projections are
+ *     fused with the gate activation, the output projection with the routing scores and the
+ *     shared expert.
+ *
+ * For one token x (d values):
+ *   l_e     = W_r[e] . x (+ b_e)                         router logits, fp32
+ *   S       = the top_k experts by l (ties -> lower index), w_e = softmax of l over S
+ *   FFN_e(x)= W_down_e ( silu(W_gate_e x) * (W_up_e x) ),  silu(z) = z / (1 + exp(-z))
+ *   y       = sum_{e in S} w_e FFN_e(x) + FFN_shared(x)
+ *
+ * Conventions shared by every call:
+ *   - Every pointer is a DEVICE pointer to memory the caller owns (allocated, kept alive and
+ *     freed by the caller), except where a comment says "host". The library never allocates,
+ *     frees or synchronises a stream, except moe_read_device_status (which synchronises).
+ *   - Every compute call is asynchronous on `stream` (NULL = the legacy default stream).
+ *   - bf16 values are passed as their uint16 bit patterns.
+ *   - Alignment: 16 bytes for every device pointer, 128 bytes for `packed` and `ws`.
+ *   - Argument errors are returned before anything is launched (MOE_ERR_INVALID_ARG,
+ *     MOE_ERR_UNSUPPORTED_SHAPE, MOE_ERR_MISALIGNED, MOE_ERR_WORKSPACE_TOO_SMALL). A failed
+ *     launch returns MOE_ERR_CUDA. Errors detected on the device (non-finite router logits,
+ *     an activation outside the fp16 operand range, a bounded wait that gave up) are ORed into
+ *     a sticky status word inside `ws`; read them with moe_read_device_status.
+ *   - Numerics of prefill: the expert GEMMs take fp16 operands with fp32 accumulation. Every
+ *     dequantized weight scale*q + bias whose exact value has at most 11 significant bits
+ *     (e.g. bias = -8*scale) is exact in fp16, x converts exactly from bf16 within the fp16
+ *     range, and the SwiGLU output reaches the down projection as an fp16 pair (about 22
+ *     significant bits). Routing weights and the combine are fp32; y is rounded once to bf16.
+ *   - Supported shapes: group == 64, d % 128 == 0, inter % 128 == 0, shared_inter == inter,
+ *     1 <= top_k <= 16, top_k <= n_experts <= 1024, 1 <= T <= 65536 (MOE_ERR_UNSUPPORTED_SHAPE).
+ *   - The library keeps no state across calls beyond a per-process cache of the driver entry
+ *     point used to encode TMA descriptors; calls on different streams with different
+ *     workspaces may run concurrently.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(MOE_BUILD) && defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object type as cudaStream_t / CUstream. */
+typedef struct CUstream_st* moe_stream_t;
+
+enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,        /* null pointer where one is required, T < 1, ...         */
+  MOE_ERR_UNSUPPORTED_SHAPE = 2,  /* dims outside the supported set listed above            */
+  MOE_ERR_MISALIGNED = 3,         /* a pointer breaks the alignment rule above              */
+  MOE_ERR_WORKSPACE_TOO_SMALL = 4,/* ws_bytes < moe_workspace_bytes(dims, T)                */
+  MOE_ERR_CUDA = 5,               /* a CUDA launch or copy failed                           */
+  MOE_ERR_NONFINITE = 6,          /* device: a router logit was NaN or infinite             */
+  MOE_ERR_DEVICE_TIMEOUT = 7,     /* device: a bounded wait inside a kernel gave up         */
+  MOE_ERR_OUT_OF_RANGE = 8        /* device: an activation (x or a SwiGLU output) exceeded the
+                                     fp16 operand range (|v| > 65504) of the expert GEMMs    */
+};
+
+/* Layer dimensions. `group` is the quantization group along the input dimension (64). */
+typedef struct moe_dims {
+  int32_t d;             /* hidden size                                  */
+  int32_t n_experts;     /* routed experts E                             */
+  int32_t top_k;         /* experts picked per token                     */
+  int32_t inter;         /* routed-expert intermediate size I            */
+  int32_t shared_inter;  /* shared-expert intermediate size (== inter)   */
+  int32_t group;         /* quantization group (== 64)                   */
+} moe_dims;
+
+/*
+ * One groupwise-affine 4-bit matrix W[rows, cols] in the canonical (MLX affine) layout,
+ * cols = input dimension (page: section "Setup", "MLX affine 4-bit checkpoint with group
+ * size 64"; section "Prefill: keep routing on the GPU, dequantize in flight"):
+ *   q      uint32[rows, cols/8]: code of column c in bits 4*(c%8) of word c/8 (low nibble first)
+ *   scale  bf16  [rows, cols/64], bias bf16 [rows, cols/64]
+ *   W[r][c] = scale[r][c/64] * code(r, c) + bias[r][c/64],  code in 0..15.
+ * Routed experts are stacked: gate/up are [E, I, d], down is [E, d, I] (leading expert axis).
+ */
+typedef struct moe_q4_view {
+  const uint32_t* q;
+  const uint16_t* scale;
+  const uint16_t* bias;
+} moe_q4_view;
+
+/* Bytes of the packed weight buffer written by moe_pack_weights (E routed + 1 shared expert).
+ * Returns 0 for unsupported dims. Host-only, no CUDA call. */
+MOE_API size_t moe_packed_bytes(const moe_dims* dims);
+
+/*
+ * Re-lays the canonical weights of all experts and the shared expert into the library's
+ * packed layout (tile-contiguous 128-row x 64-column blocks, nibbles ordered for cheap
+ * unpacking, scale and bias interleaved). The values are unchanged: packing is a pure
+ * permutation of codes plus a copy of scales and biases.
+ * packed_out: device buffer of moe_packed_bytes(dims) bytes, 128-byte aligned, caller-owned.
+ * Inputs may be freed once the stream has passed this call.
+ */
+MOE_API int moe_pack_weights(const moe_dims* dims, moe_q4_view gate, moe_q4_view up, moe_q4_view down,
+                     moe_q4_view sh_gate, moe_q4_view sh_up, moe_q4_view sh_down,
+                     void* packed_out, moe_stream_t stream);
+
+/* One layer: router weight bf16 [E, d] (row e scores expert e), optional fp32 router bias [E]
+ * (NULL = none), and the buffer filled by moe_pack_weights. All device pointers. */
+typedef struct moe_layer {
+  moe_dims dims;
+  const uint16_t* router_w;
+  const float* router_bias;
+  const void* packed;
+} moe_layer;
+
+/*
+ * Optional copies of the routing results (every field may be NULL; non-NULL fields receive a
+ * device-to-device copy at the end of the call). A = T * top_k assignments, a = t*top_k + j.
+ *   logits   fp32 [T, E]
+ *   topk_idx int32[T, top_k]  experts of token t, largest logit first, ties -> lower index
+ *   topk_w   fp32 [T, top_k]  softmax of the logits restricted to the selected experts
+ *   counts   int32[E]         histogram of assignments per expert
+ *   offsets  int32[E + 1]     exclusive prefix scan of counts
+ *   perm     int32[A]         sorted position p -> assignment a (stable: ascending a within e)
+ *   inv_perm int32[A]         assignment a -> sorted position p
+ *   tile_map int32[max_tiles, 3] rows (expert, first row within the expert, rows), experts
+ *                             ascending, tiles of moe_tile_rows() rows; max_tiles =
+ *                             min(E, A) + A / moe_tile_rows()
+ *   n_tiles  int32[1]         number of valid tile_map rows
+ *   hidden   fp16 [2, A + T, I] (prefill only) SwiGLU outputs h in sorted order as a pair of
+ *                             fp16 planes, h = plane0 + plane1 (leading part and remainder);
+ *                             rows A + t hold the shared expert on token t
+ * Decode (T = 1) fills logits, topk_idx and topk_w only.
+ */
+typedef struct moe_route_out {
+  float* logits;
+  int32_t* topk_idx;
+  float* topk_w;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* perm;
+  int32_t* inv_perm;
+  int32_t* tile_map;
+  int32_t* n_tiles;
+  uint16_t* hidden;
+} moe_route_out;
+
+/* Workspace bytes a call with up to max_tokens tokens needs (0 for unsupported dims). The
+ * workspace is caller-owned device memory, 128-byte aligned, used only while the stream runs
+ * the call; one workspace must not be shared by calls that may overlap on the GPU. Its first
+ * 256 bytes hold counters and the sticky status word: zero them once before the first call
+ * (moe_workspace_init, or zero-filled allocation); every call leaves the counters at zero. */
+MOE_API size_t moe_workspace_bytes(const moe_dims* dims, int32_t max_tokens);
+
+/* Zeroes the counters and the status word of a workspace (asynchronous on `stream`). */
+MOE_API int moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Height of a block-map tile (rows of one expert per tile), so a checker can rebuild tile_map. */
+MOE_API int32_t moe_tile_rows(void);
+
+/*
+ * Routing only (section "Prefill: keep routing on the GPU, dequantize in flight"):
+ * router logits, top-k with renormalised softmax weights, histogram, exclusive scan, stable
+ * scatter and block map, all on the device with no host round trip.
+ * x: bf16 [T, d]. logits_in: NULL, or fp32 [T, E] logits to route instead of computing
+ * x . W_r^T (+ bias) (x may then be NULL). Results go to the non-NULL fields of `out`.
+ */
+MOE_API int moe_route(const moe_layer* layer, const uint16_t* x, const float* logits_in, int32_t T,
+              moe_route_out* out, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * Prefill forward of one layer on T tokens (sections "Prefill and decode are different
+ * problems" and "Prefill: keep routing on the GPU, dequantize in flight"): routing as in
+ * moe_route, then the grouped gate/up GEMM with in-tile Q4 dequantization fused with SwiGLU,
+ * then the grouped down GEMM fused with the routing-weighted combine and the shared expert.
+ * x: bf16 [T, d]; y: bf16 [T, d] (may not alias x). `out` may be NULL.
+ */
+MOE_API int moe_prefill(const moe_layer* layer, const uint16_t* x, int32_t T, uint16_t* y,
+                moe_route_out* out, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * Batch-1 decode forward (sections "Prefill and decode are different problems" and
+ * "Decode: minimize bytes per token"): router GEMV and top-k, then Q4 GEMVs that stream only
+ * the top_k selected experts and the shared expert, gate activation fused into the input
+ * projections, routing weights and the shared expert fused into the output projection.
+ * x: bf16 [1, d]; y: bf16 [1, d]. ws: at least moe_workspace_bytes(dims, 1). `out` may be NULL.
+ */
+MOE_API int moe_decode(const moe_layer* layer, const uint16_t* x, uint16_t* y, moe_route_out* out,
+               void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Synchronises `stream`, returns the sticky device status of `ws` (MOE_OK or a device error
+ * code) and clears it. */
+MOE_API int moe_read_device_status(void* ws, moe_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+MOE_API const char* moe_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

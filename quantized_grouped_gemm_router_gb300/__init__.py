@@ -1,0 +1,26 @@
+"""GB300 (sm_103a) 4-bit quantized Mixture-of-Experts layer forward.
+
+The compute path is the CUDA library libmoe_gb300.so (C ABI in include/moe_gb300.h); this
+package is its thin Python binding. Build the library with
+``quantized_grouped_gemm_router_gb300.build.build()``.
+"""
+from .binding import (  # noqa: F401
+    ROUTE_FIELDS,
+    Layer,
+    MoeDims,
+    MoeError,
+    decode,
+    dims_of,
+    lib,
+    pack_weights,
+    packed_bytes,
+    prefill,
+    read_device_status,
+    route,
+    route_out_tensors,
+    status_string,
+    tile_rows,
+    upload_layer,
+    workspace,
+    workspace_bytes,
+)

@@ -1,0 +1,345 @@
+// Host side of the C ABI declared in include/moe_gb300.h: argument checks, workspace carve-up,
+// TMA descriptor encoding and the launch sequence of each call.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "moe_internal.h"
+
+namespace moe {
+size_t decode_smem_gateup(int d);
+size_t decode_smem_down(int k, int inter);
+int router_tile_rows();
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D map over a row-major [rows, cols] matrix of 16-bit values (bf16, or fp16 if `fp16`),
+// 128-byte swizzle, box of 64 columns x box_rows.
+bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows, bool fp16 = false) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_dims(const moe_dims* d) {
+  if (!d) return MOE_ERR_INVALID_ARG;
+  if (d->group != kGroup || d->d < kBlockRows || d->d % kBlockRows || d->d > 16384 || d->inter < kBlockRows ||
+      d->inter % kBlockRows || d->inter > 16384 || d->shared_inter != d->inter || d->top_k < 1 ||
+      d->top_k > kMaxTopK || d->n_experts < d->top_k || d->n_experts > kMaxExperts)
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  return MOE_OK;
+}
+
+int check_layer(const moe_layer* L, bool need_router) {
+  if (!L) return MOE_ERR_INVALID_ARG;
+  int st = check_dims(&L->dims);
+  if (st) return st;
+  if (!L->packed || (need_router && !L->router_w)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(L->packed, 128) || !aligned(L->router_w, 16) || !aligned(L->router_bias, 16)) return MOE_ERR_MISALIGNED;
+  return MOE_OK;
+}
+
+int check_ws(void* ws, size_t ws_bytes, const moe_dims& d, int T) {
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  if (!aligned(ws, 128)) return MOE_ERR_MISALIGNED;
+  if (ws_bytes < ws_layout(d, T).total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return MOE_OK;
+}
+
+int check_out(const moe_route_out* o) {
+  if (!o) return MOE_OK;
+  const void* ps[] = {o->logits, o->topk_idx, o->topk_w, o->counts, o->offsets, o->perm,
+                      o->inv_perm, o->tile_map, o->n_tiles, o->hidden};
+  for (const void* p : ps)
+    if (!aligned(p, 16)) return MOE_ERR_MISALIGNED;
+  return MOE_OK;
+}
+
+struct Ws {
+  uint8_t* base;
+  WsLayout L;
+  template <class T>
+  T* at(size_t off) const { return reinterpret_cast<T*>(base + off); }
+};
+
+int copy_out(void* dst, const void* src, size_t bytes, cudaStream_t s) {
+  if (!dst || bytes == 0) return MOE_OK;
+  return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// Routing on top of logits already in the workspace (or caller-given): top-k, histogram, scan,
+// scatter and block map. `yacc` non-NULL also zeroes the combine accumulator rows.
+// `x` non-NULL also writes its fp16 copy (the expert GEMMs' operand) into the workspace.
+int run_route(const moe_dims& d, const float* logits, int T, const Ws& w, float* yacc, const uint16_t* x,
+              cudaStream_t s) {
+  RouteParams p;
+  p.logits = logits;
+  p.topk_idx = w.at<int32_t>(w.L.topk_idx);
+  p.topk_w = w.at<float>(w.L.topk_w);
+  p.chunk_counts = w.at<int32_t>(w.L.chunk_counts);
+  p.chunk_base = w.at<int32_t>(w.L.chunk_base);
+  p.counts = w.at<int32_t>(w.L.counts);
+  p.offsets = w.at<int32_t>(w.L.offsets);
+  p.perm = w.at<int32_t>(w.L.perm);
+  p.inv_perm = w.at<int32_t>(w.L.inv_perm);
+  p.tile_map = w.at<int32_t>(w.L.tile_map);
+  p.n_tiles = w.at<int32_t>(w.L.n_tiles);
+  p.yacc = yacc;
+  p.x = x;
+  p.x16 = w.at<uint16_t>(w.L.x16);
+  p.hdr = w.at<WsHeader>(w.L.header);
+  p.T = T;
+  p.E = d.n_experts;
+  p.k = d.top_k;
+  p.d = d.d;
+  p.n_chunks = w.L.n_chunks;
+  return launch_route(p, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int run_router_gemm(const moe_layer* L, const uint16_t* x, int T, const Ws& w, cudaStream_t s) {
+  const moe_dims& d = L->dims;
+  CUtensorMap tb, ta;
+  if (!make_map(&tb, x, T, d.d, 16) || !make_map(&ta, L->router_w, d.n_experts, d.d, kBlockRows)) return MOE_ERR_CUDA;
+  GemmParams p = {};
+  p.k_blocks = d.d / kGroup;
+  p.m_tiles = (d.n_experts + kBlockRows - 1) / kBlockRows;
+  p.logits = w.at<float>(w.L.logits);
+  p.router_bias = L->router_bias;
+  p.hdr = w.at<WsHeader>(w.L.header);
+  p.T = T;
+  p.k = d.top_k;
+  p.E = d.n_experts;
+  p.d = d.d;
+  p.inter = d.inter;
+  const int rt = router_tile_rows();
+  const int grid = ((T + rt - 1) / rt) * p.m_tiles;
+  return launch_gemm(kModeRouter, p, &tb, &ta, grid, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int copy_route_out(const moe_dims& d, int T, const Ws& w, const moe_route_out* o, cudaStream_t s) {
+  if (!o) return MOE_OK;
+  const size_t A = (size_t)T * d.top_k, E = d.n_experts;
+  int st = MOE_OK;
+  st |= copy_out(o->logits, w.base + w.L.logits, (size_t)T * E * 4, s);
+  st |= copy_out(o->topk_idx, w.base + w.L.topk_idx, A * 4, s);
+  st |= copy_out(o->topk_w, w.base + w.L.topk_w, A * 4, s);
+  st |= copy_out(o->counts, w.base + w.L.counts, E * 4, s);
+  st |= copy_out(o->offsets, w.base + w.L.offsets, (E + 1) * 4, s);
+  st |= copy_out(o->perm, w.base + w.L.perm, A * 4, s);
+  st |= copy_out(o->inv_perm, w.base + w.L.inv_perm, A * 4, s);
+  st |= copy_out(o->tile_map, w.base + w.L.tile_map, (size_t)w.L.max_tiles * 12, s);
+  st |= copy_out(o->n_tiles, w.base + w.L.n_tiles, 4, s);
+  return st ? MOE_ERR_CUDA : MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_packed_bytes(const moe_dims* dims) {
+  if (check_dims(dims) != MOE_OK) return 0;
+  return packed_layout(*dims).total;
+}
+
+int moe_pack_weights(const moe_dims* dims, moe_q4_view gate, moe_q4_view up, moe_q4_view down, moe_q4_view sh_gate,
+                     moe_q4_view sh_up, moe_q4_view sh_down, void* packed_out, moe_stream_t stream) {
+  int st = check_dims(dims);
+  if (st) return st;
+  const moe_q4_view v[6] = {gate, up, down, sh_gate, sh_up, sh_down};
+  for (const moe_q4_view& m : v) {
+    if (!m.q || !m.scale || !m.bias) return MOE_ERR_INVALID_ARG;
+    if (!aligned(m.q, 16) || !aligned(m.scale, 2) || !aligned(m.bias, 2)) return MOE_ERR_MISALIGNED;
+  }
+  if (!packed_out) return MOE_ERR_INVALID_ARG;
+  if (!aligned(packed_out, 128)) return MOE_ERR_MISALIGNED;
+  return launch_pack(*dims, v, static_cast<uint8_t*>(packed_out), stream) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+size_t moe_workspace_bytes(const moe_dims* dims, int32_t max_tokens) {
+  if (check_dims(dims) != MOE_OK || max_tokens < 1 || max_tokens > kMaxTokens) return 0;
+  return ws_layout(*dims, max_tokens).total;
+}
+
+int moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!ws || ws_bytes < sizeof(WsHeader)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(ws, 128)) return MOE_ERR_MISALIGNED;
+  return cudaMemsetAsync(ws, 0, sizeof(WsHeader), stream) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int32_t moe_tile_rows(void) { return kTileRows; }
+
+int moe_route(const moe_layer* layer, const uint16_t* x, const float* logits_in, int32_t T, moe_route_out* out,
+              void* ws, size_t ws_bytes, moe_stream_t stream) {
+  int st = check_layer(layer, logits_in == nullptr);
+  if (st) return st;
+  if (T < 1 || T > kMaxTokens) return T < 1 ? MOE_ERR_INVALID_ARG : MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!logits_in && !x) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(logits_in, 16)) return MOE_ERR_MISALIGNED;
+  if ((st = check_out(out)) || (st = check_ws(ws, ws_bytes, layer->dims, T))) return st;
+  const moe_dims& d = layer->dims;
+  Ws w{static_cast<uint8_t*>(ws), ws_layout(d, T)};
+  const float* logits = w.at<float>(w.L.logits);
+  if (logits_in) {
+    if (cudaMemcpyAsync(w.at<float>(w.L.logits), logits_in, (size_t)T * d.n_experts * 4, cudaMemcpyDeviceToDevice,
+                        stream) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  } else if ((st = run_router_gemm(layer, x, T, w, stream))) {
+    return st;
+  }
+  if ((st = run_route(d, logits, T, w, nullptr, nullptr, stream))) return st;
+  return copy_route_out(d, T, w, out, stream);
+}
+
+int moe_prefill(const moe_layer* layer, const uint16_t* x, int32_t T, uint16_t* y, moe_route_out* out, void* ws,
+                size_t ws_bytes, moe_stream_t stream) {
+  int st = check_layer(layer, true);
+  if (st) return st;
+  if (T < 1 || !x || !y) return MOE_ERR_INVALID_ARG;
+  if (T > kMaxTokens) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(x, 16) || !aligned(y, 16)) return MOE_ERR_MISALIGNED;
+  if ((st = check_out(out)) || (st = check_ws(ws, ws_bytes, layer->dims, T))) return st;
+  const moe_dims& d = layer->dims;
+  Ws w{static_cast<uint8_t*>(ws), ws_layout(d, T)};
+  const PackedLayout P = packed_layout(d);
+  float* yacc = w.at<float>(w.L.yacc);
+  uint16_t* hidden = w.at<uint16_t>(w.L.hidden);
+  const int A = T * d.top_k;
+
+  // 1. router logits (tensor cores), 2. top-k + grouping (+ zero the combine accumulator)
+  if ((st = run_router_gemm(layer, x, T, w, stream))) return st;
+  if ((st = run_route(d, w.at<float>(w.L.logits), T, w, yacc, x, stream))) return st;
+
+  // 3. gate|up grouped GEMM + SwiGLU -> hidden; 4. down grouped GEMM + weighted combine -> yacc
+  CUtensorMap x_rows, h_rows, unused;
+  if (!make_map(&x_rows, w.at<uint16_t>(w.L.x16), T, d.d, 1, true) ||
+      !make_map(&h_rows, hidden, 2 * ((uint64_t)A + T), d.inter, 16, true))
+    return MOE_ERR_CUDA;
+  unused = x_rows;
+  GemmParams p = {};
+  p.packed = static_cast<const uint8_t*>(layer->packed);
+  p.expert_stride = P.expert_stride;
+  p.tile_map = w.at<int32_t>(w.L.tile_map);
+  p.n_tiles = w.at<int32_t>(w.L.n_tiles);
+  p.offsets = w.at<int32_t>(w.L.offsets);
+  p.perm = w.at<int32_t>(w.L.perm);
+  p.topk_w = w.at<float>(w.L.topk_w);
+  p.hidden = hidden;
+  p.yacc = yacc;
+  p.hdr = w.at<WsHeader>(w.L.header);
+  p.T = T;
+  p.k = d.top_k;
+  p.E = d.n_experts;
+  p.d = d.d;
+  p.inter = d.inter;
+  p.hidden_rows = A + T;
+  const int tiles = w.L.max_tiles + (T + kTileRows - 1) / kTileRows;
+
+  p.region_offset = 0;
+  p.m_tiles = d.inter / kBlockRows;
+  p.k_blocks = d.d / kGroup;
+  if (launch_gemm(kModeGateUp, p, &x_rows, &unused, tiles * p.m_tiles, stream) != cudaSuccess) return MOE_ERR_CUDA;
+
+  p.region_offset = P.gu_bytes;
+  p.m_tiles = d.d / kBlockRows;
+  p.k_blocks = d.inter / kGroup;
+  if (launch_gemm(kModeDown, p, &h_rows, &unused, tiles * p.m_tiles, stream) != cudaSuccess) return MOE_ERR_CUDA;
+
+  // 5. fp32 accumulator -> bf16 output
+  if (launch_cast(yacc, y, (size_t)T * d.d, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  if ((st = copy_route_out(d, T, w, out, stream))) return st;
+  if (out && out->hidden) return copy_out(out->hidden, hidden, 2 * ((size_t)A + T) * d.inter * 2, stream);
+  return MOE_OK;
+}
+
+int moe_decode(const moe_layer* layer, const uint16_t* x, uint16_t* y, moe_route_out* out, void* ws, size_t ws_bytes,
+               moe_stream_t stream) {
+  int st = check_layer(layer, true);
+  if (st) return st;
+  if (!x || !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(y, 16)) return MOE_ERR_MISALIGNED;
+  if ((st = check_out(out)) || (st = check_ws(ws, ws_bytes, layer->dims, 1))) return st;
+  const moe_dims& d = layer->dims;
+  Ws w{static_cast<uint8_t*>(ws), ws_layout(d, 1)};
+  const PackedLayout P = packed_layout(d);
+  DecodeParams p;
+  p.x = x;
+  p.router_w = layer->router_w;
+  p.router_bias = layer->router_bias;
+  p.packed = static_cast<const uint8_t*>(layer->packed);
+  p.expert_stride = P.expert_stride;
+  p.gu_bytes = P.gu_bytes;
+  p.logits = w.at<float>(w.L.logits);
+  p.topk_idx = w.at<int32_t>(w.L.topk_idx);
+  p.topk_w = w.at<float>(w.L.topk_w);
+  p.hbuf = w.at<float>(w.L.dec_h);
+  p.y = y;
+  p.hdr = w.at<WsHeader>(w.L.header);
+  p.d = d.d;
+  p.E = d.n_experts;
+  p.k = d.top_k;
+  p.inter = d.inter;
+  if (launch_decode(p, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  if (!out) return MOE_OK;
+  st = copy_out(out->logits, p.logits, (size_t)d.n_experts * 4, stream);
+  st |= copy_out(out->topk_idx, p.topk_idx, (size_t)d.top_k * 4, stream);
+  st |= copy_out(out->topk_w, p.topk_w, (size_t)d.top_k * 4, stream);
+  return st ? MOE_ERR_CUDA : MOE_OK;
+}
+
+int moe_read_device_status(void* ws, moe_stream_t stream) {
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+  int bits = 0;
+  WsHeader* h = static_cast<WsHeader*>(ws);
+  if (cudaMemcpy(&bits, &h->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemset(&h->status, 0, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+  for (int code = MOE_ERR_NONFINITE; code <= MOE_ERR_OUT_OF_RANGE; ++code)
+    if (bits & status_bit(code)) return code;
+  return MOE_OK;
+}
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case MOE_ERR_MISALIGNED: return "misaligned pointer";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA launch or copy failed";
+    case MOE_ERR_NONFINITE: return "non-finite router logit";
+    case MOE_ERR_DEVICE_TIMEOUT: return "bounded device wait gave up";
+    case MOE_ERR_OUT_OF_RANGE: return "activation outside the fp16 operand range";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

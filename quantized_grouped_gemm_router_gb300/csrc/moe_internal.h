@@ -1,0 +1,183 @@
+// Internal layouts and kernel parameter blocks of the GB300 Q4 MoE library (host + device).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe_gb300.h"
+
+namespace moe {
+
+// ------------------------------------------------------------------------------------------
+// Packed expert layout.
+//
+// Every quantized matrix is cut into blocks of 128 output rows x 64 input columns (one
+// quantization group wide). A block is 4608 bytes:
+//   [0, 4096)    codes: row r at r*32, eight uint32 words (word w = columns 8w..8w+7)
+//   [4096, 4608) per-row (scale, bias) bf16 pairs: row r at 4096 + 4r, scale in the low half
+// Inside a word, the code of column c sits in nibble slot (c/2) + 4*(c%2): slots 0..3 hold
+// columns 0,2,4,6 and slots 4..7 hold columns 1,3,5,7, so (word >> 4i) & 0x000F000F yields
+// the columns (2i, 2i+1) as the two 16-bit halves.
+//
+// Per expert (routed e = 0..E-1, then the shared expert at index E):
+//   gate|up region: for m in [0, I/128), kb in [0, d/64): gate block (m,kb) then up block
+//                   (m,kb) -> 9216 contiguous bytes per (m, kb)
+//   down region:    for m in [0, d/128), kb in [0, I/64): down block (m, kb)
+// ------------------------------------------------------------------------------------------
+constexpr int kGroup = 64;          // quantization group (input columns per block)
+constexpr int kBlockRows = 128;     // output rows per block (= MMA M)
+constexpr int kCodeBytes = kBlockRows * 32;          // 4096
+constexpr int kBlockBytes = kCodeBytes + kBlockRows * 4;  // 4608
+constexpr int kTileRows = 256;      // block-map tile height (max MMA N)
+constexpr int kMaxTopK = 16;
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTokens = 65536;
+
+struct PackedLayout {
+  size_t gu_bytes;       // gate|up region of one expert
+  size_t down_bytes;     // down region of one expert
+  size_t expert_stride;  // bytes per expert
+  size_t total;          // (E + 1) experts
+};
+
+inline PackedLayout packed_layout(const moe_dims& d) {
+  PackedLayout L;
+  L.gu_bytes = (size_t)(d.inter / kBlockRows) * (d.d / kGroup) * 2 * kBlockBytes;
+  L.down_bytes = (size_t)(d.d / kBlockRows) * (d.inter / kGroup) * kBlockBytes;
+  L.expert_stride = L.gu_bytes + L.down_bytes;
+  L.total = L.expert_stride * (size_t)(d.n_experts + 1);
+  return L;
+}
+
+// ------------------------------------------------------------------------------------------
+// Workspace layout (one call with T tokens, A = T*k assignments). Every region 256-aligned.
+// The header words must be zero before the first use of a workspace; the kernels return the
+// counters to zero at the end of every call, and the status word is sticky until read.
+// ------------------------------------------------------------------------------------------
+constexpr int kRouteChunk = 64;     // tokens per routing chunk (one CTA of the top-k kernel)
+
+struct WsHeader {
+  int status;        // sticky device status (moe_status codes ORed as bits 1 << code)
+  unsigned ticket;   // last-CTA ticket of the top-k kernel
+  unsigned dticket;  // last-CTA ticket of the decode router
+  int pad[61];
+};
+static_assert(sizeof(WsHeader) == 256, "header size");
+
+struct WsLayout {
+  size_t header, logits, topk_idx, topk_w, chunk_counts, chunk_base, counts, offsets, perm,
+      inv_perm, tile_map, n_tiles, x16, hidden, yacc, dec_h, total;
+  int n_chunks, max_tiles;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+inline int max_routed_tiles(int T, int k, int E) {
+  long long A = (long long)T * k;
+  return (int)((A < E ? A : E) + A / kTileRows);
+}
+
+inline WsLayout ws_layout(const moe_dims& d, int T) {
+  WsLayout L;
+  const size_t A = (size_t)T * d.top_k, E = (size_t)d.n_experts;
+  L.n_chunks = (T + kRouteChunk - 1) / kRouteChunk;
+  L.max_tiles = max_routed_tiles(T, d.top_k, d.n_experts);
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t r = o; o = align256(o + bytes); return r; };
+  L.header = take(sizeof(WsHeader));
+  L.logits = take((size_t)T * E * 4);
+  L.topk_idx = take(A * 4);
+  L.topk_w = take(A * 4);
+  L.chunk_counts = take((size_t)L.n_chunks * E * 4);
+  L.chunk_base = take((size_t)L.n_chunks * E * 4);
+  L.counts = take(E * 4);
+  L.offsets = take((E + 1) * 4);
+  L.perm = take(A * 4);
+  L.inv_perm = take(A * 4);
+  L.tile_map = take((size_t)L.max_tiles * 3 * 4);
+  L.n_tiles = take(4);
+  L.x16 = take((size_t)T * d.d * 2);                   // x as fp16 (expert GEMM operand)
+  L.hidden = take(2 * (A + T) * (size_t)d.inter * 2);  // SwiGLU rows: fp16 leading part, fp16 remainder
+  L.yacc = take((size_t)T * d.d * 4);
+  L.dec_h = take((size_t)(d.top_k + 1) * d.inter * 4);
+  L.total = o;
+  return L;
+}
+
+// Status bits stored in WsHeader::status.
+__host__ __device__ inline int status_bit(int code) { return 1 << code; }
+
+// ------------------------------------------------------------------------------------------
+// Kernel parameter blocks
+// ------------------------------------------------------------------------------------------
+struct RouteParams {
+  const float* logits;   // [T, E] fp32 (computed or caller-given)
+  int32_t* topk_idx;     // [T, k]
+  float* topk_w;         // [T, k]
+  int32_t* chunk_counts; // [n_chunks, E]
+  int32_t* chunk_base;   // [n_chunks, E]
+  int32_t* counts;       // [E]
+  int32_t* offsets;      // [E + 1]
+  int32_t* perm;         // [A]
+  int32_t* inv_perm;     // [A]
+  int32_t* tile_map;     // [max_tiles, 3]
+  int32_t* n_tiles;      // [1]
+  float* yacc;           // [T, d] zeroed by the top-k kernel (NULL: skip)
+  const uint16_t* x;     // [T, d] bf16 input (NULL: no conversion)
+  uint16_t* x16;         // [T, d] fp16 copy of x written by the top-k kernel
+  WsHeader* hdr;
+  int T, E, k, d, n_chunks;
+};
+
+enum GemmMode { kModeRouter = 0, kModeGateUp = 1, kModeDown = 2 };
+
+struct GemmParams {
+  // weights
+  const uint8_t* packed;      // packed experts (gate/up or down modes)
+  size_t expert_stride;       // bytes per expert
+  size_t region_offset;       // 0 (gate|up) or gu_bytes (down)
+  int m_tiles;                // output-row tiles of 128 per expert
+  int k_blocks;               // input-column blocks of 64
+  // routing
+  const int32_t* tile_map;    // [max_tiles, 3]
+  const int32_t* n_tiles;     // device count of routed tiles
+  const int32_t* offsets;     // [E + 1]
+  const int32_t* perm;        // [A]
+  const float* topk_w;        // [A]
+  // activations
+  uint16_t* hidden;           // [2, A + T, I] fp16: leading part, then remainder (gate/up writes,
+                              // down reads both planes via TMA)
+  float* yacc;                // [T, d] fp32 combine accumulator (down)
+  float* logits;              // [T, E] (router)
+  const float* router_bias;   // [E] or NULL (router)
+  WsHeader* hdr;
+  int T, k, E, d, inter;
+  int hidden_rows;            // A + T: row offset of the remainder plane of `hidden`
+};
+
+struct DecodeParams {
+  const uint16_t* x;          // [d] bf16
+  const uint16_t* router_w;   // [E, d] bf16
+  const float* router_bias;   // [E] or NULL
+  const uint8_t* packed;
+  size_t expert_stride, gu_bytes;
+  float* logits;              // [E]
+  int32_t* topk_idx;          // [k]
+  float* topk_w;              // [k]
+  float* hbuf;                // [k + 1, I] fp32 SwiGLU outputs (slot k = shared expert)
+  uint16_t* y;                // [d] bf16
+  WsHeader* hdr;
+  int d, E, k, inter;
+};
+
+// Launchers (each returns cudaGetLastError()).
+cudaError_t launch_pack(const moe_dims& d, const moe_q4_view* views, uint8_t* packed, cudaStream_t s);
+cudaError_t launch_route(const RouteParams& p, cudaStream_t s);
+cudaError_t launch_gemm(int mode, const GemmParams& p, const CUtensorMap* tmap_b, const CUtensorMap* tmap_a,
+                        int grid, cudaStream_t s);
+cudaError_t launch_cast(const float* yacc, uint16_t* y, size_t n, cudaStream_t s);
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,215 @@
+// GPU-resident routing (page "Perplexity's Lily beats MLX-LM on MacBook M5 because it only runs
+// one model", section "Prefill: keep routing on the GPU, dequantize in flight": after the top-8
+// selection, histogram, prefix scan, scatter and block map run on the GPU with no host round
+// trip). Two launches:
+//   route_topk_kernel    one CTA per 64-token chunk: warp-shuffle top-k on (orderable logit,
+//                        lower index) keys, renormalised softmax weights, per-chunk histogram
+//                        in shared memory, zeroing of the combine accumulator rows; the last
+//                        CTA to finish (ticket) scans the chunk histograms into counts, offsets,
+//                        per-chunk bases and the tile block map.
+//   route_scatter_kernel one warp per chunk: stable, atomics-free placement of the chunk's
+//                        assignments (in-warp ranks by __match_any_sync, running per-expert
+//                        counters in shared memory).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "moe_internal.h"
+#include "ptx.cuh"
+#include "topk.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kTopkThreads = 256;
+
+// Exclusive scan of up to 4*blockDim values held 4 per thread (v[0..3] are items 4t..4t+3).
+// Returns the exclusive prefix of item 4t; *total receives the sum of all items.
+__device__ int block_exclusive_scan4(const int (&v)[4], int* s_warp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int mine = v[0] + v[1] + v[2] + v[3];
+  int incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < nwarps ? s_warp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xFFFFFFFFu, w, o);
+      if (lane >= o) w += n;
+    }
+    if (lane < nwarps) s_warp[lane] = w;  // inclusive warp totals
+  }
+  __syncthreads();
+  const int before_warp = warp ? s_warp[warp - 1] : 0;
+  *total = s_warp[nwarps - 1];
+  __syncthreads();
+  return before_warp + incl - mine;
+}
+
+__global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const RouteParams p) {
+  __shared__ int s_counts[kMaxExperts];
+  __shared__ int s_warp[32];
+  __shared__ int s_last;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int c = blockIdx.x;
+  const int E = p.E, k = p.k;
+  for (int e = tid; e < E; e += blockDim.x) s_counts[e] = 0;
+  __syncthreads();
+
+  const int t_begin = c * kRouteChunk;
+  const int t_end = min(p.T, t_begin + kRouteChunk);
+  for (int t = t_begin + warp; t < t_end; t += kTopkThreads / 32) {
+    int my_e;
+    float my_w;
+    const bool bad = warp_topk_softmax(p.logits + (size_t)t * E, E, k, &my_e, &my_w);
+    if (bad && lane == 0) set_device_status(p.hdr, MOE_ERR_NONFINITE);
+    if (lane < k) {
+      const size_t a = (size_t)t * k + lane;
+      p.topk_idx[a] = my_e;
+      p.topk_w[a] = my_w;
+      atomicAdd(&s_counts[my_e], 1);
+    }
+    if (p.yacc) {
+      float4* yrow = reinterpret_cast<float4*>(p.yacc + (size_t)t * p.d);
+      for (int i = lane; i < p.d / 4; i += 32) yrow[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (p.x) {  // fp16 operand copy of x for the expert GEMMs (exact inside the fp16 range)
+      const uint4* xs = reinterpret_cast<const uint4*>(p.x + (size_t)t * p.d);
+      uint4* xd = reinterpret_cast<uint4*>(p.x16 + (size_t)t * p.d);
+      bool over = false;
+      for (int i = lane; i < p.d / 8; i += 32) {
+        const uint4 v = xs[i];
+        const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float lo = __uint_as_float(in[j] << 16), hi = __uint_as_float(in[j] & 0xFFFF0000u);
+          over |= !(fabsf(lo) <= 65504.f) || !(fabsf(hi) <= 65504.f);
+          const __half2 h = __floats2half2_rn(lo, hi);
+          o[j] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        xd[i] = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+      if (__any_sync(0xFFFFFFFFu, over) && lane == 0) set_device_status(p.hdr, MOE_ERR_OUT_OF_RANGE);
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += blockDim.x) p.chunk_counts[(size_t)c * E + e] = s_counts[e];
+
+  // Last CTA to finish turns the chunk histograms into counts, offsets, chunk bases and tiles.
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = (atomicAdd(&p.hdr->ticket, 1u) == gridDim.x - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  int cnt[4], tiles[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int e = 4 * tid + i;
+    int run = 0;
+    if (e < E) {
+      for (int cc = 0; cc < p.n_chunks; ++cc) {
+        const size_t o = (size_t)cc * E + e;
+        const int n = __ldcg(p.chunk_counts + o);
+        p.chunk_base[o] = run;  // position of chunk cc's first row inside expert e
+        run += n;
+      }
+    }
+    cnt[i] = run;
+    tiles[i] = (run + kTileRows - 1) / kTileRows;
+  }
+  int total_rows, total_tiles;
+  const int off0 = block_exclusive_scan4(cnt, s_warp, &total_rows);
+  const int tile0 = block_exclusive_scan4(tiles, s_warp, &total_tiles);
+  int off = off0, tl = tile0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int e = 4 * tid + i;
+    if (e < E) {
+      p.counts[e] = cnt[i];
+      p.offsets[e] = off;
+      for (int r = 0; r < tiles[i]; ++r) {
+        int32_t* tm = p.tile_map + 3 * (size_t)(tl + r);
+        tm[0] = e;
+        tm[1] = r * kTileRows;
+        tm[2] = min(kTileRows, cnt[i] - r * kTileRows);
+      }
+    }
+    off += cnt[i];
+    tl += tiles[i];
+  }
+  if (tid == 0) {
+    p.offsets[E] = total_rows;
+    *p.n_tiles = total_tiles;
+    p.hdr->ticket = 0u;  // ready for the next call
+  }
+}
+
+// One warp per chunk; assignments are visited in ascending order a = t*k + j, 32 at a time.
+__global__ void __launch_bounds__(32) route_scatter_kernel(const RouteParams p) {
+  __shared__ int s_run[kMaxExperts];
+  const int lane = threadIdx.x;
+  const int c = blockIdx.x;
+  const int E = p.E;
+  for (int e = lane; e < E; e += 32) s_run[e] = 0;
+  __syncwarp();
+  const int a_begin = c * kRouteChunk * p.k;
+  const int a_end = min(p.T, (c + 1) * kRouteChunk) * p.k;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int base = a_begin; base < a_end; base += 32) {
+    const int a = base + lane;
+    const bool valid = a < a_end;
+    const int e = valid ? p.topk_idx[a] : -1 - lane;  // invalid lanes get unique keys
+    const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
+    if (valid) {
+      const int rank = __popc(peers & lt_mask);
+      const int pos = p.offsets[e] + p.chunk_base[(size_t)c * E + e] + s_run[e] + rank;
+      p.perm[pos] = a;
+      p.inv_perm[a] = pos;
+    }
+    __syncwarp();
+    if (valid && (peers & lt_mask) == 0u) s_run[e] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+__global__ void __launch_bounds__(256) cast_kernel(const float* __restrict__ yacc, uint16_t* __restrict__ y, size_t n8) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
+    const float4 a = reinterpret_cast<const float4*>(yacc)[2 * i];
+    const float4 b = reinterpret_cast<const float4*>(yacc)[2 * i + 1];
+    __nv_bfloat162 o0 = __floats2bfloat162_rn(a.x, a.y), o1 = __floats2bfloat162_rn(a.z, a.w);
+    __nv_bfloat162 o2 = __floats2bfloat162_rn(b.x, b.y), o3 = __floats2bfloat162_rn(b.z, b.w);
+    uint4 o;
+    o.x = *reinterpret_cast<uint32_t*>(&o0);
+    o.y = *reinterpret_cast<uint32_t*>(&o1);
+    o.z = *reinterpret_cast<uint32_t*>(&o2);
+    o.w = *reinterpret_cast<uint32_t*>(&o3);
+    reinterpret_cast<uint4*>(y)[i] = o;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_route(const RouteParams& p, cudaStream_t s) {
+  route_topk_kernel<<<p.n_chunks, kTopkThreads, 0, s>>>(p);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  route_scatter_kernel<<<p.n_chunks, 32, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cast(const float* yacc, uint16_t* y, size_t n, cudaStream_t s) {
+  const size_t n8 = n / 8;
+  const int blocks = (int)((n8 + 255) / 256 < 1216 ? (n8 + 255) / 256 : 1216);
+  cast_kernel<<<blocks > 0 ? blocks : 1, 256, 0, s>>>(yacc, y, n8);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

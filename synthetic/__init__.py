@@ -5,6 +5,10 @@ of the layer's arithmetic.
 """
 from .moe_inputs import (  # noqa: F401
     LayerShape,
+    FULL,
+    TINY,
+    STACK_LAYERS,
+    STACK_DECODE_STEPS,
     CONFIGS,
     bf16_bits_to_f32,
     f32_to_bf16_bits,

@@ -1,0 +1,79 @@
+"""Host-side checks of the C ABI (CPU only): the library loads, exports every symbol the header
+declares, answers the host-only queries, and rejects bad arguments before launching anything.
+Every call below fails argument validation, so no CUDA work is attempted."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from quantized_grouped_gemm_router_gb300 import build as B
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "moe_gb300.h")
+
+
+@pytest.fixture(scope="module")
+def m():
+    B.build()
+    import quantized_grouped_gemm_router_gb300 as mod
+    return mod
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", text)
+
+
+def test_exports_every_declared_symbol(m):
+    names = declared_functions()
+    assert len(names) >= 10
+    lib = m.lib()
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_host_queries(m):
+    from synthetic import FULL, TINY
+    full = m.dims_of(FULL)
+    assert m.tile_rows() == 256
+    assert m.packed_bytes(full) == 257 * 1769472          # (E + 1) experts x 3*I*d*(1/2 + 4/64) bytes
+    assert m.packed_bytes(m.dims_of(TINY)) == 17 * 3 * 128 * 256 * 9 // 16
+    assert m.workspace_bytes(full, 1) > 0
+    assert m.workspace_bytes(full, 4096) > m.workspace_bytes(full, 2048)
+    assert m.workspace_bytes(full, 0) == 0 and m.workspace_bytes(full, 65537) == 0
+    for bad in (dict(group=32), dict(d=2000), dict(inter=500), dict(shared_inter=256), dict(top_k=0),
+                dict(top_k=17), dict(n_experts=4, top_k=8), dict(n_experts=2048)):
+        dims = m.dims_of(FULL)
+        for k, v in bad.items():
+            setattr(dims, k, v)
+        assert m.packed_bytes(dims) == 0 and m.workspace_bytes(dims, 16) == 0, bad
+    for code in range(8):
+        assert m.status_string(code) and m.status_string(code) != "unknown status"
+
+
+def test_argument_errors_before_launch(m):
+    from quantized_grouped_gemm_router_gb300.binding import MoeLayer, RouteOut
+    from synthetic import FULL
+    lib = m.lib()
+    dims = m.dims_of(FULL)
+    A = 1 << 20  # fake, never dereferenced: every call below fails validation first
+    layer = MoeLayer(dims, A, None, A)
+    ws_need = m.workspace_bytes(dims, 16)
+    call = lambda L, x, T, y, ws, n: lib.moe_prefill(ctypes.byref(L), x, T, y, None, ws, n, None)  # noqa: E731
+    assert call(layer, None, 16, A, A, ws_need) == 1                      # null x
+    assert call(layer, A, 0, A, A, ws_need) == 1                          # T < 1
+    assert call(layer, A, 70000, A, A, ws_need) == 2                      # T too large
+    assert call(layer, A + 8, 16, A, A, ws_need) == 3                     # misaligned x
+    assert call(layer, A, 16, A, A + 64, ws_need) == 3                    # ws not 128-aligned
+    assert call(layer, A, 16, A, A, ws_need - 1) == 4                     # workspace too small
+    bad = MoeLayer(m.dims_of(FULL), A, None, A + 16)
+    assert call(bad, A, 16, A, A, ws_need) == 3                           # packed not 128-aligned
+    bad.dims.group = 128
+    assert call(bad, A, 16, A, A, ws_need) == 2
+    out = RouteOut(*([A + 4] + [None] * 9))
+    assert lib.moe_route(ctypes.byref(layer), A, None, 16, ctypes.byref(out), A, ws_need, None) == 3
+    assert lib.moe_route(ctypes.byref(layer), None, None, 16, None, A, ws_need, None) == 1
+    assert lib.moe_decode(ctypes.byref(layer), A, None, None, A, ws_need, None) == 1
+    assert lib.moe_decode(ctypes.byref(layer), A, A, None, A, 16, None) == 4
+    assert lib.moe_workspace_init(None, 256, None) == 1
+    assert lib.moe_read_device_status(None, None) == 1

@@ -1,0 +1,236 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle, on a GB300.
+
+Routing integers are compared bit for bit on identical logits; logits, weights, hidden rows
+and outputs within the tolerances stated in tests/moe_check.py.
+"""
+import functools
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle as O  # noqa: E402
+from synthetic import CONFIGS, FULL, TINY, LayerShape, make_layer, make_tokens  # noqa: E402
+from tests import moe_check as C  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def m():
+    from quantized_grouped_gemm_router_gb300 import build as B
+    B.build()
+    import quantized_grouped_gemm_router_gb300 as mod
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return mod
+
+
+@functools.lru_cache(maxsize=8)
+def _np_layer(shape, seed, bias):
+    return make_layer(shape, seed, bias)
+
+
+_DEV_LAYERS = {}
+
+
+def dev_layer(m, shape, seed=0, bias=None):
+    key = (shape, seed, bias)
+    if key not in _DEV_LAYERS:
+        _DEV_LAYERS[key] = m.upload_layer(_np_layer(shape, seed, bias))
+    return _DEV_LAYERS[key]
+
+
+def to_dev(a):
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def run_route(m, layer, T, logits=None, x=None):
+    ws = m.workspace(layer.dims, T)
+    out = m.route(layer, None if x is None else to_dev(x), T, ws,
+                  logits_in=None if logits is None else to_dev(logits))
+    torch.cuda.synchronize()
+    assert m.read_device_status(ws) == 0
+    return C.to_np(out)
+
+
+# ------------------------------------------------------------------------------ routing
+def crafted_logits(T, E, kind, seed=0):
+    rng = np.random.default_rng(seed)
+    if kind == "normal":
+        return rng.standard_normal((T, E)).astype(np.float32)
+    if kind == "ties":
+        l = (np.round(rng.standard_normal((T, E)) * 2) / 2).astype(np.float32)
+        l[0::7] = 0.25                       # all-equal rows -> experts 0..k-1
+        l[3::7] = -0.0
+        l[3::7, 5::9] = 0.0                  # -0.0 and +0.0 tie
+        return l
+    if kind == "skew":
+        l = rng.standard_normal((T, E)).astype(np.float32)
+        l[:, :8] += 50.0                     # every token picks experts 0..7
+        return l
+    raise ValueError(kind)
+
+
+@pytest.mark.parametrize("shape", [TINY, FULL], ids=["tiny", "full"])
+@pytest.mark.parametrize("T,kind", [(1, "normal"), (64, "ties"), (65, "normal"), (300, "ties"),
+                                    (300, "skew"), (2048, "normal"), (2048, "skew"), (517, "ties")])
+def test_route_given_logits_bit_exact(m, shape, T, kind):
+    layer = dev_layer(m, shape)
+    logits = crafted_logits(T, shape.n_experts, kind, seed=T)
+    gpu = run_route(m, layer, T, logits=logits)
+    np.testing.assert_array_equal(gpu["logits"], logits)
+    C.check_routing_exact(gpu, logits, shape.n_experts, shape.top_k, m.tile_rows())
+
+
+@pytest.mark.parametrize("name", ["tiny", "prefill512", "skew2048"])
+def test_route_router_gemm(m, name):
+    shape, T, bias = CONFIGS[name]
+    npl = _np_layer(shape, 0, bias)
+    layer = dev_layer(m, shape, 0, bias)
+    x = make_tokens(T, shape.d, seed=1)
+    gpu = run_route(m, layer, T, x=x)
+    ref_logits = O.router_logits(x, npl["router_w"], npl["router_bias"])
+    tol = C.logit_tolerance(x, npl["router_w"]) + 1e-6 * np.abs(ref_logits)
+    assert np.all(np.abs(gpu["logits"].astype(np.float64) - ref_logits) <= tol)
+    C.check_routing_exact(gpu, gpu["logits"], shape.n_experts, shape.top_k, m.tile_rows())
+    diff, ok = C.selection_with_near_ties(gpu["logits"], ref_logits, tol, shape.top_k)
+    assert ok, f"tokens {diff} select different experts without a near tie"
+
+
+def test_route_nonfinite_sets_status(m):
+    layer = dev_layer(m, TINY)
+    logits = crafted_logits(8, TINY.n_experts, "normal")
+    logits[3, 2] = np.nan
+    ws = m.workspace(layer.dims, 8)
+    m.route(layer, None, 8, ws, logits_in=to_dev(logits))
+    assert m.read_device_status(ws) == 6
+    assert m.read_device_status(ws) == 0      # sticky until read, then cleared
+    m.route(layer, None, 8, ws, logits_in=to_dev(crafted_logits(8, TINY.n_experts, "normal")))
+    assert m.read_device_status(ws) == 0
+
+
+# ------------------------------------------------------------------------------ prefill
+def prefill_and_check(m, shape, T, seed=0, bias=None, npl=None, layer=None, hidden=False):
+    npl = npl if npl is not None else _np_layer(shape, seed, bias)
+    layer = layer if layer is not None else dev_layer(m, shape, seed, bias)
+    x = make_tokens(T, shape.d, seed=seed + 100)
+    ws = m.workspace(layer.dims, T)
+    out = m.route_out_tensors(layer.dims, T, "cuda", hidden=hidden)
+    y = m.prefill(layer, to_dev(x), ws, out=out)
+    torch.cuda.synchronize()
+    assert m.read_device_status(ws) == 0
+    g = C.to_np(out)
+    C.check_routing_exact(g, g["logits"], shape.n_experts, shape.top_k, m.tile_rows())
+    ref_logits = O.router_logits(x, npl["router_w"], npl["router_bias"])
+    tol = C.logit_tolerance(x, npl["router_w"]) + 1e-6 * np.abs(ref_logits)
+    diff, ok = C.selection_with_near_ties(g["logits"], ref_logits, tol, shape.top_k)
+    assert ok, f"tokens {diff} select different experts without a near tie"
+    routing = None
+    if diff:  # follow the GPU's selection, weights from the oracle's own logits
+        idx = g["topk_idx"]
+        sel = np.take_along_axis(ref_logits.astype(np.float64), idx.astype(np.int64), axis=1)
+        w = np.exp(sel - sel.max(1, keepdims=True))
+        routing = (idx, w / w.sum(1, keepdims=True))
+    ref = O.moe_forward(x, npl, tile_rows=m.tile_rows(), routing=routing)
+    stats = C.check_y(y, ref["y"])
+    print(f"prefill T={T}: {stats}")
+    if hidden:
+        H = O.hidden_sorted(x, npl, ref["grouping"])
+        planes = out["hidden"].cpu().numpy().view(np.float16).astype(np.float64)
+        C.check_y(planes[0] + planes[1], H, "hidden")
+    return stats, g
+
+
+@pytest.mark.parametrize("T", [1, 4, 37, 300])
+def test_prefill_tiny_shape(m, T):
+    prefill_and_check(m, TINY, T, hidden=True)
+
+
+def test_prefill_config_tiny(m):
+    shape, T, _ = CONFIGS["tiny"]
+    prefill_and_check(m, shape, T)
+
+
+def test_prefill_full_512(m):
+    shape, T, bias = CONFIGS["prefill512"]
+    prefill_and_check(m, shape, T, bias=bias)
+
+
+def test_prefill_full_skew_2048(m):
+    shape, T, bias = CONFIGS["skew2048"]
+    _, g = prefill_and_check(m, shape, T, bias=bias, hidden=True)
+    assert g["counts"].max() > 256   # several tiles for the heaviest experts
+
+
+def test_prefill_forced_tile_edges(m):
+    """Every token picks experts 0..k-1: each gets T rows (tiles of 256 + a ragged tail)."""
+    shape = FULL
+    npl = dict(_np_layer(shape, 3, None))
+    rb = np.zeros(shape.n_experts, dtype=np.float32)
+    rb[: shape.top_k] = 100.0
+    npl["router_bias"] = rb
+    layer = m.upload_layer(npl)
+    for T in (256, 257):
+        _, g = prefill_and_check(m, shape, T, seed=3, npl=npl, layer=layer)
+        assert np.all(g["counts"][: shape.top_k] == T)
+
+
+def test_prefill_out_of_range_sets_status(m):
+    """x beyond the fp16 operand range is reported on the device instead of silently saturating."""
+    layer = dev_layer(m, TINY)
+    x = make_tokens(8, TINY.d, seed=4)
+    x[2, 17] = 0x7F00                          # bf16 1.7e38
+    ws = m.workspace(layer.dims, 8)
+    m.prefill(layer, to_dev(x), ws)
+    assert m.read_device_status(ws) == 8
+    m.prefill(layer, to_dev(make_tokens(8, TINY.d, seed=4)), ws)
+    assert m.read_device_status(ws) == 0
+
+
+def test_prefill_repeatable(m):
+    shape = TINY
+    layer = dev_layer(m, shape)
+    x = to_dev(make_tokens(200, shape.d, seed=9))
+    ws = m.workspace(layer.dims, 200)
+    y1 = C.bf16_bits_f64(m.prefill(layer, x, ws))
+    y2 = C.bf16_bits_f64(m.prefill(layer, x, ws))
+    assert m.read_device_status(ws) == 0
+    np.testing.assert_allclose(y1, y2, rtol=1e-2, atol=1e-2)
+
+
+# ------------------------------------------------------------------------------ decode
+@pytest.mark.parametrize("shape,bias,seed", [(TINY, None, 0), (FULL, None, 0), (FULL, None, 1),
+                                             (FULL, "zipf", 2)], ids=["tiny", "full0", "full1", "zipf"])
+def test_decode(m, shape, bias, seed):
+    npl = _np_layer(shape, seed, bias)
+    layer = dev_layer(m, shape, seed, bias)
+    for step in range(3):
+        x = make_tokens(1, shape.d, seed=seed, stream=step + 1)
+        ws = m.workspace(layer.dims, 1)
+        out = m.route_out_tensors(layer.dims, 1, "cuda", want=("logits", "topk_idx", "topk_w"))
+        y = m.decode(layer, to_dev(x), ws, out=out)
+        torch.cuda.synchronize()
+        assert m.read_device_status(ws) == 0
+        g = C.to_np(out)
+        idx_ref, w_ref = O.select_experts(g["logits"], shape.top_k)
+        np.testing.assert_array_equal(g["topk_idx"], idx_ref)
+        assert np.max(np.abs(g["topk_w"] - w_ref)) <= C.W_TOL
+        ref_logits = O.router_logits(x, npl["router_w"], npl["router_bias"])
+        tol = C.logit_tolerance(x, npl["router_w"]) + 1e-6 * np.abs(ref_logits)
+        assert np.all(np.abs(g["logits"] - ref_logits) <= tol)
+        diff, ok = C.selection_with_near_ties(g["logits"], ref_logits, tol, shape.top_k)
+        assert ok and not diff
+        ref = O.moe_forward(x, npl, tile_rows=m.tile_rows())
+        C.check_y(y, ref["y"])
+
+
+def test_decode_matches_prefill_T1(m):
+    shape = FULL
+    layer = dev_layer(m, shape)
+    x = to_dev(make_tokens(1, shape.d, seed=5))
+    y_dec = C.bf16_bits_f64(m.decode(layer, x, m.workspace(layer.dims, 1)))
+    y_pre = C.bf16_bits_f64(m.prefill(layer, x, m.workspace(layer.dims, 1)))
+    C.check_y(y_dec, y_pre, "decode vs prefill")
