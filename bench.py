@@ -1,0 +1,499 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 4-bit quantized MoE layer forward (prefill and batch-1 decode).
+
+A step is one pass of the layer-stack workload: 40 independent MoE layers (d=2048, 256 experts,
+top-8, I=512, one shared expert, Q4 group-64 weights; seeds 0..39) each run on a 4096-token
+prefill chunk, then 256 batch-1 decode steps through the 40 layers with fixed random inputs per
+step. All layer weights (18.2 GB packed) stay resident in HBM and together exceed the 129 MB
+L2 many times over, so no L2 flush is needed between steps.
+
+Output: one JSON line (rank 0). `value` is MoE-layer prefill throughput in tok/s (tokens of
+one layer per second, summed over ranks); `decode_us_per_layer` is the decode time per layer.
+`--impl reference` times the CPU oracle on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "moe_layer_prefill_tok_per_s"
+UNIT = "tok/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--layers", type=int, default=40)
+    ap.add_argument("--prefill-tokens", type=int, default=4096)
+    ap.add_argument("--decode-steps", type=int, default=256)
+    ap.add_argument("--router-bias", choices=("none", "zipf"), default="none")
+    ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of replaying CUDA graphs")
+    ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--skip-check", action="store_true", help="skip the sampled oracle check")
+    ap.add_argument("--oracle-child", default=None, help=argparse.SUPPRESS)
+    return ap.parse_args(argv)
+
+
+# ------------------------------------------------------------------------------------------
+# Peaks, algorithmic work per launch
+# ------------------------------------------------------------------------------------------
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]), "source": "measured"}
+    return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def expert_bytes(d: int, inter: int) -> dict:
+    """Packed bytes of one expert: 4-bit codes plus one bf16 scale and bias per 64 weights."""
+    per_w = 0.5 + 4.0 / 64
+    return {"gate_up": int(2 * inter * d * per_w), "down": int(d * inter * per_w)}
+
+
+def algorithmic_work(d: int, E: int, k: int, inter: int, T: int) -> dict:
+    """Algorithmic FLOPs (real rows only) and bytes per launch of each kernel."""
+    A = T * k
+    eb = expert_bytes(d, inter)
+    return {
+        "prefill_router_gemm": {"flop": 2.0 * T * E * d},
+        "prefill_gate_up_gemm": {"flop": 2.0 * (A + T) * 2 * inter * d},
+        "prefill_down_gemm": {"flop": 2.0 * (A + T) * d * inter},
+        # decode: bytes of the weights that must be read (router; k+1 experts' gate/up; down)
+        "decode_router_gemv": {"bytes": E * d * 2 + d * 2 + E * 4},
+        "decode_gate_up_gemv": {"bytes": (k + 1) * eb["gate_up"] + d * 2 + (k + 1) * inter * 4},
+        "decode_down_gemv": {"bytes": (k + 1) * eb["down"] + (k + 1) * inter * 4 + d * 2},
+    }
+
+
+# ------------------------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ------------------------------------------------------------------------------------------
+_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_uuid: str | None):
+        self.uuid, self.proc, self.path = gpu_uuid, None, None
+
+    def start(self, path: str):
+        self.path = path
+        cmd = ["nvidia-smi", f"--query-gpu={_QUERY}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.uuid:
+            cmd[1:1] = ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=open(path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(_REASONS, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------------
+# Ranks (one process per GPU; replicas of the whole workload, no data-path collective)
+# ------------------------------------------------------------------------------------------
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def reduce_over_ranks(values: dict, op: str = "max") -> dict:
+    """Max (timings) or sum (work) of scalar values over all ranks; identity without a group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return dict(values)
+    keys = sorted(values)
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([float(values[k]) for k in keys], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return {k: float(v) for k, v in zip(keys, t.tolist())}
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def src_sha(*rel_paths) -> str:
+    h = hashlib.sha256()
+    for rp in rel_paths:
+        with open(os.path.join(ROOT, rp), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+# ------------------------------------------------------------------------------------------
+# CPU oracle: bounded samples of the same workload (baseline only, never the optimisation target)
+# ------------------------------------------------------------------------------------------
+def _oracle_child(spec: str) -> None:
+    """Runs inside a child process (no CUDA): times the oracle on the sample in `spec` and
+    prints one JSON object."""
+    import numpy as np  # noqa: F401
+    import oracle as O
+    from synthetic import FULL, make_layer, make_tokens
+    cfg = json.loads(spec)
+    out = {"prefill_s": [], "decode_s": []}
+    layers = {}
+    for i in range(cfg["repeats"]):
+        li = cfg["layer_ids"][i % len(cfg["layer_ids"])]
+        if li not in layers:
+            layers[li] = make_layer(FULL, seed=li, router_bias=cfg["router_bias"])
+        L = layers[li]
+        x = make_tokens(cfg["tokens"], FULL.d, seed=li, stream=1000 + i)
+        t0 = time.perf_counter()
+        O.moe_forward(x, L, tile_rows=256)
+        out["prefill_s"].append(time.perf_counter() - t0)
+        for j in range(cfg["decode_tokens"]):
+            x1 = make_tokens(1, FULL.d, seed=li, stream=2000 + 16 * i + j)
+            t0 = time.perf_counter()
+            O.moe_forward(x1, L, tile_rows=256)
+            out["decode_s"].append(time.perf_counter() - t0)
+    print(json.dumps(out))
+
+
+def run_oracle_sample(tokens: int, decode_tokens: int, repeats: int, layer_ids, router_bias) -> dict:
+    """Times the oracle in a fresh CPU-only process whose BLAS/OpenMP thread count is fixed to
+    the cores this process may use, so `cores` is the thread count actually used."""
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    env = dict(os.environ)
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[var] = str(cores)
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    spec = json.dumps({"tokens": tokens, "decode_tokens": decode_tokens, "repeats": repeats,
+                       "layer_ids": list(layer_ids), "router_bias": router_bias})
+    res = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-child", spec], env=env,
+                         capture_output=True, text=True, check=True)
+    data = json.loads(res.stdout.strip().splitlines()[-1])
+    data["cores"] = cores
+    return data
+
+
+def cpu_baseline(args) -> dict:
+    tokens = 128
+    d = run_oracle_sample(tokens, decode_tokens=4, repeats=1, layer_ids=[0],
+                          router_bias=None if args.router_bias == "none" else args.router_bias)
+    t_pre = statistics.mean(d["prefill_s"])
+    t_dec = statistics.mean(d["decode_s"])
+    return {"value": tokens / t_pre, "unit": UNIT, "cores": d["cores"], "kind": "oracle",
+            "decode_us_per_layer": t_dec * 1e6,
+            "sample": f"numpy fp64 oracle on layer 0 of the stack: one {tokens}-token prefill chunk "
+                      f"({t_pre:.1f} s) and 4 single-token decodes ({t_dec:.2f} s each)"}
+
+
+def run_reference(args, config: dict) -> None:
+    """Reference arm: the CPU oracle as it stands, same metric, unit and config, each step a
+    bounded sample (one 16-token prefill chunk and one decode token of one layer)."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    tokens = 16
+    n = args.warmup + args.steps
+    d = run_oracle_sample(tokens, decode_tokens=1, repeats=n, layer_ids=[0, 1, 2, 3],
+                          router_bias=None if args.router_bias == "none" else args.router_bias)
+    pre = d["prefill_s"][args.warmup:]
+    dec = d["decode_s"][args.warmup:]
+    value = tokens / statistics.mean(pre)
+    step_ms = 1e3 * (statistics.mean(pre) + statistics.mean(dec))
+    sample = (f"numpy fp64 oracle, each step one {tokens}-token prefill chunk and one decode token of "
+              f"one layer (layers 0..3 in turn)")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
+            "decode_us_per_layer": 1e6 * statistics.mean(dec),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": d["cores"], "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------------------
+# The GPU workload
+# ------------------------------------------------------------------------------------------
+class Workload:
+    """Device-resident layers, per-layer prefill inputs and per-step decode inputs (pinned host
+    copies kept for the end-to-end leg)."""
+
+    def __init__(self, args, device, seed_offset: int = 0):
+        import numpy as np
+        import torch
+        import quantized_grouped_gemm_router_gb300 as m
+        from synthetic import FULL, make_layer, make_tokens
+        self.m, self.shape, self.args = m, FULL, args
+        L, T, S, d = args.layers, args.prefill_tokens, args.decode_steps, FULL.d
+        rb = None if args.router_bias == "none" else args.router_bias
+        self.layers = [m.upload_layer(make_layer(FULL, seed=seed_offset + l, router_bias=rb), device)
+                       for l in range(L)]
+        self.dims = self.layers[0].dims
+        xp = np.stack([make_tokens(T, d, seed=seed_offset + l, stream=1) for l in range(L)]) if T else None
+        xd = make_tokens(S * L, d, seed=seed_offset, stream=2).reshape(S, L, d) if S else None
+        pin = lambda a: torch.from_numpy(a.view(np.int16)).pin_memory()  # noqa: E731
+        self.xp_host = pin(xp) if T else None
+        self.xd_host = pin(xd) if S else None
+        self.xp = self.xp_host.to(device) if T else None
+        self.xd = self.xd_host.to(device) if S else None
+        self.yp = torch.empty_like(self.xp) if T else None
+        self.yd = torch.empty_like(self.xd) if S else None
+        self.yp_host = torch.empty_like(self.xp_host).pin_memory() if T else None
+        self.yd_host = torch.empty_like(self.xd_host).pin_memory() if S else None
+        self.ws_p = m.workspace(self.dims, max(T, 1), device)
+        self.ws_d = m.workspace(self.dims, 1, device)
+
+    def prefill_all(self, events=None):
+        for l, layer in enumerate(self.layers):
+            self.m.prefill(layer, self.xp[l], self.ws_p, y=self.yp[l], events=None if events is None else events.get(l))
+
+    def decode_all(self, events=None):
+        for s in range(self.args.decode_steps):
+            for l, layer in enumerate(self.layers):
+                ev = None if events is None else events.get((s, l))
+                self.m.decode(layer, self.xd[s, l], self.ws_d, y=self.yd[s, l], events=ev)
+
+    def launches_per_step(self) -> int:
+        a = self.args
+        return (6 * a.layers if a.prefill_tokens else 0) + 3 * a.layers * a.decode_steps
+
+
+def capture(W: Workload, ev_pre=None, ev_dec=None, graphs: bool = True):
+    """Returns (run_prefill_step, run_decode_step): replays of CUDA graphs captured from the
+    library calls (the timed launch configuration), or the eager calls."""
+    import torch
+    if not graphs:
+        return (lambda: W.prefill_all(ev_pre)), (lambda: W.decode_all(ev_dec))
+    g_pre, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    if W.args.prefill_tokens:
+        with torch.cuda.graph(g_pre):
+            W.prefill_all(ev_pre)
+    if W.args.decode_steps:
+        with torch.cuda.graph(g_dec):
+            W.decode_all(ev_dec)
+    W.graphs = (g_pre, g_dec)
+    return g_pre.replay, g_dec.replay
+
+
+def _new_events(n):
+    import torch
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for e in evs:
+        e.record()  # materialise the CUDA event so its handle can be handed to the library
+    return evs
+
+
+def run_ours(args, config: dict) -> None:
+    import torch
+    import torch.distributed as dist
+    rank, world, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", torch.cuda.current_device())
+    cpu = None
+    if rank == 0 and not args.skip_cpu:
+        cpu = cpu_baseline(args)           # CPU oracle sample, before any GPU work
+    from quantized_grouped_gemm_router_gb300 import build as B
+    B.build()
+    W = Workload(args, device, seed_offset=1000 * rank)
+    L, T, S = args.layers, args.prefill_tokens, args.decode_steps
+
+    # per-kernel events inside the timed region: every prefill layer, every 8th decode call
+    ev_pre = {l: _new_events(6) for l in range(L)} if T else {}
+    ev_dec = {(s, l): _new_events(4) for s in range(S) for l in range(L) if (s * L + l) % 8 == 0}
+    for _ in range(2):                     # eager warm-up (also initialises the library)
+        if T:
+            W.prefill_all()
+        if S:
+            W.decode_all()
+    torch.cuda.synchronize()
+    if W.m.read_device_status(W.ws_p) or W.m.read_device_status(W.ws_d):
+        raise RuntimeError("device status set during warm-up")
+
+    run_pre, run_dec = capture(W, ev_pre, ev_dec, graphs=not args.no_graph)
+    for _ in range(args.warmup):
+        if T:
+            run_pre()
+        if S:
+            run_dec()
+    torch.cuda.synchronize()
+
+    names_pre = ["prefill_router_gemm", "prefill_route", "prefill_gate_up_gemm", "prefill_down_gemm", "prefill_cast"]
+    names_dec = ["decode_router_gemv", "decode_gate_up_gemv", "decode_down_gemv"]
+    ksum = {n: 0.0 for n in names_pre + names_dec}
+    kcnt = {n: 0 for n in names_pre + names_dec}
+    e0, e1, e2 = _new_events(3)
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(uuid)
+    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start(os.path.join(ROOT, "gpurun_out", f"bench_clocks_r{rank}.csv"))
+    wall0 = time.perf_counter()
+    pre_ms = dec_ms = 0.0
+    for _ in range(args.steps):
+        e0.record()
+        if T:
+            run_pre()
+        e1.record()
+        if S:
+            run_dec()
+        e2.record()
+        e2.synchronize()                   # read this step's sampled kernel events
+        pre_ms += e0.elapsed_time(e1)
+        dec_ms += e1.elapsed_time(e2)
+        for evs in ev_pre.values():
+            for i, n in enumerate(names_pre):
+                ksum[n] += evs[i].elapsed_time(evs[i + 1])
+                kcnt[n] += 1
+        for evs in ev_dec.values():
+            for i, n in enumerate(names_dec):
+                ksum[n] += evs[i].elapsed_time(evs[i + 1])
+                kcnt[n] += 1
+    torch.cuda.synchronize()
+    barrier()
+    wall_s = time.perf_counter() - wall0
+    clk = clocks.stop()
+    st = W.m.read_device_status(W.ws_p) | W.m.read_device_status(W.ws_d)
+    if st:
+        raise RuntimeError(f"device status {st} set during the timed region")
+
+    # end-to-end: host inputs in pinned memory, copies inside the timed region, eager calls
+    e2e = None
+    if not args.skip_e2e:
+        stream = torch.cuda.current_stream()
+        e2e_pre = e2e_dec = 0.0
+        for _ in range(args.steps):
+            e0.record()
+            if T:
+                W.xp.copy_(W.xp_host, non_blocking=True)
+                W.prefill_all()
+                W.yp_host.copy_(W.yp, non_blocking=True)
+            e1.record()
+            if S:
+                W.xd.copy_(W.xd_host, non_blocking=True)
+                W.decode_all()
+                W.yd_host.copy_(W.yd, non_blocking=True)
+            e2.record()
+            stream.synchronize()
+            e2e_pre += e0.elapsed_time(e1)
+            e2e_dec += e1.elapsed_time(e2)
+        red = reduce_over_ranks({"pre": e2e_pre, "dec": e2e_dec}, "max")
+        h2d = (W.xp_host.numel() * 2 if T else 0) + (W.xd_host.numel() * 2 if S else 0)
+        e2e = {"value": world * L * T * args.steps / (red["pre"] / 1e3) if T else None, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": h2d,
+               "decode_us_per_layer": 1e3 * red["dec"] / (args.steps * max(1, S * L)) if S else None,
+               "how": "pinned host inputs copied in, 40 eager moe_prefill calls (and 256x40 eager moe_decode "
+                      "calls) through the Python binding, outputs copied back, per step"}
+
+    red = reduce_over_ranks({"pre": pre_ms, "dec": dec_ms, "wall": wall_s}, "max")
+    kavg = {n: ksum[n] / kcnt[n] for n in ksum if kcnt[n]}
+    if rank != 0:
+        return
+    peaks = load_peaks()
+    work = algorithmic_work(W.shape.d, W.shape.n_experts, W.shape.top_k, W.shape.inter, T)
+    per_step_launches = {n: L for n in names_pre}
+    per_step_launches.update({n: L * S for n in names_dec})
+    rooflines = []
+    for n, ms in kavg.items():
+        w = work.get(n)
+        if not w:
+            continue
+        share_ms = ms * per_step_launches[n]
+        if "flop" in w:
+            ach = w["flop"] / (ms * 1e-3) / 1e12
+            peak = peaks["bf16_tflops_sustained"]
+            r = {"kernel": n, "bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                 "frac": ach / peak, "per_launch": f"{w['flop'] / 1e9:.2f} GFLOP (real rows only)"}
+        else:
+            ach = w["bytes"] / (ms * 1e-3) / 1e9
+            peak = peaks["hbm_gbs"]
+            r = {"kernel": n, "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
+                 "per_launch": f"{w['bytes'] / 1e6:.3f} MB of active weights"}
+        r.update({"avg_launch_us": ms * 1e3, "ms_per_step": share_ms,
+                  "peak_source": f"{peaks['source']} ({'sustained bf16 = fp16 dense' if 'flop' in w else 'HBM copy'})",
+                  "traffic": None})
+        rooflines.append(r)
+    rooflines.sort(key=lambda r: -r["ms_per_step"])
+    value = world * L * T * args.steps / (red["pre"] / 1e3) if T else None
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": (red["pre"] + red["dec"]) / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic", "config": config,
+        "decode_us_per_layer": 1e3 * red["dec"] / (args.steps * S * L) if S else None,
+        "prefill_us_per_layer": 1e3 * red["pre"] / (args.steps * L) if T else None,
+        "roofline": dict(rooflines[0]) if rooflines else None, "rooflines": rooflines,
+        "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": W.launches_per_step() * args.steps,
+        "clocks": clk, "wall_s_timed": red["wall"], "graphs": not args.no_graph,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.oracle_child is not None:
+        _oracle_child(args.oracle_child)
+        return
+    config = {"workload": f"layer stack: {args.layers} independent MoE layers x ({args.prefill_tokens}-token "
+                          f"prefill + {args.decode_steps} batch-1 decode steps)",
+              "layers": args.layers, "prefill_tokens": args.prefill_tokens, "decode_steps": args.decode_steps,
+              "d": 2048, "experts": 256, "top_k": 8, "inter": 512, "shared_inter": 512,
+              "weights": "Q4 affine, group 64, bf16 scale+bias", "router_bias": args.router_bias,
+              "l2": "no flush: inputs larger than L2 (40 layers of packed weights, 18.2 GB)",
+              "parallelism": f"replicas x{args.gpus}"}
+    if args.impl == "reference":
+        run_reference(args, config)
+    else:
+        run_ours(args, config)
+
+
+if __name__ == "__main__":
+    main()

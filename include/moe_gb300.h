@@ -201,6 +201,23 @@ MOE_API int moe_prefill(const moe_layer* layer, const uint16_t* x, int32_t T, ui
 MOE_API int moe_decode(const moe_layer* layer, const uint16_t* x, uint16_t* y, moe_route_out* out,
                void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/*
+ * Timed variants of moe_prefill and moe_decode for measurement: identical work, plus
+ * cudaEventRecordWithFlags(events[i], stream, cudaEventRecordExternal) at each kernel boundary
+ * so the events also become nodes of a CUDA graph captured from the call. `events` is a host
+ * array of cudaEvent_t (created by the caller with timing enabled); any entry may be NULL.
+ *   prefill: events[0] before the router GEMM, [1] before the routing kernels (top-k and
+ *            scatter), [2] before the gate/up GEMM, [3] before the down GEMM, [4] before the
+ *            output cast, [5] after it (6 entries).
+ *   decode:  events[0] before the router GEMV + top-k, [1] before the gate/up GEMV, [2] before
+ *            the down GEMV, [3] after it (4 entries).
+ */
+MOE_API int moe_prefill_timed(const moe_layer* layer, const uint16_t* x, int32_t T, uint16_t* y,
+                              moe_route_out* out, void* ws, size_t ws_bytes, moe_stream_t stream,
+                              void* const* events);
+MOE_API int moe_decode_timed(const moe_layer* layer, const uint16_t* x, uint16_t* y, moe_route_out* out,
+                             void* ws, size_t ws_bytes, moe_stream_t stream, void* const* events);
+
 /* Synchronises `stream`, returns the sticky device status of `ws` (MOE_OK or a device error
  * code) and clears it. */
 MOE_API int moe_read_device_status(void* ws, moe_stream_t stream);

@@ -76,6 +76,10 @@ def lib() -> ctypes.CDLL:
         L.moe_prefill.restype = ctypes.c_int
         L.moe_decode.argtypes = [P(MoeLayer), c_void_p, c_void_p, P(RouteOut), c_void_p, c_size_t, c_void_p]
         L.moe_decode.restype = ctypes.c_int
+        L.moe_prefill_timed.argtypes = L.moe_prefill.argtypes + [ctypes.POINTER(c_void_p)]
+        L.moe_prefill_timed.restype = ctypes.c_int
+        L.moe_decode_timed.argtypes = L.moe_decode.argtypes + [ctypes.POINTER(c_void_p)]
+        L.moe_decode_timed.restype = ctypes.c_int
         L.moe_read_device_status.argtypes = [c_void_p, c_void_p]
         L.moe_read_device_status.restype = ctypes.c_int
         L.moe_status_string.argtypes = [ctypes.c_int]
@@ -199,26 +203,43 @@ def route(layer: Layer, x, T: int, ws: torch.Tensor, logits_in=None, out: dict |
     return out
 
 
+def _events(events, n: int):
+    """Raw cudaEvent_t handles of torch.cuda.Event objects (None entries allowed)."""
+    if events is None:
+        return None
+    assert len(events) == n
+    return (c_void_p * n)(*[None if e is None else e.cuda_event for e in events])
+
+
 def prefill(layer: Layer, x: torch.Tensor, ws: torch.Tensor, y: torch.Tensor | None = None,
-            out: dict | None = None) -> torch.Tensor:
+            out: dict | None = None, events=None) -> torch.Tensor:
+    """events: optional 6 torch.cuda.Event objects (already recorded once, so they exist) that
+    the library records at its kernel boundaries (see moe_prefill_timed)."""
     _check_dev(x, torch.int16, "x")
     T = x.shape[0]
     y = y if y is not None else torch.empty_like(x)
     ro = _route_struct(out)
-    _check(lib().moe_prefill(ctypes.byref(layer.c), x.data_ptr(), T, y.data_ptr(),
-                             ctypes.byref(ro) if ro is not None else None, ws.data_ptr(), ws.numel(), _stream()),
-           "moe_prefill")
+    args = (ctypes.byref(layer.c), x.data_ptr(), T, y.data_ptr(), ctypes.byref(ro) if ro is not None else None,
+            ws.data_ptr(), ws.numel(), _stream())
+    if events is None:
+        _check(lib().moe_prefill(*args), "moe_prefill")
+    else:
+        _check(lib().moe_prefill_timed(*args, _events(events, 6)), "moe_prefill_timed")
     return y
 
 
 def decode(layer: Layer, x: torch.Tensor, ws: torch.Tensor, y: torch.Tensor | None = None,
-           out: dict | None = None) -> torch.Tensor:
+           out: dict | None = None, events=None) -> torch.Tensor:
+    """events: optional 4 torch.cuda.Event objects (see moe_decode_timed)."""
     _check_dev(x, torch.int16, "x")
     y = y if y is not None else torch.empty_like(x)
     ro = _route_struct(out)
-    _check(lib().moe_decode(ctypes.byref(layer.c), x.data_ptr(), y.data_ptr(),
-                            ctypes.byref(ro) if ro is not None else None, ws.data_ptr(), ws.numel(), _stream()),
-           "moe_decode")
+    args = (ctypes.byref(layer.c), x.data_ptr(), y.data_ptr(), ctypes.byref(ro) if ro is not None else None,
+            ws.data_ptr(), ws.numel(), _stream())
+    if events is None:
+        _check(lib().moe_decode(*args), "moe_decode")
+    else:
+        _check(lib().moe_decode_timed(*args, _events(events, 4)), "moe_decode_timed")
     return y
 
 

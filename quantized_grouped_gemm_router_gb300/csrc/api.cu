@@ -219,8 +219,8 @@ int moe_route(const moe_layer* layer, const uint16_t* x, const float* logits_in,
   return copy_route_out(d, T, w, out, stream);
 }
 
-int moe_prefill(const moe_layer* layer, const uint16_t* x, int32_t T, uint16_t* y, moe_route_out* out, void* ws,
-                size_t ws_bytes, moe_stream_t stream) {
+int moe_prefill_timed(const moe_layer* layer, const uint16_t* x, int32_t T, uint16_t* y, moe_route_out* out,
+                      void* ws, size_t ws_bytes, moe_stream_t stream, void* const* events) {
   int st = check_layer(layer, true);
   if (st) return st;
   if (T < 1 || !x || !y) return MOE_ERR_INVALID_ARG;
@@ -235,7 +235,9 @@ int moe_prefill(const moe_layer* layer, const uint16_t* x, int32_t T, uint16_t* 
   const int A = T * d.top_k;
 
   // 1. router logits (tensor cores), 2. top-k + grouping (+ zero the combine accumulator)
+  if (record_event(events, 0, stream) != cudaSuccess) return MOE_ERR_CUDA;
   if ((st = run_router_gemm(layer, x, T, w, stream))) return st;
+  if (record_event(events, 1, stream) != cudaSuccess) return MOE_ERR_CUDA;
   if ((st = run_route(d, w.at<float>(w.L.logits), T, w, yacc, x, stream))) return st;
 
   // 3. gate|up grouped GEMM + SwiGLU -> hidden; 4. down grouped GEMM + weighted combine -> yacc
@@ -266,22 +268,31 @@ int moe_prefill(const moe_layer* layer, const uint16_t* x, int32_t T, uint16_t* 
   p.region_offset = 0;
   p.m_tiles = d.inter / kBlockRows;
   p.k_blocks = d.d / kGroup;
+  if (record_event(events, 2, stream) != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_gemm(kModeGateUp, p, &x_rows, &unused, tiles * p.m_tiles, stream) != cudaSuccess) return MOE_ERR_CUDA;
 
   p.region_offset = P.gu_bytes;
   p.m_tiles = d.d / kBlockRows;
   p.k_blocks = d.inter / kGroup;
+  if (record_event(events, 3, stream) != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_gemm(kModeDown, p, &h_rows, &unused, tiles * p.m_tiles, stream) != cudaSuccess) return MOE_ERR_CUDA;
 
   // 5. fp32 accumulator -> bf16 output
+  if (record_event(events, 4, stream) != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_cast(yacc, y, (size_t)T * d.d, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  if (record_event(events, 5, stream) != cudaSuccess) return MOE_ERR_CUDA;
   if ((st = copy_route_out(d, T, w, out, stream))) return st;
   if (out && out->hidden) return copy_out(out->hidden, hidden, 2 * ((size_t)A + T) * d.inter * 2, stream);
   return MOE_OK;
 }
 
-int moe_decode(const moe_layer* layer, const uint16_t* x, uint16_t* y, moe_route_out* out, void* ws, size_t ws_bytes,
-               moe_stream_t stream) {
+int moe_prefill(const moe_layer* layer, const uint16_t* x, int32_t T, uint16_t* y, moe_route_out* out, void* ws,
+                size_t ws_bytes, moe_stream_t stream) {
+  return moe_prefill_timed(layer, x, T, y, out, ws, ws_bytes, stream, nullptr);
+}
+
+int moe_decode_timed(const moe_layer* layer, const uint16_t* x, uint16_t* y, moe_route_out* out, void* ws,
+                     size_t ws_bytes, moe_stream_t stream, void* const* events) {
   int st = check_layer(layer, true);
   if (st) return st;
   if (!x || !y) return MOE_ERR_INVALID_ARG;
@@ -307,12 +318,17 @@ int moe_decode(const moe_layer* layer, const uint16_t* x, uint16_t* y, moe_route
   p.E = d.n_experts;
   p.k = d.top_k;
   p.inter = d.inter;
-  if (launch_decode(p, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_decode(p, stream, events) != cudaSuccess) return MOE_ERR_CUDA;
   if (!out) return MOE_OK;
   st = copy_out(out->logits, p.logits, (size_t)d.n_experts * 4, stream);
   st |= copy_out(out->topk_idx, p.topk_idx, (size_t)d.top_k * 4, stream);
   st |= copy_out(out->topk_w, p.topk_w, (size_t)d.top_k * 4, stream);
   return st ? MOE_ERR_CUDA : MOE_OK;
+}
+
+int moe_decode(const moe_layer* layer, const uint16_t* x, uint16_t* y, moe_route_out* out, void* ws, size_t ws_bytes,
+               moe_stream_t stream) {
+  return moe_decode_timed(layer, x, y, out, ws, ws_bytes, stream, nullptr);
 }
 
 int moe_read_device_status(void* ws, moe_stream_t stream) {

@@ -229,20 +229,21 @@ size_t decode_smem_down(int k, int inter) {
   return ((size_t)(k + 1) * inter + items + items * kDownRows) * sizeof(float);
 }
 
-cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s) {
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s, void* const* events) {
   const size_t sm_gu = decode_smem_gateup(p.d), sm_dn = decode_smem_down(p.k, p.inter);
   static cudaError_t a1 = cudaFuncSetAttribute(decode_gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
   static cudaError_t a2 = cudaFuncSetAttribute(decode_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
   if (a1 != cudaSuccess) return a1;
   if (a2 != cudaSuccess) return a2;
+  cudaError_t err = record_event(events, 0, s);
+  if (err != cudaSuccess) return err;
   decode_router_kernel<<<(p.E + 7) / 8, kDecThreads, 0, s>>>(p);
-  cudaError_t err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
+  if ((err = cudaGetLastError()) != cudaSuccess || (err = record_event(events, 1, s)) != cudaSuccess) return err;
   decode_gateup_kernel<<<(p.k + 1) * (p.inter / kGateUpRows), kDecThreads, sm_gu, s>>>(p);
-  err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
+  if ((err = cudaGetLastError()) != cudaSuccess || (err = record_event(events, 2, s)) != cudaSuccess) return err;
   decode_down_kernel<<<p.d / kDownRows, kDecThreads, sm_dn, s>>>(p);
-  return cudaGetLastError();
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  return record_event(events, 3, s);
 }
 
 }  // namespace moe

@@ -178,6 +178,12 @@ cudaError_t launch_route(const RouteParams& p, cudaStream_t s);
 cudaError_t launch_gemm(int mode, const GemmParams& p, const CUtensorMap* tmap_b, const CUtensorMap* tmap_a,
                         int grid, cudaStream_t s);
 cudaError_t launch_cast(const float* yacc, uint16_t* y, size_t n, cudaStream_t s);
-cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s);
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s, void* const* events);
+
+// Records events[i] (if the array and the entry are non-NULL) on the stream; capturable.
+inline cudaError_t record_event(void* const* events, int i, cudaStream_t s) {
+  if (!events || !events[i]) return cudaSuccess;
+  return cudaEventRecordWithFlags(static_cast<cudaEvent_t>(events[i]), s, cudaEventRecordExternal);
+}
 
 }  // namespace moe
