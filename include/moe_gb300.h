@@ -202,6 +202,29 @@ MOE_API int moe_decode(const moe_layer* layer, const uint16_t* x, uint16_t* y, m
                void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /*
+ * Allocation-free batch-1 decode. The paper has no counterpart to this call; it exists for
+ * callers that cannot allocate device memory: code embedded in a host application that owns
+ * every device allocation and only lends it input and output buffers, and code that must not
+ * allocate after start-up because cudaMalloc can synchronise the device and can fail under
+ * memory pressure. It computes exactly what moe_decode computes, with the same kernels, but its
+ * scratch (logits, selected experts and weights, SwiGLU rows, counters) lives in a fixed 64 KiB
+ * device array inside the library instead of a caller workspace.
+ *   - x, y: bf16 [1, d] device buffers owned by the caller, as for moe_decode.
+ *   - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine.
+ *   - The 64 KiB array is held on every device that loads the library until the process exits.
+ *     Shapes whose scratch (256 + 4E + 8k + 4(k+1)I bytes, each part rounded up to 256) does
+ *     not fit return MOE_ERR_UNSUPPORTED_SHAPE before anything is launched.
+ *   - The first call on a device looks up the array's device address (once per device, with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call uses the same array, which keeps the last call's contents; the call clears
+ *     what must start at zero. Calls that overlap on the GPU (other streams or host threads)
+ *     race on the array: serialise them.
+ *   - Device-side errors (e.g. non-finite logits) are not reported by this variant: it has no
+ *     status word the caller can read. Argument errors are returned as for moe_decode.
+ */
+MOE_API int moe_decode_noalloc(const moe_layer* layer, const uint16_t* x, uint16_t* y, moe_stream_t stream);
+
+/*
  * Timed variants of moe_prefill and moe_decode for measurement: identical work, plus
  * cudaEventRecordWithFlags(events[i], stream, cudaEventRecordExternal) at each kernel boundary
  * so the events also become nodes of a CUDA graph captured from the call. `events` is a host

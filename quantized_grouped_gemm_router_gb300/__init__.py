@@ -10,6 +10,7 @@ from .binding import (  # noqa: F401
     MoeDims,
     MoeError,
     decode,
+    decode_noalloc,
     dims_of,
     lib,
     pack_weights,

@@ -80,6 +80,8 @@ def lib() -> ctypes.CDLL:
         L.moe_prefill_timed.restype = ctypes.c_int
         L.moe_decode_timed.argtypes = L.moe_decode.argtypes + [ctypes.POINTER(c_void_p)]
         L.moe_decode_timed.restype = ctypes.c_int
+        L.moe_decode_noalloc.argtypes = [P(MoeLayer), c_void_p, c_void_p, c_void_p]
+        L.moe_decode_noalloc.restype = ctypes.c_int
         L.moe_read_device_status.argtypes = [c_void_p, c_void_p]
         L.moe_read_device_status.restype = ctypes.c_int
         L.moe_status_string.argtypes = [ctypes.c_int]
@@ -240,6 +242,15 @@ def decode(layer: Layer, x: torch.Tensor, ws: torch.Tensor, y: torch.Tensor | No
         _check(lib().moe_decode(*args), "moe_decode")
     else:
         _check(lib().moe_decode_timed(*args, _events(events, 4)), "moe_decode_timed")
+    return y
+
+
+def decode_noalloc(layer: Layer, x: torch.Tensor, y: torch.Tensor) -> torch.Tensor:
+    """Batch-1 decode through moe_decode_noalloc: no workspace, the library allocates nothing."""
+    _check_dev(x, torch.int16, "x")
+    _check_dev(y, torch.int16, "y")
+    _check(lib().moe_decode_noalloc(ctypes.byref(layer.c), x.data_ptr(), y.data_ptr(), _stream()),
+           "moe_decode_noalloc")
     return y
 
 

@@ -1,0 +1,57 @@
+"""The allocation-free decode entry point (moe_decode_noalloc) against the regular one.
+
+moe_decode_noalloc serves callers that cannot allocate device memory (a host application that
+owns all device memory and lends only input/output buffers, or code that must not allocate
+after start-up). Called through the C ABI, it must return what moe_decode returns on the same
+inputs, within the output tolerance the other tests use, on two calls in a row (the second call
+reuses the library's fixed scratch array left over from the first). This file is collected last
+and passes both alone in a fresh process and after the other tests.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from synthetic import FULL, TINY, make_layer, make_tokens  # noqa: E402
+from tests import moe_check as C  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def m():
+    from quantized_grouped_gemm_router_gb300 import build as B
+    B.build()
+    import quantized_grouped_gemm_router_gb300 as mod
+    assert torch.cuda.is_available()
+    return mod
+
+
+@pytest.mark.parametrize("shape,seed", [(FULL, 7), (TINY, 8)], ids=["full", "tiny"])
+def test_decode_noalloc_matches_decode(m, shape, seed):
+    layer = m.upload_layer(make_layer(shape, seed=seed))
+    ws = m.workspace(layer.dims, 1)
+    lib = m.lib()
+    stream = torch.cuda.current_stream().cuda_stream
+    for call in range(2):                       # two calls in a row share the static scratch
+        x = torch.from_numpy(make_tokens(1, shape.d, seed=seed, stream=call + 1).view(np.int16)).cuda()
+        y_ref = m.decode(layer, x, ws)
+        y = torch.full_like(x, 0x7FC0)            # NaN fill: every element must be written
+        rc = lib.moe_decode_noalloc(ctypes.byref(layer.c), ctypes.c_void_p(x.data_ptr()),
+                                    ctypes.c_void_p(y.data_ptr()), ctypes.c_void_p(stream))
+        assert rc == 0, m.status_string(rc)
+        torch.cuda.synchronize()
+        C.check_y(C.bf16_bits_f64(y), C.bf16_bits_f64(y_ref), f"call {call}")
+    assert m.read_device_status(ws) == 0
+
+
+def test_decode_noalloc_rejects_oversized_shape(m):
+    from quantized_grouped_gemm_router_gb300.binding import MoeLayer
+    dims = m.dims_of(FULL)
+    dims.inter = 4096          # (k+1) * I * 4 bytes of SwiGLU rows exceed the fixed scratch
+    dims.shared_inter = 4096
+    A = 1 << 20                # never dereferenced: the shape check fails first
+    layer = MoeLayer(dims, A, None, A)
+    assert m.lib().moe_decode_noalloc(ctypes.byref(layer), A, A, None) == 2
