@@ -197,6 +197,11 @@ MOE_API int moe_prefill(const moe_layer* layer, const uint16_t* x, int32_t T, ui
  * the top_k selected experts and the shared expert, gate activation fused into the input
  * projections, routing weights and the shared expert fused into the output projection.
  * x: bf16 [1, d]; y: bf16 [1, d]. ws: at least moe_workspace_bytes(dims, 1). `out` may be NULL.
+ * Decode supports d <= 3072 (MOE_ERR_UNSUPPORTED_SHAPE otherwise). The kernels are chained with
+ * programmatic dependent launch: each loads the static weights it needs (router rows, the
+ * shared expert) before waiting for the work that precedes it in the stream, so `layer`'s
+ * weights must not be written by that preceding work. The result is deterministic (fixed
+ * summation order).
  */
 MOE_API int moe_decode(const moe_layer* layer, const uint16_t* x, uint16_t* y, moe_route_out* out,
                void* ws, size_t ws_bytes, moe_stream_t stream);
@@ -207,13 +212,14 @@ MOE_API int moe_decode(const moe_layer* layer, const uint16_t* x, uint16_t* y, m
  * every device allocation and only lends it input and output buffers, and code that must not
  * allocate after start-up because cudaMalloc can synchronise the device and can fail under
  * memory pressure. It computes exactly what moe_decode computes, with the same kernels, but its
- * scratch (logits, selected experts and weights, SwiGLU rows, counters) lives in a fixed 64 KiB
- * device array inside the library instead of a caller workspace.
+ * scratch (logits, selected experts and weights, per-block partial outputs, counters) lives in a
+ * fixed 2 MiB device array inside the library instead of a caller workspace.
  *   - x, y: bf16 [1, d] device buffers owned by the caller, as for moe_decode.
  *   - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine.
- *   - The 64 KiB array is held on every device that loads the library until the process exits.
- *     Shapes whose scratch (256 + 4E + 8k + 4(k+1)I bytes, each part rounded up to 256) does
- *     not fit return MOE_ERR_UNSUPPORTED_SHAPE before anything is launched.
+ *   - The 2 MiB array is held on every device that loads the library until the process exits.
+ *     Shapes whose scratch (256 + 4E + 8k + 4d(k+1)I/32 bytes, each part rounded up to 256)
+ *     does not fit return MOE_ERR_UNSUPPORTED_SHAPE before anything is launched (d=2048,
+ *     E=256, k=8, I=512 needs 1.13 MiB).
  *   - The first call on a device looks up the array's device address (once per device, with
  *     that device current); make that first call before any stream capture.
  *   - Every call uses the same array, which keeps the last call's contents; the call clears
@@ -232,8 +238,10 @@ MOE_API int moe_decode_noalloc(const moe_layer* layer, const uint16_t* x, uint16
  *   prefill: events[0] before the router GEMM, [1] before the routing kernels (top-k and
  *            scatter), [2] before the gate/up GEMM, [3] before the down GEMM, [4] before the
  *            output cast, [5] after it (6 entries).
- *   decode:  events[0] before the router GEMV + top-k, [1] before the gate/up GEMV, [2] before
- *            the down GEMV, [3] after it (4 entries).
+ *   decode:  events[0] before the router GEMV + top-k, [1] before the expert kernel (gate/up
+ *            GEMV + SwiGLU + this block's down partial), [2] before the combine of the partial
+ *            outputs, [3] after it (4 entries). Events between the kernels also stop them from
+ *            overlapping through programmatic dependent launch.
  */
 MOE_API int moe_prefill_timed(const moe_layer* layer, const uint16_t* x, int32_t T, uint16_t* y,
                               moe_route_out* out, void* ws, size_t ws_bytes, moe_stream_t stream,

@@ -297,6 +297,7 @@ int moe_decode_timed(const moe_layer* layer, const uint16_t* x, uint16_t* y, moe
   if (st) return st;
   if (!x || !y) return MOE_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(y, 16)) return MOE_ERR_MISALIGNED;
+  if (layer->dims.d > kDecodeMaxD) return MOE_ERR_UNSUPPORTED_SHAPE;
   if ((st = check_out(out)) || (st = check_ws(ws, ws_bytes, layer->dims, 1))) return st;
   const moe_dims& d = layer->dims;
   Ws w{static_cast<uint8_t*>(ws), ws_layout(d, 1)};
@@ -311,7 +312,7 @@ int moe_decode_timed(const moe_layer* layer, const uint16_t* x, uint16_t* y, moe
   p.logits = w.at<float>(w.L.logits);
   p.topk_idx = w.at<int32_t>(w.L.topk_idx);
   p.topk_w = w.at<float>(w.L.topk_w);
-  p.hbuf = w.at<float>(w.L.dec_h);
+  p.partials = w.at<float>(w.L.dec_part);
   p.y = y;
   p.hdr = w.at<WsHeader>(w.L.header);
   p.d = d.d;

@@ -3,21 +3,35 @@
 // Page "Perplexity's Lily beats MLX-LM on MacBook M5 because it only runs one model":
 // section "Prefill and decode are different problems" (decode at batch 1 is a matrix-vector
 // product bound by memory bandwidth; "minimize bytes moved per token"), section "Decode:
-// minimize bytes per token" (fusion of the input projections with the gate activation and of
-// the output projection with the routing scores and the shared expert), section "What didn't
-// work" (the GEMV runs near the weight-read rate and its arithmetic barely matters).
+// minimize bytes per token" (the input projections fused with the gate activation, the output
+// projection with the routing scores and the shared expert; dependency-aware overlap of
+// kernels), section "What didn't work" (the GEMV runs near the weight-read rate).
 //
-// Three launches on one stream:
-//   decode_router_kernel  one warp per expert: logit = W_r[e] . x (+ b_e); the last CTA to
-//                         finish selects the top k and their renormalised weights
-//   decode_gateup_kernel  one CTA per (selected or shared expert, 32 intermediate rows):
-//                         gate and up GEMV rows over the packed blocks, SwiGLU in registers
-//   decode_down_kernel    one CTA per 16 output rows: the down GEMV of all k+1 experts, scaled
-//                         by the routing weights (shared expert weight 1) and summed in a fixed
-//                         order (deterministic, no atomics), written as bf16
-// Weights stream with 128-bit non-allocating loads; per group of 64 inputs the dot product is
-// scale * sum(q*x) + bias * sum(x), with sum(x) computed once per input vector.
+// Three launches chained with programmatic dependent launch (PDL): each kernel lets its
+// successor start at once, and does everything that does not depend on its predecessor's
+// results (loading static weights) before waiting for it.
+//   decode_router_kernel  two experts per CTA: logit = W_r[e] . x (+ b_e); the router weight
+//                         slice is loaded before the wait; the last CTA to finish selects the
+//                         top k and their renormalised weights
+//   decode_expert_kernel  one CTA per (selected or shared expert, 32 intermediate rows): all of
+//                         its gate/up rows and its 32-column slice of the down projection are
+//                         bulk-copied to shared memory as soon as the expert is known (the
+//                         shared expert's CTAs before routing is known); gate/up + SwiGLU,
+//                         scaled by the routing weight, then this slice's contribution to every
+//                         output row (split-K over the intermediate dimension)
+//   decode_reduce_kernel  y = sum of the per-CTA partial rows in a fixed order -> bf16
+// The GEMV inner products run on the tensor cores (mma.sync m16n8k16, fp16 in, fp32
+// accumulate): the packed nibble pairs of a row map directly onto the MMA fragment layout, so
+// each weight costs about one ALU operation instead of three for an fp32 FMA loop, which on
+// GB300 would otherwise take as long as streaming the weights. The GEMV vector occupies one
+// column of B (x for gate/up; the SwiGLU output as an fp16 leading part and remainder in two
+// columns for down), and each 64-column group's scale and bias are applied to the fp32
+// accumulator: sum (s*q + b) v = s * sum(q v) + b * sum(v). For gate/up the codes enter the MMA
+// as (1024 + q) (one LOP3 per pair; x is small, so the fp32 accumulation keeps sum(q x) to about
+// 1e-5 relative) and the offset is removed with the group's sum of x; for down the codes are made
+// exact first, because the SwiGLU values are large.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "moe_internal.h"
 #include "ptx.cuh"
@@ -26,9 +40,15 @@
 namespace moe {
 namespace {
 
-constexpr int kDecThreads = 256;
-constexpr int kGateUpRows = 32;   // intermediate rows per gate/up CTA
-constexpr int kDownRows = 16;     // output rows per down CTA
+constexpr int kRThreads = 256;         // router: two experts per CTA, 128 threads each
+constexpr int kRMaxChunks = kDecodeMaxD / 8 / 128;
+constexpr int kXThreads = 512;         // expert kernel: 16 warps to hide MMA and smem latency
+constexpr int kXWarps = kXThreads / 32;
+constexpr int kYThreads = 512;         // reduce: 16 output rows x 32 groups of partial rows
+constexpr int kYRows = 16;
+constexpr int kXMaxGUChunks = 4;       // gate/up run split into up to 4 copies (own barriers)
+constexpr int kGUStage = 2 * (2 * kDecPartRows * 16 + kDecPartRows * 4);  // gate + up slice of one kb
+constexpr int kDnStage = kHalfBytes + kBlockRows * 4;                     // down half-block + sb
 
 __device__ __forceinline__ uint4 ld_stream(const void* p) {
   uint4 r;
@@ -37,55 +57,82 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
                : "l"(p));
   return r;
 }
-__device__ __forceinline__ uint32_t ld_stream32(const void* p) {
-  uint32_t r;
-  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(r) : "l"(p));
-  return r;
-}
 __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
-// One row of one 64-column block: sum_c (scale*q_c + bias) * x_c, with x (64 fp32 values,
-// shared memory) and gsum = sum_c x_c. Codes are read as (128 + q) bf16 pairs, so the
-// accumulated value is sum (128 + q) x; scale*acc + (bias - 128*scale)*gsum removes the offset.
-__device__ __forceinline__ float dot_block(const uint4 c0, const uint4 c1, uint32_t sb, const float* xs, float gsum) {
-  const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-  float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t t = ((words[c] >> (4 * i)) & 0x000F000Fu) | 0x43004300u;
-      acc0 = fmaf(bf16lo(t), xs[8 * c + 2 * i], acc0);
-      acc1 = fmaf(bf16hi(t), xs[8 * c + 2 * i + 1], acc1);
-    }
-  }
-  const float s = bf16lo(sb), b = bf16hi(sb);
-  return s * (acc0 + acc1) + (b - 128.f * s) * gsum;
+// Nibble pair `sh/4` of a packed word (columns 2i, 2i+1 of its eight) as the fp16 pair
+// (1024 + q0, 1024 + q1); the caller removes 1024 * sum(v) after the product.
+__device__ __forceinline__ uint32_t q_pair_offset(uint32_t w, int sh) {
+  return ((w >> sh) & 0x000F000Fu) | 0x64006400u;
+}
+// The same pair as exact fp16 codes (q0, q1).
+__device__ __forceinline__ uint32_t q_pair(uint32_t w, int sh) {
+  uint32_t t = ((w >> sh) & 0x000F000Fu) | 0x64006400u;  // (1024 + q) in fp16
+  __half2 v = __hsub2(*reinterpret_cast<__half2*>(&t), __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400)));
+  return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__global__ void __launch_bounds__(kDecThreads) decode_router_kernel(const DecodeParams p) {
+// D = A(16x16, fp16, row-major) * B(16x8, fp16, column-major) + 0, fp32 result.
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%11,%12,%13};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(d[0]), "f"(d[1]), "f"(d[2]), "f"(d[3]));
+}
+
+template <class Kernel, class... Args>
+cudaError_t launch_pdl(Kernel kernel, int grid, int block, size_t smem, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+__global__ void __launch_bounds__(kRThreads) decode_router_kernel(const DecodeParams p) {
+  __shared__ float s_part[kRThreads / 32];
   __shared__ int s_last;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e = blockIdx.x * (kDecThreads / 32) + warp;
-  if (e < p.E) {
-    const uint16_t* w = p.router_w + (size_t)e * p.d;
-    float acc = 0.f;
-    for (int i = lane * 8; i < p.d; i += 256) {
-      const uint4 xv = *reinterpret_cast<const uint4*>(p.x + i);
-      const uint4 wv = ld_stream(w + i);
-      const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w}, wa[4] = {wv.x, wv.y, wv.z, wv.w};
+  const int half = threadIdx.x >> 7, t = threadIdx.x & 127, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * 2 + half;
+  const int nch = p.d >> 3;  // 8-element chunks per row
+  uint4 w[kRMaxChunks];
+#pragma unroll
+  for (int i = 0; i < kRMaxChunks; ++i) {  // static weights: load before waiting on the predecessor
+    const int c = t + 128 * i;
+    w[i] = (e < p.E && c < nch) ? ld_stream(p.router_w + (size_t)e * p.d + 8 * c) : make_uint4(0, 0, 0, 0);
+  }
+  pdl_launch_dependents();
+  pdl_wait();
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < kRMaxChunks; ++i) {
+    const int c = t + 128 * i;
+    if (e < p.E && c < nch) {
+      const uint4 xv = __ldcg(reinterpret_cast<const uint4*>(p.x) + c);
+      const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w}, wa[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         acc = fmaf(bf16lo(xa[j]), bf16lo(wa[j]), acc);
         acc = fmaf(bf16hi(xa[j]), bf16hi(wa[j]), acc);
       }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
-    if (lane == 0) p.logits[e] = acc + (p.router_bias ? p.router_bias[e] : 0.f);
   }
-  __threadfence();
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+  if (lane == 0) s_part[warp] = acc;
+  __syncthreads();
+  if (t == 0 && e < p.E) {
+    const float* sp = s_part + 4 * half;
+    p.logits[e] = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + (p.router_bias ? p.router_bias[e] : 0.f);
+    __threadfence();  // the logit is visible before this CTA takes its ticket
+  }
   __syncthreads();
   if (threadIdx.x == 0) s_last = (atomicAdd(&p.hdr->dticket, 1u) == gridDim.x - 1);
   __syncthreads();
@@ -104,145 +151,245 @@ __global__ void __launch_bounds__(kDecThreads) decode_router_kernel(const Decode
   }
 }
 
-// Dynamic shared memory: x as fp32 [d], group sums [d/64], partials [8 warps][2][32].
-__global__ void __launch_bounds__(kDecThreads) decode_gateup_kernel(const DecodeParams p) {
-  extern __shared__ float dsm[];
-  float* s_x = dsm;
-  float* s_gs = s_x + p.d;
-  float* s_part = s_gs + p.d / kGroup;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int per_slot = p.inter / kGateUpRows;
-  const int slot = blockIdx.x / per_slot;
-  const int f0 = (blockIdx.x % per_slot) * kGateUpRows;
-  const int expert = slot < p.k ? p.topk_idx[slot] : p.E;
-  for (int i = tid; i < p.d; i += kDecThreads) s_x[i] = __uint_as_float((uint32_t)p.x[i] << 16);
-  __syncthreads();
-  const int KB = p.d / kGroup;
-  for (int g = tid; g < KB; g += kDecThreads) {
-    float s = 0.f;
-    for (int c = 0; c < kGroup; ++c) s += s_x[g * kGroup + c];
-    s_gs[g] = s;
-  }
-  __syncthreads();
-  const int m = f0 / kBlockRows, r = f0 % kBlockRows + lane;
-  const uint8_t* gu = p.packed + (size_t)expert * p.expert_stride + (size_t)m * KB * 2 * kBlockBytes;
-  float g_acc = 0.f, u_acc = 0.f;
-  for (int kb0 = warp; kb0 < KB; kb0 += 4 * (kDecThreads / 32)) {
-    uint4 gc[4][2], uc[4][2];
-    uint32_t gsb[4], usb[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {  // issue every load of up to four blocks before any math
-      const int kb = kb0 + i * (kDecThreads / 32);
-      if (kb < KB) {
-        const uint8_t* blk = gu + (size_t)kb * 2 * kBlockBytes;
-        gc[i][0] = ld_stream(blk + r * 32);
-        gc[i][1] = ld_stream(blk + r * 32 + 16);
-        gsb[i] = ld_stream32(blk + kCodeBytes + r * 4);
-        uc[i][0] = ld_stream(blk + kBlockBytes + r * 32);
-        uc[i][1] = ld_stream(blk + kBlockBytes + r * 32 + 16);
-        usb[i] = ld_stream32(blk + kBlockBytes + kCodeBytes + r * 4);
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int kb = kb0 + i * (kDecThreads / 32);
-      if (kb < KB) {
-        g_acc += dot_block(gc[i][0], gc[i][1], gsb[i], s_x + kb * kGroup, s_gs[kb]);
-        u_acc += dot_block(uc[i][0], uc[i][1], usb[i], s_x + kb * kGroup, s_gs[kb]);
-      }
-    }
-  }
-  s_part[(warp * 2 + 0) * 32 + lane] = g_acc;
-  s_part[(warp * 2 + 1) * 32 + lane] = u_acc;
-  __syncthreads();
-  if (warp == 0) {
-    float g = 0.f, u = 0.f;
-    for (int w = 0; w < kDecThreads / 32; ++w) {
-      g += s_part[(w * 2 + 0) * 32 + lane];
-      u += s_part[(w * 2 + 1) * 32 + lane];
-    }
-    p.hbuf[(size_t)slot * p.inter + f0 + lane] = g / (1.f + expf(-g)) * u;
-  }
+// Shared memory of the expert kernel (offsets in bytes, each 16-aligned).
+struct XSmem {
+  int gu, dn, x16, xsum, red, h, misc, bars, total;
+};
+__host__ __device__ inline int up16(int v) { return (v + 15) & ~15; }
+__host__ __device__ inline XSmem x_smem(int d) {
+  const int KB = d / kGroup, DM = d / kBlockRows;
+  XSmem L;
+  L.gu = 0;                                           // KB entries of gate/up rows
+  L.dn = L.gu + KB * kGUStage;                        // DM code halves, then DM scale runs
+  L.x16 = up16(L.dn + DM * kDnStage);                 // x as fp16 pairs
+  L.xsum = up16(L.x16 + d * 2);                       // per-group sums of x
+  L.red = up16(L.xsum + KB * 4);                      // [warp][gate/up][32 rows] partial dots
+  L.h = up16(L.red + kXWarps * 2 * kDecPartRows * 4); // h leading part, remainder (fp16), sum
+  L.misc = up16(L.h + 2 * kDecPartRows * 2 + 16);     // abort flag
+  L.bars = up16(L.misc + 16);
+  L.total = L.bars + (kXMaxGUChunks + 1) * 8;
+  return L;
 }
 
-// Dynamic shared memory: h [(k+1) * I], group sums [(k+1) * I/64], partials [(k+1)*I/64][16].
-__global__ void __launch_bounds__(kDecThreads) decode_down_kernel(const DecodeParams p) {
-  extern __shared__ float dsm[];
-  const int KBI = p.inter / kGroup;
-  const int slots = p.k + 1, items = slots * KBI;
-  float* s_h = dsm;
-  float* s_hs = s_h + slots * p.inter;
-  float* s_part = s_hs + items;
-  const int tid = threadIdx.x;
-  for (int i = tid; i < slots * p.inter; i += kDecThreads) s_h[i] = __ldcg(p.hbuf + i);
-  __syncthreads();
-  for (int it = tid; it < items; it += kDecThreads) {
-    float s = 0.f;
-    for (int c = 0; c < kGroup; ++c) s += s_h[it * kGroup + c];
-    s_hs[it] = s;
+__global__ void __launch_bounds__(kXThreads, 1) decode_expert_kernel(const DecodeParams p) {
+  extern __shared__ __align__(128) uint8_t xs[];
+  const XSmem L = x_smem(p.d);
+  const int KB = p.d / kGroup, DM = p.d / kBlockRows, KBI = p.inter / kGroup;
+  const int parts = p.inter / kDecPartRows;
+  const int slot = blockIdx.x / parts, part = blockIdx.x % parts;
+  const bool shared = (slot == p.k);
+  const int m = part / (kBlockRows / kDecPartRows);          // gate/up row block
+  const int kbd = part / 2, hd = part % 2;                    // down: column group of I and its half
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t bars = smem_u32(xs + L.bars);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(xs + L.misc);
+  const int NGU = min(kXMaxGUChunks, KB);  // barriers 0..NGU-1: gate/up pieces; NGU: down
+  if (tid == 0) {
+    for (int i = 0; i <= NGU; ++i) mbar_init(bars + 8u * i, 1);
+    *s_abort = 0;
+    fence_barrier_init();
   }
   __syncthreads();
-  const int i0 = blockIdx.x * kDownRows;
-  const int m = i0 / kBlockRows, rin = i0 % kBlockRows;
-  const int row = tid % kDownRows, lane_item = tid / kDownRows;
-  const int n_il = kDecThreads / kDownRows;
-  for (int it0 = lane_item; it0 < items; it0 += 4 * n_il) {
-    uint4 c[4][2];
-    uint32_t sb[4];
+
+  // Lane 0 of warp 0 issues this CTA's copies: the contiguous run of its 32 gate and up rows for
+  // every column block (KB * 2304 bytes, in NGU pieces), then its 32-column half of every down
+  // row block (DM * 2048 bytes of codes) and the matching scale/bias rows (DM * 512 bytes).
+  auto issue = [&](int expert) {
+    if (lane != 0) return;
+    const uint8_t* eb = p.packed + (size_t)expert * p.expert_stride;
+    const uint8_t* gu = eb + gu_offset(m, part % (kBlockRows / kDecPartRows), 0, KB);
+    for (int c = 0; c < NGU; ++c) {
+      const int kb0 = c * KB / NGU, kb1 = (c + 1) * KB / NGU;
+      const uint32_t bytes = (uint32_t)(kb1 - kb0) * kGUStage;
+      mbar_arrive_expect_tx(bars + 8u * c, bytes);
+      tma_bulk_g2s(smem_u32(xs + L.gu + kb0 * kGUStage), gu + (size_t)kb0 * kGUStage, bytes, bars + 8u * c);
+    }
+    const uint8_t* dn = eb + p.gu_bytes;
+    mbar_arrive_expect_tx(bars + 8u * NGU, (uint32_t)(DM * (kHalfBytes + kSBBytes)));
+    tma_bulk_g2s(smem_u32(xs + L.dn), dn + dn_code_offset(kbd, hd, 0, DM), DM * kHalfBytes, bars + 8u * NGU);
+    tma_bulk_g2s(smem_u32(xs + L.dn + DM * kHalfBytes), dn + dn_sb_offset(kbd, 0, DM, KBI), DM * kSBBytes,
+                 bars + 8u * NGU);
+  };
+
+  if (shared && warp == 0) issue(p.E);  // static weights: before waiting on the router
+  pdl_launch_dependents();
+  pdl_wait();
+  const int expert = shared ? p.E : __ldcg(p.topk_idx + slot);
+  const float wslot = shared ? 1.f : __ldcg(p.topk_w + slot);
+  if (!shared && warp == 0) issue(expert);
+
+  // x -> fp16 pairs in shared memory, and the per-64-group sums of x (fp32)
+  uint32_t* x2 = reinterpret_cast<uint32_t*>(xs + L.x16);
+  float* xsum = reinterpret_cast<float*>(xs + L.xsum);
+  const int nch = p.d / 8;
+  for (int base = 0; base < nch; base += kXThreads) {
+    const int c = base + tid;
+    float part_sum = 0.f;
+    if (c < nch) {
+      const uint4 v = __ldcg(reinterpret_cast<const uint4*>(p.x) + c);
+      const uint32_t in[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int it = it0 + i * n_il;
-      if (it < items) {
-        const int slot = it / KBI, kb = it % KBI;
-        const int expert = slot < p.k ? __ldcg(p.topk_idx + slot) : p.E;
-        const uint8_t* blk = p.packed + (size_t)expert * p.expert_stride + p.gu_bytes +
-                             ((size_t)m * KBI + kb) * kBlockBytes;
-        c[i][0] = ld_stream(blk + (rin + row) * 32);
-        c[i][1] = ld_stream(blk + (rin + row) * 32 + 16);
-        sb[i] = ld_stream32(blk + kCodeBytes + (rin + row) * 4);
+      for (int j = 0; j < 4; ++j) {
+        const float lo = bf16lo(in[j]), hi = bf16hi(in[j]);
+        part_sum += lo + hi;
+        const __half2 h2 = __floats2half2_rn(lo, hi);
+        x2[4 * c + j] = *reinterpret_cast<const uint32_t*>(&h2);
       }
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int it = it0 + i * n_il;
-      if (it < items) s_part[it * kDownRows + row] = dot_block(c[i][0], c[i][1], sb[i], s_h + it * kGroup, s_hs[it]);
-    }
+    for (int o = 1; o < 8; o <<= 1) part_sum += __shfl_xor_sync(0xFFFFFFFFu, part_sum, o);
+    if (c < nch && (c & 7) == 0) xsum[c >> 3] = part_sum;
   }
   __syncthreads();
-  if (tid < kDownRows) {
-    float y = 0.f;
-    for (int slot = 0; slot < slots; ++slot) {
-      float ys = 0.f;
-      for (int kb = 0; kb < KBI; ++kb) ys += s_part[(slot * KBI + kb) * kDownRows + tid];
-      const float w = slot < p.k ? __ldcg(p.topk_w + slot) : 1.f;
-      y += w * ys;
+
+  // ---- gate/up: warp w takes K blocks w, w+8, ...; 2 row tiles of 16 per matrix
+  const int g = lane >> 2, tig = lane & 3, sh = 4 * tig;
+  float acc[2][2][2] = {};  // [gate/up][row tile][row g, row g+8] (meaningful on tig == 0)
+  for (int kb = warp; kb < KB; kb += kXWarps) {
+    int chunk = 0;
+    while (kb >= (chunk + 1) * KB / NGU) ++chunk;
+    if (!mbar_wait(bars + 8u * chunk, 0, s_abort)) break;
+    const uint8_t* st = xs + L.gu + kb * kGUStage;
+    uint32_t b0[4], b1[4];
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4) {
+      const int kk = (kb * kGroup + c4 * 16) / 2 + tig;
+      b0[c4] = g == 0 ? x2[kk] : 0u;
+      b1[c4] = g == 0 ? x2[kk + 4] : 0u;
     }
-    p.y[i0 + tid] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
+    const float xg = xsum[kb];
+#pragma unroll
+    for (int mat = 0; mat < 2; ++mat) {
+      const uint8_t* ms = st + mat * (kGUStage / 2);
+#pragma unroll
+      for (int rt = 0; rt < 2; ++rt) {
+        const int R0 = rt * 16 + g, R1 = R0 + 8;
+        const uint4 r0a = *reinterpret_cast<const uint4*>(ms + R0 * 16);
+        const uint4 r0b = *reinterpret_cast<const uint4*>(ms + kDecPartRows * 16 + R0 * 16);
+        const uint4 r1a = *reinterpret_cast<const uint4*>(ms + R1 * 16);
+        const uint4 r1b = *reinterpret_cast<const uint4*>(ms + kDecPartRows * 16 + R1 * 16);
+        const uint32_t w0[8] = {r0a.x, r0a.y, r0a.z, r0a.w, r0b.x, r0b.y, r0b.z, r0b.w};
+        const uint32_t w1[8] = {r1a.x, r1a.y, r1a.z, r1a.w, r1b.x, r1b.y, r1b.z, r1b.w};
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4)
+          mma16816(d, q_pair_offset(w0[2 * c4], sh), q_pair_offset(w1[2 * c4], sh),
+                   q_pair_offset(w0[2 * c4 + 1], sh), q_pair_offset(w1[2 * c4 + 1], sh), b0[c4], b1[c4]);
+        // d = sum (1024 + q) x over the group: s*q + b weights give s*d + (b - 1024 s) * sum(x)
+        const uint32_t sb0 = *reinterpret_cast<const uint32_t*>(ms + 2 * kDecPartRows * 16 + R0 * 4);
+        const uint32_t sb1 = *reinterpret_cast<const uint32_t*>(ms + 2 * kDecPartRows * 16 + R1 * 4);
+        acc[mat][rt][0] += bf16lo(sb0) * d[0] + (bf16hi(sb0) - 1024.f * bf16lo(sb0)) * xg;
+        acc[mat][rt][1] += bf16lo(sb1) * d[2] + (bf16hi(sb1) - 1024.f * bf16lo(sb1)) * xg;
+      }
+    }
+  }
+  float* red = reinterpret_cast<float*>(xs + L.red);
+  if (tig == 0) {
+#pragma unroll
+    for (int mat = 0; mat < 2; ++mat)
+#pragma unroll
+      for (int rt = 0; rt < 2; ++rt) {
+        red[(warp * 2 + mat) * kDecPartRows + rt * 16 + g] = acc[mat][rt][0];
+        red[(warp * 2 + mat) * kDecPartRows + rt * 16 + g + 8] = acc[mat][rt][1];
+      }
+  }
+  __syncthreads();
+  __half* hh = reinterpret_cast<__half*>(xs + L.h);
+  __half* hl = hh + kDecPartRows;
+  float* hsum = reinterpret_cast<float*>(xs + L.h + 2 * kDecPartRows * 2);
+  if (warp == 0) {  // SwiGLU of this CTA's 32 rows, scaled by the routing weight
+    float gs = 0.f, us = 0.f;
+    for (int w = 0; w < kXWarps; ++w) {
+      gs += red[(w * 2 + 0) * kDecPartRows + lane];
+      us += red[(w * 2 + 1) * kDecPartRows + lane];
+    }
+    const float h = gs / (1.f + expf(-gs)) * us * wslot;
+    const __half hi = __float2half_rn(h);
+    hh[lane] = hi;
+    hl[lane] = __float2half_rn(h - __half2float(hi));
+    float tot = h;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xFFFFFFFFu, tot, o);
+    if (lane == 0) *hsum = tot;
+    if (__any_sync(0xFFFFFFFFu, !(fabsf(h) <= 65504.f)) && lane == 0) set_device_status(p.hdr, MOE_ERR_OUT_OF_RANGE);
+  }
+  __syncthreads();
+
+  // ---- down: this CTA's 32 columns of W_down against every output row (split-K partial)
+  const bool down_ok = mbar_wait(bars + 8u * NGU, 0, s_abort);
+  const uint32_t* hh2 = reinterpret_cast<const uint32_t*>(hh);
+  const uint32_t* hl2 = reinterpret_cast<const uint32_t*>(hl);
+  uint32_t bd0[2], bd1[2];
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {  // column 0: leading part of h, column 1: remainder
+    bd0[c] = g == 0 ? hh2[c * 8 + tig] : (g == 1 ? hl2[c * 8 + tig] : 0u);
+    bd1[c] = g == 0 ? hh2[c * 8 + 4 + tig] : (g == 1 ? hl2[c * 8 + 4 + tig] : 0u);
+  }
+  const float hs = *hsum;
+  float* out = p.partials + (size_t)blockIdx.x * p.d;
+  for (int tile = warp; down_ok && tile < DM * 8; tile += kXWarps) {
+    const int mm = tile >> 3, R0 = (tile & 7) * 16 + g, R1 = R0 + 8;
+    const uint8_t* ds = xs + L.dn + mm * kHalfBytes;
+    const uint8_t* dsb = xs + L.dn + DM * kHalfBytes + mm * kSBBytes;
+    const uint4 c0 = *reinterpret_cast<const uint4*>(ds + R0 * 16);
+    const uint4 c1 = *reinterpret_cast<const uint4*>(ds + R1 * 16);
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    mma16816(d, q_pair(c0.x, sh), q_pair(c1.x, sh), q_pair(c0.y, sh), q_pair(c1.y, sh), bd0[0], bd1[0]);
+    mma16816(d, q_pair(c0.z, sh), q_pair(c1.z, sh), q_pair(c0.w, sh), q_pair(c1.w, sh), bd0[1], bd1[1]);
+    if (tig == 0) {
+      const uint32_t sb0 = *reinterpret_cast<const uint32_t*>(dsb + R0 * 4);
+      const uint32_t sb1 = *reinterpret_cast<const uint32_t*>(dsb + R1 * 4);
+      out[mm * kBlockRows + R0] = bf16lo(sb0) * (d[0] + d[1]) + bf16hi(sb0) * hs;
+      out[mm * kBlockRows + R1] = bf16lo(sb1) * (d[2] + d[3]) + bf16hi(sb1) * hs;
+    }
+  }
+  if (tid == 0 && *s_abort) set_device_status(p.hdr, MOE_ERR_DEVICE_TIMEOUT);
+}
+
+// y[i] = sum over the expert-kernel CTAs c (ascending) of partials[c][i], rounded to bf16.
+// Thread (row r, group q) sums a contiguous range of c with batched loads; the 32 group sums of
+// a row are then added in group order, so the result does not depend on timing.
+__global__ void __launch_bounds__(kYThreads) decode_reduce_kernel(const DecodeParams p, int n_parts) {
+  constexpr int kGroups = kYThreads / kYRows;
+  __shared__ float s[kGroups][kYRows];
+  pdl_launch_dependents();
+  pdl_wait();
+  const int r = threadIdx.x % kYRows, q = threadIdx.x / kYRows;
+  const int row = blockIdx.x * kYRows + r;
+  const int per = (n_parts + kGroups - 1) / kGroups, c_end = min(n_parts, (q + 1) * per);
+  float acc = 0.f;
+  for (int c0 = q * per; c0 < c_end; c0 += 8) {
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = (c0 + j < c_end) ? __ldcg(p.partials + (size_t)(c0 + j) * p.d + row) : 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc += v[j];
+  }
+  s[q][r] = acc;
+  __syncthreads();
+  if (q == 0) {
+    float y = 0.f;
+    for (int i = 0; i < kGroups; ++i) y += s[i][r];
+    p.y[row] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
   }
 }
 
 }  // namespace
 
-size_t decode_smem_gateup(int d) { return ((size_t)d + d / kGroup + 2 * kDecThreads) * sizeof(float); }
-size_t decode_smem_down(int k, int inter) {
-  const size_t items = (size_t)(k + 1) * (inter / kGroup);
-  return ((size_t)(k + 1) * inter + items + items * kDownRows) * sizeof(float);
-}
-
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s, void* const* events) {
-  const size_t sm_gu = decode_smem_gateup(p.d), sm_dn = decode_smem_down(p.k, p.inter);
-  static cudaError_t a1 = cudaFuncSetAttribute(decode_gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-  static cudaError_t a2 = cudaFuncSetAttribute(decode_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-  if (a1 != cudaSuccess) return a1;
-  if (a2 != cudaSuccess) return a2;
+  const moe_dims dims = {p.d, p.E, p.k, p.inter, p.inter, kGroup};
+  const int n_parts = decode_parts(dims);
+  const int smem = x_smem(p.d).total;
+  static cudaError_t attr =
+      cudaFuncSetAttribute(decode_expert_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, x_smem(kDecodeMaxD).total);
+  if (attr != cudaSuccess) return attr;
   cudaError_t err = record_event(events, 0, s);
   if (err != cudaSuccess) return err;
-  decode_router_kernel<<<(p.E + 7) / 8, kDecThreads, 0, s>>>(p);
-  if ((err = cudaGetLastError()) != cudaSuccess || (err = record_event(events, 1, s)) != cudaSuccess) return err;
-  decode_gateup_kernel<<<(p.k + 1) * (p.inter / kGateUpRows), kDecThreads, sm_gu, s>>>(p);
-  if ((err = cudaGetLastError()) != cudaSuccess || (err = record_event(events, 2, s)) != cudaSuccess) return err;
-  decode_down_kernel<<<p.d / kDownRows, kDecThreads, sm_dn, s>>>(p);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  if ((err = launch_pdl(decode_router_kernel, (p.E + 1) / 2, kRThreads, 0, s, p)) != cudaSuccess) return err;
+  if ((err = record_event(events, 1, s)) != cudaSuccess) return err;
+  if ((err = launch_pdl(decode_expert_kernel, n_parts, kXThreads, (size_t)smem, s, p)) != cudaSuccess) return err;
+  if ((err = record_event(events, 2, s)) != cudaSuccess) return err;
+  if ((err = launch_pdl(decode_reduce_kernel, p.d / kYRows, kYThreads, 0, s, p, n_parts)) != cudaSuccess) return err;
   return record_event(events, 3, s);
 }
 

@@ -197,15 +197,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
-    const uint8_t* wsrc = p.packed + (size_t)expert * p.expert_stride + p.region_offset +
-                          (size_t)m * KB * C::kWBytes;
+    const uint8_t* ebase = p.packed + (size_t)expert * p.expert_stride + p.region_offset;
     for (int kb = 0; kb < KB; ++kb) {
       if constexpr (MODE != kModeRouter) {
         const int s = kb % C::kStagesW;
         if (!mbar_wait(empty_w(s), ((kb / C::kStagesW) & 1) ^ 1, s_abort)) break;
         if (lane == 0) {
           mbar_arrive_expect_tx(full_w(s), C::kWBytes);
-          tma_bulk_g2s(smem_u32(w_tile(s)), wsrc + (size_t)kb * C::kWBytes, C::kWBytes, full_w(s));
+          const uint32_t dst = smem_u32(w_tile(s));
+          if (MODE == kModeGateUp) {  // four 32-row quarters: [gate | up] each
+            for (int q = 0; q < 4; ++q)
+              tma_bulk_g2s(dst + q * kGUQuarter, ebase + gu_offset(m, q, kb, KB), kGUQuarter, full_w(s));
+          } else {                    // code halves of columns 0..31 and 32..63, then scale/bias
+            const int DM = p.m_tiles;
+            tma_bulk_g2s(dst, ebase + dn_code_offset(kb, 0, m, DM), kHalfBytes, full_w(s));
+            tma_bulk_g2s(dst + kHalfBytes, ebase + dn_code_offset(kb, 1, m, DM), kHalfBytes, full_w(s));
+            tma_bulk_g2s(dst + kCodeBytes, ebase + dn_sb_offset(kb, m, DM, KB), kSBBytes, full_w(s));
+          }
         }
       } else {
         const int s = kb % C::kStagesA;
@@ -268,10 +276,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(empty_a(sa), ((kb / C::kStagesA) & 1) ^ 1, s_abort)) break;
 #pragma unroll
         for (int a = 0; a < C::kNumA; ++a) {
-          const uint8_t* blk = w_tile(sw) + a * kBlockBytes;
-          const uint4 c0 = *reinterpret_cast<const uint4*>(blk + r * 32);
-          const uint4 c1 = *reinterpret_cast<const uint4*>(blk + r * 32 + 16);
-          const uint32_t sbw = *reinterpret_cast<const uint32_t*>(blk + kCodeBytes + r * 4);
+          // stage layout: gate/up = 4 quarters x [gate rows | up rows], each (half 0, half 1,
+          // scale/bias) for 32 rows; down = (half 0, half 1, scale/bias) for 128 rows
+          const uint8_t* blk;
+          int rr, half_stride;
+          if (MODE == kModeGateUp) {
+            blk = w_tile(sw) + (r / kQuarterRows) * kGUQuarter + a * kGUMat;
+            rr = r % kQuarterRows;
+            half_stride = kQuarterRows * 16;
+          } else {
+            blk = w_tile(sw);
+            rr = r;
+            half_stride = kHalfBytes;
+          }
+          const uint4 c0 = *reinterpret_cast<const uint4*>(blk + rr * 16);
+          const uint4 c1 = *reinterpret_cast<const uint4*>(blk + half_stride + rr * 16);
+          const uint32_t sbw = *reinterpret_cast<const uint32_t*>(blk + 2 * half_stride + rr * 4);
           // bf16 scale and bias -> fp16 (exact inside the fp16 range)
           const __half sh = __float2half_rn(__uint_as_float(sbw << 16));
           const __half bh = __float2half_rn(__uint_as_float(sbw & 0xFFFF0000u));

@@ -14,26 +14,48 @@ namespace moe {
 // Packed expert layout.
 //
 // Every quantized matrix is cut into blocks of 128 output rows x 64 input columns (one
-// quantization group wide). A block is 4608 bytes:
-//   [0, 4096)    codes: row r at r*32, eight uint32 words (word w = columns 8w..8w+7)
-//   [4096, 4608) per-row (scale, bias) bf16 pairs: row r at 4096 + 4r, scale in the low half
-// Inside a word, the code of column c sits in nibble slot (c/2) + 4*(c%2): slots 0..3 hold
-// columns 0,2,4,6 and slots 4..7 hold columns 1,3,5,7, so (word >> 4i) & 0x000F000F yields
-// the columns (2i, 2i+1) as the two 16-bit halves.
+// quantization group wide). Inside a block, the codes of each row are two 16-byte halves
+// (columns 0..31 and 32..63, four uint32 words each, word w = columns 8w..8w+7) and each row has
+// one (scale, bias) bf16 pair (scale in the low half). Inside a word, the code of column c sits
+// in nibble slot (c/2) + 4*(c%2): slots 0..3 hold columns 0,2,4,6 and slots 4..7 hold columns
+// 1,3,5,7, so (word >> 4i) & 0x000F000F yields the columns (2i, 2i+1) as the two 16-bit halves.
 //
-// Per expert (routed e = 0..E-1, then the shared expert at index E):
-//   gate|up region: for m in [0, I/128), kb in [0, d/64): gate block (m,kb) then up block
-//                   (m,kb) -> 9216 contiguous bytes per (m, kb)
-//   down region:    for m in [0, d/128), kb in [0, I/64): down block (m, kb)
+// The blocks are stored so that both consumers read long contiguous runs:
+//   gate|up region (I/128 row blocks m, 4 quarters q of 32 rows, d/64 column blocks kb):
+//     entry (m, q, kb) at ((m*4 + q) * KB + kb) * 2304 holds the gate rows of the quarter
+//     (half 0: 32 x 16 B, half 1: 32 x 16 B, scale/bias: 32 x 4 B = 1152 B) then the up rows
+//     (1152 B). A decode block reading 32 intermediate rows streams one contiguous
+//     KB * 2304-byte run; a prefill CTA reading a 128-row block gathers 4 quarter entries.
+//   down region (I/64 column groups kbd, 2 halves hd, d/128 row blocks mm):
+//     codes (kbd, hd, mm) at ((kbd*2 + hd) * DM + mm) * 2048: 128 rows x 16 B;
+//     then scale/bias (kbd, mm) at codes_end + (kbd * DM + mm) * 512: 128 rows x 4 B.
+//     A decode block reading a 32-column slice of W_down streams DM * 2048 contiguous bytes
+//     of codes plus DM * 512 bytes of scales; a prefill CTA gathers 2 halves + 1 scale run.
+// Per expert (routed e = 0..E-1, then the shared expert at index E): gate|up then down.
 // ------------------------------------------------------------------------------------------
 constexpr int kGroup = 64;          // quantization group (input columns per block)
 constexpr int kBlockRows = 128;     // output rows per block (= MMA M)
-constexpr int kCodeBytes = kBlockRows * 32;          // 4096
+constexpr int kHalfBytes = kBlockRows * 16;          // 2048: codes of one 32-column half
+constexpr int kCodeBytes = 2 * kHalfBytes;           // 4096
 constexpr int kBlockBytes = kCodeBytes + kBlockRows * 4;  // 4608
+constexpr int kQuarterRows = 32;
+constexpr int kGUMat = 2 * kQuarterRows * 16 + kQuarterRows * 4;  // 1152: one matrix's quarter
+constexpr int kGUQuarter = 2 * kGUMat;                             // 2304: gate + up quarter
+constexpr int kSBBytes = kBlockRows * 4;                           // 512
 constexpr int kTileRows = 256;      // block-map tile height (max MMA N)
 constexpr int kMaxTopK = 16;
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTokens = 65536;
+
+__host__ __device__ inline size_t gu_offset(int m, int q, int kb, int KB) {
+  return ((size_t)(m * 4 + q) * KB + kb) * kGUQuarter;
+}
+__host__ __device__ inline size_t dn_code_offset(int kbd, int hd, int mm, int DM) {
+  return ((size_t)(kbd * 2 + hd) * DM + mm) * kHalfBytes;
+}
+__host__ __device__ inline size_t dn_sb_offset(int kbd, int mm, int DM, int KBI) {
+  return (size_t)KBI * 2 * DM * kHalfBytes + ((size_t)kbd * DM + mm) * kSBBytes;
+}
 
 struct PackedLayout {
   size_t gu_bytes;       // gate|up region of one expert
@@ -68,11 +90,18 @@ static_assert(sizeof(WsHeader) == 256, "header size");
 
 struct WsLayout {
   size_t header, logits, topk_idx, topk_w, chunk_counts, chunk_base, counts, offsets, perm,
-      inv_perm, tile_map, n_tiles, x16, hidden, yacc, dec_h, total;
+      inv_perm, tile_map, n_tiles, x16, hidden, yacc, dec_part, total;
   int n_chunks, max_tiles;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Decode: one expert-kernel CTA per (selected or shared expert, 32 intermediate rows); each
+// writes a partial output row of d floats that the combine kernel sums in a fixed order.
+constexpr int kDecPartRows = 32;
+constexpr int kDecodeMaxD = 3072;   // the expert kernel keeps all its weight slices in smem
+inline int decode_parts(const moe_dims& d) { return (d.top_k + 1) * (d.inter / kDecPartRows); }
+inline size_t decode_partial_bytes(const moe_dims& d) { return (size_t)decode_parts(d) * d.d * 4; }
 
 inline int max_routed_tiles(int T, int k, int E) {
   long long A = (long long)T * k;
@@ -101,7 +130,7 @@ inline WsLayout ws_layout(const moe_dims& d, int T) {
   L.x16 = take((size_t)T * d.d * 2);                   // x as fp16 (expert GEMM operand)
   L.hidden = take(2 * (A + T) * (size_t)d.inter * 2);  // SwiGLU rows: fp16 leading part, fp16 remainder
   L.yacc = take((size_t)T * d.d * 4);
-  L.dec_h = take((size_t)(d.top_k + 1) * d.inter * 4);
+  L.dec_part = take(decode_partial_bytes(d));
   L.total = o;
   return L;
 }
@@ -166,7 +195,7 @@ struct DecodeParams {
   float* logits;              // [E]
   int32_t* topk_idx;          // [k]
   float* topk_w;              // [k]
-  float* hbuf;                // [k + 1, I] fp32 SwiGLU outputs (slot k = shared expert)
+  float* partials;            // [(k + 1) * I / 32, d] fp32 per-CTA partial outputs
   uint16_t* y;                // [d] bf16
   WsHeader* hdr;
   int d, E, k, inter;

@@ -5,7 +5,8 @@
 // forbids device allocation after start-up because cudaMalloc can synchronise the whole device
 // and can fail under memory pressure in the middle of serving. For them this entry point runs
 // the same decode kernels as moe_decode with its scratch (router logits, the selected experts and
-// weights, the SwiGLU rows and the kernels' counters) held in a fixed file-scope device array.
+// weights, the per-block partial output rows and the kernels' counters) held in a fixed
+// file-scope device array.
 //
 // That array lives as long as the library stays loaded, on every device that loads it, and
 // every call shares it: two calls that overlap on the GPU (different streams, or different
@@ -20,15 +21,15 @@ namespace moe {
 namespace {
 
 // Largest scratch this entry point can use. A shape needs
-//   256 (counters, status) + 4 E + 8 k + 4 (k + 1) I bytes, each part rounded up to 256 bytes;
-// d=2048, E=256, k=8, I=512 needs 20.5 KiB.
-constexpr size_t kNoAllocScratchBytes = 64 * 1024;
+//   256 (counters, status) + 4 E + 8 k + 4 d (k + 1) I / 32 bytes, each part rounded up to 256;
+// d=2048, E=256, k=8, I=512 needs 1.13 MiB.
+constexpr size_t kNoAllocScratchBytes = 2 * 1024 * 1024;
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
 
 struct ScratchLayout {
-  size_t header, logits, topk_idx, topk_w, hbuf, total;
+  size_t header, logits, topk_idx, topk_w, partials, total;
 };
 
 ScratchLayout scratch_layout(const moe_dims& d) {
@@ -39,7 +40,7 @@ ScratchLayout scratch_layout(const moe_dims& d) {
   L.logits = take((size_t)d.n_experts * 4);
   L.topk_idx = take((size_t)d.top_k * 4);
   L.topk_w = take((size_t)d.top_k * 4);
-  L.hbuf = take((size_t)(d.top_k + 1) * d.inter * 4);
+  L.partials = take(decode_partial_bytes(d));
   L.total = o;
   return L;
 }
@@ -67,7 +68,7 @@ cudaError_t scratch_address(void** out) {
 int check_dims_noalloc(const moe_dims& d) {
   if (d.group != kGroup || d.d < kBlockRows || d.d % kBlockRows || d.d > 16384 || d.inter < kBlockRows ||
       d.inter % kBlockRows || d.inter > 16384 || d.shared_inter != d.inter || d.top_k < 1 || d.top_k > kMaxTopK ||
-      d.n_experts < d.top_k || d.n_experts > kMaxExperts)
+      d.n_experts < d.top_k || d.n_experts > kMaxExperts || d.d > kDecodeMaxD)
     return MOE_ERR_UNSUPPORTED_SHAPE;
   return MOE_OK;
 }
@@ -106,7 +107,7 @@ extern "C" int moe_decode_noalloc(const moe_layer* layer, const uint16_t* x, uin
   p.logits = reinterpret_cast<float*>(s + L.logits);
   p.topk_idx = reinterpret_cast<int32_t*>(s + L.topk_idx);
   p.topk_w = reinterpret_cast<float*>(s + L.topk_w);
-  p.hbuf = reinterpret_cast<float*>(s + L.hbuf);
+  p.partials = reinterpret_cast<float*>(s + L.partials);
   p.y = y;
   p.hdr = hdr;
   p.d = d.d;

@@ -31,38 +31,40 @@ __global__ void __launch_bounds__(128) pack_kernel(const PackArgs a) {
   const int n_gu = (a.inter / kBlockRows) * kb_d;  // (m, kb) pairs of the gate|up region
   int blk = blockIdx.x;
   const bool shared = (e == a.n_experts);
-  moe_q4_view src;
-  int cols, rows, m, kb;
-  size_t dst_off;
-  if (blk < 2 * n_gu) {
-    const int pair = blk >> 1, which = blk & 1;      // 0 gate, 1 up
-    m = pair / kb_d;
-    kb = pair % kb_d;
-    cols = a.d;
-    rows = a.inter;
-    src = which ? (shared ? a.sh_up : a.up) : (shared ? a.sh_gate : a.gate);
-    dst_off = ((size_t)pair * 2 + which) * kBlockBytes;
-  } else {
-    blk -= 2 * n_gu;
-    m = blk / kb_i;
-    kb = blk % kb_i;
-    cols = a.inter;
-    rows = a.d;
-    src = shared ? a.sh_down : a.down;
-    dst_off = a.gu_bytes + (size_t)blk * kBlockBytes;
-  }
   const size_t lead = shared ? 0 : (size_t)e;
   const int r = threadIdx.x;
-  const size_t row = (size_t)m * kBlockRows + r;
-  const size_t words_per_row = cols / 8, groups_per_row = cols / kGroup;
-  const uint32_t* q = src.q + (lead * rows + row) * words_per_row + (size_t)kb * 8;
-  const size_t g = (lead * rows + row) * groups_per_row + kb;
-  uint8_t* dst = a.packed + (size_t)e * a.expert_stride + dst_off;
-  uint32_t* dq = reinterpret_cast<uint32_t*>(dst + (size_t)r * 32);
-#pragma unroll
-  for (int w = 0; w < 8; ++w) dq[w] = permute_nibbles(q[w]);
-  const uint32_t sb = (uint32_t)src.scale[g] | ((uint32_t)src.bias[g] << 16);
-  *reinterpret_cast<uint32_t*>(dst + kCodeBytes + (size_t)r * 4) = sb;
+  uint8_t* eb = a.packed + (size_t)e * a.expert_stride;
+  uint32_t words[8];
+  uint32_t sb;
+  if (blk < 2 * n_gu) {  // gate or up block (m, kb)
+    const int pair = blk >> 1, which = blk & 1;      // 0 gate, 1 up
+    const int m = pair / kb_d, kb = pair % kb_d;
+    const moe_q4_view src = which ? (shared ? a.sh_up : a.up) : (shared ? a.sh_gate : a.gate);
+    const size_t row = (size_t)m * kBlockRows + r;
+    const uint32_t* q = src.q + (lead * a.inter + row) * (a.d / 8) + (size_t)kb * 8;
+    const size_t g = (lead * a.inter + row) * kb_d + kb;
+    for (int w = 0; w < 8; ++w) words[w] = permute_nibbles(q[w]);
+    sb = (uint32_t)src.scale[g] | ((uint32_t)src.bias[g] << 16);
+    const int qtr = r / kQuarterRows, rr = r % kQuarterRows;
+    uint8_t* dst = eb + gu_offset(m, qtr, kb, kb_d) + which * kGUMat;
+    for (int w = 0; w < 8; ++w)
+      reinterpret_cast<uint32_t*>(dst + (w >> 2) * kQuarterRows * 16 + rr * 16)[w & 3] = words[w];
+    *reinterpret_cast<uint32_t*>(dst + 2 * kQuarterRows * 16 + rr * 4) = sb;
+  } else {               // down block (mm, kbd)
+    blk -= 2 * n_gu;
+    const int DM = a.d / kBlockRows;
+    const int mm = blk / kb_i, kbd = blk % kb_i;
+    const moe_q4_view src = shared ? a.sh_down : a.down;
+    const size_t row = (size_t)mm * kBlockRows + r;
+    const uint32_t* q = src.q + (lead * a.d + row) * (a.inter / 8) + (size_t)kbd * 8;
+    const size_t g = (lead * a.d + row) * kb_i + kbd;
+    for (int w = 0; w < 8; ++w) words[w] = permute_nibbles(q[w]);
+    sb = (uint32_t)src.scale[g] | ((uint32_t)src.bias[g] << 16);
+    uint8_t* dn = eb + a.gu_bytes;
+    for (int w = 0; w < 8; ++w)
+      reinterpret_cast<uint32_t*>(dn + dn_code_offset(kbd, w >> 2, mm, DM) + r * 16)[w & 3] = words[w];
+    *reinterpret_cast<uint32_t*>(dn + dn_sb_offset(kbd, mm, DM, kb_i) + r * 4) = sb;
+  }
 }
 
 }  // namespace

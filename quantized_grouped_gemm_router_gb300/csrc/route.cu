@@ -1,12 +1,13 @@
 // GPU-resident routing (page "Perplexity's Lily beats MLX-LM on MacBook M5 because it only runs
 // one model", section "Prefill: keep routing on the GPU, dequantize in flight": after the top-8
 // selection, histogram, prefix scan, scatter and block map run on the GPU with no host round
-// trip). Two launches:
-//   route_topk_kernel    one CTA per 64-token chunk: warp-shuffle top-k on (orderable logit,
-//                        lower index) keys, renormalised softmax weights, per-chunk histogram
-//                        in shared memory, zeroing of the combine accumulator rows; the last
-//                        CTA to finish (ticket) scans the chunk histograms into counts, offsets,
-//                        per-chunk bases and the tile block map.
+// trip). Three launches:
+//   route_topk_kernel    16 tokens per CTA: warp top-k on order-preserving logit keys (ties to
+//                        the lower index), renormalised softmax weights; the fp16 copy of x and
+//                        the zeroing of the combine accumulator rows
+//   route_hist_kernel    one CTA per 64-token chunk: histogram in shared memory; the last CTA to
+//                        finish (ticket) scans the chunk histograms into counts, offsets,
+//                        per-chunk bases and the tile block map
 //   route_scatter_kernel one warp per chunk: stable, atomics-free placement of the chunk's
 //                        assignments (in-warp ranks by __match_any_sync, running per-expert
 //                        counters in shared memory).
@@ -21,6 +22,7 @@ namespace moe {
 namespace {
 
 constexpr int kTopkThreads = 256;
+constexpr int kTopkTokens = 16;   // tokens per CTA of the top-k kernel
 
 // Exclusive scan of up to 4*blockDim values held 4 per thread (v[0..3] are items 4t..4t+3).
 // Returns the exclusive prefix of item 4t; *total receives the sum of all items.
@@ -51,57 +53,65 @@ __device__ int block_exclusive_scan4(const int (&v)[4], int* s_warp, int* total)
   return before_warp + incl - mine;
 }
 
+// Top-k of kTopkTokens tokens per CTA (two per warp), then the CTA's share of the fp16 copy of
+// x and of the zeroing of the combine accumulator (wide grid: this is the launch that moves
+// the bytes).
 __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const RouteParams p) {
-  __shared__ int s_counts[kMaxExperts];
-  __shared__ int s_warp[32];
-  __shared__ int s_last;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int c = blockIdx.x;
   const int E = p.E, k = p.k;
-  for (int e = tid; e < E; e += blockDim.x) s_counts[e] = 0;
-  __syncthreads();
-
-  const int t_begin = c * kRouteChunk;
-  const int t_end = min(p.T, t_begin + kRouteChunk);
+  const int t_begin = blockIdx.x * kTopkTokens;
+  const int t_end = min(p.T, t_begin + kTopkTokens);
   for (int t = t_begin + warp; t < t_end; t += kTopkThreads / 32) {
     int my_e;
     float my_w;
     const bool bad = warp_topk_softmax(p.logits + (size_t)t * E, E, k, &my_e, &my_w);
     if (bad && lane == 0) set_device_status(p.hdr, MOE_ERR_NONFINITE);
     if (lane < k) {
-      const size_t a = (size_t)t * k + lane;
-      p.topk_idx[a] = my_e;
-      p.topk_w[a] = my_w;
-      atomicAdd(&s_counts[my_e], 1);
-    }
-    if (p.yacc) {
-      float4* yrow = reinterpret_cast<float4*>(p.yacc + (size_t)t * p.d);
-      for (int i = lane; i < p.d / 4; i += 32) yrow[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    if (p.x) {  // fp16 operand copy of x for the expert GEMMs (exact inside the fp16 range)
-      const uint4* xs = reinterpret_cast<const uint4*>(p.x + (size_t)t * p.d);
-      uint4* xd = reinterpret_cast<uint4*>(p.x16 + (size_t)t * p.d);
-      bool over = false;
-      for (int i = lane; i < p.d / 8; i += 32) {
-        const uint4 v = xs[i];
-        const uint32_t in[4] = {v.x, v.y, v.z, v.w};
-        uint32_t o[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float lo = __uint_as_float(in[j] << 16), hi = __uint_as_float(in[j] & 0xFFFF0000u);
-          over |= !(fabsf(lo) <= 65504.f) || !(fabsf(hi) <= 65504.f);
-          const __half2 h = __floats2half2_rn(lo, hi);
-          o[j] = *reinterpret_cast<const uint32_t*>(&h);
-        }
-        xd[i] = make_uint4(o[0], o[1], o[2], o[3]);
-      }
-      if (__any_sync(0xFFFFFFFFu, over) && lane == 0) set_device_status(p.hdr, MOE_ERR_OUT_OF_RANGE);
+      p.topk_idx[(size_t)t * k + lane] = my_e;
+      p.topk_w[(size_t)t * k + lane] = my_w;
     }
   }
+  const int n8 = (t_end - t_begin) * p.d / 8;  // 8-element chunks of this CTA's rows
+  if (p.x) {  // fp16 operand copy of x for the expert GEMMs (exact inside the fp16 range)
+    const uint4* xs = reinterpret_cast<const uint4*>(p.x + (size_t)t_begin * p.d);
+    uint4* xd = reinterpret_cast<uint4*>(p.x16 + (size_t)t_begin * p.d);
+    bool over = false;
+    for (int i = tid; i < n8; i += kTopkThreads) {
+      const uint4 v = xs[i];
+      const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float lo = __uint_as_float(in[j] << 16), hi = __uint_as_float(in[j] & 0xFFFF0000u);
+        over |= !(fabsf(lo) <= 65504.f) || !(fabsf(hi) <= 65504.f);
+        const __half2 h = __floats2half2_rn(lo, hi);
+        o[j] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      xd[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (__any_sync(0xFFFFFFFFu, over) && lane == 0) set_device_status(p.hdr, MOE_ERR_OUT_OF_RANGE);
+  }
+  if (p.yacc) {
+    float4* yrow = reinterpret_cast<float4*>(p.yacc + (size_t)t_begin * p.d);
+    for (int i = tid; i < 2 * n8; i += kTopkThreads) yrow[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+// Histogram of one kRouteChunk-token chunk in shared memory. The last CTA to finish (ticket)
+// turns the chunk histograms into counts, offsets, chunk bases and the tile block map.
+__global__ void __launch_bounds__(kTopkThreads) route_hist_kernel(const RouteParams p) {
+  __shared__ int s_counts[kMaxExperts];
+  __shared__ int s_warp[32];
+  __shared__ int s_last;
+  const int tid = threadIdx.x;
+  const int c = blockIdx.x;
+  const int E = p.E, k = p.k;
+  for (int e = tid; e < E; e += blockDim.x) s_counts[e] = 0;
+  __syncthreads();
+  const int a_begin = c * kRouteChunk * k, a_end = min(p.T, (c + 1) * kRouteChunk) * k;
+  for (int a = a_begin + tid; a < a_end; a += blockDim.x) atomicAdd(&s_counts[p.topk_idx[a]], 1);
   __syncthreads();
   for (int e = tid; e < E; e += blockDim.x) p.chunk_counts[(size_t)c * E + e] = s_counts[e];
-
-  // Last CTA to finish turns the chunk histograms into counts, offsets, chunk bases and tiles.
   __threadfence();
   __syncthreads();
   if (tid == 0) s_last = (atomicAdd(&p.hdr->ticket, 1u) == gridDim.x - 1);
@@ -198,9 +208,11 @@ __global__ void __launch_bounds__(256) cast_kernel(const float* __restrict__ yac
 }  // namespace
 
 cudaError_t launch_route(const RouteParams& p, cudaStream_t s) {
-  route_topk_kernel<<<p.n_chunks, kTopkThreads, 0, s>>>(p);
+  route_topk_kernel<<<(p.T + kTopkTokens - 1) / kTopkTokens, kTopkThreads, 0, s>>>(p);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
+  route_hist_kernel<<<p.n_chunks, kTopkThreads, 0, s>>>(p);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
   route_scatter_kernel<<<p.n_chunks, 32, 0, s>>>(p);
   return cudaGetLastError();
 }

@@ -2,10 +2,8 @@
 // MacBook M5 because it only runs one model", section "Why Qwen3.6-35B-A3B is a weird
 // workload": the router scores the experts and picks the top k).
 //
-// Each (logit, expert) pair becomes a 64-bit key: an order-preserving image of the fp32 logit
-// in the high word (-0.0 folded onto +0.0) and (0xFFFFFFFF - expert) in the low word, so the
-// largest key is the largest logit and, among equal logits, the lowest expert index. k rounds
-// of a shuffle max-reduction pick the experts in descending order.
+// Logits become order-preserving unsigned keys (-0.0 folded onto +0.0); the largest key is the
+// largest logit, and equal logits are split by the lower expert index.
 #pragma once
 
 #include <stdint.h>
@@ -24,51 +22,57 @@ __device__ __forceinline__ float from_orderable_f32(uint32_t k) {
   return __uint_as_float(b);
 }
 
-__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const unsigned long long w = __shfl_xor_sync(0xFFFFFFFFu, v, o);
-    v = w > v ? w : v;
-  }
-  return v;
-}
-
-// Whole warp: selects the top k (k <= 16 <= 32) of row[0..E) (E <= 1024). Lane j < k returns
-// its slot's expert in *e_out and weight in *w_out. Returns true (on every lane) if any logit
-// of the row was NaN or infinite; the selection then stays within [0, E) but is meaningless.
+// Whole warp: selects the top k (k <= 16 <= 32) of row[0..E) (E <= 32 * SLOTS). Lane j < k
+// returns its slot's expert in *e_out and weight in *w_out. Returns true (on every lane) if any
+// logit of the row was NaN or infinite; the selection then stays within [0, E) but is
+// meaningless.
+//
+// Lane l holds experts l, l+32, ... as order-preserving 32-bit keys and keeps its best untaken
+// one (largest key, lowest index among equal keys). Each round takes the warp maximum of the
+// lanes' bests with one redux.sync, then the lowest expert index among the lanes holding that
+// maximum with a second one; only the winning lane rescans its own keys.
+template <int SLOTS>
 __device__ __forceinline__ bool warp_topk_softmax(const float* row, int E, int k, int* e_out, float* w_out) {
   const int lane = threadIdx.x & 31;
-  const int per_lane = (E + 31) >> 5;
-  unsigned long long key[32];
+  uint32_t key[SLOTS];
   bool bad = false;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    key[i] = 0ull;
+  for (int i = 0; i < SLOTS; ++i) {
     const int e = lane + 32 * i;
-    if (i < per_lane && e < E) {
+    key[i] = 0u;  // below every finite logit's key
+    if (e < E) {
       const float v = __ldcg(row + e);
       bad |= !isfinite(v);
-      key[i] = ((unsigned long long)orderable_f32(v) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)e);
+      key[i] = max(orderable_f32(v), 1u);
     }
   }
+  uint32_t taken = 0u, bv = 0u;
+  int bi = 0;
+  auto local_best = [&]() {
+    bv = 0u;
+    bi = 0;
+#pragma unroll
+    for (int i = 0; i < SLOTS; ++i)
+      if (!((taken >> i) & 1u) && key[i] > bv) {
+        bv = key[i];
+        bi = i;
+      }
+  };
+  local_best();
   int my_e = 0;
   float my_v = 0.f;
 #pragma unroll 1
   for (int j = 0; j < k; ++j) {
-    unsigned long long best = 0ull;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) best = key[i] > best ? key[i] : best;
-    best = warp_max_u64(best);
-    const int e = (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFull));
-    if ((e & 31) == lane) {
-      const int slot = e >> 5;
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (i == slot) key[i] = 0ull;
-    }
+    const uint32_t vmax = __reduce_max_sync(0xFFFFFFFFu, bv);
+    const uint32_t cand = (bv == vmax && bv != 0u) ? (uint32_t)(lane + 32 * bi) : 0xFFFFFFFFu;
+    const uint32_t emin = __reduce_min_sync(0xFFFFFFFFu, cand);
     if (lane == j) {
-      my_e = e;
-      my_v = from_orderable_f32((uint32_t)(best >> 32));
+      my_e = (int)emin;
+      my_v = from_orderable_f32(vmax);
+    }
+    if ((int)(emin & 31u) == lane) {
+      taken |= 1u << (emin >> 5);
+      local_best();
     }
   }
   // Softmax restricted to the selected experts; slot 0 holds the largest logit.
@@ -80,6 +84,12 @@ __device__ __forceinline__ bool warp_topk_softmax(const float* row, int E, int k
   *e_out = min(max(my_e, 0), E - 1);
   *w_out = ex / sum;
   return __any_sync(0xFFFFFFFFu, bad);
+}
+
+// Dispatch on the number of experts per lane.
+__device__ __forceinline__ bool warp_topk_softmax(const float* row, int E, int k, int* e_out, float* w_out) {
+  if (E <= 256) return warp_topk_softmax<8>(row, E, k, e_out, w_out);
+  return warp_topk_softmax<32>(row, E, k, e_out, w_out);
 }
 
 }  // namespace moe

@@ -50,7 +50,7 @@ def test_decode_noalloc_matches_decode(m, shape, seed):
 def test_decode_noalloc_rejects_oversized_shape(m):
     from quantized_grouped_gemm_router_gb300.binding import MoeLayer
     dims = m.dims_of(FULL)
-    dims.inter = 4096          # (k+1) * I * 4 bytes of SwiGLU rows exceed the fixed scratch
+    dims.inter = 4096          # 4 d (k+1) I / 32 bytes of partial outputs exceed the fixed scratch
     dims.shared_inter = 4096
     A = 1 << 20                # never dereferenced: the shape check fails first
     layer = MoeLayer(dims, A, None, A)
