@@ -222,9 +222,9 @@ MOE_API int moe_decode(const moe_layer* layer, const uint16_t* x, uint16_t* y, m
  *     E=256, k=8, I=512 needs 1.13 MiB).
  *   - The first call on a device looks up the array's device address (once per device, with
  *     that device current); make that first call before any stream capture.
- *   - Every call uses the same array, which keeps the last call's contents; the call clears
- *     what must start at zero. Calls that overlap on the GPU (other streams or host threads)
- *     race on the array: serialise them.
+ *   - Every call uses the same array, which keeps the last call's contents; each call writes
+ *     everything it later reads, so nothing has to start at zero. Calls that overlap on the GPU
+ *     (other streams or host threads) race on the array: serialise them.
  *   - Device-side errors (e.g. non-finite logits) are not reported by this variant: it has no
  *     status word the caller can read. Argument errors are returned as for moe_decode.
  */

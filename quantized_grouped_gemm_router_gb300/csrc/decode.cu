@@ -11,15 +11,17 @@
 // successor start at once, and does everything that does not depend on its predecessor's
 // results (loading static weights) before waiting for it.
 //   decode_router_kernel  two experts per CTA: logit = W_r[e] . x (+ b_e); the router weight
-//                         slice is loaded before the wait; the last CTA to finish selects the
-//                         top k and their renormalised weights
-//   decode_expert_kernel  one CTA per (selected or shared expert, 32 intermediate rows): all of
-//                         its gate/up rows and its 32-column slice of the down projection are
-//                         bulk-copied to shared memory as soon as the expert is known (the
-//                         shared expert's CTAs before routing is known); gate/up + SwiGLU,
-//                         scaled by the routing weight, then this slice's contribution to every
-//                         output row (split-K over the intermediate dimension)
-//   decode_reduce_kernel  y = sum of the per-CTA partial rows in a fixed order -> bf16
+//                         slice is loaded before the wait
+//   decode_expert_kernel  one CTA per (selected or shared expert, 32 intermediate rows): routed
+//                         CTAs select the top k from the logits themselves (warp top-k, ties
+//                         to the lower index); all of a CTA's gate/up
+//                         rows and its 32-column slice of the down projection are bulk-copied
+//                         to shared memory as soon as the expert is known (the shared expert's
+//                         CTAs before routing is known); gate/up + SwiGLU, scaled by the routing
+//                         weight, then this slice's contribution to every output row (split-K
+//                         over the intermediate dimension); clusters of 8 (or 4) CTAs of one
+//                         expert add their partial rows through distributed shared memory
+//   decode_reduce_kernel  y = sum of the clusters' partial rows in a fixed order -> bf16
 // The GEMV inner products run on the tensor cores (mma.sync m16n8k16, fp16 in, fp32
 // accumulate): the packed nibble pairs of a row map directly onto the MMA fragment layout, so
 // each weight costs about one ALU operation instead of three for an fp32 FMA loop, which on
@@ -33,9 +35,14 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <mutex>
+
 #include "moe_internal.h"
 #include "ptx.cuh"
 #include "topk.cuh"
+
+#include <cooperative_groups.h>
+namespace cg = cooperative_groups;
 
 namespace moe {
 namespace {
@@ -81,24 +88,32 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(d[0]), "f"(d[1]), "f"(d[2]), "f"(d[3]));
 }
 
+// Launch with programmatic dependent launch (and an optional thread-block cluster size).
 template <class Kernel, class... Args>
-cudaError_t launch_pdl(Kernel kernel, int grid, int block, size_t smem, cudaStream_t s, Args... args) {
+cudaError_t launch_pdl(Kernel kernel, int grid, int block, size_t smem, int cluster, cudaStream_t s, Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(block);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  int n = 1;
+  if (cluster > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    n = 2;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 __global__ void __launch_bounds__(kRThreads) decode_router_kernel(const DecodeParams p) {
   __shared__ float s_part[kRThreads / 32];
-  __shared__ int s_last;
   const int half = threadIdx.x >> 7, t = threadIdx.x & 127, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x * 2 + half;
   const int nch = p.d >> 3;  // 8-element chunks per row
@@ -131,23 +146,6 @@ __global__ void __launch_bounds__(kRThreads) decode_router_kernel(const DecodePa
   if (t == 0 && e < p.E) {
     const float* sp = s_part + 4 * half;
     p.logits[e] = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + (p.router_bias ? p.router_bias[e] : 0.f);
-    __threadfence();  // the logit is visible before this CTA takes its ticket
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) s_last = (atomicAdd(&p.hdr->dticket, 1u) == gridDim.x - 1);
-  __syncthreads();
-  if (!s_last || warp != 0) return;
-  __threadfence();
-  int my_e;
-  float my_w;
-  const bool bad = warp_topk_softmax(p.logits, p.E, p.k, &my_e, &my_w);
-  if (lane < p.k) {
-    p.topk_idx[lane] = my_e;
-    p.topk_w[lane] = my_w;
-  }
-  if (lane == 0) {
-    if (bad) set_device_status(p.hdr, MOE_ERR_NONFINITE);
-    p.hdr->dticket = 0u;
   }
 }
 
@@ -214,33 +212,57 @@ __global__ void __launch_bounds__(kXThreads, 1) decode_expert_kernel(const Decod
   if (shared && warp == 0) issue(p.E);  // static weights: before waiting on the router
   pdl_launch_dependents();
   pdl_wait();
-  const int expert = shared ? p.E : __ldcg(p.topk_idx + slot);
-  const float wslot = shared ? 1.f : __ldcg(p.topk_w + slot);
-  if (!shared && warp == 0) issue(expert);
-
-  // x -> fp16 pairs in shared memory, and the per-64-group sums of x (fp32)
-  uint32_t* x2 = reinterpret_cast<uint32_t*>(xs + L.x16);
-  float* xsum = reinterpret_cast<float*>(xs + L.xsum);
-  const int nch = p.d / 8;
-  for (int base = 0; base < nch; base += kXThreads) {
-    const int c = base + tid;
-    float part_sum = 0.f;
-    if (c < nch) {
-      const uint4 v = __ldcg(reinterpret_cast<const uint4*>(p.x) + c);
-      const uint32_t in[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float lo = bf16lo(in[j]), hi = bf16hi(in[j]);
-        part_sum += lo + hi;
-        const __half2 h2 = __floats2half2_rn(lo, hi);
-        x2[4 * c + j] = *reinterpret_cast<const uint32_t*>(&h2);
+  __shared__ float s_wslot;
+  if (warp == 0) {
+    // Routed blocks select the top k themselves from the router's logits (each block gets the
+    // same, deterministic answer), then issue their copies; block 0 also publishes the routing.
+    float wslot = 1.f;
+    if (!shared || blockIdx.x == 0) {
+      int my_e;
+      float my_w;
+      const bool bad = warp_topk_softmax(p.logits, p.E, p.k, &my_e, &my_w);
+      if (blockIdx.x == 0) {
+        if (lane < p.k) {
+          p.topk_idx[lane] = my_e;
+          p.topk_w[lane] = my_w;
+        }
+        if (bad && lane == 0) set_device_status(p.hdr, MOE_ERR_NONFINITE);
+      }
+      if (!shared) {
+        const int expert = __shfl_sync(0xFFFFFFFFu, my_e, slot);
+        wslot = __shfl_sync(0xFFFFFFFFu, my_w, slot);
+        issue(expert);
       }
     }
+    if (lane == 0) s_wslot = wslot;
+  } else {
+    // Meanwhile the other warps stage x as fp16 pairs and its per-64-group sums (fp32).
+    uint32_t* x2w = reinterpret_cast<uint32_t*>(xs + L.x16);
+    float* xsw = reinterpret_cast<float*>(xs + L.xsum);
+    const int nch = p.d / 8, t = tid - 32, nt = kXThreads - 32;
+    for (int base = 0; base < nch; base += nt) {
+      const int c = base + t;
+      float part_sum = 0.f;
+      if (c < nch) {
+        const uint4 v = __ldcg(reinterpret_cast<const uint4*>(p.x) + c);
+        const uint32_t in[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int o = 1; o < 8; o <<= 1) part_sum += __shfl_xor_sync(0xFFFFFFFFu, part_sum, o);
-    if (c < nch && (c & 7) == 0) xsum[c >> 3] = part_sum;
+        for (int j = 0; j < 4; ++j) {
+          const float lo = bf16lo(in[j]), hi = bf16hi(in[j]);
+          part_sum += lo + hi;
+          const __half2 h2 = __floats2half2_rn(lo, hi);
+          x2w[4 * c + j] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+      }
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) part_sum += __shfl_xor_sync(0xFFFFFFFFu, part_sum, o);
+      if (c < nch && (c & 7) == 0) xsw[c >> 3] = part_sum;
+    }
   }
   __syncthreads();
+  const float wslot = s_wslot;
+  const uint32_t* x2 = reinterpret_cast<const uint32_t*>(xs + L.x16);
+  const float* xsum = reinterpret_cast<const float*>(xs + L.xsum);
 
   // ---- gate/up: warp w takes K blocks w, w+8, ...; 2 row tiles of 16 per matrix
   const int g = lane >> 2, tig = lane & 3, sh = 4 * tig;
@@ -326,8 +348,8 @@ __global__ void __launch_bounds__(kXThreads, 1) decode_expert_kernel(const Decod
     bd1[c] = g == 0 ? hh2[c * 8 + 4 + tig] : (g == 1 ? hl2[c * 8 + 4 + tig] : 0u);
   }
   const float hs = *hsum;
-  float* out = p.partials + (size_t)blockIdx.x * p.d;
-  for (int tile = warp; down_ok && tile < DM * 8; tile += kXWarps) {
+  float* out = reinterpret_cast<float*>(xs + L.gu);  // this block's partial row (gate/up data is dead)
+  for (int tile = warp; tile < DM * 8; tile += kXWarps) {
     const int mm = tile >> 3, R0 = (tile & 7) * 16 + g, R1 = R0 + 8;
     const uint8_t* ds = xs + L.dn + mm * kHalfBytes;
     const uint8_t* dsb = xs + L.dn + DM * kHalfBytes + mm * kSBBytes;
@@ -343,10 +365,27 @@ __global__ void __launch_bounds__(kXThreads, 1) decode_expert_kernel(const Decod
       out[mm * kBlockRows + R1] = bf16lo(sb1) * (d[2] + d[3]) + bf16hi(sb1) * hs;
     }
   }
+  if (!down_ok && tid == 0) *s_abort = 1;
+
+  // Sum the cluster's partial rows through distributed shared memory: block rank r of the
+  // cluster adds rows [r*d/cs, (r+1)*d/cs) of every block's partial, in rank order, and writes
+  // them as row blockIdx.x / cs of the global partials.
+  cg::cluster_group cluster = cg::this_cluster();
+  cluster.sync();
+  const int cs = (int)cluster.num_blocks(), rank = (int)cluster.block_rank();
+  const int span = p.d / cs;
+  float* gout = p.partials + (size_t)(blockIdx.x / cs) * p.d;
+  for (int i = tid; i < span; i += kXThreads) {
+    const int row = rank * span + i;
+    float acc = 0.f;
+    for (int q = 0; q < cs; ++q) acc += cluster.map_shared_rank(out, q)[row];
+    gout[row] = acc;
+  }
+  cluster.sync();
   if (tid == 0 && *s_abort) set_device_status(p.hdr, MOE_ERR_DEVICE_TIMEOUT);
 }
 
-// y[i] = sum over the expert-kernel CTAs c (ascending) of partials[c][i], rounded to bf16.
+// y[i] = sum over the expert-kernel clusters c (ascending) of partials[c][i], rounded to bf16.
 // Thread (row r, group q) sums a contiguous range of c with batched loads; the 32 group sums of
 // a row are then added in group order, so the result does not depend on timing.
 __global__ void __launch_bounds__(kYThreads) decode_reduce_kernel(const DecodeParams p, int n_parts) {
@@ -374,6 +413,42 @@ __global__ void __launch_bounds__(kYThreads) decode_reduce_kernel(const DecodePa
   }
 }
 
+// Largest cluster size (8, 4 or 2 blocks of one expert) whose clusters can all be resident at
+// once, so the expert kernel runs in a single wave; 1 if none can. Cached per shape.
+int expert_cluster_size(const moe_dims& dims, int smem) {
+  struct Entry { int n_parts, smem, cluster; };
+  static std::mutex mu;
+  static Entry cache[16];
+  static int n_cache = 0;
+  const int n_parts = decode_parts(dims), parts = dims.inter / kDecPartRows;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n_cache; ++i)
+    if (cache[i].n_parts == n_parts && cache[i].smem == smem) return cache[i].cluster;
+  int chosen = 1;
+  for (int cs = 8; cs >= 2; cs /= 2) {
+    if (parts % cs) continue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(n_parts);
+    cfg.blockDim = dim3(kXThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int active = 0;
+    if (cudaOccupancyMaxActiveClusters(&active, decode_expert_kernel, &cfg) == cudaSuccess && active * cs >= n_parts) {
+      chosen = cs;
+      break;
+    }
+  }
+  cudaGetLastError();  // an unsupported query leaves no sticky error behind
+  if (n_cache < 16) cache[n_cache++] = {n_parts, smem, chosen};
+  return chosen;
+}
+
 }  // namespace
 
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s, void* const* events) {
@@ -383,13 +458,17 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s, void* const* ev
   static cudaError_t attr =
       cudaFuncSetAttribute(decode_expert_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, x_smem(kDecodeMaxD).total);
   if (attr != cudaSuccess) return attr;
+  const int cluster = expert_cluster_size(dims, smem);
   cudaError_t err = record_event(events, 0, s);
   if (err != cudaSuccess) return err;
-  if ((err = launch_pdl(decode_router_kernel, (p.E + 1) / 2, kRThreads, 0, s, p)) != cudaSuccess) return err;
+  if ((err = launch_pdl(decode_router_kernel, (p.E + 1) / 2, kRThreads, 0, 1, s, p)) != cudaSuccess) return err;
   if ((err = record_event(events, 1, s)) != cudaSuccess) return err;
-  if ((err = launch_pdl(decode_expert_kernel, n_parts, kXThreads, (size_t)smem, s, p)) != cudaSuccess) return err;
+  if ((err = launch_pdl(decode_expert_kernel, n_parts, kXThreads, (size_t)smem, cluster, s, p)) != cudaSuccess)
+    return err;
   if ((err = record_event(events, 2, s)) != cudaSuccess) return err;
-  if ((err = launch_pdl(decode_reduce_kernel, p.d / kYRows, kYThreads, 0, s, p, n_parts)) != cudaSuccess) return err;
+  if ((err = launch_pdl(decode_reduce_kernel, p.d / kYRows, kYThreads, 0, 1, s, p, n_parts / cluster)) !=
+      cudaSuccess)
+    return err;
   return record_event(events, 3, s);
 }
 

@@ -93,9 +93,9 @@ extern "C" int moe_decode_noalloc(const moe_layer* layer, const uint16_t* x, uin
   void* base = nullptr;
   if (scratch_address(&base) != cudaSuccess) return MOE_ERR_CUDA;
   uint8_t* s = static_cast<uint8_t*>(base);
-  // The last-block counter must start at zero; a call that gave up half-way could leave it set.
+  // Nothing in the scratch must start at zero: every call writes the logits, the routing and
+  // the partial rows before it reads them; the status word is written only on device errors.
   WsHeader* hdr = reinterpret_cast<WsHeader*>(s + L.header);
-  if (cudaMemsetAsync(&hdr->dticket, 0, sizeof(unsigned), stream) != cudaSuccess) return MOE_ERR_CUDA;
   const PackedLayout P = packed_layout(d);
   DecodeParams p;
   p.x = x;
