@@ -42,7 +42,7 @@ constexpr int kQuarterRows = 32;
 constexpr int kGUMat = 2 * kQuarterRows * 16 + kQuarterRows * 4;  // 1152: one matrix's quarter
 constexpr int kGUQuarter = 2 * kGUMat;                             // 2304: gate + up quarter
 constexpr int kSBBytes = kBlockRows * 4;                           // 512
-constexpr int kTileRows = 256;      // block-map tile height (max MMA N)
+constexpr int kTileRows = 128;      // block-map tile height (max MMA N of the prefill GEMMs)
 constexpr int kMaxTopK = 16;
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTokens = 65536;

@@ -166,14 +166,14 @@ def test_prefill_full_skew_2048(m):
 
 
 def test_prefill_forced_tile_edges(m):
-    """Every token picks experts 0..k-1: each gets T rows (tiles of 256 + a ragged tail)."""
+    """Every token picks experts 0..k-1: each gets T rows (whole tiles, then a ragged tail)."""
     shape = FULL
     npl = dict(_np_layer(shape, 3, None))
     rb = np.zeros(shape.n_experts, dtype=np.float32)
     rb[: shape.top_k] = 100.0
     npl["router_bias"] = rb
     layer = m.upload_layer(npl)
-    for T in (256, 257):
+    for T in (2 * m.tile_rows(), 2 * m.tile_rows() + 1):
         _, g = prefill_and_check(m, shape, T, seed=3, npl=npl, layer=layer)
         assert np.all(g["counts"][: shape.top_k] == T)
 
