@@ -48,6 +48,12 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uin
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_row_maps(RowMaps* m, const void* ptr, uint64_t rows, uint64_t cols, bool fp16) {
+  for (int i = 0; i < 4; ++i)
+    if (!make_map(&m->box[i], ptr, rows, cols, 128u >> i, fp16)) return false;
+  return true;
+}
+
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 int check_dims(const moe_dims* d) {
@@ -127,8 +133,10 @@ int run_route(const moe_dims& d, const float* logits, int T, const Ws& w, float*
 
 int run_router_gemm(const moe_layer* L, const uint16_t* x, int T, const Ws& w, cudaStream_t s) {
   const moe_dims& d = L->dims;
-  CUtensorMap tb, ta;
-  if (!make_map(&tb, x, T, d.d, 16) || !make_map(&ta, L->router_w, d.n_experts, d.d, kBlockRows)) return MOE_ERR_CUDA;
+  RowMaps tb;
+  CUtensorMap ta;
+  if (!make_row_maps(&tb, x, T, d.d, false) || !make_map(&ta, L->router_w, d.n_experts, d.d, kBlockRows))
+    return MOE_ERR_CUDA;
   GemmParams p = {};
   p.k_blocks = d.d / kGroup;
   p.m_tiles = (d.n_experts + kBlockRows - 1) / kBlockRows;
@@ -241,11 +249,11 @@ int moe_prefill_timed(const moe_layer* layer, const uint16_t* x, int32_t T, uint
   if ((st = run_route(d, w.at<float>(w.L.logits), T, w, yacc, x, stream))) return st;
 
   // 3. gate|up grouped GEMM + SwiGLU -> hidden; 4. down grouped GEMM + weighted combine -> yacc
-  CUtensorMap x_rows, h_rows, unused;
-  if (!make_map(&x_rows, w.at<uint16_t>(w.L.x16), T, d.d, 1, true) ||
-      !make_map(&h_rows, hidden, 2 * ((uint64_t)A + T), d.inter, 16, true))
+  RowMaps x_rows, h_rows;
+  if (!make_row_maps(&x_rows, w.at<uint16_t>(w.L.x16), (uint64_t)A + T, d.d, true) ||
+      !make_row_maps(&h_rows, hidden, 2 * ((uint64_t)A + T), d.inter, true))
     return MOE_ERR_CUDA;
-  unused = x_rows;
+  const CUtensorMap& unused = x_rows.box[0];
   GemmParams p = {};
   p.packed = static_cast<const uint8_t*>(layer->packed);
   p.expert_stride = P.expert_stride;

@@ -15,8 +15,8 @@
 // output rows) in a fixed stride; every ring of stages keeps running across items:
 //   warp 0      weight producer: TMA bulk copies of packed Q4 blocks into a deep ring (router
 //               mode: 2-D tiles of the bf16 router weight)
-//   warp 1      activation producer: the tile's token rows (through the scatter permutation)
-//               by TMA gather4, or contiguous rows by 2-D tiled loads
+//   warp 1      activation producer: a tile's rows are contiguous (expert-sorted fp16 x, hidden
+//               rows, or token rows), fetched by 2-D TMA boxes of 128/64/32/16 rows
 //   warp 2      allocates TMEM; lane 0 issues tcgen05.mma into one of two accumulator buffers
 //   warps 3-10  dequantize nibbles into 128-byte-swizzled fp16 A tiles in shared memory
 //   warps 11-14 epilogue from the other accumulator buffer while the next tile accumulates:
@@ -79,11 +79,13 @@ struct Smem {
   static constexpr int a_off = 0;
   static constexpr int b_off = a_off + C::kStagesA * C::kNumA * kATileBytes;
   static constexpr int w_off = b_off + C::kStagesB * C::kNumB * kBTile;
+  // down projection: each epilogue warp keeps its own copy of the tile's (token, weight) list
+  static constexpr int kListRows = MODE == kModeDown ? C::kRows : 0;
   static constexpr int tok_off = w_off + C::kStagesW * C::kWBytes;
-  static constexpr int wgt_off = tok_off + 2 * C::kRows * 4;
-  static constexpr int bar_off = wgt_off + 2 * C::kRows * 4;
-  // full/empty per ring stage, then acc_full[2], acc_empty[2], tok_full[2]
-  static constexpr int n_bars = 2 * (C::kStagesW + C::kStagesA + C::kStagesB) + 6;
+  static constexpr int wgt_off = tok_off + kNumEpiWarps * kListRows * 4;
+  static constexpr int bar_off = wgt_off + kNumEpiWarps * kListRows * 4;
+  // full/empty per ring stage, then acc_full[2], acc_empty[2]
+  static constexpr int n_bars = 2 * (C::kStagesW + C::kStagesA + C::kStagesB) + 4;
   static constexpr int misc_off = bar_off + n_bars * 8;
   static constexpr int bytes = misc_off + 16;
   static constexpr int alloc = bytes + 1024;  // slack for 1024-byte alignment of the base
@@ -150,7 +152,7 @@ __device__ __forceinline__ Item decode_item(const GemmParams& p, int item, int n
 
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
-    moe_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmap_b,
+    moe_gemm_kernel(const GemmParams p, const __grid_constant__ RowMaps maps_b,
                     const __grid_constant__ CUtensorMap tmap_a) {
   using C = Cfg<MODE>;
   using S = Smem<MODE>;
@@ -172,8 +174,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if ((int)blockIdx.x >= n_items) return;  // nothing for this CTA (uniform: before any set-up)
   const int KB = p.k_blocks;
 
-  int32_t* s_tok = reinterpret_cast<int32_t*>(smem + S::tok_off);  // [2][kRows]
-  float* s_wgt = reinterpret_cast<float*>(smem + S::wgt_off);      // [2][kRows]
+  int32_t* s_tok = reinterpret_cast<int32_t*>(smem + S::tok_off);  // [epilogue warp][kListRows]
+  float* s_wgt = reinterpret_cast<float*>(smem + S::wgt_off);      // [epilogue warp][kListRows]
   const uint32_t bars = base + S::bar_off;
   auto full_w = [&](int s) { return bars + 8u * s; };
   auto empty_w = [&](int s) { return bars + 8u * (C::kStagesW + s); };
@@ -184,7 +186,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t acc_bars = bars + 8u * (2 * (C::kStagesW + C::kStagesA + C::kStagesB));
   auto acc_full = [&](int b) { return acc_bars + 8u * b; };
   auto acc_empty = [&](int b) { return acc_bars + 8u * (2 + b); };
-  auto tok_full = [&](int b) { return acc_bars + 8u * (4 + b); };
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + S::misc_off);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + S::misc_off + 4);
   auto a_tile = [&](int stage, int which) { return base + S::a_off + (stage * C::kNumA + which) * kATileBytes; };
@@ -208,7 +209,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(acc_full(b), 1);
       mbar_init(acc_empty(b), kEpiThreads);
-      mbar_init(tok_full(b), 1);
     }
     *s_abort = 0;
     fence_barrier_init();
@@ -217,10 +217,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(s_tmem), S::kTmemCols);
     tmem_relinquish();
   }
-  if (warp == kWarpB) {
-    prefetch_tmap(&tmap_b);
-    if (MODE == kModeRouter) prefetch_tmap(&tmap_a);
-  }
+  if (warp == kWarpB && lane < 4) prefetch_tmap(&maps_b.box[lane]);
+  if (warp == kWarpW && lane == 0 && MODE == kModeRouter) prefetch_tmap(&tmap_a);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -261,52 +259,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kWarpB) {
     // ------------------------------------------------------------ activation (B) producer
-    uint32_t g = 0;
-    int n = 0;  // items done by this CTA: accumulator buffer = n & 1
-    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++n) {
-      const Item it = decode_item<MODE>(p, item, n_routed);
-      const int buf = n & 1;
-      // The token list of this buffer is free once the epilogue released the item two back.
-      if (!mbar_wait(acc_empty(buf), ((n >> 1) & 1) ^ 1, s_abort)) break;
-      int32_t* tok = s_tok + buf * C::kRows;
-      float* wgt = s_wgt + buf * C::kRows;
-      // Padding rows up to the MMA's N repeat the tile's last valid row; results are discarded.
-      for (int j = lane; j < it.n16; j += 32) {
-        const int jj = min(j, it.nrows - 1);
-        int t;
-        float w = 1.f;
-        if (MODE == kModeRouter || it.shared) {
-          t = it.r0 + jj;
-        } else {
-          const int a = p.perm[it.row0 + jj];
-          t = a / p.k;
-          if (MODE == kModeDown) w = p.topk_w[a];
-        }
-        tok[j] = t;
-        wgt[j] = w;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tok_full(buf));
+    // Rows of the tile: the padded rows up to n16 belong to the next tile or lie beyond the
+    // tensor (zero fill); their accumulator columns are never read.
+    if (lane == 0) {
+      uint32_t g = 0;
       bool ok = true;
-      for (int kb = 0; kb < KB; ++kb, ++g) {
-        const int sb = g % C::kStagesB;
-        if (!(ok = mbar_wait(empty_b(sb), ((g / C::kStagesB) & 1) ^ 1, s_abort))) break;
-        if (lane == 0) mbar_arrive_expect_tx(full_b(sb), (uint32_t)(C::kNumB * it.n16 * 128));
-        __syncwarp();
-        if (MODE == kModeGateUp) {
-          for (int q = lane; q < it.n16 / 4; q += 32)
-            tma_gather4(b_tile(sb, 0) + q * 512, &tmap_b, kb * kGroup, tok[4 * q], tok[4 * q + 1], tok[4 * q + 2],
-                        tok[4 * q + 3], full_b(sb));
-        } else {
-          for (int q = lane; q < it.n16 / 16; q += 32) {
-            tma_load_2d(b_tile(sb, 0) + q * 2048, &tmap_b, kb * kGroup, it.row0 + 16 * q, full_b(sb));
-            if (C::kNumB == 2)
-              tma_load_2d(b_tile(sb, 1) + q * 2048, &tmap_b, kb * kGroup, p.hidden_rows + it.row0 + 16 * q,
-                          full_b(sb));
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+        const Item it = decode_item<MODE>(p, item, n_routed);
+        for (int kb = 0; kb < KB; ++kb, ++g) {
+          const int sb = g % C::kStagesB;
+          if (!(ok = mbar_wait(empty_b(sb), ((g / C::kStagesB) & 1) ^ 1, s_abort))) break;
+          mbar_arrive_expect_tx(full_b(sb), (uint32_t)(C::kNumB * it.n16 * 128));
+          int row = 0;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int h = 128 >> i;
+            if (it.n16 - row >= h) {
+#pragma unroll
+              for (int plane = 0; plane < C::kNumB; ++plane)
+                tma_load_2d(b_tile(sb, plane) + row * 128, &maps_b.box[i], kb * kGroup,
+                            plane * p.hidden_rows + it.row0 + row, full_b(sb));
+              row += h;
+            }
           }
         }
       }
-      if (!ok) break;
     }
   } else if (warp == kWarpMMA) {
     // ------------------------------------------------------------ MMA issuer
@@ -397,13 +374,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++n) {
       const Item it = decode_item<MODE>(p, item, n_routed);
       const int buf = n & 1;
+      int32_t* tok = s_tok + (warp - kWarpEpi0) * S::kListRows;
+      float* wgt = s_wgt + (warp - kWarpEpi0) * S::kListRows;
+      if (MODE == kModeDown) {  // this warp's (token, routing weight) list, read before the wait
+        __syncwarp();
+        for (int j = lane; j < it.nrows; j += 32) {
+          if (it.shared) {
+            tok[j] = it.r0 + j;
+            wgt[j] = 1.f;
+          } else {
+            const int a = p.perm[it.row0 + j];
+            tok[j] = a / p.k;
+            wgt[j] = p.topk_w[a];
+          }
+        }
+        __syncwarp();
+      }
       if (!mbar_wait(acc_full(buf), (n >> 1) & 1, s_abort)) break;
-      if (!mbar_wait(tok_full(buf), (n >> 1) & 1, s_abort)) break;
       tc_fence_after();
       const int orow = it.m * kBlockRows + q * 32 + lane;  // output row (feature / expert)
       const uint32_t taddr = tmem_base + lane_addr + buf * S::kAccCols;
-      const int32_t* tok = s_tok + buf * C::kRows;
-      const float* wgt = s_wgt + buf * C::kRows;
       for (int j0 = 0; j0 < it.n16; j0 += 16) {
         uint32_t acc0[16], acc1[16];
         tmem_ld16(taddr + j0, acc0);
@@ -432,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(acc_empty(buf));  // the accumulator buffer and its token list are free again
+      mbar_arrive(acc_empty(buf));  // the accumulator buffer is free again
     }
     if (MODE == kModeGateUp && __any_sync(0xFFFFFFFFu, over) && lane == 0)
       set_device_status(p.hdr, MOE_ERR_OUT_OF_RANGE);
@@ -460,7 +450,7 @@ int num_sms() {
 }
 
 template <int MODE>
-cudaError_t launch_mode(const GemmParams& p, const CUtensorMap* tb, const CUtensorMap* ta, int max_items,
+cudaError_t launch_mode(const GemmParams& p, const RowMaps* tb, const CUtensorMap* ta, int max_items,
                         cudaStream_t s) {
   static cudaError_t attr = cudaFuncSetAttribute(moe_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  Smem<MODE>::alloc);
@@ -474,7 +464,7 @@ cudaError_t launch_mode(const GemmParams& p, const CUtensorMap* tb, const CUtens
 
 // `grid` is an upper bound on the number of work items; the persistent grid is at most one CTA
 // per SM, and each CTA reads the actual work list size on the device.
-cudaError_t launch_gemm(int mode, const GemmParams& p, const CUtensorMap* tmap_b, const CUtensorMap* tmap_a, int grid,
+cudaError_t launch_gemm(int mode, const GemmParams& p, const RowMaps* tmap_b, const CUtensorMap* tmap_a, int grid,
                         cudaStream_t s) {
   if (grid <= 0) return cudaSuccess;
   switch (mode) {

@@ -127,7 +127,7 @@ inline WsLayout ws_layout(const moe_dims& d, int T) {
   L.inv_perm = take(A * 4);
   L.tile_map = take((size_t)L.max_tiles * 3 * 4);
   L.n_tiles = take(4);
-  L.x16 = take((size_t)T * d.d * 2);                   // x as fp16 (expert GEMM operand)
+  L.x16 = take((A + T) * (size_t)d.d * 2);             // fp16 x: A expert-sorted rows, then T token rows
   L.hidden = take(2 * (A + T) * (size_t)d.inter * 2);  // SwiGLU rows: fp16 leading part, fp16 remainder
   L.yacc = take((size_t)T * d.d * 4);
   L.dec_part = take(decode_partial_bytes(d));
@@ -155,7 +155,8 @@ struct RouteParams {
   int32_t* n_tiles;      // [1]
   float* yacc;           // [T, d] zeroed by the top-k kernel (NULL: skip)
   const uint16_t* x;     // [T, d] bf16 input (NULL: no conversion)
-  uint16_t* x16;         // [T, d] fp16 copy of x written by the top-k kernel
+  uint16_t* x16;         // [A + T, d] fp16 x: rows A.. in token order (top-k kernel), rows 0..A-1 in
+                         // expert-sorted order (row gather after the scatter)
   WsHeader* hdr;
   int T, E, k, d, n_chunks;
 };
@@ -204,8 +205,13 @@ struct DecodeParams {
 // Launchers (each returns cudaGetLastError()).
 cudaError_t launch_pack(const moe_dims& d, const moe_q4_view* views, uint8_t* packed, cudaStream_t s);
 cudaError_t launch_route(const RouteParams& p, cudaStream_t s);
-cudaError_t launch_gemm(int mode, const GemmParams& p, const CUtensorMap* tmap_b, const CUtensorMap* tmap_a,
-                        int grid, cudaStream_t s);
+// Tensor maps over one row-major operand with 64-column boxes of 128, 64, 32 and 16 rows: a tile of
+// n16 rows is fetched with at most four copies and no rows beyond the tile.
+struct RowMaps {
+  CUtensorMap box[4];
+};
+cudaError_t launch_gemm(int mode, const GemmParams& p, const RowMaps* maps_b, const CUtensorMap* tmap_a, int grid,
+                        cudaStream_t s);
 cudaError_t launch_cast(const float* yacc, uint16_t* y, size_t n, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s, void* const* events);
 

@@ -1,7 +1,7 @@
 // GPU-resident routing (page "Perplexity's Lily beats MLX-LM on MacBook M5 because it only runs
 // one model", section "Prefill: keep routing on the GPU, dequantize in flight": after the top-8
 // selection, histogram, prefix scan, scatter and block map run on the GPU with no host round
-// trip). Three launches:
+// trip). Three launches (four in prefill):
 //   route_topk_kernel    16 tokens per CTA: warp top-k on order-preserving logit keys (ties to
 //                        the lower index), renormalised softmax weights; the fp16 copy of x and
 //                        the zeroing of the combine accumulator rows
@@ -10,7 +10,9 @@
 //                        per-chunk bases and the tile block map
 //   route_scatter_kernel one warp per chunk: stable, atomics-free placement of the chunk's
 //                        assignments (in-warp ranks by __match_any_sync, running per-expert
-//                        counters in shared memory).
+//                        counters in shared memory)
+//   route_rows_kernel    (prefill) copies each assignment's fp16 token row to its sorted
+//                        position, so the grouped GEMM reads every tile as contiguous rows.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -74,7 +76,7 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const RoutePar
   const int n8 = (t_end - t_begin) * p.d / 8;  // 8-element chunks of this CTA's rows
   if (p.x) {  // fp16 operand copy of x for the expert GEMMs (exact inside the fp16 range)
     const uint4* xs = reinterpret_cast<const uint4*>(p.x + (size_t)t_begin * p.d);
-    uint4* xd = reinterpret_cast<uint4*>(p.x16 + (size_t)t_begin * p.d);
+    uint4* xd = reinterpret_cast<uint4*>(p.x16 + ((size_t)p.T * p.k + t_begin) * p.d);
     bool over = false;
     for (int i = tid; i < n8; i += kTopkThreads) {
       const uint4 v = xs[i];
@@ -190,6 +192,19 @@ __global__ void __launch_bounds__(32) route_scatter_kernel(const RouteParams p) 
   }
 }
 
+// One warp per sorted row: x16[pos] = x16[A + perm[pos] / k] (16-byte copies, d/8 per row).
+__global__ void __launch_bounds__(256) route_rows_kernel(const RouteParams p) {
+  const int A = p.T * p.k, n16 = p.d / 8;
+  const int warps = gridDim.x * (blockDim.x >> 5);
+  const int lane = threadIdx.x & 31;
+  for (int pos = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); pos < A; pos += warps) {
+    const int t = p.perm[pos] / p.k;
+    const uint4* src = reinterpret_cast<const uint4*>(p.x16 + ((size_t)A + t) * p.d);
+    uint4* dst = reinterpret_cast<uint4*>(p.x16 + (size_t)pos * p.d);
+    for (int i = lane; i < n16; i += 32) dst[i] = src[i];
+  }
+}
+
 __global__ void __launch_bounds__(256) cast_kernel(const float* __restrict__ yacc, uint16_t* __restrict__ y, size_t n8) {
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
     const float4 a = reinterpret_cast<const float4*>(yacc)[2 * i];
@@ -214,6 +229,10 @@ cudaError_t launch_route(const RouteParams& p, cudaStream_t s) {
   route_hist_kernel<<<p.n_chunks, kTopkThreads, 0, s>>>(p);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   route_scatter_kernel<<<p.n_chunks, 32, 0, s>>>(p);
+  if ((err = cudaGetLastError()) != cudaSuccess || !p.x) return err;
+  const int rows = p.T * p.k, per_cta = 8;  // 8 warps of 256 threads
+  const int blocks = (rows + per_cta - 1) / per_cta < 152 * 8 ? (rows + per_cta - 1) / per_cta : 152 * 8;
+  route_rows_kernel<<<blocks, 256, 0, s>>>(p);
   return cudaGetLastError();
 }
 
