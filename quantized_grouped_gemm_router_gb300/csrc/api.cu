@@ -34,24 +34,51 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D map over a row-major [rows, cols] matrix of 16-bit values (bf16, or fp16 if `fp16`),
-// 128-byte swizzle, box of 64 columns x box_rows.
-bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows, bool fp16 = false) {
+bool encode(CUtensorMap* m, CUtensorMapDataType type, cuuint32_t rank, const void* ptr, const cuuint64_t* dims,
+            const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swz) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * 2};
-  const cuuint32_t box[2] = {64, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(m, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return fn(m, type, rank, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool make_row_maps(RowMaps* m, const void* ptr, uint64_t rows, uint64_t cols, bool fp16) {
-  for (int i = 0; i < 4; ++i)
-    if (!make_map(&m->box[i], ptr, rows, cols, 128u >> i, fp16)) return false;
+// A row-major [rows, cols] 16-bit matrix seen as (64 columns, rows, cols / 64 column blocks), so
+// that one box (64 x box_rows x kb) lands in shared memory as kb consecutive [box_rows][64] tiles,
+// 128-byte swizzled.
+bool make_rows_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows, uint32_t kb,
+                   bool fp16) {
+  const cuuint64_t dims[3] = {64, rows, cols / 64};
+  const cuuint64_t strides[2] = {cols * 2, 128};
+  const cuuint32_t box[3] = {64, box_rows, kb};
+  return encode(m, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims, strides, box,
+                CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// rows[i]: boxes of 16 (i + 1) rows x kb column blocks (tiles of up to 96 rows).
+bool make_gemm_rows(GemmMaps* g, const void* ptr, uint64_t rows, uint64_t cols, uint32_t kb, bool fp16) {
+  for (int i = 0; i < 6; ++i)
+    if (!make_rows_map(&g->rows[i], ptr, rows, cols, 16u * (i + 1), kb, fp16)) return false;
+  g->a = g->rows[0];
+  g->a2 = g->rows[0];
   return true;
+}
+
+// The down region of every expert as u64 words: codes (256 words, m block, (K block, half),
+// expert) and scale/bias (64 words, m block, K block, expert); one box covers kb K blocks of one
+// m block (see dn_code_offset / dn_sb_offset).
+bool make_down_weight_maps(GemmMaps* g, const uint8_t* packed, const PackedLayout& P, const moe_dims& d, uint32_t kb) {
+  const uint64_t DM = d.d / kBlockRows, KBD = d.inter / kGroup, E1 = (uint64_t)d.n_experts + 1;
+  const uint8_t* codes = packed + P.gu_bytes;
+  const uint8_t* sb = codes + dn_sb_offset(0, 0, (int)DM, (int)KBD);
+  const cuuint64_t cdims[4] = {kHalfBytes / 8, DM, 2 * KBD, E1};
+  const cuuint64_t cstr[3] = {kHalfBytes, DM * kHalfBytes, P.expert_stride};
+  const cuuint32_t cbox[4] = {kHalfBytes / 8, 1, 2 * kb, 1};
+  const cuuint64_t sdims[4] = {kSBBytes / 8, DM, KBD, E1};
+  const cuuint64_t sstr[3] = {kSBBytes, DM * kSBBytes, P.expert_stride};
+  const cuuint32_t sbox[4] = {kSBBytes / 8, 1, kb, 1};
+  return encode(&g->a, CU_TENSOR_MAP_DATA_TYPE_UINT64, 4, codes, cdims, cstr, cbox, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+         encode(&g->a2, CU_TENSOR_MAP_DATA_TYPE_UINT64, 4, sb, sdims, sstr, sbox, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -133,9 +160,10 @@ int run_route(const moe_dims& d, const float* logits, int T, const Ws& w, float*
 
 int run_router_gemm(const moe_layer* L, const uint16_t* x, int T, const Ws& w, cudaStream_t s) {
   const moe_dims& d = L->dims;
-  RowMaps tb;
-  CUtensorMap ta;
-  if (!make_row_maps(&tb, x, T, d.d, false) || !make_map(&ta, L->router_w, d.n_experts, d.d, kBlockRows))
+  GemmMaps maps;
+  const uint32_t kb = gemm_kb_per_stage(kModeRouter);
+  if (!make_gemm_rows(&maps, x, T, d.d, kb, false) ||
+      !make_rows_map(&maps.a, L->router_w, d.n_experts, d.d, kBlockRows, kb, false))
     return MOE_ERR_CUDA;
   GemmParams p = {};
   p.k_blocks = d.d / kGroup;
@@ -150,7 +178,7 @@ int run_router_gemm(const moe_layer* L, const uint16_t* x, int T, const Ws& w, c
   p.inter = d.inter;
   const int rt = router_tile_rows();
   const int grid = ((T + rt - 1) / rt) * p.m_tiles;
-  return launch_gemm(kModeRouter, p, &tb, &ta, grid, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  return launch_gemm(kModeRouter, p, &maps, grid, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 int copy_route_out(const moe_dims& d, int T, const Ws& w, const moe_route_out* o, cudaStream_t s) {
@@ -249,11 +277,11 @@ int moe_prefill_timed(const moe_layer* layer, const uint16_t* x, int32_t T, uint
   if ((st = run_route(d, w.at<float>(w.L.logits), T, w, yacc, x, stream))) return st;
 
   // 3. gate|up grouped GEMM + SwiGLU -> hidden; 4. down grouped GEMM + weighted combine -> yacc
-  RowMaps x_rows, h_rows;
-  if (!make_row_maps(&x_rows, w.at<uint16_t>(w.L.x16), (uint64_t)A + T, d.d, true) ||
-      !make_row_maps(&h_rows, hidden, 2 * ((uint64_t)A + T), d.inter, true))
+  GemmMaps x_maps, h_maps;
+  if (!make_gemm_rows(&x_maps, w.at<uint16_t>(w.L.x16), (uint64_t)A + T, d.d, gemm_kb_per_stage(kModeGateUp), true) ||
+      !make_gemm_rows(&h_maps, hidden, 2 * ((uint64_t)A + T), d.inter, gemm_kb_per_stage(kModeDown), true) ||
+      !make_down_weight_maps(&h_maps, static_cast<const uint8_t*>(layer->packed), P, d, gemm_kb_per_stage(kModeDown)))
     return MOE_ERR_CUDA;
-  const CUtensorMap& unused = x_rows.box[0];
   GemmParams p = {};
   p.packed = static_cast<const uint8_t*>(layer->packed);
   p.expert_stride = P.expert_stride;
@@ -277,13 +305,13 @@ int moe_prefill_timed(const moe_layer* layer, const uint16_t* x, int32_t T, uint
   p.m_tiles = d.inter / kBlockRows;
   p.k_blocks = d.d / kGroup;
   if (record_event(events, 2, stream) != cudaSuccess) return MOE_ERR_CUDA;
-  if (launch_gemm(kModeGateUp, p, &x_rows, &unused, tiles * p.m_tiles, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_gemm(kModeGateUp, p, &x_maps, tiles * p.m_tiles, stream) != cudaSuccess) return MOE_ERR_CUDA;
 
   p.region_offset = P.gu_bytes;
   p.m_tiles = d.d / kBlockRows;
   p.k_blocks = d.inter / kGroup;
   if (record_event(events, 3, stream) != cudaSuccess) return MOE_ERR_CUDA;
-  if (launch_gemm(kModeDown, p, &h_rows, &unused, tiles * p.m_tiles, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_gemm(kModeDown, p, &h_maps, tiles * p.m_tiles, stream) != cudaSuccess) return MOE_ERR_CUDA;
 
   // 5. fp32 accumulator -> bf16 output
   if (record_event(events, 4, stream) != cudaSuccess) return MOE_ERR_CUDA;

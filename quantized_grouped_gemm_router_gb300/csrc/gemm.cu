@@ -2,26 +2,36 @@
 //
 // Page "Perplexity's Lily beats MLX-LM on MacBook M5 because it only runs one model", section
 // "Prefill: keep routing on the GPU, dequantize in flight": the grouped GEMM dequantizes one
-// small tile of groupwise-affine Q4 weights at a time in on-chip memory, accumulates in FP32,
-// and never materialises the expanded weights; section "Decode: minimize bytes per token"
-// (fusion): input projections fused with the gate activation, output projection fused with the
-// routing scores and the shared expert.
+// small tile of groupwise-affine Q4 weights at a time on chip, accumulates in FP32, and never
+// materialises the expanded weights; section "Decode: minimize bytes per token" (fusion): input
+// projections fused with the gate activation, output projection fused with the routing scores
+// and the shared expert.
 //
 // GB300 design (swap-AB): the dequantized weight slab is MMA operand A (M = 128 output rows),
-// the expert's token rows are operand B (N = rows of the tile rounded up to 16, <= 128, set
-// per tile at run time), so an expert with few rows still issues dense MMAs.
+// the expert's token rows are operand B (N = rows of the tile rounded up to 16, set per tile at
+// run time), so an expert with few rows still issues dense MMAs. Dequantized A tiles go from
+// registers straight into tensor memory (tcgen05.st) and the MMA reads A from there; shared
+// memory only carries the packed codes and the B rows.
+//
+// Two GB300 facts shape the pipeline (measured on this part):
+//   * a TMA copy costs a roughly fixed ~0.2-0.3 us of issue time however small it is, so every
+//     copy here moves several K steps at once (3-D / 4-D tensor maps, bulk copies of >= 9 KB);
+//   * one thread issues at most one tcgen05.mma per ~40-60 cycles, so tiles of < 200 rows need
+//     two issuing warps (each with its own accumulator) to keep the tensor core busy.
 //
 // Persistent, warp-specialised CTAs (one per SM) walk the work items (block-map tile x 128
-// output rows) in a fixed stride; every ring of stages keeps running across items:
-//   warp 0      weight producer: TMA bulk copies of packed Q4 blocks into a deep ring (router
-//               mode: 2-D tiles of the bf16 router weight)
-//   warp 1      activation producer: a tile's rows are contiguous (expert-sorted fp16 x, hidden
-//               rows, or token rows), fetched by 2-D TMA boxes of 128/64/32/16 rows
-//   warp 2      allocates TMEM; lane 0 issues tcgen05.mma into one of two accumulator buffers
-//   warps 3-10  dequantize nibbles into 128-byte-swizzled fp16 A tiles in shared memory
-//   warps 11-14 epilogue from the other accumulator buffer while the next tile accumulates:
-//               SwiGLU -> hidden rows (gate/up), routing weight x accumulator -> fp32 red.add
-//               into the token's output row (down), or logits + bias (router)
+// output rows) in a fixed stride; every ring keeps running across items:
+//   warp 0       weight producer: packed Q4 stages (kS K blocks) by bulk / tensor copies (router
+//                mode: bf16 router weight tiles, which the MMA reads from shared memory directly)
+//   warp 1       activation producer: the tile's contiguous rows (expert-sorted fp16 x, hidden
+//                rows, or token rows) for kS K blocks in one 3-D tensor copy per operand plane
+//   warps 2, 15  MMA issuers (whole warp runs the loop, one elected lane issues); warp 2 also
+//                owns the TMEM allocation
+//   warps 3-10   dequantize nibbles into fp16 A tiles in tensor memory (each warp writes the 32
+//                TMEM lanes its index may access)
+//   warps 11-14  epilogue from one of two accumulator buffers while the next tile accumulates:
+//                SwiGLU -> hidden rows (gate/up), routing weight x accumulator -> fp32 red.add
+//                into the token's output row (down), or logits + bias (router)
 // Every mbarrier wait is bounded; a timeout raises a CTA-wide abort flag, every role leaves its
 // loop, TMEM is freed and MOE_ERR_DEVICE_TIMEOUT is recorded.
 #include <cuda_bf16.h>
@@ -36,35 +46,37 @@ namespace {
 constexpr int kRouterRows = 64;    // token rows per router tile
 constexpr int kWarpW = 0, kWarpB = 1, kWarpMMA = 2, kWarpDq0 = 3, kNumDqWarps = 8;
 constexpr int kWarpEpi0 = kWarpDq0 + kNumDqWarps, kNumEpiWarps = 4;
-constexpr int kThreads = (kWarpEpi0 + kNumEpiWarps) * 32;  // 480
+constexpr int kWarpMMA2 = kWarpEpi0 + kNumEpiWarps;        // second MMA issuer
+constexpr int kThreads = (kWarpMMA2 + 1) * 32;             // 512
 constexpr int kDqThreads = kNumDqWarps * 32;               // 256
 constexpr int kEpiThreads = kNumEpiWarps * 32;             // 128
+constexpr int kATileBytes = kBlockRows * 128;              // 128 rows x 64 16-bit values
 
 // kNumA: weight operands per K step (gate and up share the B tile); kNumB: B operands per K step
-// (the down projection reads the hidden rows as two fp16 planes into one accumulator);
-// kFp16: fp16 operands (expert GEMMs) or bf16 operands (router).
+// (the down projection reads the hidden rows as two fp16 planes); kIssuers: MMA-issuing warps,
+// each with its own accumulator (gate / up, or leading / remainder plane); kS: K blocks per
+// weight and activation stage; kStagesW / kStagesB: stages of the weight and activation rings
+// (each kS K blocks); kStagesA: TMEM A tiles (one K block each); kWStage: bytes of one weight stage.
 template <int MODE>
 struct Cfg;
 template <>
 struct Cfg<kModeGateUp> {
-  static constexpr int kNumA = 2, kNumB = 1, kStagesW = 9, kStagesA = 2, kStagesB = 4, kRows = kTileRows;
-  static constexpr int kWBytes = 4 * kGUQuarter;  // the 4 quarters of a 128-row block: gate + up
-  static constexpr bool kFp16 = true;
+  static constexpr int kNumA = 2, kNumB = 1, kIssuers = 2, kS = 4, kStagesW = 3, kStagesB = 2, kStagesA = 2;
+  static constexpr int kRows = kTileRows, kWStage = 4 * kS * kGUQuarter;  // 4 row quarters x kS blocks
+  static constexpr bool kFp16 = true, kQ4 = true;
 };
 template <>
 struct Cfg<kModeDown> {
-  static constexpr int kNumA = 1, kNumB = 2, kStagesW = 16, kStagesA = 2, kStagesB = 3, kRows = kTileRows;
-  static constexpr int kWBytes = kBlockBytes;     // two code halves + scale/bias of one block
-  static constexpr bool kFp16 = true;
+  static constexpr int kNumA = 1, kNumB = 2, kIssuers = 2, kS = 2, kStagesW = 4, kStagesB = 3, kStagesA = 4;
+  static constexpr int kRows = kTileRows, kWStage = kS * kBlockBytes;     // codes (2 kS halves), then kS sb
+  static constexpr bool kFp16 = true, kQ4 = true;
 };
 template <>
 struct Cfg<kModeRouter> {
-  static constexpr int kNumA = 1, kNumB = 1, kStagesW = 0, kStagesA = 4, kStagesB = 4, kRows = kRouterRows;
-  static constexpr int kWBytes = 0;
-  static constexpr bool kFp16 = false;
+  static constexpr int kNumA = 1, kNumB = 1, kIssuers = 1, kS = 4, kStagesW = 2, kStagesB = 2, kStagesA = 0;
+  static constexpr int kRows = kRouterRows, kWStage = kS * kATileBytes;  // bf16 A tiles, read by the MMA
+  static constexpr bool kFp16 = false, kQ4 = false;
 };
-
-constexpr int kATileBytes = kBlockRows * 128;  // 128 rows x 64 16-bit values
 
 constexpr int tmem_cols_for(int cols) {
   return cols <= 32 ? 32 : cols <= 64 ? 64 : cols <= 128 ? 128 : cols <= 256 ? 256 : 512;
@@ -73,15 +85,19 @@ constexpr int tmem_cols_for(int cols) {
 template <int MODE>
 struct Smem {
   using C = Cfg<MODE>;
-  static constexpr int kBTile = C::kRows * 128;
-  static constexpr int kAccCols = C::kNumA * C::kRows;  // one accumulator buffer
-  static constexpr int kTmemCols = tmem_cols_for(2 * kAccCols);
-  static constexpr int a_off = 0;
-  static constexpr int b_off = a_off + C::kStagesA * C::kNumA * kATileBytes;
-  static constexpr int w_off = b_off + C::kStagesB * C::kNumB * kBTile;
+  static constexpr int kPlaneBytes = C::kS * C::kRows * 128;  // one operand plane of a B stage
+  static constexpr int kBStage = C::kNumB * kPlaneBytes;
+  static constexpr int kAccCols = C::kIssuers * C::kRows;     // one accumulator buffer
+  // TMEM columns: two accumulator buffers, then (Q4 modes) the A tiles, 32 columns per 128x64 tile
+  static constexpr int kACol = 2 * kAccCols;
+  static constexpr int kTmemNeed = kACol + C::kStagesA * C::kNumA * 32;
+  static constexpr int kTmemCols = tmem_cols_for(kTmemNeed);
+  static_assert(kTmemNeed <= 512, "tensor memory budget");
   // down projection: each epilogue warp keeps its own copy of the tile's (token, weight) list
   static constexpr int kListRows = MODE == kModeDown ? C::kRows : 0;
-  static constexpr int tok_off = w_off + C::kStagesW * C::kWBytes;
+  static constexpr int w_off = 0;
+  static constexpr int b_off = w_off + C::kStagesW * C::kWStage;
+  static constexpr int tok_off = b_off + C::kStagesB * kBStage;
   static constexpr int wgt_off = tok_off + kNumEpiWarps * kListRows * 4;
   static constexpr int bar_off = wgt_off + kNumEpiWarps * kListRows * 4;
   // full/empty per ring stage, then acc_full[2], acc_empty[2]
@@ -89,6 +105,8 @@ struct Smem {
   static constexpr int misc_off = bar_off + n_bars * 8;
   static constexpr int bytes = misc_off + 16;
   static constexpr int alloc = bytes + 1024;  // slack for 1024-byte alignment of the base
+  static_assert(alloc <= 232448, "shared memory budget");
+  static_assert(C::kWStage % 1024 == 0 && kPlaneBytes % 1024 == 0, "stage alignment");
 };
 
 // 8 packed codes (one word, nibble order of the packed layout) -> 8 fp16 weights
@@ -152,8 +170,7 @@ __device__ __forceinline__ Item decode_item(const GemmParams& p, int item, int n
 
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
-    moe_gemm_kernel(const GemmParams p, const __grid_constant__ RowMaps maps_b,
-                    const __grid_constant__ CUtensorMap tmap_a) {
+    moe_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
   using C = Cfg<MODE>;
   using S = Smem<MODE>;
   extern __shared__ uint8_t smem_raw[];
@@ -188,26 +205,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto acc_empty = [&](int b) { return acc_bars + 8u * (2 + b); };
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + S::misc_off);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + S::misc_off + 4);
-  auto a_tile = [&](int stage, int which) { return base + S::a_off + (stage * C::kNumA + which) * kATileBytes; };
-  auto b_tile = [&](int stage, int plane) { return base + S::b_off + (stage * C::kNumB + plane) * S::kBTile; };
-  auto w_tile = [&](int stage) { return smem + S::w_off + stage * C::kWBytes; };
+  auto w_stage = [&](int s) { return smem + S::w_off + s * C::kWStage; };
+  auto b_stage = [&](int s) { return base + S::b_off + s * S::kBStage; };
+  auto a_tmem = [&](uint32_t tbase, int stage, int which) { return tbase + S::kACol + (stage * C::kNumA + which) * 32; };
 
   // ---------------------------------------------------------------- set-up
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStagesW; ++s) {
       mbar_init(full_w(s), 1);
-      mbar_init(empty_w(s), kDqThreads);
+      mbar_init(empty_w(s), C::kQ4 ? kDqThreads : C::kIssuers);
     }
     for (int s = 0; s < C::kStagesA; ++s) {
-      mbar_init(full_a(s), MODE == kModeRouter ? 1 : kDqThreads);
-      mbar_init(empty_a(s), 1);
+      mbar_init(full_a(s), kDqThreads);
+      mbar_init(empty_a(s), C::kIssuers);
     }
     for (int s = 0; s < C::kStagesB; ++s) {
       mbar_init(full_b(s), 1);
-      mbar_init(empty_b(s), 1);
+      mbar_init(empty_b(s), C::kIssuers);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(acc_full(b), 1);
+      mbar_init(acc_full(b), C::kIssuers);
       mbar_init(acc_empty(b), kEpiThreads);
     }
     *s_abort = 0;
@@ -217,151 +234,174 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(s_tmem), S::kTmemCols);
     tmem_relinquish();
   }
-  if (warp == kWarpB && lane < 4) prefetch_tmap(&maps_b.box[lane]);
-  if (warp == kWarpW && lane == 0 && MODE == kModeRouter) prefetch_tmap(&tmap_a);
+  if (warp == kWarpB && lane < 6) prefetch_tmap(&maps.rows[lane]);
+  if (warp == kWarpW && lane == 0 && MODE != kModeGateUp) prefetch_tmap(&maps.a);
+  if (warp == kWarpW && lane == 1 && MODE == kModeDown) prefetch_tmap(&maps.a2);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
 
   if (warp == kWarpW) {
-    // ------------------------------------------------------------ weight (A) producer
+    // ------------------------------------------------------------ weight producer
     if (lane == 0) {
-      uint32_t g = 0;  // running K-block counter across this CTA's items
-      for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+      uint32_t gw = 0;  // running weight-stage counter across this CTA's items
+      bool ok = true;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
         const Item it = decode_item<MODE>(p, item, n_routed);
         const uint8_t* ebase = p.packed + (size_t)it.expert * p.expert_stride + p.region_offset;
-        bool ok = true;
-        for (int kb = 0; kb < KB && ok; ++kb, ++g) {
-          if constexpr (MODE != kModeRouter) {
-            const int s = g % C::kStagesW;
-            if (!(ok = mbar_wait(empty_w(s), ((g / C::kStagesW) & 1) ^ 1, s_abort))) break;
-            mbar_arrive_expect_tx(full_w(s), C::kWBytes);
-            const uint32_t dst = smem_u32(w_tile(s));
-            if (MODE == kModeGateUp) {  // four 32-row quarters: [gate | up] each
-              for (int q = 0; q < 4; ++q)
-                tma_bulk_g2s(dst + q * kGUQuarter, ebase + gu_offset(it.m, q, kb, KB), kGUQuarter, full_w(s));
-            } else {                    // code halves of columns 0..31 and 32..63, then scale/bias
-              const int DM = p.m_tiles;
-              tma_bulk_g2s(dst, ebase + dn_code_offset(kb, 0, it.m, DM), kHalfBytes, full_w(s));
-              tma_bulk_g2s(dst + kHalfBytes, ebase + dn_code_offset(kb, 1, it.m, DM), kHalfBytes, full_w(s));
-              tma_bulk_g2s(dst + kCodeBytes, ebase + dn_sb_offset(kb, it.m, DM, KB), kSBBytes, full_w(s));
-            }
+        for (int kb0 = 0; kb0 < KB; kb0 += C::kS, ++gw) {
+          const int s = gw % C::kStagesW;
+          if (!(ok = mbar_wait(empty_w(s), ((gw / C::kStagesW) & 1) ^ 1, s_abort))) break;
+          const uint32_t dst = smem_u32(w_stage(s));
+          if (MODE == kModeGateUp) {
+            // quarter q of the 128-row block: K blocks kb0.. are contiguous, 2304 bytes each
+            const int nk = min(C::kS, KB - kb0);
+            mbar_arrive_expect_tx(full_w(s), (uint32_t)(4 * nk * kGUQuarter));
+            for (int q = 0; q < 4; ++q)
+              tma_bulk_g2s(dst + q * C::kS * kGUQuarter, ebase + gu_offset(it.m, q, kb0, KB), nk * kGUQuarter,
+                           full_w(s));
+          } else if (MODE == kModeDown) {
+            // codes of (K block, half) pieces kb0*2 .. kb0*2+2kS-1 of block m, then their scale/bias
+            mbar_arrive_expect_tx(full_w(s), (uint32_t)C::kWStage);
+            tma_load_4d(dst, &maps.a, 0, it.m, 2 * kb0, it.expert, full_w(s));
+            tma_load_4d(dst + 2 * C::kS * kHalfBytes, &maps.a2, 0, it.m, kb0, it.expert, full_w(s));
           } else {
-            const int s = g % C::kStagesA;
-            if (!(ok = mbar_wait(empty_a(s), ((g / C::kStagesA) & 1) ^ 1, s_abort))) break;
-            mbar_arrive_expect_tx(full_a(s), kATileBytes);
-            tma_load_2d(a_tile(s, 0), &tmap_a, kb * kGroup, it.m * kBlockRows, full_a(s));
+            mbar_arrive_expect_tx(full_w(s), (uint32_t)C::kWStage);
+            tma_load_3d(dst, &maps.a, 0, it.m * kBlockRows, kb0, full_w(s));
           }
         }
-        if (!ok) break;
       }
     }
   } else if (warp == kWarpB) {
     // ------------------------------------------------------------ activation (B) producer
-    // Rows of the tile: the padded rows up to n16 belong to the next tile or lie beyond the
-    // tensor (zero fill); their accumulator columns are never read.
+    // One copy per plane brings n16 rows x kS K blocks, laid out [K block][row][64 values]; rows
+    // past the tile's end belong to the next tile or lie beyond the tensor (zero fill) and their
+    // accumulator columns are never read.
     if (lane == 0) {
-      uint32_t g = 0;
+      uint32_t gb = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
         const Item it = decode_item<MODE>(p, item, n_routed);
-        for (int kb = 0; kb < KB; ++kb, ++g) {
-          const int sb = g % C::kStagesB;
-          if (!(ok = mbar_wait(empty_b(sb), ((g / C::kStagesB) & 1) ^ 1, s_abort))) break;
-          mbar_arrive_expect_tx(full_b(sb), (uint32_t)(C::kNumB * it.n16 * 128));
-          int row = 0;
+        const CUtensorMap* map = &maps.rows[it.n16 / 16 - 1];
+        for (int kb0 = 0; kb0 < KB; kb0 += C::kS, ++gb) {
+          const int s = gb % C::kStagesB;
+          if (!(ok = mbar_wait(empty_b(s), ((gb / C::kStagesB) & 1) ^ 1, s_abort))) break;
+          mbar_arrive_expect_tx(full_b(s), (uint32_t)(C::kNumB * C::kS * it.n16 * 128));
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int h = 128 >> i;
-            if (it.n16 - row >= h) {
-#pragma unroll
-              for (int plane = 0; plane < C::kNumB; ++plane)
-                tma_load_2d(b_tile(sb, plane) + row * 128, &maps_b.box[i], kb * kGroup,
-                            plane * p.hidden_rows + it.row0 + row, full_b(sb));
-              row += h;
-            }
-          }
+          for (int plane = 0; plane < C::kNumB; ++plane)
+            tma_load_3d(b_stage(s) + plane * S::kPlaneBytes, map, 0, plane * p.hidden_rows + it.row0, kb0, full_b(s));
         }
       }
     }
-  } else if (warp == kWarpMMA) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      uint32_t g = 0;
+  } else if (warp == kWarpMMA || warp == kWarpMMA2) {
+    // ------------------------------------------------------------ MMA issuers
+    // Issuer i accumulates gate (i = 0) or up (i = 1) rows, or the products of the leading (i = 0)
+    // or remainder (i = 1) fp16 plane of the hidden rows, into columns i * kRows of the buffer.
+    // The whole warp runs the loop (uniform operands); one elected lane issues each instruction.
+    const int issuer = warp == kWarpMMA ? 0 : 1;
+    if (issuer < C::kIssuers) {
+      uint32_t g = 0, gb = 0, gw = 0;
       int n = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++n) {
         const Item it = decode_item<MODE>(p, item, n_routed);
         const int buf = n & 1;
-        if (!(ok = mbar_wait(acc_empty(buf), ((n >> 1) & 1) ^ 1, s_abort))) break;
+        if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(acc_empty(buf), ((n >> 1) & 1) ^ 1, s_abort)))) break;
         tc_fence_after();
         const uint32_t idesc = idesc_f16(kBlockRows, it.n16, C::kFp16);
-        const uint32_t acc = tmem_base + buf * S::kAccCols;
-        for (int kb = 0; kb < KB; ++kb, ++g) {
-          const int sa = g % C::kStagesA, sb = g % C::kStagesB;
-          ok = mbar_wait(full_a(sa), (g / C::kStagesA) & 1, s_abort) &&
-               mbar_wait(full_b(sb), (g / C::kStagesB) & 1, s_abort);
+        const uint32_t acc = tmem_base + buf * S::kAccCols + issuer * C::kRows;
+        const int a = C::kNumA == 2 ? issuer : 0, b = C::kNumB == 2 ? issuer : 0;
+        for (int kb0 = 0; kb0 < KB && ok; kb0 += C::kS, ++gb) {
+          const int nk = min(C::kS, KB - kb0);
+          const int sb = gb % C::kStagesB, sw = gw % max(C::kStagesW, 1);
+          ok = __all_sync(0xFFFFFFFFu, mbar_wait(full_b(sb), (gb / C::kStagesB) & 1, s_abort) &&
+                                           (C::kQ4 || mbar_wait(full_w(sw), (gw / C::kStagesW) & 1, s_abort)));
           if (!ok) break;
-          tc_fence_after();
-#pragma unroll
-          for (int ks = 0; ks < kGroup / 16; ++ks) {
-#pragma unroll
-            for (int b = 0; b < C::kNumB; ++b) {
-              const uint64_t bdesc = sw128_desc(b_tile(sb, b) + ks * 32);
-#pragma unroll
-              for (int a = 0; a < C::kNumA; ++a)
-                umma_f16_ss(acc + a * C::kRows, sw128_desc(a_tile(sa, a) + ks * 32), bdesc, idesc,
-                            (kb | ks | b) != 0);
+          const uint32_t bplane = b_stage(sb) + b * S::kPlaneBytes;
+          for (int j = 0; j < nk; ++j, ++g) {
+            const int sa = C::kQ4 ? (int)(g % C::kStagesA) : 0;
+            if constexpr (C::kQ4) {
+              if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(full_a(sa), (g / C::kStagesA) & 1, s_abort)))) break;
             }
+            tc_fence_after();
+            const uint32_t btile = bplane + j * it.n16 * 128;  // [K block][n16 rows][128 bytes]
+#pragma unroll
+            for (int ks = 0; ks < kGroup / 16; ++ks) {
+              const uint64_t bdesc = sw128_desc(btile + ks * 32);
+              const uint32_t accumulate = ((kb0 + j) | ks) != 0;
+              if constexpr (C::kQ4)
+                umma_f16_ts_elect(acc, a_tmem(tmem_base, sa, a) + ks * 8, bdesc, idesc, accumulate);
+              else
+                umma_f16_ss_elect(acc, sw128_desc(smem_u32(w_stage(sw)) + j * kATileBytes + ks * 32), bdesc, idesc,
+                                  accumulate);
+            }
+            if constexpr (C::kQ4) umma_commit_elect(empty_a(sa));
           }
-          umma_commit(empty_a(sa));
-          umma_commit(empty_b(sb));
+          if (!ok) break;
+          umma_commit_elect(empty_b(sb));
+          if constexpr (!C::kQ4) {
+            umma_commit_elect(empty_w(sw));
+            ++gw;
+          }
         }
-        if (ok) umma_commit(acc_full(buf));
+        if (ok) umma_commit_elect(acc_full(buf));
       }
     }
   } else if (warp < kWarpEpi0) {
     // ------------------------------------------------------------ dequant (Q4 modes)
-    if constexpr (MODE != kModeRouter) {
-      const int t = threadIdx.x - kWarpDq0 * 32;  // 0..255
-      uint32_t g = 0;
+    // Warp -> (TMEM lane quadrant, part): gate/up parts are the two matrices (a thread writes
+    // one row's 64 values, 32 columns); the down part is the K half (16 columns).
+    if constexpr (C::kQ4) {
+      const int quad = warp & 3, part = (warp - kWarpDq0) >> 2;
+      const int r = quad * 32 + lane;  // weight row within the 128-row block
+      const uint32_t lanes = (uint32_t)(quad * 32) << 16;
+      uint32_t g = 0, gw = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-        for (int kb = 0; kb < KB; ++kb, ++g) {
-          const int sw = g % C::kStagesW, sa = g % C::kStagesA;
-          ok = mbar_wait(full_w(sw), (g / C::kStagesW) & 1, s_abort) &&
-               mbar_wait(empty_a(sa), ((g / C::kStagesA) & 1) ^ 1, s_abort);
-          if (!ok) break;
-          if (MODE == kModeGateUp) {
-            // thread = (matrix, row): the row's 8 words -> 8 swizzled 16-byte chunks
-            const int mat = t >> 7, r = t & 127, rr = r & (kQuarterRows - 1);
-            const uint8_t* src = w_tile(sw) + (r / kQuarterRows) * kGUQuarter + mat * kGUMat;
-            const uint4 c0 = *reinterpret_cast<const uint4*>(src + rr * 16);
-            const uint4 c1 = *reinterpret_cast<const uint4*>(src + kQuarterRows * 16 + rr * 16);
+        for (int kb0 = 0; kb0 < KB && ok; kb0 += C::kS, ++gw) {
+          const int nk = min(C::kS, KB - kb0);
+          const int sw = gw % C::kStagesW;
+          // tcgen05.st is warp-collective: every lane takes the same exit on an abort
+          if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(full_w(sw), (gw / C::kStagesW) & 1, s_abort)))) break;
+          const uint8_t* ws = w_stage(sw);
+          for (int j = 0; j < nk; ++j, ++g) {
+            const int sa = g % C::kStagesA;
+            constexpr int kWords = MODE == kModeGateUp ? 8 : 4;
+            uint32_t words[kWords], sbw;
+            if constexpr (MODE == kModeGateUp) {
+              const uint8_t* src = ws + (quad * C::kS + j) * kGUQuarter + part * kGUMat;
+              const uint4 c0 = *reinterpret_cast<const uint4*>(src + lane * 16);
+              const uint4 c1 = *reinterpret_cast<const uint4*>(src + kQuarterRows * 16 + lane * 16);
+              sbw = *reinterpret_cast<const uint32_t*>(src + 2 * kQuarterRows * 16 + lane * 4);
+              words[0] = c0.x, words[1] = c0.y, words[2] = c0.z, words[3] = c0.w;
+              words[4] = c1.x, words[5] = c1.y, words[6] = c1.z, words[7] = c1.w;
+            } else {
+              const uint4 cw = *reinterpret_cast<const uint4*>(ws + (2 * j + part) * kHalfBytes + r * 16);
+              sbw = *reinterpret_cast<const uint32_t*>(ws + 2 * C::kS * kHalfBytes + j * kSBBytes + r * 4);
+              words[0] = cw.x, words[1] = cw.y, words[2] = cw.z, words[3] = cw.w;
+            }
+            if (j == nk - 1) mbar_arrive(empty_w(sw));  // the stage's codes are all in registers
+            if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(empty_a(sa), ((g / C::kStagesA) & 1) ^ 1, s_abort)))) break;
+            tc_fence_after();
             __half2 s2, b2;
-            scale_bias(*reinterpret_cast<const uint32_t*>(src + 2 * kQuarterRows * 16 + rr * 4), s2, b2);
-            const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-            uint8_t* arow = smem + (a_tile(sa, mat) - base) + r * 128;
+            scale_bias(sbw, s2, b2);
+            const uint32_t dst = a_tmem(tmem_base, sa, MODE == kModeGateUp ? part : 0) + lanes +
+                                 (MODE == kModeGateUp ? 0 : part * 16);
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-              *reinterpret_cast<uint4*>(arow + ((c ^ (r & 7)) << 4)) = dequant8(words[c], s2, b2);
-          } else {
-            // thread = (row, half): the 4 words of one 32-column half
-            const int r = t & 127, h = t >> 7;
-            const uint8_t* src = w_tile(sw);
-            const uint4 cw = *reinterpret_cast<const uint4*>(src + h * kHalfBytes + r * 16);
-            __half2 s2, b2;
-            scale_bias(*reinterpret_cast<const uint32_t*>(src + kCodeBytes + r * 4), s2, b2);
-            const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
-            uint8_t* arow = smem + (a_tile(sa, 0) - base) + r * 128;
+            for (int h = 0; h < kWords / 4; ++h) {
+              uint32_t v[16];
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-              *reinterpret_cast<uint4*>(arow + (((4 * h + c) ^ (r & 7)) << 4)) = dequant8(words[c], s2, b2);
+              for (int c = 0; c < 4; ++c) {
+                const uint4 o = dequant8(words[4 * h + c], s2, b2);
+                v[4 * c] = o.x, v[4 * c + 1] = o.y, v[4 * c + 2] = o.z, v[4 * c + 3] = o.w;
+              }
+              tmem_st16(dst + 16 * h, v);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(full_a(sa));
           }
-          fence_proxy_async_smem();
-          mbar_arrive(full_a(sa));
-          mbar_arrive(empty_w(sw));
         }
       }
     }
@@ -390,14 +430,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
       }
-      if (!mbar_wait(acc_full(buf), (n >> 1) & 1, s_abort)) break;
+      // tcgen05.ld is warp-collective: every lane takes the same exit on an abort
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(acc_full(buf), (n >> 1) & 1, s_abort))) break;
       tc_fence_after();
       const int orow = it.m * kBlockRows + q * 32 + lane;  // output row (feature / expert)
       const uint32_t taddr = tmem_base + lane_addr + buf * S::kAccCols;
       for (int j0 = 0; j0 < it.n16; j0 += 16) {
         uint32_t acc0[16], acc1[16];
         tmem_ld16(taddr + j0, acc0);
-        if (C::kNumA == 2) tmem_ld16(taddr + C::kRows + j0, acc1);
+        if (C::kIssuers == 2) tmem_ld16(taddr + C::kRows + j0, acc1);
         tmem_wait_ld();
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) {
@@ -405,8 +446,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j >= it.nrows) break;
           const float v0 = __uint_as_float(acc0[jj]);
           if (MODE == kModeGateUp) {
+            // SiLU(gate) * up; the exponent is clamped so 1 + e^-g stays finite (SiLU(-80) ~ -1e-33)
             const float u = __uint_as_float(acc1[jj]);
-            const float h = v0 / (1.f + expf(-v0)) * u;
+            const float h = __fdividef(v0, 1.f + __expf(-fmaxf(v0, -80.f))) * u;
             const __half hi = __float2half_rn(h);
             const __half lo = __float2half_rn(h - __half2float(hi));
             over |= !(fabsf(h) <= 65504.f);
@@ -414,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             p.hidden[o] = __half_as_ushort(hi);
             p.hidden[o + (size_t)p.hidden_rows * p.inter] = __half_as_ushort(lo);
           } else if (MODE == kModeDown) {
-            atomicAdd(p.yacc + (size_t)tok[j] * p.d + orow, v0 * wgt[j]);
+            atomicAdd(p.yacc + (size_t)tok[j] * p.d + orow, (v0 + __uint_as_float(acc1[jj])) * wgt[j]);
           } else {
             if (orow < p.E)
               p.logits[(size_t)(it.r0 + j) * p.E + orow] = v0 + (p.router_bias ? p.router_bias[orow] : 0.f);
@@ -450,13 +492,12 @@ int num_sms() {
 }
 
 template <int MODE>
-cudaError_t launch_mode(const GemmParams& p, const RowMaps* tb, const CUtensorMap* ta, int max_items,
-                        cudaStream_t s) {
+cudaError_t launch_mode(const GemmParams& p, const GemmMaps* maps, int max_items, cudaStream_t s) {
   static cudaError_t attr = cudaFuncSetAttribute(moe_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  Smem<MODE>::alloc);
   if (attr != cudaSuccess) return attr;
   const int grid = max_items < num_sms() ? max_items : num_sms();  // persistent: one CTA per SM
-  moe_gemm_kernel<MODE><<<grid, kThreads, Smem<MODE>::alloc, s>>>(p, *tb, *ta);
+  moe_gemm_kernel<MODE><<<grid, kThreads, Smem<MODE>::alloc, s>>>(p, *maps);
   return cudaGetLastError();
 }
 
@@ -464,14 +505,17 @@ cudaError_t launch_mode(const GemmParams& p, const RowMaps* tb, const CUtensorMa
 
 // `grid` is an upper bound on the number of work items; the persistent grid is at most one CTA
 // per SM, and each CTA reads the actual work list size on the device.
-cudaError_t launch_gemm(int mode, const GemmParams& p, const RowMaps* tmap_b, const CUtensorMap* tmap_a, int grid,
-                        cudaStream_t s) {
+cudaError_t launch_gemm(int mode, const GemmParams& p, const GemmMaps* maps, int grid, cudaStream_t s) {
   if (grid <= 0) return cudaSuccess;
   switch (mode) {
-    case kModeRouter: return launch_mode<kModeRouter>(p, tmap_b, tmap_a, grid, s);
-    case kModeGateUp: return launch_mode<kModeGateUp>(p, tmap_b, tmap_a, grid, s);
-    default: return launch_mode<kModeDown>(p, tmap_b, tmap_a, grid, s);
+    case kModeRouter: return launch_mode<kModeRouter>(p, maps, grid, s);
+    case kModeGateUp: return launch_mode<kModeGateUp>(p, maps, grid, s);
+    default: return launch_mode<kModeDown>(p, maps, grid, s);
   }
+}
+
+int gemm_kb_per_stage(int mode) {
+  return mode == kModeRouter ? Cfg<kModeRouter>::kS : mode == kModeGateUp ? Cfg<kModeGateUp>::kS : Cfg<kModeDown>::kS;
 }
 
 int router_tile_rows() { return kRouterRows; }
