@@ -25,13 +25,15 @@
 //                mode: bf16 router weight tiles, which the MMA reads from shared memory directly)
 //   warp 1       activation producer: the tile's contiguous rows (expert-sorted fp16 x, hidden
 //                rows, or token rows) for kS K blocks in one 3-D tensor copy per operand plane
-//   warps 2, 15  MMA issuers (whole warp runs the loop, one elected lane issues); warp 2 also
+//   warps 2, 11  MMA issuers (whole warp runs the loop, one elected lane issues); warp 2 also
 //                owns the TMEM allocation
 //   warps 3-10   dequantize nibbles into fp16 A tiles in tensor memory (each warp writes the 32
 //                TMEM lanes its index may access)
-//   warps 11-14  epilogue from one of two accumulator buffers while the next tile accumulates:
-//                SwiGLU -> hidden rows (gate/up), routing weight x accumulator -> fp32 red.add
-//                into the token's output row (down), or logits + bias (router)
+//   warps 12-19  epilogue (two warps per TMEM lane quadrant, alternate 16-column chunks) from
+//                one of two accumulator buffers while the next tile accumulates: SwiGLU ->
+//                hidden rows (gate/up), routing weight x accumulator -> fp32 red.add into the
+//                token's output row (down), or logits + bias (router); eight warps keep enough
+//                reductions in flight
 // Every mbarrier wait is bounded; a timeout raises a CTA-wide abort flag, every role leaves its
 // loop, TMEM is freed and MOE_ERR_DEVICE_TIMEOUT is recorded.
 #include <cuda_bf16.h>
@@ -45,11 +47,11 @@ namespace {
 
 constexpr int kRouterRows = 64;    // token rows per router tile
 constexpr int kWarpW = 0, kWarpB = 1, kWarpMMA = 2, kWarpDq0 = 3, kNumDqWarps = 8;
-constexpr int kWarpEpi0 = kWarpDq0 + kNumDqWarps, kNumEpiWarps = 4;
-constexpr int kWarpMMA2 = kWarpEpi0 + kNumEpiWarps;        // second MMA issuer
-constexpr int kThreads = (kWarpMMA2 + 1) * 32;             // 512
+constexpr int kWarpMMA2 = kWarpDq0 + kNumDqWarps;          // second MMA issuer (warp 11)
+constexpr int kWarpEpi0 = kWarpMMA2 + 1, kNumEpiWarps = 8;  // warps 12-19
+constexpr int kThreads = (kWarpEpi0 + kNumEpiWarps) * 32;  // 640
 constexpr int kDqThreads = kNumDqWarps * 32;               // 256
-constexpr int kEpiThreads = kNumEpiWarps * 32;             // 128
+constexpr int kEpiThreads = kNumEpiWarps * 32;             // 256
 constexpr int kATileBytes = kBlockRows * 128;              // 128 rows x 64 16-bit values
 
 // kNumA: weight operands per K step (gate and up share the B tile); kNumB: B operands per K step
@@ -407,7 +409,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    static_assert(kWarpEpi0 % 4 == 0 && kNumEpiWarps == 8, "two epilogue warps per lane quadrant");
     const int q = warp & 3;                          // TMEM lane quadrant this warp may access
+    const int half = (warp - kWarpEpi0) >> 2;        // this warp takes 16-column chunks half, half+2, ...
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
     bool over = false;
     int n = 0;
@@ -419,6 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (MODE == kModeDown) {  // this warp's (token, routing weight) list, read before the wait
         __syncwarp();
         for (int j = lane; j < it.nrows; j += 32) {
+          if (((j >> 4) & 1) != half) continue;    // only the rows of this warp's chunks
           if (it.shared) {
             tok[j] = it.r0 + j;
             wgt[j] = 1.f;
@@ -435,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int orow = it.m * kBlockRows + q * 32 + lane;  // output row (feature / expert)
       const uint32_t taddr = tmem_base + lane_addr + buf * S::kAccCols;
-      for (int j0 = 0; j0 < it.n16; j0 += 16) {
+      for (int j0 = 16 * half; j0 < it.n16; j0 += 32) {
         uint32_t acc0[16], acc1[16];
         tmem_ld16(taddr + j0, acc0);
         if (C::kIssuers == 2) tmem_ld16(taddr + C::kRows + j0, acc1);
