@@ -145,6 +145,7 @@ int run_route(const moe_dims& d, const float* logits, int T, const Ws& w, float*
   p.perm = w.at<int32_t>(w.L.perm);
   p.inv_perm = w.at<int32_t>(w.L.inv_perm);
   p.tile_map = w.at<int32_t>(w.L.tile_map);
+  p.tile_row0 = w.at<int32_t>(w.L.tile_row0);
   p.n_tiles = w.at<int32_t>(w.L.n_tiles);
   p.yacc = yacc;
   p.x = x;
@@ -286,6 +287,7 @@ int moe_prefill_timed(const moe_layer* layer, const uint16_t* x, int32_t T, uint
   p.packed = static_cast<const uint8_t*>(layer->packed);
   p.expert_stride = P.expert_stride;
   p.tile_map = w.at<int32_t>(w.L.tile_map);
+  p.tile_row0 = w.at<int32_t>(w.L.tile_row0);
   p.n_tiles = w.at<int32_t>(w.L.n_tiles);
   p.offsets = w.at<int32_t>(w.L.offsets);
   p.perm = w.at<int32_t>(w.L.perm);

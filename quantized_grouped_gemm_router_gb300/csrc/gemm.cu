@@ -111,17 +111,23 @@ struct Smem {
   static_assert(C::kWStage % 1024 == 0 && kPlaneBytes % 1024 == 0, "stage alignment");
 };
 
-// 8 packed codes (one word, nibble order of the packed layout) -> 8 fp16 weights
-// w = scale * q + bias as one fused multiply-add rounded once to fp16 (exact whenever the value
-// has at most 11 significant bits, e.g. bias = -8 * scale).
+// 8 packed codes (one word, nibble order of the packed layout) -> 8 fp16 weights, pairs of
+// columns (2i, 2i+1) = nibbles (i, i+4). Integer ops issue at half the fp16x2 rate, so the
+// fields are taken where they lie: nibbles 0/4 sit in mantissa bits [3:0] of 1024.0 and nibbles
+// 1/5 in bits [7:4] of 64.0 (ulp 1/16), then one byte swap brings nibbles 2/6 and 3/7 to the
+// same places: 1 PRMT + 4 LOP3 per word. Each pair becomes (base + q) exactly, base is
+// subtracted exactly, and w = scale * q + bias is one fused multiply-add rounded once to fp16
+// (exact whenever the value has at most 11 significant bits, e.g. bias = -8 * scale).
 __device__ __forceinline__ uint4 dequant8(uint32_t w, __half2 s2, __half2 b2) {
   const __half2 k1024 = __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400));
+  const __half2 k64 = __halves2half2(__ushort_as_half(0x5400), __ushort_as_half(0x5400));
+  const uint32_t sw = __byte_perm(w, 0, 0x2301);  // swap the bytes inside each 16-bit half
+  uint32_t t[4] = {(w & 0x000F000Fu) | 0x64006400u, (w & 0x00F000F0u) | 0x54005400u,
+                   (sw & 0x000F000Fu) | 0x64006400u, (sw & 0x00F000F0u) | 0x54005400u};
   uint32_t o[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    uint32_t t = ((w >> (4 * i)) & 0x000F000Fu) | 0x64006400u;  // fp16 pair (1024 + q)
-    __half2 v = *reinterpret_cast<__half2*>(&t);
-    v = __hsub2(v, k1024);                                        // exact: q
+    __half2 v = __hsub2(*reinterpret_cast<__half2*>(&t[i]), (i & 1) ? k64 : k1024);  // exact: q
     v = __hfma2(v, s2, b2);
     o[i] = *reinterpret_cast<uint32_t*>(&v);
   }
@@ -158,7 +164,7 @@ __device__ __forceinline__ Item decode_item(const GemmParams& p, int item, int n
     it.expert = p.tile_map[3 * tile];
     it.r0 = p.tile_map[3 * tile + 1];
     it.nrows = p.tile_map[3 * tile + 2];
-    it.row0 = p.offsets[it.expert] + it.r0;
+    it.row0 = p.tile_row0[tile];  // no dependent load: the router stored offsets[expert] + r0
   } else {
     it.r0 = (tile - n_routed) * kTileRows;
     it.expert = p.E;
@@ -249,8 +255,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t gw = 0;  // running weight-stage counter across this CTA's items
       bool ok = true;
+      Item nxt = decode_item<MODE>(p, blockIdx.x, n_routed);
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-        const Item it = decode_item<MODE>(p, item, n_routed);
+        const Item it = nxt;
+        if (item + (int)gridDim.x < n_items) nxt = decode_item<MODE>(p, item + gridDim.x, n_routed);
         const uint8_t* ebase = p.packed + (size_t)it.expert * p.expert_stride + p.region_offset;
         for (int kb0 = 0; kb0 < KB; kb0 += C::kS, ++gw) {
           const int s = gw % C::kStagesW;
@@ -283,8 +291,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t gb = 0;
       bool ok = true;
+      Item nxt = decode_item<MODE>(p, blockIdx.x, n_routed);
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-        const Item it = decode_item<MODE>(p, item, n_routed);
+        const Item it = nxt;
+        if (item + (int)gridDim.x < n_items) nxt = decode_item<MODE>(p, item + gridDim.x, n_routed);
         const CUtensorMap* map = &maps.rows[it.n16 / 16 - 1];
         for (int kb0 = 0; kb0 < KB; kb0 += C::kS, ++gb) {
           const int s = gb % C::kStagesB;
@@ -306,8 +316,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t g = 0, gb = 0, gw = 0;
       int n = 0;
       bool ok = true;
+      Item nxt = decode_item<MODE>(p, blockIdx.x, n_routed);
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++n) {
-        const Item it = decode_item<MODE>(p, item, n_routed);
+        const Item it = nxt;
+        if (item + (int)gridDim.x < n_items) nxt = decode_item<MODE>(p, item + gridDim.x, n_routed);
         const int buf = n & 1;
         if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(acc_empty(buf), ((n >> 1) & 1) ^ 1, s_abort)))) break;
         tc_fence_after();
@@ -415,8 +427,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
     bool over = false;
     int n = 0;
+    Item nxt = decode_item<MODE>(p, blockIdx.x, n_routed);
     for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++n) {
-      const Item it = decode_item<MODE>(p, item, n_routed);
+      const Item it = nxt;
+      if (item + (int)gridDim.x < n_items) nxt = decode_item<MODE>(p, item + gridDim.x, n_routed);
       const int buf = n & 1;
       int32_t* tok = s_tok + (warp - kWarpEpi0) * S::kListRows;
       float* wgt = s_wgt + (warp - kWarpEpi0) * S::kListRows;

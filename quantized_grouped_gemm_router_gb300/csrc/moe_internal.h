@@ -90,7 +90,7 @@ static_assert(sizeof(WsHeader) == 256, "header size");
 
 struct WsLayout {
   size_t header, logits, topk_idx, topk_w, chunk_counts, chunk_base, counts, offsets, perm,
-      inv_perm, tile_map, n_tiles, x16, hidden, yacc, dec_part, total;
+      inv_perm, tile_map, tile_row0, n_tiles, x16, hidden, yacc, dec_part, total;
   int n_chunks, max_tiles;
 };
 
@@ -126,6 +126,7 @@ inline WsLayout ws_layout(const moe_dims& d, int T) {
   L.perm = take(A * 4);
   L.inv_perm = take(A * 4);
   L.tile_map = take((size_t)L.max_tiles * 3 * 4);
+  L.tile_row0 = take((size_t)L.max_tiles * 4);
   L.n_tiles = take(4);
   L.x16 = take((A + T) * (size_t)d.d * 2);             // fp16 x: A expert-sorted rows, then T token rows
   L.hidden = take(2 * (A + T) * (size_t)d.inter * 2);  // SwiGLU rows: fp16 leading part, fp16 remainder
@@ -152,6 +153,7 @@ struct RouteParams {
   int32_t* perm;         // [A]
   int32_t* inv_perm;     // [A]
   int32_t* tile_map;     // [max_tiles, 3]
+  int32_t* tile_row0;    // [max_tiles] sorted row of each tile's first row (offsets[expert] + row)
   int32_t* n_tiles;      // [1]
   float* yacc;           // [T, d] zeroed by the top-k kernel (NULL: skip)
   const uint16_t* x;     // [T, d] bf16 input (NULL: no conversion)
@@ -172,6 +174,7 @@ struct GemmParams {
   int k_blocks;               // input-column blocks of 64
   // routing
   const int32_t* tile_map;    // [max_tiles, 3]
+  const int32_t* tile_row0;   // [max_tiles]
   const int32_t* n_tiles;     // device count of routed tiles
   const int32_t* offsets;     // [E + 1]
   const int32_t* perm;        // [A]

@@ -152,6 +152,7 @@ __global__ void __launch_bounds__(kTopkThreads) route_hist_kernel(const RoutePar
         tm[0] = e;
         tm[1] = r * kTileRows;
         tm[2] = min(kTileRows, cnt[i] - r * kTileRows);
+        p.tile_row0[tl + r] = off + r * kTileRows;
       }
     }
     off += cnt[i];
