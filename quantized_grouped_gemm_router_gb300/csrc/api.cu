@@ -55,10 +55,25 @@ bool make_rows_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols
                 CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// rows[i]: boxes of 16 (i + 1) rows x kb column blocks (tiles of up to 96 rows).
+// rows[i]: boxes of 16 (i + 1) rows x kb column blocks (tiles of up to 192 rows).
 bool make_gemm_rows(GemmMaps* g, const void* ptr, uint64_t rows, uint64_t cols, uint32_t kb, bool fp16) {
-  for (int i = 0; i < 6; ++i)
+  for (int i = 0; i < 12; ++i)
     if (!make_rows_map(&g->rows[i], ptr, rows, cols, 16u * (i + 1), kb, fp16)) return false;
+  g->a = g->rows[0];
+  g->a2 = g->rows[0];
+  return true;
+}
+
+// Both fp16 planes of the hidden rows [2, rows, cols] as (64 columns, rows, plane, cols / 64):
+// one box brings a tile's leading and remainder rows for kb column blocks, [kb][plane][row][64].
+bool make_gemm_planes(GemmMaps* g, const void* ptr, uint64_t rows, uint64_t cols, uint32_t kb) {
+  for (int i = 0; i < 12; ++i) {
+    const cuuint64_t dims[4] = {64, rows, 2, cols / 64};
+    const cuuint64_t strides[3] = {cols * 2, rows * cols * 2, 128};
+    const cuuint32_t box[4] = {64, 16u * (i + 1), 2, kb};
+    if (!encode(&g->rows[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, ptr, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return false;
+  }
   g->a = g->rows[0];
   g->a2 = g->rows[0];
   return true;
@@ -162,9 +177,8 @@ int run_route(const moe_dims& d, const float* logits, int T, const Ws& w, float*
 int run_router_gemm(const moe_layer* L, const uint16_t* x, int T, const Ws& w, cudaStream_t s) {
   const moe_dims& d = L->dims;
   GemmMaps maps;
-  const uint32_t kb = gemm_kb_per_stage(kModeRouter);
-  if (!make_gemm_rows(&maps, x, T, d.d, kb, false) ||
-      !make_rows_map(&maps.a, L->router_w, d.n_experts, d.d, kBlockRows, kb, false))
+  if (!make_gemm_rows(&maps, x, T, d.d, gemm_kb_per_stage(kModeRouter), false) ||
+      !make_rows_map(&maps.a, L->router_w, d.n_experts, d.d, kBlockRows, gemm_kw_per_stage(kModeRouter), false))
     return MOE_ERR_CUDA;
   GemmParams p = {};
   p.k_blocks = d.d / kGroup;
@@ -280,8 +294,8 @@ int moe_prefill_timed(const moe_layer* layer, const uint16_t* x, int32_t T, uint
   // 3. gate|up grouped GEMM + SwiGLU -> hidden; 4. down grouped GEMM + weighted combine -> yacc
   GemmMaps x_maps, h_maps;
   if (!make_gemm_rows(&x_maps, w.at<uint16_t>(w.L.x16), (uint64_t)A + T, d.d, gemm_kb_per_stage(kModeGateUp), true) ||
-      !make_gemm_rows(&h_maps, hidden, 2 * ((uint64_t)A + T), d.inter, gemm_kb_per_stage(kModeDown), true) ||
-      !make_down_weight_maps(&h_maps, static_cast<const uint8_t*>(layer->packed), P, d, gemm_kb_per_stage(kModeDown)))
+      !make_gemm_planes(&h_maps, hidden, (uint64_t)A + T, d.inter, gemm_kb_per_stage(kModeDown)) ||
+      !make_down_weight_maps(&h_maps, static_cast<const uint8_t*>(layer->packed), P, d, gemm_kw_per_stage(kModeDown)))
     return MOE_ERR_CUDA;
   GemmParams p = {};
   p.packed = static_cast<const uint8_t*>(layer->packed);
@@ -304,7 +318,7 @@ int moe_prefill_timed(const moe_layer* layer, const uint16_t* x, int32_t T, uint
   const int tiles = w.L.max_tiles + (T + kTileRows - 1) / kTileRows;
 
   p.region_offset = 0;
-  p.m_tiles = d.inter / kBlockRows;
+  p.m_tiles = d.inter / gemm_out_rows(kModeGateUp);
   p.k_blocks = d.d / kGroup;
   if (record_event(events, 2, stream) != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_gemm(kModeGateUp, p, &x_maps, tiles * p.m_tiles, stream) != cudaSuccess) return MOE_ERR_CUDA;

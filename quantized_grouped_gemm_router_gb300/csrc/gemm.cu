@@ -7,33 +7,40 @@
 // projections fused with the gate activation, output projection fused with the routing scores
 // and the shared expert.
 //
-// GB300 design (swap-AB): the dequantized weight slab is MMA operand A (M = 128 output rows),
-// the expert's token rows are operand B (N = rows of the tile rounded up to 16, set per tile at
-// run time), so an expert with few rows still issues dense MMAs. Dequantized A tiles go from
-// registers straight into tensor memory (tcgen05.st) and the MMA reads A from there; shared
-// memory only carries the packed codes and the B rows.
+// GB300 design (swap-AB): the dequantized weight slab is MMA operand A (M = 128 rows), the
+// tile's token rows are operand B (N = rows of the tile rounded up to 16, up to 192, set per
+// tile at run time), so an expert with few rows still issues dense MMAs. Dequantized A tiles go
+// from registers straight into tensor memory (tcgen05.st) and the MMA reads A from there; shared
+// memory only carries the packed codes and the B rows. One accumulator per tile:
+//   gate/up: A stacks 64 gate rows over the same 64 features' up rows, so gate and up of a tile
+//            share one M=128 accumulator and a tile can be 192 rows with two accumulator
+//            buffers in TMEM (2 x 192 + 4 A tiles x 32 = 512 columns);
+//   down:    the hidden rows' leading and remainder fp16 planes accumulate into the same
+//            accumulator (two MMAs per K step).
+// Fewer, taller tiles mean each weight is dequantized fewer times per FLOP.
 //
-// Two GB300 facts shape the pipeline (measured on this part):
+// Three GB300 facts shape the pipeline (measured on this part):
 //   * a TMA copy costs a roughly fixed ~0.2-0.3 us of issue time however small it is, so every
 //     copy here moves several K steps at once (3-D / 4-D tensor maps, bulk copies of >= 9 KB);
-//   * one thread issues at most one tcgen05.mma per ~40-60 cycles, so tiles of < 200 rows need
-//     two issuing warps (each with its own accumulator) to keep the tensor core busy.
+//   * one thread issues at most one tcgen05.mma per ~40-60 cycles, so two warps issue, each
+//     into its own column range of the accumulator (the tile's rows split in two);
+//   * integer ALU ops issue at half the rate of fp16x2 ops; the dequant uses few of them.
 //
-// Persistent, warp-specialised CTAs (one per SM) walk the work items (block-map tile x 128
-// output rows) in a fixed stride; every ring keeps running across items:
-//   warp 0       weight producer: packed Q4 stages (kS K blocks) by bulk / tensor copies (router
-//                mode: bf16 router weight tiles, which the MMA reads from shared memory directly)
+// Persistent, warp-specialised CTAs (one per SM) walk the work items (block-map tile x output
+// row block) in a fixed stride; every ring keeps running across items:
+//   warp 0       weight producer: packed Q4 stages (kSW K blocks) by bulk / tensor copies
+//                (router mode: bf16 router weight tiles, which the MMA reads from shared memory)
 //   warp 1       activation producer: the tile's contiguous rows (expert-sorted fp16 x, hidden
-//                rows, or token rows) for kS K blocks in one 3-D tensor copy per operand plane
-//   warps 2, 11  MMA issuers (whole warp runs the loop, one elected lane issues); warp 2 also
-//                owns the TMEM allocation
+//                rows of both planes, or token rows) for kSB K blocks in one tensor copy
+//   warps 2, 11  MMA issuers (whole warp runs the loop, one elected lane issues), each for one
+//                half of the tile's rows; warp 2 also owns the TMEM allocation
 //   warps 3-10   dequantize nibbles into fp16 A tiles in tensor memory (each warp writes the 32
 //                TMEM lanes its index may access)
 //   warps 12-19  epilogue (two warps per TMEM lane quadrant, alternate 16-column chunks) from
 //                one of two accumulator buffers while the next tile accumulates: SwiGLU ->
-//                hidden rows (gate/up), routing weight x accumulator -> fp32 red.add into the
-//                token's output row (down), or logits + bias (router); eight warps keep enough
-//                reductions in flight
+//                hidden rows (gate/up; the up-lane warp hands its values to the gate-lane warp
+//                through shared memory), routing weight x accumulator -> fp32 red.add into the
+//                token's output row (down), or logits + bias (router)
 // Every mbarrier wait is bounded; a timeout raises a CTA-wide abort flag, every role leaves its
 // loop, TMEM is freed and MOE_ERR_DEVICE_TIMEOUT is recorded.
 #include <cuda_bf16.h>
@@ -54,29 +61,32 @@ constexpr int kDqThreads = kNumDqWarps * 32;               // 256
 constexpr int kEpiThreads = kNumEpiWarps * 32;             // 256
 constexpr int kATileBytes = kBlockRows * 128;              // 128 rows x 64 16-bit values
 
-// kNumA: weight operands per K step (gate and up share the B tile); kNumB: B operands per K step
-// (the down projection reads the hidden rows as two fp16 planes); kIssuers: MMA-issuing warps,
-// each with its own accumulator (gate / up, or leading / remainder plane); kS: K blocks per
-// weight and activation stage; kStagesW / kStagesB: stages of the weight and activation rings
-// (each kS K blocks); kStagesA: TMEM A tiles (one K block each); kWStage: bytes of one weight stage.
+// kIssuers: MMA-issuing warps (each takes a column range of the one accumulator); kSW / kSB: K
+// blocks per weight / activation stage; kStagesW / kStagesB: stages of the weight and activation
+// rings; kStagesA: TMEM A tiles (one K block each); kWStage: bytes of one weight stage;
+// kPlanes: B operand planes per K block (down: leading and remainder fp16 parts of the hidden
+// rows); kRows: maximum tile rows (MMA N); kMRows: output rows of one work item.
 template <int MODE>
 struct Cfg;
 template <>
 struct Cfg<kModeGateUp> {
-  static constexpr int kNumA = 2, kNumB = 1, kIssuers = 2, kS = 4, kStagesW = 3, kStagesB = 2, kStagesA = 2;
-  static constexpr int kRows = kTileRows, kWStage = 4 * kS * kGUQuarter;  // 4 row quarters x kS blocks
+  static constexpr int kIssuers = 2, kSW = 4, kSB = 2, kStagesW = 3, kStagesB = 3, kStagesA = 4, kPlanes = 1;
+  static constexpr int kRows = kTileRows, kMRows = 64;             // 64 features: gate rows over up rows
+  static constexpr int kWStage = 2 * kSW * kGUQuarter;            // two row quarters x kSW blocks
   static constexpr bool kFp16 = true, kQ4 = true;
 };
 template <>
 struct Cfg<kModeDown> {
-  static constexpr int kNumA = 1, kNumB = 2, kIssuers = 2, kS = 2, kStagesW = 4, kStagesB = 3, kStagesA = 4;
-  static constexpr int kRows = kTileRows, kWStage = kS * kBlockBytes;     // codes (2 kS halves), then kS sb
+  static constexpr int kIssuers = 2, kSW = 2, kSB = 2, kStagesW = 3, kStagesB = 2, kStagesA = 4, kPlanes = 2;
+  static constexpr int kRows = kTileRows, kMRows = kBlockRows;
+  static constexpr int kWStage = kSW * kBlockBytes;                // codes (2 kSW halves), then kSW sb
   static constexpr bool kFp16 = true, kQ4 = true;
 };
 template <>
 struct Cfg<kModeRouter> {
-  static constexpr int kNumA = 1, kNumB = 1, kIssuers = 1, kS = 4, kStagesW = 2, kStagesB = 2, kStagesA = 0;
-  static constexpr int kRows = kRouterRows, kWStage = kS * kATileBytes;  // bf16 A tiles, read by the MMA
+  static constexpr int kIssuers = 1, kSW = 4, kSB = 4, kStagesW = 2, kStagesB = 2, kStagesA = 0, kPlanes = 1;
+  static constexpr int kRows = kRouterRows, kMRows = kBlockRows;
+  static constexpr int kWStage = kSW * kATileBytes;                // bf16 A tiles, read by the MMA
   static constexpr bool kFp16 = false, kQ4 = false;
 };
 
@@ -84,31 +94,34 @@ constexpr int tmem_cols_for(int cols) {
   return cols <= 32 ? 32 : cols <= 64 ? 64 : cols <= 128 ? 128 : cols <= 256 ? 256 : 512;
 }
 
+constexpr int kXPairs = 4, kXSlots = 2;  // gate/up epilogue exchange: warp pairs x buffered chunks
+
 template <int MODE>
 struct Smem {
   using C = Cfg<MODE>;
-  static constexpr int kPlaneBytes = C::kS * C::kRows * 128;  // one operand plane of a B stage
-  static constexpr int kBStage = C::kNumB * kPlaneBytes;
-  static constexpr int kAccCols = C::kIssuers * C::kRows;     // one accumulator buffer
+  static constexpr int kBStage = C::kSB * C::kPlanes * C::kRows * 128;  // [kb][plane][rows][128 B]
+  static constexpr int kAccCols = C::kRows;                             // one accumulator buffer
   // TMEM columns: two accumulator buffers, then (Q4 modes) the A tiles, 32 columns per 128x64 tile
   static constexpr int kACol = 2 * kAccCols;
-  static constexpr int kTmemNeed = kACol + C::kStagesA * C::kNumA * 32;
+  static constexpr int kTmemNeed = kACol + C::kStagesA * 32;
   static constexpr int kTmemCols = tmem_cols_for(kTmemNeed);
   static_assert(kTmemNeed <= 512, "tensor memory budget");
-  // down projection: each epilogue warp keeps its own copy of the tile's (token, weight) list
-  static constexpr int kListRows = MODE == kModeDown ? C::kRows : 0;
+  // down: each epilogue warp keeps the (token, weight) list of its own chunks (half the rows)
+  static constexpr int kListRows = MODE == kModeDown ? C::kRows / 2 : 0;
+  static constexpr int kXBytes = MODE == kModeGateUp ? kXPairs * kXSlots * 16 * 32 * 4 : 0;
   static constexpr int w_off = 0;
   static constexpr int b_off = w_off + C::kStagesW * C::kWStage;
-  static constexpr int tok_off = b_off + C::kStagesB * kBStage;
+  static constexpr int x_off = b_off + C::kStagesB * kBStage;
+  static constexpr int tok_off = x_off + kXBytes;
   static constexpr int wgt_off = tok_off + kNumEpiWarps * kListRows * 4;
   static constexpr int bar_off = wgt_off + kNumEpiWarps * kListRows * 4;
-  // full/empty per ring stage, then acc_full[2], acc_empty[2]
-  static constexpr int n_bars = 2 * (C::kStagesW + C::kStagesA + C::kStagesB) + 4;
+  // full/empty per ring stage, acc_full[2], acc_empty[2], xfull/xempty[pairs][slots]
+  static constexpr int n_bars = 2 * (C::kStagesW + C::kStagesA + C::kStagesB) + 4 + 2 * kXPairs * kXSlots;
   static constexpr int misc_off = bar_off + n_bars * 8;
   static constexpr int bytes = misc_off + 16;
   static constexpr int alloc = bytes + 1024;  // slack for 1024-byte alignment of the base
   static_assert(alloc <= 232448, "shared memory budget");
-  static_assert(C::kWStage % 1024 == 0 && kPlaneBytes % 1024 == 0, "stage alignment");
+  static_assert(C::kWStage % 1024 == 0 && kBStage % 1024 == 0, "stage alignment");
 };
 
 // 8 packed codes (one word, nibble order of the packed layout) -> 8 fp16 weights, pairs of
@@ -142,8 +155,8 @@ __device__ __forceinline__ void scale_bias(uint32_t sbw, __half2& s2, __half2& b
   b2 = __halves2half2(bh, bh);
 }
 
-// One work item: a block-map tile (or a shared-expert / router row tile) x one 128-row block of
-// the output features.
+// One work item: a block-map tile (or a shared-expert / router row tile) x one block of output
+// rows (gate/up: 64 features, stacked gate over up; down / router: 128 rows).
 struct Item {
   int expert, r0, nrows, row0, m, n16;
   bool shared;
@@ -199,8 +212,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if ((int)blockIdx.x >= n_items) return;  // nothing for this CTA (uniform: before any set-up)
   const int KB = p.k_blocks;
 
-  int32_t* s_tok = reinterpret_cast<int32_t*>(smem + S::tok_off);  // [epilogue warp][kListRows]
-  float* s_wgt = reinterpret_cast<float*>(smem + S::wgt_off);      // [epilogue warp][kListRows]
   const uint32_t bars = base + S::bar_off;
   auto full_w = [&](int s) { return bars + 8u * s; };
   auto empty_w = [&](int s) { return bars + 8u * (C::kStagesW + s); };
@@ -211,11 +222,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t acc_bars = bars + 8u * (2 * (C::kStagesW + C::kStagesA + C::kStagesB));
   auto acc_full = [&](int b) { return acc_bars + 8u * b; };
   auto acc_empty = [&](int b) { return acc_bars + 8u * (2 + b); };
+  auto xfull = [&](int pr, int sl) { return acc_bars + 8u * (4 + pr * kXSlots + sl); };
+  auto xempty = [&](int pr, int sl) { return acc_bars + 8u * (4 + kXPairs * kXSlots + pr * kXSlots + sl); };
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + S::misc_off);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + S::misc_off + 4);
   auto w_stage = [&](int s) { return smem + S::w_off + s * C::kWStage; };
   auto b_stage = [&](int s) { return base + S::b_off + s * S::kBStage; };
-  auto a_tmem = [&](uint32_t tbase, int stage, int which) { return tbase + S::kACol + (stage * C::kNumA + which) * 32; };
+  auto a_tmem = [&](uint32_t tbase, int stage) { return tbase + S::kACol + stage * 32; };
 
   // ---------------------------------------------------------------- set-up
   if (threadIdx.x == 0) {
@@ -235,6 +248,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(acc_full(b), C::kIssuers);
       mbar_init(acc_empty(b), kEpiThreads);
     }
+    for (int pr = 0; pr < kXPairs; ++pr)
+      for (int sl = 0; sl < kXSlots; ++sl) {
+        mbar_init(xfull(pr, sl), 32);
+        mbar_init(xempty(pr, sl), 32);
+      }
     *s_abort = 0;
     fence_barrier_init();
   }
@@ -242,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(s_tmem), S::kTmemCols);
     tmem_relinquish();
   }
-  if (warp == kWarpB && lane < 6) prefetch_tmap(&maps.rows[lane]);
+  if (warp == kWarpB && lane < 12) prefetch_tmap(&maps.rows[lane]);
   if (warp == kWarpW && lane == 0 && MODE != kModeGateUp) prefetch_tmap(&maps.a);
   if (warp == kWarpW && lane == 1 && MODE == kModeDown) prefetch_tmap(&maps.a2);
   tc_fence_before();
@@ -260,22 +278,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Item it = nxt;
         if (item + (int)gridDim.x < n_items) nxt = decode_item<MODE>(p, item + gridDim.x, n_routed);
         const uint8_t* ebase = p.packed + (size_t)it.expert * p.expert_stride + p.region_offset;
-        for (int kb0 = 0; kb0 < KB; kb0 += C::kS, ++gw) {
+        for (int kb0 = 0; kb0 < KB; kb0 += C::kSW, ++gw) {
           const int s = gw % C::kStagesW;
           if (!(ok = mbar_wait(empty_w(s), ((gw / C::kStagesW) & 1) ^ 1, s_abort))) break;
           const uint32_t dst = smem_u32(w_stage(s));
           if (MODE == kModeGateUp) {
-            // quarter q of the 128-row block: K blocks kb0.. are contiguous, 2304 bytes each
-            const int nk = min(C::kS, KB - kb0);
-            mbar_arrive_expect_tx(full_w(s), (uint32_t)(4 * nk * kGUQuarter));
-            for (int q = 0; q < 4; ++q)
-              tma_bulk_g2s(dst + q * C::kS * kGUQuarter, ebase + gu_offset(it.m, q, kb0, KB), nk * kGUQuarter,
+            // features 64h..64h+63 = quarters 2(h%2), 2(h%2)+1 of block h/2; K blocks kb0.. of a
+            // quarter are contiguous, 2304 bytes each (gate then up)
+            const int nk = min(C::kSW, KB - kb0), m = it.m >> 1, q0 = 2 * (it.m & 1);
+            mbar_arrive_expect_tx(full_w(s), (uint32_t)(2 * nk * kGUQuarter));
+            for (int qq = 0; qq < 2; ++qq)
+              tma_bulk_g2s(dst + qq * C::kSW * kGUQuarter, ebase + gu_offset(m, q0 + qq, kb0, KB), nk * kGUQuarter,
                            full_w(s));
           } else if (MODE == kModeDown) {
-            // codes of (K block, half) pieces kb0*2 .. kb0*2+2kS-1 of block m, then their scale/bias
+            // codes of (K block, half) pieces kb0*2 .. kb0*2+2kSW-1 of block m, then their scale/bias
             mbar_arrive_expect_tx(full_w(s), (uint32_t)C::kWStage);
             tma_load_4d(dst, &maps.a, 0, it.m, 2 * kb0, it.expert, full_w(s));
-            tma_load_4d(dst + 2 * C::kS * kHalfBytes, &maps.a2, 0, it.m, kb0, it.expert, full_w(s));
+            tma_load_4d(dst + 2 * C::kSW * kHalfBytes, &maps.a2, 0, it.m, kb0, it.expert, full_w(s));
           } else {
             mbar_arrive_expect_tx(full_w(s), (uint32_t)C::kWStage);
             tma_load_3d(dst, &maps.a, 0, it.m * kBlockRows, kb0, full_w(s));
@@ -285,9 +304,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kWarpB) {
     // ------------------------------------------------------------ activation (B) producer
-    // One copy per plane brings n16 rows x kS K blocks, laid out [K block][row][64 values]; rows
-    // past the tile's end belong to the next tile or lie beyond the tensor (zero fill) and their
-    // accumulator columns are never read.
+    // One copy brings n16 rows x kSB K blocks (x both planes), laid out [K block][plane][row][64
+    // values]; rows past the tile's end belong to the next tile or lie beyond the tensor (zero
+    // fill) and their accumulator columns are never read.
     if (lane == 0) {
       uint32_t gb = 0;
       bool ok = true;
@@ -296,21 +315,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Item it = nxt;
         if (item + (int)gridDim.x < n_items) nxt = decode_item<MODE>(p, item + gridDim.x, n_routed);
         const CUtensorMap* map = &maps.rows[it.n16 / 16 - 1];
-        for (int kb0 = 0; kb0 < KB; kb0 += C::kS, ++gb) {
+        for (int kb0 = 0; kb0 < KB; kb0 += C::kSB, ++gb) {
           const int s = gb % C::kStagesB;
           if (!(ok = mbar_wait(empty_b(s), ((gb / C::kStagesB) & 1) ^ 1, s_abort))) break;
-          mbar_arrive_expect_tx(full_b(s), (uint32_t)(C::kNumB * C::kS * it.n16 * 128));
-#pragma unroll
-          for (int plane = 0; plane < C::kNumB; ++plane)
-            tma_load_3d(b_stage(s) + plane * S::kPlaneBytes, map, 0, plane * p.hidden_rows + it.row0, kb0, full_b(s));
+          mbar_arrive_expect_tx(full_b(s), (uint32_t)(C::kSB * C::kPlanes * it.n16 * 128));
+          if (C::kPlanes == 2)
+            tma_load_4d(b_stage(s), map, 0, it.row0, 0, kb0, full_b(s));
+          else
+            tma_load_3d(b_stage(s), map, 0, it.row0, kb0, full_b(s));
         }
       }
     }
   } else if (warp == kWarpMMA || warp == kWarpMMA2) {
     // ------------------------------------------------------------ MMA issuers
-    // Issuer i accumulates gate (i = 0) or up (i = 1) rows, or the products of the leading (i = 0)
-    // or remainder (i = 1) fp16 plane of the hidden rows, into columns i * kRows of the buffer.
-    // The whole warp runs the loop (uniform operands); one elected lane issues each instruction.
+    // Issuer i owns accumulator columns [c0, c0 + n) = its half of the tile's rows (n may be 0 for
+    // a 16-row tile; the issuer then only keeps the barrier counts). The whole warp runs the loop
+    // (uniform operands); one elected lane issues each instruction.
     const int issuer = warp == kWarpMMA ? 0 : 1;
     if (issuer < C::kIssuers) {
       uint32_t g = 0, gb = 0, gw = 0;
@@ -323,95 +343,96 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int buf = n & 1;
         if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(acc_empty(buf), ((n >> 1) & 1) ^ 1, s_abort)))) break;
         tc_fence_after();
-        const uint32_t idesc = idesc_f16(kBlockRows, it.n16, C::kFp16);
-        const uint32_t acc = tmem_base + buf * S::kAccCols + issuer * C::kRows;
-        const int a = C::kNumA == 2 ? issuer : 0, b = C::kNumB == 2 ? issuer : 0;
-        for (int kb0 = 0; kb0 < KB && ok; kb0 += C::kS, ++gb) {
-          const int nk = min(C::kS, KB - kb0);
-          const int sb = gb % C::kStagesB, sw = gw % max(C::kStagesW, 1);
-          ok = __all_sync(0xFFFFFFFFu, mbar_wait(full_b(sb), (gb / C::kStagesB) & 1, s_abort) &&
-                                           (C::kQ4 || mbar_wait(full_w(sw), (gw / C::kStagesW) & 1, s_abort)));
-          if (!ok) break;
-          const uint32_t bplane = b_stage(sb) + b * S::kPlaneBytes;
-          for (int j = 0; j < nk; ++j, ++g) {
-            const int sa = C::kQ4 ? (int)(g % C::kStagesA) : 0;
+        const int half16 = C::kIssuers == 2 ? 16 * ((it.n16 / 16 + 1) / 2) : it.n16;
+        const int c0 = issuer == 0 ? 0 : half16, ncols = issuer == 0 ? half16 : it.n16 - half16;
+        const uint32_t idesc = idesc_f16(kBlockRows, ncols > 0 ? ncols : 16, C::kFp16);
+        const uint32_t acc = tmem_base + buf * S::kAccCols + c0;
+        int kb = 0;  // K block of this item
+        for (int s0 = 0; s0 < KB && ok; s0 += C::kSB, ++gb) {
+          const int nkb = min(C::kSB, KB - s0);
+          const int sb = gb % C::kStagesB;
+          if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(full_b(sb), (gb / C::kStagesB) & 1, s_abort)))) break;
+          for (int j = 0; j < nkb; ++j, ++kb, ++g) {
+            // weights of this K block: TMEM tile (Q4 modes) or a shared-memory tile of a stage
+            const int sa = C::kQ4 ? (int)(g % C::kStagesA) : 0, sw = C::kQ4 ? 0 : (int)(gw % C::kStagesW);
+            const int jw = C::kQ4 ? 0 : kb % C::kSW;
             if constexpr (C::kQ4) {
               if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(full_a(sa), (g / C::kStagesA) & 1, s_abort)))) break;
+            } else if (jw == 0) {
+              if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(full_w(sw), (gw / C::kStagesW) & 1, s_abort)))) break;
             }
             tc_fence_after();
-            const uint32_t btile = bplane + j * it.n16 * 128;  // [K block][n16 rows][128 bytes]
+            if (ncols > 0) {
 #pragma unroll
-            for (int ks = 0; ks < kGroup / 16; ++ks) {
-              const uint64_t bdesc = sw128_desc(btile + ks * 32);
-              const uint32_t accumulate = ((kb0 + j) | ks) != 0;
-              if constexpr (C::kQ4)
-                umma_f16_ts_elect(acc, a_tmem(tmem_base, sa, a) + ks * 8, bdesc, idesc, accumulate);
-              else
-                umma_f16_ss_elect(acc, sw128_desc(smem_u32(w_stage(sw)) + j * kATileBytes + ks * 32), bdesc, idesc,
-                                  accumulate);
+              for (int ks = 0; ks < kGroup / 16; ++ks) {
+#pragma unroll
+                for (int b = 0; b < C::kPlanes; ++b) {
+                  const uint32_t btile = b_stage(sb) + ((j * C::kPlanes + b) * it.n16 + c0) * 128;
+                  const uint64_t bdesc = sw128_desc(btile + ks * 32);
+                  const uint32_t accumulate = (kb | ks | b) != 0;
+                  if constexpr (C::kQ4)
+                    umma_f16_ts_elect(acc, a_tmem(tmem_base, sa) + ks * 8, bdesc, idesc, accumulate);
+                  else
+                    umma_f16_ss_elect(acc, sw128_desc(smem_u32(w_stage(sw)) + jw * kATileBytes + ks * 32), bdesc, idesc,
+                                      accumulate);
+                }
+              }
             }
-            if constexpr (C::kQ4) umma_commit_elect(empty_a(sa));
+            if constexpr (C::kQ4) {
+              umma_commit_elect(empty_a(sa));
+            } else if (jw == C::kSW - 1 || kb == KB - 1) {
+              umma_commit_elect(empty_w(sw));
+              ++gw;
+            }
           }
           if (!ok) break;
           umma_commit_elect(empty_b(sb));
-          if constexpr (!C::kQ4) {
-            umma_commit_elect(empty_w(sw));
-            ++gw;
-          }
         }
         if (ok) umma_commit_elect(acc_full(buf));
       }
     }
   } else if (warp < kWarpEpi0) {
     // ------------------------------------------------------------ dequant (Q4 modes)
-    // Warp -> (TMEM lane quadrant, part): gate/up parts are the two matrices (a thread writes
-    // one row's 64 values, 32 columns); the down part is the K half (16 columns).
+    // Warp -> (TMEM lane quadrant, K half): a thread writes 32 values (16 columns) of one A row.
+    // gate/up rows 0..63 are gate features, 64..127 the same features' up rows.
     if constexpr (C::kQ4) {
       const int quad = warp & 3, part = (warp - kWarpDq0) >> 2;
-      const int r = quad * 32 + lane;  // weight row within the 128-row block
+      const int r = quad * 32 + lane;  // A row
       const uint32_t lanes = (uint32_t)(quad * 32) << 16;
       uint32_t g = 0, gw = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-        for (int kb0 = 0; kb0 < KB && ok; kb0 += C::kS, ++gw) {
-          const int nk = min(C::kS, KB - kb0);
+        for (int kb0 = 0; kb0 < KB && ok; kb0 += C::kSW, ++gw) {
+          const int nk = min(C::kSW, KB - kb0);
           const int sw = gw % C::kStagesW;
           // tcgen05.st is warp-collective: every lane takes the same exit on an abort
           if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(full_w(sw), (gw / C::kStagesW) & 1, s_abort)))) break;
           const uint8_t* ws = w_stage(sw);
           for (int j = 0; j < nk; ++j, ++g) {
             const int sa = g % C::kStagesA;
-            constexpr int kWords = MODE == kModeGateUp ? 8 : 4;
-            uint32_t words[kWords], sbw;
+            uint4 cw;
+            uint32_t sbw;
             if constexpr (MODE == kModeGateUp) {
-              const uint8_t* src = ws + (quad * C::kS + j) * kGUQuarter + part * kGUMat;
-              const uint4 c0 = *reinterpret_cast<const uint4*>(src + lane * 16);
-              const uint4 c1 = *reinterpret_cast<const uint4*>(src + kQuarterRows * 16 + lane * 16);
+              const uint8_t* src = ws + ((quad & 1) * C::kSW + j) * kGUQuarter + (quad >> 1) * kGUMat;
+              cw = *reinterpret_cast<const uint4*>(src + part * kQuarterRows * 16 + lane * 16);
               sbw = *reinterpret_cast<const uint32_t*>(src + 2 * kQuarterRows * 16 + lane * 4);
-              words[0] = c0.x, words[1] = c0.y, words[2] = c0.z, words[3] = c0.w;
-              words[4] = c1.x, words[5] = c1.y, words[6] = c1.z, words[7] = c1.w;
             } else {
-              const uint4 cw = *reinterpret_cast<const uint4*>(ws + (2 * j + part) * kHalfBytes + r * 16);
-              sbw = *reinterpret_cast<const uint32_t*>(ws + 2 * C::kS * kHalfBytes + j * kSBBytes + r * 4);
-              words[0] = cw.x, words[1] = cw.y, words[2] = cw.z, words[3] = cw.w;
+              cw = *reinterpret_cast<const uint4*>(ws + (2 * j + part) * kHalfBytes + r * 16);
+              sbw = *reinterpret_cast<const uint32_t*>(ws + 2 * C::kSW * kHalfBytes + j * kSBBytes + r * 4);
             }
             if (j == nk - 1) mbar_arrive(empty_w(sw));  // the stage's codes are all in registers
             if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(empty_a(sa), ((g / C::kStagesA) & 1) ^ 1, s_abort)))) break;
             tc_fence_after();
             __half2 s2, b2;
             scale_bias(sbw, s2, b2);
-            const uint32_t dst = a_tmem(tmem_base, sa, MODE == kModeGateUp ? part : 0) + lanes +
-                                 (MODE == kModeGateUp ? 0 : part * 16);
+            const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+            uint32_t v[16];
 #pragma unroll
-            for (int h = 0; h < kWords / 4; ++h) {
-              uint32_t v[16];
-#pragma unroll
-              for (int c = 0; c < 4; ++c) {
-                const uint4 o = dequant8(words[4 * h + c], s2, b2);
-                v[4 * c] = o.x, v[4 * c + 1] = o.y, v[4 * c + 2] = o.z, v[4 * c + 3] = o.w;
-              }
-              tmem_st16(dst + 16 * h, v);
+            for (int c = 0; c < 4; ++c) {
+              const uint4 o = dequant8(words[c], s2, b2);
+              v[4 * c] = o.x, v[4 * c + 1] = o.y, v[4 * c + 2] = o.z, v[4 * c + 3] = o.w;
             }
+            tmem_st16(a_tmem(tmem_base, sa) + lanes + part * 16, v);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(full_a(sa));
@@ -425,63 +446,96 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;                          // TMEM lane quadrant this warp may access
     const int half = (warp - kWarpEpi0) >> 2;        // this warp takes 16-column chunks half, half+2, ...
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
-    bool over = false;
+    int32_t* tok = reinterpret_cast<int32_t*>(smem + S::tok_off) + (warp - kWarpEpi0) * S::kListRows;
+    float* wgt = reinterpret_cast<float*>(smem + S::wgt_off) + (warp - kWarpEpi0) * S::kListRows;
+    // gate/up: the gate-lane warp (quadrants 0, 1) and the up-lane warp (quadrants 2, 3) of the
+    // same features and chunks form pair `pr`; the up warp passes its 16 x 32 values through slot
+    // (u & 1) of the pair's exchange buffer, [value][lane] to avoid bank conflicts
+    const int pr = (q & 1) + 2 * half;
+    const bool gate_warp = q < 2;
+    float* xbuf = reinterpret_cast<float*>(smem + S::x_off) + pr * kXSlots * 16 * 32;
+    uint32_t u = 0;  // chunks exchanged so far by this pair
+    bool over = false, ok = true;
     int n = 0;
     Item nxt = decode_item<MODE>(p, blockIdx.x, n_routed);
-    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++n) {
+    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++n) {
       const Item it = nxt;
       if (item + (int)gridDim.x < n_items) nxt = decode_item<MODE>(p, item + gridDim.x, n_routed);
       const int buf = n & 1;
-      int32_t* tok = s_tok + (warp - kWarpEpi0) * S::kListRows;
-      float* wgt = s_wgt + (warp - kWarpEpi0) * S::kListRows;
       if (MODE == kModeDown) {  // this warp's (token, routing weight) list, read before the wait
         __syncwarp();
         for (int j = lane; j < it.nrows; j += 32) {
-          if (((j >> 4) & 1) != half) continue;    // only the rows of this warp's chunks
+          if (((j >> 4) & 1) != half) continue;       // only the rows of this warp's chunks
+          const int li = ((j >> 5) << 4) | (j & 15);   // position among this warp's rows
           if (it.shared) {
-            tok[j] = it.r0 + j;
-            wgt[j] = 1.f;
+            tok[li] = it.r0 + j;
+            wgt[li] = 1.f;
           } else {
             const int a = p.perm[it.row0 + j];
-            tok[j] = a / p.k;
-            wgt[j] = p.topk_w[a];
+            tok[li] = a / p.k;
+            wgt[li] = p.topk_w[a];
           }
         }
         __syncwarp();
       }
       // tcgen05.ld is warp-collective: every lane takes the same exit on an abort
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(acc_full(buf), (n >> 1) & 1, s_abort))) break;
+      if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(acc_full(buf), (n >> 1) & 1, s_abort)))) break;
       tc_fence_after();
-      const int orow = it.m * kBlockRows + q * 32 + lane;  // output row (feature / expert)
       const uint32_t taddr = tmem_base + lane_addr + buf * S::kAccCols;
-      for (int j0 = 16 * half; j0 < it.n16; j0 += 32) {
-        uint32_t acc0[16], acc1[16];
-        tmem_ld16(taddr + j0, acc0);
-        if (C::kIssuers == 2) tmem_ld16(taddr + C::kRows + j0, acc1);
+      for (int j0 = 16 * half; j0 < it.n16 && ok; j0 += 32) {
+        uint32_t acc[16];
+        tmem_ld16(taddr + j0, acc);
         tmem_wait_ld();
+        if (MODE == kModeGateUp) {
+          const int sl = u & 1;
+          float* xs = xbuf + sl * 16 * 32;
+          if (!gate_warp) {  // hand the up values to the gate warp
+            if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(xempty(pr, sl), ((u >> 1) & 1) ^ 1, s_abort)))) break;
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
-          const int j = j0 + jj;
-          if (j >= it.nrows) break;
-          const float v0 = __uint_as_float(acc0[jj]);
-          if (MODE == kModeGateUp) {
-            // SiLU(gate) * up; the exponent is clamped so 1 + e^-g stays finite (SiLU(-80) ~ -1e-33)
-            const float u = __uint_as_float(acc1[jj]);
-            const float h = __fdividef(v0, 1.f + __expf(-fmaxf(v0, -80.f))) * u;
-            const __half hi = __float2half_rn(h);
-            const __half lo = __float2half_rn(h - __half2float(hi));
-            over |= !(fabsf(h) <= 65504.f);
-            const size_t o = (size_t)(it.row0 + j) * p.inter + orow;
-            p.hidden[o] = __half_as_ushort(hi);
-            p.hidden[o + (size_t)p.hidden_rows * p.inter] = __half_as_ushort(lo);
-          } else if (MODE == kModeDown) {
-            atomicAdd(p.yacc + (size_t)tok[j] * p.d + orow, (v0 + __uint_as_float(acc1[jj])) * wgt[j]);
+            for (int jj = 0; jj < 16; ++jj) xs[jj * 32 + lane] = __uint_as_float(acc[jj]);
+            mbar_arrive(xfull(pr, sl));
           } else {
-            if (orow < p.E)
-              p.logits[(size_t)(it.r0 + j) * p.E + orow] = v0 + (p.router_bias ? p.router_bias[orow] : 0.f);
+            if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(xfull(pr, sl), (u >> 1) & 1, s_abort)))) break;
+            float up[16];
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) up[jj] = xs[jj * 32 + lane];
+            mbar_arrive(xempty(pr, sl));
+            const int f = it.m * 64 + (q & 1) * 32 + lane;  // feature
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              const int j = j0 + jj;
+              // SiLU(gate) * up; the exponent is clamped so 1 + e^-g stays finite (SiLU(-80) ~ -1e-33)
+              const float gv = __uint_as_float(acc[jj]);
+              const float h = __fdividef(gv, 1.f + __expf(-fmaxf(gv, -80.f))) * up[jj];
+              const __half hi = __float2half_rn(h);
+              const __half lo = __float2half_rn(h - __half2float(hi));
+              if (j < it.nrows) {
+                over |= !(fabsf(h) <= 65504.f);
+                const size_t o = (size_t)(it.row0 + j) * p.inter + f;
+                p.hidden[o] = __half_as_ushort(hi);
+                p.hidden[o + (size_t)p.hidden_rows * p.inter] = __half_as_ushort(lo);
+              }
+            }
+          }
+          ++u;
+        } else {
+          const int orow = it.m * kBlockRows + q * 32 + lane;  // output row (feature / expert)
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const int j = j0 + jj;
+            if (j < it.nrows) {
+              const float v = __uint_as_float(acc[jj]);
+              if (MODE == kModeDown) {
+                const int li = ((j >> 5) << 4) | jj;
+                atomicAdd(p.yacc + (size_t)tok[li] * p.d + orow, v * wgt[li]);
+              } else if (orow < p.E) {
+                p.logits[(size_t)(it.r0 + j) * p.E + orow] = v + (p.router_bias ? p.router_bias[orow] : 0.f);
+              }
+            }
           }
         }
       }
+      if (!ok) break;
       tc_fence_before();
       mbar_arrive(acc_empty(buf));  // the accumulator buffer is free again
     }
@@ -534,7 +588,16 @@ cudaError_t launch_gemm(int mode, const GemmParams& p, const GemmMaps* maps, int
 }
 
 int gemm_kb_per_stage(int mode) {
-  return mode == kModeRouter ? Cfg<kModeRouter>::kS : mode == kModeGateUp ? Cfg<kModeGateUp>::kS : Cfg<kModeDown>::kS;
+  return mode == kModeRouter ? Cfg<kModeRouter>::kSB : mode == kModeGateUp ? Cfg<kModeGateUp>::kSB : Cfg<kModeDown>::kSB;
+}
+
+int gemm_kw_per_stage(int mode) {
+  return mode == kModeRouter ? Cfg<kModeRouter>::kSW : mode == kModeGateUp ? Cfg<kModeGateUp>::kSW : Cfg<kModeDown>::kSW;
+}
+
+int gemm_out_rows(int mode) {
+  return mode == kModeRouter ? Cfg<kModeRouter>::kMRows : mode == kModeGateUp ? Cfg<kModeGateUp>::kMRows
+                                                                               : Cfg<kModeDown>::kMRows;
 }
 
 int router_tile_rows() { return kRouterRows; }

@@ -42,7 +42,7 @@ constexpr int kQuarterRows = 32;
 constexpr int kGUMat = 2 * kQuarterRows * 16 + kQuarterRows * 4;  // 1152: one matrix's quarter
 constexpr int kGUQuarter = 2 * kGUMat;                             // 2304: gate + up quarter
 constexpr int kSBBytes = kBlockRows * 4;                           // 512
-constexpr int kTileRows = 96;       // block-map tile height (max MMA N of the prefill GEMMs)
+constexpr int kTileRows = 192;      // block-map tile height (max MMA N of the prefill GEMMs)
 constexpr int kMaxTopK = 16;
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTokens = 65536;
@@ -209,19 +209,23 @@ struct DecodeParams {
 cudaError_t launch_pack(const moe_dims& d, const moe_q4_view* views, uint8_t* packed, cudaStream_t s);
 cudaError_t launch_route(const RouteParams& p, cudaStream_t s);
 // Tensor maps of the prefill GEMMs.
-//   rows.box[i]: a row-major [rows, cols] 16-bit operand seen as (64 columns, rows, cols / 64
-//                column blocks), 128-byte swizzle, box = 64 columns x 16 (i + 1) rows x kb_per
-//                column blocks: one copy brings a whole tile's rows for several K steps.
-//   a:  router mode: the bf16 router weight [E, d] in the same 3-D form (box 128 rows);
+//   rows[i]: the activation operand for tiles of 16 (i + 1) rows, box = 64 columns x 16 (i + 1)
+//            rows x kSB column blocks: gate/up and router see a row-major [rows, cols] 16-bit
+//            matrix as (64 columns, rows, cols / 64); down sees both fp16 planes of the hidden
+//            rows as (64 columns, rows, plane, cols / 64). One copy lands as consecutive
+//            [rows][64] tiles (128-byte swizzled), a whole tile's rows for several K steps.
+//   a:  router mode: the bf16 router weight [E, d] in the 3-D form (box 128 rows);
 //       down mode: the packed down codes of every expert as u64 words (256 words, m block,
-//       (K block, half), expert), box = one m block x 2 kb_per (K block, half) pieces.
+//       (K block, half), expert), box = one m block x 2 kSW (K block, half) pieces.
 //   a2: down mode: the down scale/bias words (64 words, m block, K block, expert).
 struct GemmMaps {
-  CUtensorMap rows[6];
+  CUtensorMap rows[12];
   CUtensorMap a, a2;
 };
 cudaError_t launch_gemm(int mode, const GemmParams& p, const GemmMaps* maps, int grid, cudaStream_t s);
-int gemm_kb_per_stage(int mode);  // K blocks that one activation / weight copy covers
+int gemm_kb_per_stage(int mode);  // K blocks that one activation copy covers
+int gemm_kw_per_stage(int mode);  // K blocks that one weight stage covers
+int gemm_out_rows(int mode);      // output rows of one work item (gate/up: 64 features)
 cudaError_t launch_cast(const float* yacc, uint16_t* y, size_t n, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s, void* const* events);
 

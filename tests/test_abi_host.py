@@ -35,7 +35,7 @@ def test_exports_every_declared_symbol(m):
 def test_host_queries(m):
     from synthetic import FULL, TINY
     full = m.dims_of(FULL)
-    assert m.tile_rows() == 96
+    assert m.tile_rows() == 192
     assert m.packed_bytes(full) == 257 * 1769472          # (E + 1) experts x 3*I*d*(1/2 + 4/64) bytes
     assert m.packed_bytes(m.dims_of(TINY)) == 17 * 3 * 128 * 256 * 9 // 16
     assert m.workspace_bytes(full, 1) > 0
