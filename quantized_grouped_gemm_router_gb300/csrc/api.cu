@@ -159,6 +159,7 @@ int run_route(const moe_dims& d, const float* logits, int T, const Ws& w, float*
   p.offsets = w.at<int32_t>(w.L.offsets);
   p.perm = w.at<int32_t>(w.L.perm);
   p.inv_perm = w.at<int32_t>(w.L.inv_perm);
+  p.row_tw = w.at<int2>(w.L.row_tw);
   p.tile_map = w.at<int32_t>(w.L.tile_map);
   p.tile_row0 = w.at<int32_t>(w.L.tile_row0);
   p.n_tiles = w.at<int32_t>(w.L.n_tiles);
@@ -305,6 +306,7 @@ int moe_prefill_timed(const moe_layer* layer, const uint16_t* x, int32_t T, uint
   p.n_tiles = w.at<int32_t>(w.L.n_tiles);
   p.offsets = w.at<int32_t>(w.L.offsets);
   p.perm = w.at<int32_t>(w.L.perm);
+  p.row_tw = w.at<int2>(w.L.row_tw);
   p.topk_w = w.at<float>(w.L.topk_w);
   p.hidden = hidden;
   p.yacc = yacc;

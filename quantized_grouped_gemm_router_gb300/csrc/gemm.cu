@@ -63,21 +63,22 @@ constexpr int kATileBytes = kBlockRows * 128;              // 128 rows x 64 16-b
 
 // kIssuers: MMA-issuing warps (each takes a column range of the one accumulator); kSW / kSB: K
 // blocks per weight / activation stage; kStagesW / kStagesB: stages of the weight and activation
-// rings; kStagesA: TMEM A tiles (one K block each); kWStage: bytes of one weight stage;
+// rings; kStagesA: TMEM A stages (kAK = 2 K blocks each, matching the activation stages, so the
+// MMA warps wait and commit once per 2 K blocks); kWStage: bytes of one weight stage;
 // kPlanes: B operand planes per K block (down: leading and remainder fp16 parts of the hidden
 // rows); kRows: maximum tile rows (MMA N); kMRows: output rows of one work item.
 template <int MODE>
 struct Cfg;
 template <>
 struct Cfg<kModeGateUp> {
-  static constexpr int kIssuers = 2, kSW = 4, kSB = 2, kStagesW = 3, kStagesB = 3, kStagesA = 4, kPlanes = 1;
+  static constexpr int kIssuers = 2, kSW = 4, kSB = 2, kStagesW = 3, kStagesB = 3, kStagesA = 2, kPlanes = 1;
   static constexpr int kRows = kTileRows, kMRows = 64;             // 64 features: gate rows over up rows
   static constexpr int kWStage = 2 * kSW * kGUQuarter;            // two row quarters x kSW blocks
   static constexpr bool kFp16 = true, kQ4 = true;
 };
 template <>
 struct Cfg<kModeDown> {
-  static constexpr int kIssuers = 2, kSW = 2, kSB = 2, kStagesW = 3, kStagesB = 2, kStagesA = 4, kPlanes = 2;
+  static constexpr int kIssuers = 2, kSW = 2, kSB = 2, kStagesW = 3, kStagesB = 2, kStagesA = 2, kPlanes = 2;
   static constexpr int kRows = kTileRows, kMRows = kBlockRows;
   static constexpr int kWStage = kSW * kBlockBytes;                // codes (2 kSW halves), then kSW sb
   static constexpr bool kFp16 = true, kQ4 = true;
@@ -95,6 +96,7 @@ constexpr int tmem_cols_for(int cols) {
 }
 
 constexpr int kXPairs = 4, kXSlots = 2;  // gate/up epilogue exchange: warp pairs x buffered chunks
+constexpr int kAK = 2;                   // K blocks per TMEM A stage (32 columns each)
 
 template <int MODE>
 struct Smem {
@@ -103,7 +105,8 @@ struct Smem {
   static constexpr int kAccCols = C::kRows;                             // one accumulator buffer
   // TMEM columns: two accumulator buffers, then (Q4 modes) the A tiles, 32 columns per 128x64 tile
   static constexpr int kACol = 2 * kAccCols;
-  static constexpr int kTmemNeed = kACol + C::kStagesA * 32;
+  static constexpr int kTmemNeed = kACol + C::kStagesA * kAK * 32;
+  static_assert(!C::kQ4 || (C::kSB == kAK && C::kSW % kAK == 0), "A stages follow the activation stages");
   static constexpr int kTmemCols = tmem_cols_for(kTmemNeed);
   static_assert(kTmemNeed <= 512, "tensor memory budget");
   // down: each epilogue warp keeps the (token, weight) list of its own chunks (half the rows)
@@ -228,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + S::misc_off + 4);
   auto w_stage = [&](int s) { return smem + S::w_off + s * C::kWStage; };
   auto b_stage = [&](int s) { return base + S::b_off + s * S::kBStage; };
-  auto a_tmem = [&](uint32_t tbase, int stage) { return tbase + S::kACol + stage * 32; };
+  auto a_tmem = [&](uint32_t tbase, int stage) { return tbase + S::kACol + stage * kAK * 32; };
 
   // ---------------------------------------------------------------- set-up
   if (threadIdx.x == 0) {
@@ -333,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (uniform operands); one elected lane issues each instruction.
     const int issuer = warp == kWarpMMA ? 0 : 1;
     if (issuer < C::kIssuers) {
-      uint32_t g = 0, gb = 0, gw = 0;
+      uint32_t gb = 0, gw = 0;
       int n = 0;
       bool ok = true;
       Item nxt = decode_item<MODE>(p, blockIdx.x, n_routed);
@@ -350,16 +353,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         int kb = 0;  // K block of this item
         for (int s0 = 0; s0 < KB && ok; s0 += C::kSB, ++gb) {
           const int nkb = min(C::kSB, KB - s0);
-          const int sb = gb % C::kStagesB;
-          if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(full_b(sb), (gb / C::kStagesB) & 1, s_abort)))) break;
-          for (int j = 0; j < nkb; ++j, ++kb, ++g) {
-            // weights of this K block: TMEM tile (Q4 modes) or a shared-memory tile of a stage
-            const int sa = C::kQ4 ? (int)(g % C::kStagesA) : 0, sw = C::kQ4 ? 0 : (int)(gw % C::kStagesW);
-            const int jw = C::kQ4 ? 0 : kb % C::kSW;
-            if constexpr (C::kQ4) {
-              if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(full_a(sa), (g / C::kStagesA) & 1, s_abort)))) break;
-            } else if (jw == 0) {
-              if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(full_w(sw), (gw / C::kStagesW) & 1, s_abort)))) break;
+          constexpr int kSA = C::kStagesA > 0 ? C::kStagesA : 1;  // router mode has no A stages
+          const int sb = gb % C::kStagesB, sa = C::kQ4 ? (int)(gb % kSA) : 0;
+          ok = __all_sync(0xFFFFFFFFu, mbar_wait(full_b(sb), (gb / C::kStagesB) & 1, s_abort) &&
+                                           (!C::kQ4 || mbar_wait(full_a(sa), (gb / kSA) & 1, s_abort)));
+          if (!ok) break;
+          for (int j = 0; j < nkb; ++j, ++kb) {
+            // router weights: a shared-memory tile of the current weight stage
+            const int sw = C::kQ4 ? 0 : (int)(gw % C::kStagesW), jw = C::kQ4 ? 0 : kb % C::kSW;
+            if constexpr (!C::kQ4) {
+              if (jw == 0 && !(ok = __all_sync(0xFFFFFFFFu, mbar_wait(full_w(sw), (gw / C::kStagesW) & 1, s_abort))))
+                break;
             }
             tc_fence_after();
             if (ncols > 0) {
@@ -371,21 +375,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const uint64_t bdesc = sw128_desc(btile + ks * 32);
                   const uint32_t accumulate = (kb | ks | b) != 0;
                   if constexpr (C::kQ4)
-                    umma_f16_ts_elect(acc, a_tmem(tmem_base, sa) + ks * 8, bdesc, idesc, accumulate);
+                    umma_f16_ts_elect(acc, a_tmem(tmem_base, sa) + j * 32 + ks * 8, bdesc, idesc, accumulate);
                   else
                     umma_f16_ss_elect(acc, sw128_desc(smem_u32(w_stage(sw)) + jw * kATileBytes + ks * 32), bdesc, idesc,
                                       accumulate);
                 }
               }
             }
-            if constexpr (C::kQ4) {
-              umma_commit_elect(empty_a(sa));
-            } else if (jw == C::kSW - 1 || kb == KB - 1) {
-              umma_commit_elect(empty_w(sw));
-              ++gw;
+            if constexpr (!C::kQ4) {
+              if (jw == C::kSW - 1 || kb == KB - 1) {
+                umma_commit_elect(empty_w(sw));
+                ++gw;
+              }
             }
           }
           if (!ok) break;
+          if constexpr (C::kQ4) umma_commit_elect(empty_a(sa));
           umma_commit_elect(empty_b(sb));
         }
         if (ok) umma_commit_elect(acc_full(buf));
@@ -399,40 +404,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int quad = warp & 3, part = (warp - kWarpDq0) >> 2;
       const int r = quad * 32 + lane;  // A row
       const uint32_t lanes = (uint32_t)(quad * 32) << 16;
-      uint32_t g = 0, gw = 0;
+      uint32_t ga = 0, gw = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
         for (int kb0 = 0; kb0 < KB && ok; kb0 += C::kSW, ++gw) {
-          const int nk = min(C::kSW, KB - kb0);
+          const int nk = min(C::kSW, KB - kb0);  // even: KB and kSW are
           const int sw = gw % C::kStagesW;
           // tcgen05.st is warp-collective: every lane takes the same exit on an abort
           if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(full_w(sw), (gw / C::kStagesW) & 1, s_abort)))) break;
           const uint8_t* ws = w_stage(sw);
-          for (int j = 0; j < nk; ++j, ++g) {
-            const int sa = g % C::kStagesA;
-            uint4 cw;
-            uint32_t sbw;
-            if constexpr (MODE == kModeGateUp) {
-              const uint8_t* src = ws + ((quad & 1) * C::kSW + j) * kGUQuarter + (quad >> 1) * kGUMat;
-              cw = *reinterpret_cast<const uint4*>(src + part * kQuarterRows * 16 + lane * 16);
-              sbw = *reinterpret_cast<const uint32_t*>(src + 2 * kQuarterRows * 16 + lane * 4);
-            } else {
-              cw = *reinterpret_cast<const uint4*>(ws + (2 * j + part) * kHalfBytes + r * 16);
-              sbw = *reinterpret_cast<const uint32_t*>(ws + 2 * C::kSW * kHalfBytes + j * kSBBytes + r * 4);
-            }
-            if (j == nk - 1) mbar_arrive(empty_w(sw));  // the stage's codes are all in registers
-            if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(empty_a(sa), ((g / C::kStagesA) & 1) ^ 1, s_abort)))) break;
-            tc_fence_after();
-            __half2 s2, b2;
-            scale_bias(sbw, s2, b2);
-            const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
-            uint32_t v[16];
+          for (int j0 = 0; j0 < nk; j0 += kAK, ++ga) {
+            const int sa = ga % C::kStagesA;
+            uint4 cw[kAK];
+            uint32_t sbw[kAK];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const uint4 o = dequant8(words[c], s2, b2);
-              v[4 * c] = o.x, v[4 * c + 1] = o.y, v[4 * c + 2] = o.z, v[4 * c + 3] = o.w;
+            for (int t = 0; t < kAK; ++t) {
+              const int j = j0 + t;
+              if constexpr (MODE == kModeGateUp) {
+                const uint8_t* src = ws + ((quad & 1) * C::kSW + j) * kGUQuarter + (quad >> 1) * kGUMat;
+                cw[t] = *reinterpret_cast<const uint4*>(src + part * kQuarterRows * 16 + lane * 16);
+                sbw[t] = *reinterpret_cast<const uint32_t*>(src + 2 * kQuarterRows * 16 + lane * 4);
+              } else {
+                cw[t] = *reinterpret_cast<const uint4*>(ws + (2 * j + part) * kHalfBytes + r * 16);
+                sbw[t] = *reinterpret_cast<const uint32_t*>(ws + 2 * C::kSW * kHalfBytes + j * kSBBytes + r * 4);
+              }
             }
-            tmem_st16(a_tmem(tmem_base, sa) + lanes + part * 16, v);
+            if (j0 + kAK >= nk) mbar_arrive(empty_w(sw));  // the stage's codes are all in registers
+            if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(empty_a(sa), ((ga / C::kStagesA) & 1) ^ 1, s_abort)))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int t = 0; t < kAK; ++t) {
+              __half2 s2, b2;
+              scale_bias(sbw[t], s2, b2);
+              const uint32_t words[4] = {cw[t].x, cw[t].y, cw[t].z, cw[t].w};
+              uint32_t v[16];
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                const uint4 o = dequant8(words[c], s2, b2);
+                v[4 * c] = o.x, v[4 * c + 1] = o.y, v[4 * c + 2] = o.z, v[4 * c + 3] = o.w;
+              }
+              tmem_st16(a_tmem(tmem_base, sa) + lanes + t * 32 + part * 16, v);
+            }
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(full_a(sa));
@@ -471,9 +483,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tok[li] = it.r0 + j;
             wgt[li] = 1.f;
           } else {
-            const int a = p.perm[it.row0 + j];
-            tok[li] = a / p.k;
-            wgt[li] = p.topk_w[a];
+            const int2 tw = p.row_tw[it.row0 + j];  // written by the router's scatter
+            tok[li] = tw.x;
+            wgt[li] = __int_as_float(tw.y);
           }
         }
         __syncwarp();

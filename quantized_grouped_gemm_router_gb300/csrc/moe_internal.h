@@ -90,7 +90,7 @@ static_assert(sizeof(WsHeader) == 256, "header size");
 
 struct WsLayout {
   size_t header, logits, topk_idx, topk_w, chunk_counts, chunk_base, counts, offsets, perm,
-      inv_perm, tile_map, tile_row0, n_tiles, x16, hidden, yacc, dec_part, total;
+      inv_perm, row_tw, tile_map, tile_row0, n_tiles, x16, hidden, yacc, dec_part, total;
   int n_chunks, max_tiles;
 };
 
@@ -125,6 +125,7 @@ inline WsLayout ws_layout(const moe_dims& d, int T) {
   L.offsets = take((E + 1) * 4);
   L.perm = take(A * 4);
   L.inv_perm = take(A * 4);
+  L.row_tw = take(A * 8);
   L.tile_map = take((size_t)L.max_tiles * 3 * 4);
   L.tile_row0 = take((size_t)L.max_tiles * 4);
   L.n_tiles = take(4);
@@ -152,6 +153,7 @@ struct RouteParams {
   int32_t* offsets;      // [E + 1]
   int32_t* perm;         // [A]
   int32_t* inv_perm;     // [A]
+  int2* row_tw;          // [A] (token, routing weight bits) of each expert-sorted row
   int32_t* tile_map;     // [max_tiles, 3]
   int32_t* tile_row0;    // [max_tiles] sorted row of each tile's first row (offsets[expert] + row)
   int32_t* n_tiles;      // [1]
@@ -178,6 +180,7 @@ struct GemmParams {
   const int32_t* n_tiles;     // device count of routed tiles
   const int32_t* offsets;     // [E + 1]
   const int32_t* perm;        // [A]
+  const int2* row_tw;         // [A] (token, routing weight bits) of each expert-sorted row
   const float* topk_w;        // [A]
   // activations
   uint16_t* hidden;           // [2, A + T, I] fp16: leading part, then remainder (gate/up writes,

@@ -186,6 +186,7 @@ __global__ void __launch_bounds__(32) route_scatter_kernel(const RouteParams p) 
       const int pos = p.offsets[e] + p.chunk_base[(size_t)c * E + e] + s_run[e] + rank;
       p.perm[pos] = a;
       p.inv_perm[a] = pos;
+      p.row_tw[pos] = make_int2(a / p.k, __float_as_int(p.topk_w[a]));
     }
     __syncwarp();
     if (valid && (peers & lt_mask) == 0u) s_run[e] += __popc(peers);
@@ -199,7 +200,7 @@ __global__ void __launch_bounds__(256) route_rows_kernel(const RouteParams p) {
   const int warps = gridDim.x * (blockDim.x >> 5);
   const int lane = threadIdx.x & 31;
   for (int pos = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); pos < A; pos += warps) {
-    const int t = p.perm[pos] / p.k;
+    const int t = p.row_tw[pos].x;
     const uint4* src = reinterpret_cast<const uint4*>(p.x16 + ((size_t)A + t) * p.d);
     uint4* dst = reinterpret_cast<uint4*>(p.x16 + (size_t)pos * p.d);
     for (int i = lane; i < n16; i += 32) dst[i] = src[i];
