@@ -19,9 +19,8 @@
 //                         to shared memory as soon as the expert is known (the shared expert's
 //                         CTAs before routing is known); gate/up + SwiGLU, scaled by the routing
 //                         weight, then this slice's contribution to every output row (split-K
-//                         over the intermediate dimension); clusters of 8 (or 4) CTAs of one
-//                         expert add their partial rows through distributed shared memory
-//   decode_reduce_kernel  y = sum of the clusters' partial rows in a fixed order -> bf16
+//                         over the intermediate dimension), written as the CTA's partial row
+//   decode_reduce_kernel  y = sum of the partial rows in a fixed order -> bf16
 // The GEMV inner products run on the tensor cores (mma.sync m16n8k16, fp16 in, fp32
 // accumulate): the packed nibble pairs of a row map directly onto the MMA fragment layout, so
 // each weight costs about one ALU operation instead of three for an fp32 FMA loop, which on
@@ -41,8 +40,6 @@
 #include "ptx.cuh"
 #include "topk.cuh"
 
-#include <cooperative_groups.h>
-namespace cg = cooperative_groups;
 
 namespace moe {
 namespace {
@@ -53,7 +50,7 @@ constexpr int kXThreads = 512;         // expert kernel: 16 warps to hide MMA an
 constexpr int kXWarps = kXThreads / 32;
 constexpr int kYThreads = 512;         // reduce: 16 output rows x 32 groups of partial rows
 constexpr int kYRows = 16;
-constexpr int kXMaxGUChunks = 4;       // gate/up run split into up to 4 copies (own barriers)
+constexpr int kXMaxGUChunks = 2;       // gate/up run split into up to 2 copies (own barriers)
 constexpr int kGUStage = 2 * (2 * kDecPartRows * 16 + kDecPartRows * 4);  // gate + up slice of one kb
 constexpr int kDnStage = kHalfBytes + kBlockRows * 4;                     // down half-block + sb
 
@@ -189,24 +186,25 @@ __global__ void __launch_bounds__(kXThreads, 1) decode_expert_kernel(const Decod
   }
   __syncthreads();
 
-  // Lane 0 of warp 0 issues this CTA's copies: the contiguous run of its 32 gate and up rows for
-  // every column block (KB * 2304 bytes, in NGU pieces), then its 32-column half of every down
-  // row block (DM * 2048 bytes of codes) and the matching scale/bias rows (DM * 512 bytes).
+  // Lanes 0..NGU of warp 0 issue this CTA's copies, one piece each (a thread's TMA copies to
+  // different barriers are issued one after another, ~0.25 us apart): the contiguous run of its 32
+  // gate and up rows for every column block (KB * 2304 bytes, in NGU pieces), then its 32-column
+  // half of every down row block (DM * 2048 bytes of codes) and the matching scale/bias rows.
   auto issue = [&](int expert) {
-    if (lane != 0) return;
     const uint8_t* eb = p.packed + (size_t)expert * p.expert_stride;
-    const uint8_t* gu = eb + gu_offset(m, part % (kBlockRows / kDecPartRows), 0, KB);
-    for (int c = 0; c < NGU; ++c) {
-      const int kb0 = c * KB / NGU, kb1 = (c + 1) * KB / NGU;
+    if (lane < NGU) {
+      const uint8_t* gu = eb + gu_offset(m, part % (kBlockRows / kDecPartRows), 0, KB);
+      const int c = lane, kb0 = c * KB / NGU, kb1 = (c + 1) * KB / NGU;
       const uint32_t bytes = (uint32_t)(kb1 - kb0) * kGUStage;
       mbar_arrive_expect_tx(bars + 8u * c, bytes);
       tma_bulk_g2s(smem_u32(xs + L.gu + kb0 * kGUStage), gu + (size_t)kb0 * kGUStage, bytes, bars + 8u * c);
+    } else if (lane == NGU) {
+      const uint8_t* dn = eb + p.gu_bytes;
+      mbar_arrive_expect_tx(bars + 8u * NGU, (uint32_t)(DM * (kHalfBytes + kSBBytes)));
+      tma_bulk_g2s(smem_u32(xs + L.dn), dn + dn_code_offset(kbd, hd, 0, DM), DM * kHalfBytes, bars + 8u * NGU);
+      tma_bulk_g2s(smem_u32(xs + L.dn + DM * kHalfBytes), dn + dn_sb_offset(kbd, 0, DM, KBI), DM * kSBBytes,
+                   bars + 8u * NGU);
     }
-    const uint8_t* dn = eb + p.gu_bytes;
-    mbar_arrive_expect_tx(bars + 8u * NGU, (uint32_t)(DM * (kHalfBytes + kSBBytes)));
-    tma_bulk_g2s(smem_u32(xs + L.dn), dn + dn_code_offset(kbd, hd, 0, DM), DM * kHalfBytes, bars + 8u * NGU);
-    tma_bulk_g2s(smem_u32(xs + L.dn + DM * kHalfBytes), dn + dn_sb_offset(kbd, 0, DM, KBI), DM * kSBBytes,
-                 bars + 8u * NGU);
   };
 
   if (shared && warp == 0) issue(p.E);  // static weights: before waiting on the router
@@ -348,44 +346,43 @@ __global__ void __launch_bounds__(kXThreads, 1) decode_expert_kernel(const Decod
     bd1[c] = g == 0 ? hh2[c * 8 + 4 + tig] : (g == 1 ? hl2[c * 8 + 4 + tig] : 0u);
   }
   const float hs = *hsum;
-  float* out = reinterpret_cast<float*>(xs + L.gu);  // this block's partial row (gate/up data is dead)
-  for (int tile = warp; tile < DM * 8; tile += kXWarps) {
-    const int mm = tile >> 3, R0 = (tile & 7) * 16 + g, R1 = R0 + 8;
-    const uint8_t* ds = xs + L.dn + mm * kHalfBytes;
-    const uint8_t* dsb = xs + L.dn + DM * kHalfBytes + mm * kSBBytes;
-    const uint4 c0 = *reinterpret_cast<const uint4*>(ds + R0 * 16);
-    const uint4 c1 = *reinterpret_cast<const uint4*>(ds + R1 * 16);
-    float d[4] = {0.f, 0.f, 0.f, 0.f};
-    mma16816(d, q_pair(c0.x, sh), q_pair(c1.x, sh), q_pair(c0.y, sh), q_pair(c1.y, sh), bd0[0], bd1[0]);
-    mma16816(d, q_pair(c0.z, sh), q_pair(c1.z, sh), q_pair(c0.w, sh), q_pair(c1.w, sh), bd0[1], bd1[1]);
-    if (tig == 0) {
-      const uint32_t sb0 = *reinterpret_cast<const uint32_t*>(dsb + R0 * 4);
-      const uint32_t sb1 = *reinterpret_cast<const uint32_t*>(dsb + R1 * 4);
-      out[mm * kBlockRows + R0] = bf16lo(sb0) * (d[0] + d[1]) + bf16hi(sb0) * hs;
-      out[mm * kBlockRows + R1] = bf16lo(sb1) * (d[2] + d[3]) + bf16hi(sb1) * hs;
+  // Each warp owns DM * 8 / 16 row tiles of 16; all of its code words are read first so the
+  // shared-memory latency overlaps, then the MMAs run back to back. Row results go straight to
+  // this CTA's partial row in global memory (16 consecutive floats per tile).
+  float* gout = p.partials + (size_t)blockIdx.x * p.d;
+  constexpr int kMaxTilesPerWarp = kDecodeMaxD / 16 / kXWarps;  // 12 for d = 3072
+  const int ntw = DM * 8 / kXWarps;                              // tiles per warp (exact: d % 128 == 0)
+  uint4 c0[kMaxTilesPerWarp], c1[kMaxTilesPerWarp];
+#pragma unroll
+  for (int i = 0; i < kMaxTilesPerWarp; ++i) {
+    if (i < ntw) {
+      const int tile = warp + i * kXWarps, mm = tile >> 3, R0 = (tile & 7) * 16 + g;
+      const uint8_t* ds = xs + L.dn + mm * kHalfBytes;
+      c0[i] = *reinterpret_cast<const uint4*>(ds + R0 * 16);
+      c1[i] = *reinterpret_cast<const uint4*>(ds + (R0 + 8) * 16);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kMaxTilesPerWarp; ++i) {
+    if (i < ntw) {
+      const int tile = warp + i * kXWarps, mm = tile >> 3, R0 = (tile & 7) * 16 + g, R1 = R0 + 8;
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      mma16816(d, q_pair(c0[i].x, sh), q_pair(c1[i].x, sh), q_pair(c0[i].y, sh), q_pair(c1[i].y, sh), bd0[0], bd1[0]);
+      mma16816(d, q_pair(c0[i].z, sh), q_pair(c1[i].z, sh), q_pair(c0[i].w, sh), q_pair(c1[i].w, sh), bd0[1], bd1[1]);
+      if (tig == 0) {
+        const uint8_t* dsb = xs + L.dn + DM * kHalfBytes + mm * kSBBytes;
+        const uint32_t sb0 = *reinterpret_cast<const uint32_t*>(dsb + R0 * 4);
+        const uint32_t sb1 = *reinterpret_cast<const uint32_t*>(dsb + R1 * 4);
+        gout[mm * kBlockRows + R0] = bf16lo(sb0) * (d[0] + d[1]) + bf16hi(sb0) * hs;
+        gout[mm * kBlockRows + R1] = bf16lo(sb1) * (d[2] + d[3]) + bf16hi(sb1) * hs;
+      }
     }
   }
   if (!down_ok && tid == 0) *s_abort = 1;
-
-  // Sum the cluster's partial rows through distributed shared memory: block rank r of the
-  // cluster adds rows [r*d/cs, (r+1)*d/cs) of every block's partial, in rank order, and writes
-  // them as row blockIdx.x / cs of the global partials.
-  cg::cluster_group cluster = cg::this_cluster();
-  cluster.sync();
-  const int cs = (int)cluster.num_blocks(), rank = (int)cluster.block_rank();
-  const int span = p.d / cs;
-  float* gout = p.partials + (size_t)(blockIdx.x / cs) * p.d;
-  for (int i = tid; i < span; i += kXThreads) {
-    const int row = rank * span + i;
-    float acc = 0.f;
-    for (int q = 0; q < cs; ++q) acc += cluster.map_shared_rank(out, q)[row];
-    gout[row] = acc;
-  }
-  cluster.sync();
   if (tid == 0 && *s_abort) set_device_status(p.hdr, MOE_ERR_DEVICE_TIMEOUT);
 }
 
-// y[i] = sum over the expert-kernel clusters c (ascending) of partials[c][i], rounded to bf16.
+// y[i] = sum over the expert-kernel CTAs c (ascending) of partials[c][i], rounded to bf16.
 // Thread (row r, group q) sums a contiguous range of c with batched loads; the 32 group sums of
 // a row are then added in group order, so the result does not depend on timing.
 __global__ void __launch_bounds__(kYThreads) decode_reduce_kernel(const DecodeParams p, int n_parts) {
@@ -413,61 +410,34 @@ __global__ void __launch_bounds__(kYThreads) decode_reduce_kernel(const DecodePa
   }
 }
 
-// Largest cluster size (8, 4 or 2 blocks of one expert) whose clusters can all be resident at
-// once, so the expert kernel runs in a single wave; 1 if none can. Cached per shape.
-int expert_cluster_size(const moe_dims& dims, int smem) {
-  struct Entry { int n_parts, smem, cluster; };
-  static std::mutex mu;
-  static Entry cache[16];
-  static int n_cache = 0;
-  const int n_parts = decode_parts(dims), parts = dims.inter / kDecPartRows;
-  std::lock_guard<std::mutex> lock(mu);
-  for (int i = 0; i < n_cache; ++i)
-    if (cache[i].n_parts == n_parts && cache[i].smem == smem) return cache[i].cluster;
-  int chosen = 1;
-  for (int cs = 8; cs >= 2; cs /= 2) {
-    if (parts % cs) continue;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(n_parts);
-    cfg.blockDim = dim3(kXThreads);
-    cfg.dynamicSmemBytes = smem;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = cs;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int active = 0;
-    if (cudaOccupancyMaxActiveClusters(&active, decode_expert_kernel, &cfg) == cudaSuccess && active * cs >= n_parts) {
-      chosen = cs;
-      break;
-    }
-  }
-  cudaGetLastError();  // an unsupported query leaves no sticky error behind
-  if (n_cache < 16) cache[n_cache++] = {n_parts, smem, chosen};
-  return chosen;
-}
-
 }  // namespace
 
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s, void* const* events) {
   const moe_dims dims = {p.d, p.E, p.k, p.inter, p.inter, kGroup};
   const int n_parts = decode_parts(dims);
   const int smem = x_smem(p.d).total;
-  static cudaError_t attr =
-      cudaFuncSetAttribute(decode_expert_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, x_smem(kDecodeMaxD).total);
+  // The router and reduce kernels ask for the largest shared-memory carveout, so that the SMs
+  // they run on can take an expert-kernel CTA (~160 KB of shared memory) as soon as PDL lets it
+  // start, instead of waiting for the SM to drain and change its L1/shared split.
+  static cudaError_t attr = [] {
+    cudaError_t e = cudaFuncSetAttribute(decode_expert_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         x_smem(kDecodeMaxD).total);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(decode_router_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(decode_reduce_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
+    return e;
+  }();
   if (attr != cudaSuccess) return attr;
-  const int cluster = expert_cluster_size(dims, smem);
   cudaError_t err = record_event(events, 0, s);
   if (err != cudaSuccess) return err;
   if ((err = launch_pdl(decode_router_kernel, (p.E + 1) / 2, kRThreads, 0, 1, s, p)) != cudaSuccess) return err;
   if ((err = record_event(events, 1, s)) != cudaSuccess) return err;
-  if ((err = launch_pdl(decode_expert_kernel, n_parts, kXThreads, (size_t)smem, cluster, s, p)) != cudaSuccess)
-    return err;
+  if ((err = launch_pdl(decode_expert_kernel, n_parts, kXThreads, (size_t)smem, 1, s, p)) != cudaSuccess) return err;
   if ((err = record_event(events, 2, s)) != cudaSuccess) return err;
-  if ((err = launch_pdl(decode_reduce_kernel, p.d / kYRows, kYThreads, 0, 1, s, p, n_parts / cluster)) !=
-      cudaSuccess)
+  if ((err = launch_pdl(decode_reduce_kernel, p.d / kYRows, kYThreads, 0, 1, s, p, n_parts)) != cudaSuccess)
     return err;
   return record_event(events, 3, s);
 }

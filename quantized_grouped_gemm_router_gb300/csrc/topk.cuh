@@ -86,8 +86,74 @@ __device__ __forceinline__ bool warp_topk_softmax(const float* row, int E, int k
   return __any_sync(0xFFFFFFFFu, bad);
 }
 
-// Dispatch on the number of experts per lane.
+// Compare-exchange keeping a >= b (descending order).
+__device__ __forceinline__ void cx_desc(uint64_t& a, uint64_t& b) {
+  const uint64_t hi = a > b ? a : b, lo = a > b ? b : a;
+  a = hi;
+  b = lo;
+}
+// Sorts 8 keys descending (Batcher's odd-even merge network, 19 compare-exchanges).
+__device__ __forceinline__ void sort8_desc(uint64_t (&v)[8]) {
+  cx_desc(v[0], v[1]); cx_desc(v[2], v[3]); cx_desc(v[4], v[5]); cx_desc(v[6], v[7]);
+  cx_desc(v[0], v[2]); cx_desc(v[1], v[3]); cx_desc(v[4], v[6]); cx_desc(v[5], v[7]);
+  cx_desc(v[1], v[2]); cx_desc(v[5], v[6]);
+  cx_desc(v[0], v[4]); cx_desc(v[1], v[5]); cx_desc(v[2], v[6]); cx_desc(v[3], v[7]);
+  cx_desc(v[2], v[4]); cx_desc(v[3], v[5]);
+  cx_desc(v[1], v[2]); cx_desc(v[3], v[4]); cx_desc(v[5], v[6]);
+}
+
+// Whole warp, E <= 256, k <= 8: the same selection and weights as warp_topk_softmax<8>, with no
+// serial rounds. Every expert gets the unique key (orderable logit << 32) | ~index, so a larger
+// key is a larger logit, or an equal logit with a lower index. Each lane sorts its 8 keys; five
+// butterfly steps then merge the lane's sorted top 8 with its partner's (a bitonic merge keeps
+// the larger half), after which every lane holds the warp's top 8 in order.
+__device__ __forceinline__ bool warp_top8_softmax(const float* row, int E, int k, int* e_out, float* w_out) {
+  const int lane = threadIdx.x & 31;
+  uint64_t v[8];
+  bool bad = false;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = 0ull;  // below every real key
+    if (e < E) {
+      const float x = __ldcg(row + e);
+      bad |= !isfinite(x);
+      v[i] = ((uint64_t)max(orderable_f32(x), 1u) << 32) | (uint32_t)~(uint32_t)e;
+    }
+  }
+  sort8_desc(v);
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    uint64_t o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = __shfl_xor_sync(0xFFFFFFFFu, v[i], off);
+    // v descending, o descending: max(v[i], o[7-i]) is a bitonic sequence holding the top 8
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = v[i] > o[7 - i] ? v[i] : o[7 - i];
+    cx_desc(v[0], v[4]); cx_desc(v[1], v[5]); cx_desc(v[2], v[6]); cx_desc(v[3], v[7]);
+    cx_desc(v[0], v[2]); cx_desc(v[1], v[3]); cx_desc(v[4], v[6]); cx_desc(v[5], v[7]);
+    cx_desc(v[0], v[1]); cx_desc(v[2], v[3]); cx_desc(v[4], v[5]); cx_desc(v[6], v[7]);
+  }
+  uint64_t mine = v[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i)
+    if (lane == i) mine = v[i];
+  const int my_e = (int)~(uint32_t)mine;
+  const float my_v = from_orderable_f32((uint32_t)(mine >> 32));
+  // Softmax restricted to the selected experts; slot 0 holds the largest logit.
+  const float vmax = from_orderable_f32((uint32_t)(v[0] >> 32));
+  const float ex = lane < k ? expf(my_v - vmax) : 0.f;
+  float sum = ex;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+  *e_out = min(max(my_e, 0), E - 1);
+  *w_out = ex / sum;
+  return __any_sync(0xFFFFFFFFu, bad);
+}
+
+// Dispatch on the number of experts per lane and on k.
 __device__ __forceinline__ bool warp_topk_softmax(const float* row, int E, int k, int* e_out, float* w_out) {
+  if (E <= 256 && k <= 8) return warp_top8_softmax(row, E, k, e_out, w_out);
   if (E <= 256) return warp_topk_softmax<8>(row, E, k, e_out, w_out);
   return warp_topk_softmax<32>(row, E, k, e_out, w_out);
 }
