@@ -28,9 +28,9 @@
 // column of B (x for gate/up; the SwiGLU output as an fp16 leading part and remainder in two
 // columns for down), and each 64-column group's scale and bias are applied to the fp32
 // accumulator: sum (s*q + b) v = s * sum(q v) + b * sum(v). For gate/up the codes enter the MMA
-// as (1024 + q) (one LOP3 per pair; x is small, so the fp32 accumulation keeps sum(q x) to about
-// 1e-5 relative) and the offset is removed with the group's sum of x; for down the codes are made
-// exact first, because the SwiGLU values are large.
+// as (1024 + q) (one LOP3 per pair) and the offset is removed with the group's sum of x (gate/up)
+// or of h (down); the fp32 accumulation keeps sum(q v) to about 1e-5 relative, far below the
+// rounding of the fp16 operands.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -69,13 +69,6 @@ __device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v &
 __device__ __forceinline__ uint32_t q_pair_offset(uint32_t w, int sh) {
   return ((w >> sh) & 0x000F000Fu) | 0x64006400u;
 }
-// The same pair as exact fp16 codes (q0, q1).
-__device__ __forceinline__ uint32_t q_pair(uint32_t w, int sh) {
-  uint32_t t = ((w >> sh) & 0x000F000Fu) | 0x64006400u;  // (1024 + q) in fp16
-  __half2 v = __hsub2(*reinterpret_cast<__half2*>(&t), __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400)));
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
 // D = A(16x16, fp16, row-major) * B(16x8, fp16, column-major) + 0, fp32 result.
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
@@ -367,14 +360,17 @@ __global__ void __launch_bounds__(kXThreads, 1) decode_expert_kernel(const Decod
     if (i < ntw) {
       const int tile = warp + i * kXWarps, mm = tile >> 3, R0 = (tile & 7) * 16 + g, R1 = R0 + 8;
       float d[4] = {0.f, 0.f, 0.f, 0.f};
-      mma16816(d, q_pair(c0[i].x, sh), q_pair(c1[i].x, sh), q_pair(c0[i].y, sh), q_pair(c1[i].y, sh), bd0[0], bd1[0]);
-      mma16816(d, q_pair(c0[i].z, sh), q_pair(c1[i].z, sh), q_pair(c0[i].w, sh), q_pair(c1[i].w, sh), bd0[1], bd1[1]);
+      mma16816(d, q_pair_offset(c0[i].x, sh), q_pair_offset(c1[i].x, sh), q_pair_offset(c0[i].y, sh),
+               q_pair_offset(c1[i].y, sh), bd0[0], bd1[0]);
+      mma16816(d, q_pair_offset(c0[i].z, sh), q_pair_offset(c1[i].z, sh), q_pair_offset(c0[i].w, sh),
+               q_pair_offset(c1[i].w, sh), bd0[1], bd1[1]);
       if (tig == 0) {
         const uint8_t* dsb = xs + L.dn + DM * kHalfBytes + mm * kSBBytes;
         const uint32_t sb0 = *reinterpret_cast<const uint32_t*>(dsb + R0 * 4);
         const uint32_t sb1 = *reinterpret_cast<const uint32_t*>(dsb + R1 * 4);
-        gout[mm * kBlockRows + R0] = bf16lo(sb0) * (d[0] + d[1]) + bf16hi(sb0) * hs;
-        gout[mm * kBlockRows + R1] = bf16lo(sb1) * (d[2] + d[3]) + bf16hi(sb1) * hs;
+        // d = sum (1024 + q) h over the 32 columns: s*q + b weights give s*d + (b - 1024 s) * sum(h)
+        gout[mm * kBlockRows + R0] = bf16lo(sb0) * (d[0] + d[1]) + (bf16hi(sb0) - 1024.f * bf16lo(sb0)) * hs;
+        gout[mm * kBlockRows + R1] = bf16lo(sb1) * (d[2] + d[3]) + (bf16hi(sb1) - 1024.f * bf16lo(sb1)) * hs;
       }
     }
   }

@@ -121,21 +121,30 @@ __global__ void __launch_bounds__(kTopkThreads) route_hist_kernel(const RoutePar
   if (!s_last) return;
   __threadfence();
 
+  // Per expert, the running sum over the chunks (chunk bases) and the total. Thread t takes
+  // experts t, t + blockDim, ...; the chunk counts are read 16 at a time so their loads overlap.
+  for (int e = tid; e < E; e += blockDim.x) {
+    int run = 0;
+    for (int cc0 = 0; cc0 < p.n_chunks; cc0 += 16) {
+      int v[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = cc0 + j < p.n_chunks ? __ldcg(p.chunk_counts + (size_t)(cc0 + j) * E + e) : 0;
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (cc0 + j < p.n_chunks) {
+          p.chunk_base[(size_t)(cc0 + j) * E + e] = run;  // position of chunk cc's first row inside expert e
+          run += v[j];
+        }
+    }
+    s_counts[e] = run;  // this CTA's own histogram is no longer needed
+  }
+  __syncthreads();
   int cnt[4], tiles[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int e = 4 * tid + i;
-    int run = 0;
-    if (e < E) {
-      for (int cc = 0; cc < p.n_chunks; ++cc) {
-        const size_t o = (size_t)cc * E + e;
-        const int n = __ldcg(p.chunk_counts + o);
-        p.chunk_base[o] = run;  // position of chunk cc's first row inside expert e
-        run += n;
-      }
-    }
-    cnt[i] = run;
-    tiles[i] = (run + kTileRows - 1) / kTileRows;
+    cnt[i] = e < E ? s_counts[e] : 0;
+    tiles[i] = (cnt[i] + kTileRows - 1) / kTileRows;
   }
   int total_rows, total_tiles;
   const int off0 = block_exclusive_scan4(cnt, s_warp, &total_rows);
@@ -171,7 +180,8 @@ __global__ void __launch_bounds__(32) route_scatter_kernel(const RouteParams p) 
   const int lane = threadIdx.x;
   const int c = blockIdx.x;
   const int E = p.E;
-  for (int e = lane; e < E; e += 32) s_run[e] = 0;
+  // each expert's next free position for this chunk, loaded once (independent loads)
+  for (int e = lane; e < E; e += 32) s_run[e] = p.offsets[e] + p.chunk_base[(size_t)c * E + e];
   __syncwarp();
   const int a_begin = c * kRouteChunk * p.k;
   const int a_end = min(p.T, (c + 1) * kRouteChunk) * p.k;
@@ -183,7 +193,7 @@ __global__ void __launch_bounds__(32) route_scatter_kernel(const RouteParams p) 
     const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
     if (valid) {
       const int rank = __popc(peers & lt_mask);
-      const int pos = p.offsets[e] + p.chunk_base[(size_t)c * E + e] + s_run[e] + rank;
+      const int pos = s_run[e] + rank;
       p.perm[pos] = a;
       p.inv_perm[a] = pos;
       p.row_tw[pos] = make_int2(a / p.k, __float_as_int(p.topk_w[a]));
