@@ -50,7 +50,7 @@ constexpr int kXThreads = 512;         // expert kernel: 16 warps to hide MMA an
 constexpr int kXWarps = kXThreads / 32;
 constexpr int kYThreads = 512;         // reduce: 16 output rows x 32 groups of partial rows
 constexpr int kYRows = 16;
-constexpr int kXMaxGUChunks = 2;       // gate/up run split into up to 2 copies (own barriers)
+constexpr int kXMaxGUChunks = 4;       // gate/up run split into up to 4 copies (own barriers, own lanes)
 constexpr int kGUStage = 2 * (2 * kDecPartRows * 16 + kDecPartRows * 4);  // gate + up slice of one kb
 constexpr int kDnStage = kHalfBytes + kBlockRows * 4;                     // down half-block + sb
 

@@ -8,9 +8,9 @@
 //   route_hist_kernel    one CTA per 64-token chunk: histogram in shared memory; the last CTA to
 //                        finish (ticket) scans the chunk histograms into counts, offsets,
 //                        per-chunk bases and the tile block map
-//   route_scatter_kernel one warp per chunk: stable, atomics-free placement of the chunk's
-//                        assignments (in-warp ranks by __match_any_sync, running per-expert
-//                        counters in shared memory)
+//   route_scatter_kernel one CTA per chunk: stable placement of the chunk's assignments (per-warp
+//                        histograms and a prefix in warp order, then in-warp ranks by
+//                        __match_any_sync; no global atomics)
 //   route_rows_kernel    (prefill) copies each assignment's fp16 token row to its sorted
 //                        position, so the grouped GEMM reads every tile as contiguous rows.
 #include <cuda_bf16.h>
@@ -174,32 +174,49 @@ __global__ void __launch_bounds__(kTopkThreads) route_hist_kernel(const RoutePar
   }
 }
 
-// One warp per chunk; assignments are visited in ascending order a = t*k + j, 32 at a time.
-__global__ void __launch_bounds__(32) route_scatter_kernel(const RouteParams p) {
-  __shared__ int s_run[kMaxExperts];
-  const int lane = threadIdx.x;
+// One CTA of kScatterWarps warps per chunk. Warp w takes the chunk's w-th run of consecutive
+// assignments (a = t*k + j ascending); a per-warp histogram and a prefix over the warps (in
+// warp order) give each warp its experts' first free positions, then each warp places its run
+// 32 assignments at a time (in-warp ranks by __match_any_sync): the result is the stable order.
+constexpr int kScatterWarps = 8;
+__global__ void __launch_bounds__(kScatterWarps * 32) route_scatter_kernel(const RouteParams p) {
+  __shared__ int s_run[kScatterWarps][kMaxExperts];  // counts, then first free positions
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int c = blockIdx.x;
   const int E = p.E;
-  // each expert's next free position for this chunk, loaded once (independent loads)
-  for (int e = lane; e < E; e += 32) s_run[e] = p.offsets[e] + p.chunk_base[(size_t)c * E + e];
-  __syncwarp();
+  for (int i = threadIdx.x; i < kScatterWarps * E; i += blockDim.x) s_run[i / E][i % E] = 0;
+  __syncthreads();
   const int a_begin = c * kRouteChunk * p.k;
   const int a_end = min(p.T, (c + 1) * kRouteChunk) * p.k;
+  const int per = (a_end - a_begin + kScatterWarps - 1) / kScatterWarps;
+  const int w_begin = min(a_end, a_begin + w * per), w_end = min(a_end, w_begin + per);
+  for (int a = w_begin + lane; a < w_end; a += 32) atomicAdd(&s_run[w][p.topk_idx[a]], 1);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int pos = p.offsets[e] + p.chunk_base[(size_t)c * E + e];
+#pragma unroll
+    for (int v = 0; v < kScatterWarps; ++v) {
+      const int n = s_run[v][e];
+      s_run[v][e] = pos;
+      pos += n;
+    }
+  }
+  __syncthreads();
+  int* run = s_run[w];
   const unsigned lt_mask = (1u << lane) - 1u;
-  for (int base = a_begin; base < a_end; base += 32) {
+  for (int base = w_begin; base < w_end; base += 32) {
     const int a = base + lane;
-    const bool valid = a < a_end;
+    const bool valid = a < w_end;
     const int e = valid ? p.topk_idx[a] : -1 - lane;  // invalid lanes get unique keys
     const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
     if (valid) {
-      const int rank = __popc(peers & lt_mask);
-      const int pos = s_run[e] + rank;
+      const int pos = run[e] + __popc(peers & lt_mask);
       p.perm[pos] = a;
       p.inv_perm[a] = pos;
       p.row_tw[pos] = make_int2(a / p.k, __float_as_int(p.topk_w[a]));
     }
     __syncwarp();
-    if (valid && (peers & lt_mask) == 0u) s_run[e] += __popc(peers);
+    if (valid && (peers & lt_mask) == 0u) run[e] += __popc(peers);
     __syncwarp();
   }
 }
@@ -240,7 +257,7 @@ cudaError_t launch_route(const RouteParams& p, cudaStream_t s) {
   if (err != cudaSuccess) return err;
   route_hist_kernel<<<p.n_chunks, kTopkThreads, 0, s>>>(p);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  route_scatter_kernel<<<p.n_chunks, 32, 0, s>>>(p);
+  route_scatter_kernel<<<p.n_chunks, kScatterWarps * 32, 0, s>>>(p);
   if ((err = cudaGetLastError()) != cudaSuccess || !p.x) return err;
   const int rows = p.T * p.k, per_cta = 8;  // 8 warps of 256 threads
   const int blocks = (rows + per_cta - 1) / per_cta < 152 * 8 ? (rows + per_cta - 1) / per_cta : 152 * 8;
