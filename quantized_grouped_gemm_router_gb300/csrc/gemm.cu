@@ -475,17 +475,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (item + (int)gridDim.x < n_items) nxt = decode_item<MODE>(p, item + gridDim.x, n_routed);
       const int buf = n & 1;
       if (MODE == kModeDown) {  // this warp's (token, routing weight) list, read before the wait
+        constexpr int kPer = (C::kRows + 31) / 32;
+        int2 tw[kPer];
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {  // all loads first: they overlap
+          const int j = lane + 32 * i;
+          const bool mine = j < it.nrows && ((j >> 4) & 1) == half;  // only the rows of this warp's chunks
+          tw[i] = mine && !it.shared ? p.row_tw[it.row0 + j]          // written by the router's scatter
+                                     : make_int2(it.r0 + j, __float_as_int(1.f));
+        }
         __syncwarp();
-        for (int j = lane; j < it.nrows; j += 32) {
-          if (((j >> 4) & 1) != half) continue;       // only the rows of this warp's chunks
-          const int li = ((j >> 5) << 4) | (j & 15);   // position among this warp's rows
-          if (it.shared) {
-            tok[li] = it.r0 + j;
-            wgt[li] = 1.f;
-          } else {
-            const int2 tw = p.row_tw[it.row0 + j];  // written by the router's scatter
-            tok[li] = tw.x;
-            wgt[li] = __int_as_float(tw.y);
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+          const int j = lane + 32 * i;
+          if (j < it.nrows && ((j >> 4) & 1) == half) {
+            const int li = ((j >> 5) << 4) | (j & 15);  // position among this warp's rows
+            tok[li] = tw[i].x;
+            wgt[li] = __int_as_float(tw[i].y);
           }
         }
         __syncwarp();
