@@ -355,8 +355,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int nkb = min(C::kSB, KB - s0);
           constexpr int kSA = C::kStagesA > 0 ? C::kStagesA : 1;  // router mode has no A stages
           const int sb = gb % C::kStagesB, sa = C::kQ4 ? (int)(gb % kSA) : 0;
-          ok = __all_sync(0xFFFFFFFFu, mbar_wait(full_b(sb), (gb / C::kStagesB) & 1, s_abort) &&
-                                           (!C::kQ4 || mbar_wait(full_a(sa), (gb / kSA) & 1, s_abort)));
+          // Q4 modes: the dequant warps see the activation stage land before they mark the A
+          // stage full, so one wait covers both operands (each wait costs the issuing warp ~100
+          // cycles even when the barrier is already complete)
+          ok = __all_sync(0xFFFFFFFFu, C::kQ4 ? mbar_wait(full_a(sa), (gb / kSA) & 1, s_abort)
+                                              : mbar_wait(full_b(sb), (gb / C::kStagesB) & 1, s_abort));
           if (!ok) break;
           for (int j = 0; j < nkb; ++j, ++kb) {
             // router weights: a shared-memory tile of the current weight stage
@@ -447,6 +450,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tmem_wait_st();
             tc_fence_before();
+            // the MMA warp waits only on full_a: make it imply this stage's activation rows too
+            if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(full_b(ga % C::kStagesB), (ga / C::kStagesB) & 1, s_abort))))
+              break;
             mbar_arrive(full_a(sa));
           }
         }
