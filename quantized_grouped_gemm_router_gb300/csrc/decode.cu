@@ -24,7 +24,10 @@
 // The GEMV inner products run on the tensor cores (mma.sync m16n8k16, fp16 in, fp32
 // accumulate): the packed nibble pairs of a row map directly onto the MMA fragment layout, so
 // each weight costs about one ALU operation instead of three for an fp32 FMA loop, which on
-// GB300 would otherwise take as long as streaming the weights. The GEMV vector occupies one
+// GB300 would otherwise take as long as streaming the weights. The order of the reduction index
+// inside an MMA is free as long as A and B agree: lane (g, tig) takes the four column pairs of
+// its own code word tig of each row (and B the matching pairs of the vector), so a warp reads
+// a tile's codes as contiguous 128-byte lines, with no lanes reading the same word. The GEMV vector occupies one
 // column of B (x for gate/up; the SwiGLU output as an fp16 leading part and remainder in two
 // columns for down), and each 64-column group's scale and bias are applied to the fp32
 // accumulator: sum (s*q + b) v = s * sum(q v) + b * sum(v). For gate/up the codes enter the MMA
@@ -256,19 +259,18 @@ __global__ void __launch_bounds__(kXThreads, 1) decode_expert_kernel(const Decod
   const float* xsum = reinterpret_cast<const float*>(xs + L.xsum);
 
   // ---- gate/up: warp w takes K blocks w, w+8, ...; 2 row tiles of 16 per matrix
-  const int g = lane >> 2, tig = lane & 3, sh = 4 * tig;
+  const int g = lane >> 2, tig = lane & 3;
   float acc[2][2][2] = {};  // [gate/up][row tile][row g, row g+8] (meaningful on tig == 0)
   for (int kb = warp; kb < KB; kb += kXWarps) {
     int chunk = 0;
     while (kb >= (chunk + 1) * KB / NGU) ++chunk;
     if (!mbar_wait(bars + 8u * chunk, 0, s_abort)) break;
     const uint8_t* st = xs + L.gu + kb * kGUStage;
-    uint32_t b0[4], b1[4];
-#pragma unroll
-    for (int c4 = 0; c4 < 4; ++c4) {
-      const int kk = (kb * kGroup + c4 * 16) / 2 + tig;
-      b0[c4] = g == 0 ? x2[kk] : 0u;
-      b1[c4] = g == 0 ? x2[kk + 4] : 0u;
+    // B: x for the columns of this lane's two code words (tig and tig + 4): 4 consecutive pairs each
+    uint4 xa = make_uint4(0u, 0u, 0u, 0u), xb = xa;
+    if (g == 0) {
+      xa = *reinterpret_cast<const uint4*>(x2 + kb * (kGroup / 2) + 4 * tig);
+      xb = *reinterpret_cast<const uint4*>(x2 + kb * (kGroup / 2) + 16 + 4 * tig);
     }
     const float xg = xsum[kb];
 #pragma unroll
@@ -277,17 +279,17 @@ __global__ void __launch_bounds__(kXThreads, 1) decode_expert_kernel(const Decod
 #pragma unroll
       for (int rt = 0; rt < 2; ++rt) {
         const int R0 = rt * 16 + g, R1 = R0 + 8;
-        const uint4 r0a = *reinterpret_cast<const uint4*>(ms + R0 * 16);
-        const uint4 r0b = *reinterpret_cast<const uint4*>(ms + kDecPartRows * 16 + R0 * 16);
-        const uint4 r1a = *reinterpret_cast<const uint4*>(ms + R1 * 16);
-        const uint4 r1b = *reinterpret_cast<const uint4*>(ms + kDecPartRows * 16 + R1 * 16);
-        const uint32_t w0[8] = {r0a.x, r0a.y, r0a.z, r0a.w, r0b.x, r0b.y, r0b.z, r0b.w};
-        const uint32_t w1[8] = {r1a.x, r1a.y, r1a.z, r1a.w, r1b.x, r1b.y, r1b.z, r1b.w};
+        // lane (g, tig) reads word tig (columns 8 tig..8 tig+7) and word tig + 4 of rows R0 and R1;
+        // a warp's read of one word per row is one contiguous 128-byte line
+        const uint32_t w0a = *reinterpret_cast<const uint32_t*>(ms + R0 * 16 + 4 * tig);
+        const uint32_t w1a = *reinterpret_cast<const uint32_t*>(ms + R1 * 16 + 4 * tig);
+        const uint32_t w0b = *reinterpret_cast<const uint32_t*>(ms + kDecPartRows * 16 + R0 * 16 + 4 * tig);
+        const uint32_t w1b = *reinterpret_cast<const uint32_t*>(ms + kDecPartRows * 16 + R1 * 16 + 4 * tig);
         float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4)
-          mma16816(d, q_pair_offset(w0[2 * c4], sh), q_pair_offset(w1[2 * c4], sh),
-                   q_pair_offset(w0[2 * c4 + 1], sh), q_pair_offset(w1[2 * c4 + 1], sh), b0[c4], b1[c4]);
+        mma16816(d, q_pair_offset(w0a, 0), q_pair_offset(w1a, 0), q_pair_offset(w0a, 4), q_pair_offset(w1a, 4), xa.x, xa.y);
+        mma16816(d, q_pair_offset(w0a, 8), q_pair_offset(w1a, 8), q_pair_offset(w0a, 12), q_pair_offset(w1a, 12), xa.z, xa.w);
+        mma16816(d, q_pair_offset(w0b, 0), q_pair_offset(w1b, 0), q_pair_offset(w0b, 4), q_pair_offset(w1b, 4), xb.x, xb.y);
+        mma16816(d, q_pair_offset(w0b, 8), q_pair_offset(w1b, 8), q_pair_offset(w0b, 12), q_pair_offset(w1b, 12), xb.z, xb.w);
         // d = sum (1024 + q) x over the group: s*q + b weights give s*d + (b - 1024 s) * sum(x)
         const uint32_t sb0 = *reinterpret_cast<const uint32_t*>(ms + 2 * kDecPartRows * 16 + R0 * 4);
         const uint32_t sb1 = *reinterpret_cast<const uint32_t*>(ms + 2 * kDecPartRows * 16 + R1 * 4);
@@ -332,12 +334,10 @@ __global__ void __launch_bounds__(kXThreads, 1) decode_expert_kernel(const Decod
   const bool down_ok = mbar_wait(bars + 8u * NGU, 0, s_abort);
   const uint32_t* hh2 = reinterpret_cast<const uint32_t*>(hh);
   const uint32_t* hl2 = reinterpret_cast<const uint32_t*>(hl);
-  uint32_t bd0[2], bd1[2];
-#pragma unroll
-  for (int c = 0; c < 2; ++c) {  // column 0: leading part of h, column 1: remainder
-    bd0[c] = g == 0 ? hh2[c * 8 + tig] : (g == 1 ? hl2[c * 8 + tig] : 0u);
-    bd1[c] = g == 0 ? hh2[c * 8 + 4 + tig] : (g == 1 ? hl2[c * 8 + 4 + tig] : 0u);
-  }
+  // B: column 0 the leading part of h, column 1 its remainder, for this lane's code word (columns
+  // 8 tig..8 tig+7 of the CTA's 32): 4 consecutive pairs
+  uint4 hb = make_uint4(0u, 0u, 0u, 0u);
+  if (g < 2) hb = *reinterpret_cast<const uint4*>((g == 0 ? hh2 : hl2) + 4 * tig);
   const float hs = *hsum;
   // Each warp owns DM * 8 / 16 row tiles of 16; all of its code words are read first so the
   // shared-memory latency overlaps, then the MMAs run back to back. Row results go straight to
@@ -345,14 +345,14 @@ __global__ void __launch_bounds__(kXThreads, 1) decode_expert_kernel(const Decod
   float* gout = p.partials + (size_t)blockIdx.x * p.d;
   constexpr int kMaxTilesPerWarp = kDecodeMaxD / 16 / kXWarps;  // 12 for d = 3072
   const int ntw = DM * 8 / kXWarps;                              // tiles per warp (exact: d % 128 == 0)
-  uint4 c0[kMaxTilesPerWarp], c1[kMaxTilesPerWarp];
+  uint32_t c0[kMaxTilesPerWarp], c1[kMaxTilesPerWarp];
 #pragma unroll
   for (int i = 0; i < kMaxTilesPerWarp; ++i) {
-    if (i < ntw) {
+    if (i < ntw) {  // lane (g, tig): word tig of rows R0 and R0 + 8 of the tile
       const int tile = warp + i * kXWarps, mm = tile >> 3, R0 = (tile & 7) * 16 + g;
       const uint8_t* ds = xs + L.dn + mm * kHalfBytes;
-      c0[i] = *reinterpret_cast<const uint4*>(ds + R0 * 16);
-      c1[i] = *reinterpret_cast<const uint4*>(ds + (R0 + 8) * 16);
+      c0[i] = *reinterpret_cast<const uint32_t*>(ds + R0 * 16 + 4 * tig);
+      c1[i] = *reinterpret_cast<const uint32_t*>(ds + (R0 + 8) * 16 + 4 * tig);
     }
   }
 #pragma unroll
@@ -360,10 +360,10 @@ __global__ void __launch_bounds__(kXThreads, 1) decode_expert_kernel(const Decod
     if (i < ntw) {
       const int tile = warp + i * kXWarps, mm = tile >> 3, R0 = (tile & 7) * 16 + g, R1 = R0 + 8;
       float d[4] = {0.f, 0.f, 0.f, 0.f};
-      mma16816(d, q_pair_offset(c0[i].x, sh), q_pair_offset(c1[i].x, sh), q_pair_offset(c0[i].y, sh),
-               q_pair_offset(c1[i].y, sh), bd0[0], bd1[0]);
-      mma16816(d, q_pair_offset(c0[i].z, sh), q_pair_offset(c1[i].z, sh), q_pair_offset(c0[i].w, sh),
-               q_pair_offset(c1[i].w, sh), bd0[1], bd1[1]);
+      mma16816(d, q_pair_offset(c0[i], 0), q_pair_offset(c1[i], 0), q_pair_offset(c0[i], 4),
+               q_pair_offset(c1[i], 4), hb.x, hb.y);
+      mma16816(d, q_pair_offset(c0[i], 8), q_pair_offset(c1[i], 8), q_pair_offset(c0[i], 12),
+               q_pair_offset(c1[i], 12), hb.z, hb.w);
       if (tig == 0) {
         const uint8_t* dsb = xs + L.dn + DM * kHalfBytes + mm * kSBBytes;
         const uint32_t sb0 = *reinterpret_cast<const uint32_t*>(dsb + R0 * 4);
