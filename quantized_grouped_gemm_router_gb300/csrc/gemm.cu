@@ -432,7 +432,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sbw[t] = *reinterpret_cast<const uint32_t*>(ws + 2 * C::kSW * kHalfBytes + j * kSBBytes + r * 4);
               }
             }
-            if (j0 + kAK >= nk) mbar_arrive(empty_w(sw));  // the stage's codes are all in registers
             if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(empty_a(sa), ((ga / C::kStagesA) & 1) ^ 1, s_abort)))) break;
             tc_fence_after();
 #pragma unroll
@@ -448,6 +447,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               tmem_st16(a_tmem(tmem_base, sa) + lanes + t * 32 + part * 16, v);
             }
+            // The weight stage is released only once its codes have been consumed (the values
+            // above depend on them). Arriving right after issuing the shared-memory loads let the
+            // next TMA copy overwrite the stage before every load had read it: the copy is an
+            // async-proxy write, which the barrier's release does not order after generic reads.
+            if (j0 + kAK >= nk) mbar_arrive(empty_w(sw));
             tmem_wait_st();
             tc_fence_before();
             // the MMA warp waits only on full_a: make it imply this stage's activation rows too
