@@ -201,6 +201,32 @@ def test_prefill_repeatable(m):
     np.testing.assert_allclose(y1, y2, rtol=1e-2, atol=1e-2)
 
 
+
+def test_prefill_full_replays_identical(m):
+    """Two full-size layers prefilled alternately, 12 times each: the hidden rows (no atomics on
+    their path) must be bit-identical every time and y equal up to the rounding order of the
+    fp32 combine (one bf16 unit). Catches pipeline races that corrupt an occasional work item."""
+    T = 4096
+    layers = [dev_layer(m, FULL, seed) for seed in (0, 1)]
+    xs = [to_dev(make_tokens(T, FULL.d, seed=50 + seed)) for seed in (0, 1)]
+    ws = m.workspace(layers[0].dims, T)
+
+    def run(i):
+        out = m.route_out_tensors(layers[i].dims, T, "cuda", want=("n_tiles", "hidden"), hidden=True)
+        y = m.prefill(layers[i], xs[i], ws, out=out)
+        return out["hidden"].clone(), y.float()
+
+    first = [run(0), run(1)]
+    for rep in range(12):
+        for i in (0, 1):
+            h, y = run(i)
+            h0, y0 = first[i]
+            assert torch.equal(h, h0), f"replay {rep} layer {i}: hidden rows differ"
+            bad = (y - y0).abs() > 2.0 ** -7 * torch.clamp(y0.abs(), min=1e-3) + 1e-6
+            assert not bool(bad.any()), f"replay {rep} layer {i}: {int(bad.sum())} outputs differ"
+    torch.cuda.synchronize()
+    assert m.read_device_status(ws) == 0
+
 # ------------------------------------------------------------------------------ decode
 @pytest.mark.parametrize("shape,bias,seed", [(TINY, None, 0), (FULL, None, 0), (FULL, None, 1),
                                              (FULL, "zipf", 2)], ids=["tiny", "full0", "full1", "zipf"])
