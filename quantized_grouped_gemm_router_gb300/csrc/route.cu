@@ -178,6 +178,7 @@ __global__ void __launch_bounds__(kTopkThreads) route_hist_kernel(const RoutePar
 // assignments (a = t*k + j ascending); a per-warp histogram and a prefix over the warps (in
 // warp order) give each warp its experts' first free positions, then each warp places its run
 // 32 assignments at a time (in-warp ranks by __match_any_sync): the result is the stable order.
+// No atomics: every counter has a single writer (the lowest lane of an expert's peer group).
 constexpr int kScatterWarps = 8;
 __global__ void __launch_bounds__(kScatterWarps * 32) route_scatter_kernel(const RouteParams p) {
   __shared__ int s_run[kScatterWarps][kMaxExperts];  // counts, then first free positions
@@ -190,7 +191,17 @@ __global__ void __launch_bounds__(kScatterWarps * 32) route_scatter_kernel(const
   const int a_end = min(p.T, (c + 1) * kRouteChunk) * p.k;
   const int per = (a_end - a_begin + kScatterWarps - 1) / kScatterWarps;
   const int w_begin = min(a_end, a_begin + w * per), w_end = min(a_end, w_begin + per);
-  for (int a = w_begin + lane; a < w_end; a += 32) atomicAdd(&s_run[w][p.topk_idx[a]], 1);
+  const unsigned lt_mask = (1u << lane) - 1u;
+  // This warp's histogram, 32 assignments at a time: the lowest lane of each expert's peer group
+  // adds the group's size (one writer per counter, no atomics).
+  for (int base = w_begin; base < w_end; base += 32) {
+    const int a = base + lane;
+    const bool valid = a < w_end;
+    const int e = valid ? p.topk_idx[a] : -1 - lane;  // invalid lanes get unique keys
+    const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
+    if (valid && (peers & lt_mask) == 0u) s_run[w][e] += __popc(peers);
+    __syncwarp();
+  }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int pos = p.offsets[e] + p.chunk_base[(size_t)c * E + e];
@@ -203,7 +214,6 @@ __global__ void __launch_bounds__(kScatterWarps * 32) route_scatter_kernel(const
   }
   __syncthreads();
   int* run = s_run[w];
-  const unsigned lt_mask = (1u << lane) - 1u;
   for (int base = w_begin; base < w_end; base += 32) {
     const int a = base + lane;
     const bool valid = a < w_end;
