@@ -45,7 +45,10 @@ def parse_args(argv=None):
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of replaying CUDA graphs")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
-    ap.add_argument("--skip-check", action="store_true", help="skip the sampled oracle check")
+    ap.add_argument("--skip-check", action="store_true",
+                    help="accepted for older command lines; the sampled oracle check of this launch "
+                         "configuration is tests/test_gpu_bench_config.py")
+    ap.add_argument("--skip-diag", action="store_true", help="skip the decode diagnostics (after the timed region)")
     ap.add_argument("--oracle-child", default=None, help=argparse.SUPPRESS)
     return ap.parse_args(argv)
 
@@ -221,10 +224,39 @@ def _oracle_child(spec: str) -> None:
     print(json.dumps(out))
 
 
-def run_oracle_sample(tokens: int, decode_tokens: int, repeats: int, layer_ids, router_bias) -> dict:
-    """Times the oracle in a fresh CPU-only process whose BLAS/OpenMP thread count is fixed to
-    the cores this process may use, so `cores` is the thread count actually used."""
-    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+def host_cores() -> int:
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+
+
+def host_info() -> dict:
+    """nproc, CPU model and machine of the host the oracle runs on."""
+    import platform
+    model = ""
+    try:
+        for ln in open("/proc/cpuinfo"):
+            key = ln.split(":")[0].strip().lower()
+            if key in ("model name", "cpu model", "hardware") and ":" in ln:
+                model = ln.split(":", 1)[1].strip()
+                break
+    except OSError:
+        pass
+    if not model:
+        try:
+            out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+            for ln in out.splitlines():
+                if ln.lower().startswith("model name"):
+                    model = ln.split(":", 1)[1].strip()
+                    break
+        except (OSError, subprocess.SubprocessError):
+            pass
+    return {"nproc": os.cpu_count(), "cpu_model": model or "unknown", "machine": platform.machine()}
+
+
+def run_oracle_sample(tokens: int, decode_tokens: int, repeats: int, layer_ids, router_bias, threads=None) -> dict:
+    """Times the oracle in a fresh CPU-only process whose BLAS/OpenMP thread count is fixed (all
+    the cores this process may use unless `threads` is given), so `cores` is the thread count
+    actually used."""
+    cores = threads or host_cores()
     env = dict(os.environ)
     for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
         env[var] = str(cores)
@@ -239,15 +271,25 @@ def run_oracle_sample(tokens: int, decode_tokens: int, repeats: int, layer_ids, 
 
 
 def cpu_baseline(args) -> dict:
+    """The oracle on all the host's cores (the reported value) and on one thread (a smaller
+    sample), with the host's core count, CPU model and machine."""
+    rb = None if args.router_bias == "none" else args.router_bias
     tokens = 128
-    d = run_oracle_sample(tokens, decode_tokens=4, repeats=1, layer_ids=[0],
-                          router_bias=None if args.router_bias == "none" else args.router_bias)
+    d = run_oracle_sample(tokens, decode_tokens=4, repeats=1, layer_ids=[0], router_bias=rb)
     t_pre = statistics.mean(d["prefill_s"])
     t_dec = statistics.mean(d["decode_s"])
+    t1 = 32
+    d1 = run_oracle_sample(t1, decode_tokens=2, repeats=1, layer_ids=[0], router_bias=rb, threads=1)
+    t1_pre = statistics.mean(d1["prefill_s"])
+    t1_dec = statistics.mean(d1["decode_s"])
     return {"value": tokens / t_pre, "unit": UNIT, "cores": d["cores"], "kind": "oracle",
             "decode_us_per_layer": t_dec * 1e6,
             "sample": f"numpy fp64 oracle on layer 0 of the stack: one {tokens}-token prefill chunk "
-                      f"({t_pre:.1f} s) and 4 single-token decodes ({t_dec:.2f} s each)"}
+                      f"({t_pre:.1f} s) and 4 single-token decodes ({t_dec:.2f} s each)",
+            "single_thread": {"value": t1 / t1_pre, "unit": UNIT, "decode_us_per_layer": t1_dec * 1e6,
+                              "sample": f"one {t1}-token prefill chunk ({t1_pre:.1f} s) and 2 single-token "
+                                        f"decodes ({t1_dec:.2f} s each), 1 thread"},
+            "host": host_info()}
 
 
 def run_reference(args, config: dict) -> None:
@@ -461,6 +503,8 @@ def run_ours(args, config: dict) -> None:
                "how": "pinned host inputs copied in, 40 eager moe_prefill calls (and 256x40 eager moe_decode "
                       "calls) through the Python binding, outputs copied back, per step"}
 
+    diag = decode_diagnostics(W) if S and not args.skip_diag else None
+
     red = reduce_over_ranks({"pre": pre_ms, "dec": dec_ms, "wall": wall_s}, "max")
     kavg = {n: ksum[n] / kcnt[n] for n in ksum if kcnt[n]}
     if rank != 0:
@@ -501,11 +545,58 @@ def run_ours(args, config: dict) -> None:
         "decode_us_per_layer": 1e3 * red["dec"] / (args.steps * S * L) if S else None,
         "prefill_us_per_layer": 1e3 * red["pre"] / (args.steps * L) if T else None,
         "roofline": dict(rooflines[0]) if rooflines else None, "rooflines": rooflines,
-        "cpu_baseline": cpu, "e2e": e2e,
+        "cpu_baseline": cpu, "e2e": e2e, "decode_diagnostics": diag,
         "gpu_launches": W.launches_per_step() * args.steps,
         "clocks": clk, "wall_s_timed": red["wall"], "graphs": not args.no_graph,
     }
     print(json.dumps(line), flush=True)
+
+
+def decode_diagnostics(W, steps: int = 8) -> dict:
+    """The page's two decode ablations (section "What didn't work"), after the timed region:
+    the decode chain with the GEMV arithmetic deleted, and a read-only probe of the expert kernel's
+    weight copies alone, each captured in a CUDA graph over the stack's layers like the timed
+    decode. The fraction is the decode's weight-read rate over the probe's (the page reports 90.3%
+    for its GEMV); the arithmetic share is the time the arithmetic adds to the chain."""
+    import torch
+    L, S = len(W.layers), W.args.decode_steps
+    m = W.m
+
+    def one(mode):
+        def body():
+            for s in range(steps):
+                for l, layer in enumerate(W.layers):
+                    if mode == 0:
+                        m.decode(layer, W.xd[s % S, l], W.ws_d, y=W.yd[s % S, l])
+                    else:
+                        m.decode_diag(layer, W.xd[s % S, l], W.ws_d, mode, y=W.yd[s % S, l])
+        body()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            body()
+        g.replay()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ts = []
+        for _ in range(3):
+            a.record()
+            g.replay()
+            b.record()
+            b.synchronize()
+            ts.append(a.elapsed_time(b) * 1e3 / (steps * L))
+        return min(ts)
+
+    t_dec, t_nomath, t_read = one(0), one(m.DECODE_DIAG_NO_MATH), one(m.DECODE_DIAG_READ_ONLY)
+    if m.read_device_status(W.ws_d):
+        raise RuntimeError("device status set during the decode diagnostics")
+    sh = W.shape
+    expert_bytes = (sh.top_k + 1) * (3 * sh.inter * sh.d // 2 + 3 * (sh.inter * sh.d // 64) * 4)
+    return {"decode_us_per_layer": t_dec, "no_math_us_per_layer": t_nomath, "read_only_us_per_layer": t_read,
+            "expert_bytes_per_layer": expert_bytes, "read_only_GBps": expert_bytes / (t_read * 1e3),
+            "decode_weight_GBps": expert_bytes / (t_dec * 1e3), "frac_of_read_only_rate": t_read / t_dec,
+            "arithmetic_share": 1.0 - t_nomath / t_dec,
+            "how": f"{L} layers x {steps} steps per CUDA graph, best of 3 replays; read-only probe: the "
+                   "expert kernel's weight copies for experts 0..k-1 and the shared expert, launched alone"}
 
 
 def main(argv=None):

@@ -249,6 +249,24 @@ MOE_API int moe_prefill_timed(const moe_layer* layer, const uint16_t* x, int32_t
 MOE_API int moe_decode_timed(const moe_layer* layer, const uint16_t* x, uint16_t* y, moe_route_out* out,
                              void* ws, size_t ws_bytes, moe_stream_t stream, void* const* events);
 
+/*
+ * Decode diagnostics: the two ablations the page uses to locate the decode bound (section
+ * "What didn't work": the GEMV's rate against the fastest sustained weight-read rate of its access
+ * pattern, and the effect of deleting its arithmetic). Arguments as for moe_decode (no routing
+ * outputs); the same checks and error codes, plus MOE_ERR_INVALID_ARG for an unknown mode.
+ *   MOE_DECODE_DIAG_NO_MATH    the full kernel chain with the GEMV arithmetic deleted: router,
+ *                              top-k, the same weight copies and waits, zero partial rows, the
+ *                              reduce; y becomes zeros.
+ *   MOE_DECODE_DIAG_READ_ONLY  the expert kernel's weight copies alone (experts 0..k-1 and the
+ *                              shared expert), each block waiting for its own; no router, no
+ *                              chaining; x and y are not accessed (they must still be valid,
+ *                              16-byte aligned pointers).
+ */
+#define MOE_DECODE_DIAG_NO_MATH 1
+#define MOE_DECODE_DIAG_READ_ONLY 2
+MOE_API int moe_decode_diag(const moe_layer* layer, const uint16_t* x, uint16_t* y, void* ws, size_t ws_bytes,
+                            int mode, moe_stream_t stream);
+
 /* Synchronises `stream`, returns the sticky device status of `ws` (MOE_OK or a device error
  * code) and clears it. */
 MOE_API int moe_read_device_status(void* ws, moe_stream_t stream);

@@ -11,6 +11,9 @@ from .binding import (  # noqa: F401
     MoeError,
     decode,
     decode_noalloc,
+    decode_diag,
+    DECODE_DIAG_NO_MATH,
+    DECODE_DIAG_READ_ONLY,
     dims_of,
     lib,
     pack_weights,

@@ -80,6 +80,8 @@ def lib() -> ctypes.CDLL:
         L.moe_prefill_timed.restype = ctypes.c_int
         L.moe_decode_timed.argtypes = L.moe_decode.argtypes + [ctypes.POINTER(c_void_p)]
         L.moe_decode_timed.restype = ctypes.c_int
+        L.moe_decode_diag.argtypes = [P(MoeLayer), c_void_p, c_void_p, c_void_p, c_size_t, ctypes.c_int, c_void_p]
+        L.moe_decode_diag.restype = ctypes.c_int
         L.moe_decode_noalloc.argtypes = [P(MoeLayer), c_void_p, c_void_p, c_void_p]
         L.moe_decode_noalloc.restype = ctypes.c_int
         L.moe_read_device_status.argtypes = [c_void_p, c_void_p]
@@ -242,6 +244,19 @@ def decode(layer: Layer, x: torch.Tensor, ws: torch.Tensor, y: torch.Tensor | No
         _check(lib().moe_decode(*args), "moe_decode")
     else:
         _check(lib().moe_decode_timed(*args, _events(events, 4)), "moe_decode_timed")
+    return y
+
+
+DECODE_DIAG_NO_MATH, DECODE_DIAG_READ_ONLY = 1, 2
+
+
+def decode_diag(layer: Layer, x: torch.Tensor, ws: torch.Tensor, mode: int, y: torch.Tensor | None = None) -> torch.Tensor:
+    """moe_decode_diag: the decode chain with the GEMV arithmetic deleted (mode 1) or the expert
+    kernel's weight copies alone (mode 2)."""
+    _check_dev(x, torch.int16, "x")
+    y = y if y is not None else torch.empty_like(x)
+    _check(lib().moe_decode_diag(ctypes.byref(layer.c), x.data_ptr(), y.data_ptr(), ws.data_ptr(), ws.numel(),
+                                 int(mode), _stream()), "moe_decode_diag")
     return y
 
 

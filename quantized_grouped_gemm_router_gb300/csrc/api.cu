@@ -213,6 +213,42 @@ int copy_route_out(const moe_dims& d, int T, const Ws& w, const moe_route_out* o
   return st ? MOE_ERR_CUDA : MOE_OK;
 }
 
+// moe_decode_timed (mode 0) and moe_decode_diag: argument checks, parameter block, launch.
+int decode_common(const moe_layer* layer, const uint16_t* x, uint16_t* y, moe_route_out* out, void* ws,
+                  size_t ws_bytes, moe_stream_t stream, void* const* events, int mode) {
+  int st = check_layer(layer, true);
+  if (st) return st;
+  if (!x || !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(y, 16)) return MOE_ERR_MISALIGNED;
+  if (layer->dims.d > kDecodeMaxD) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if ((st = check_out(out)) || (st = check_ws(ws, ws_bytes, layer->dims, 1))) return st;
+  const moe_dims& d = layer->dims;
+  Ws w{static_cast<uint8_t*>(ws), ws_layout(d, 1)};
+  const PackedLayout P = packed_layout(d);
+  DecodeParams p;
+  p.x = x;
+  p.router_w = layer->router_w;
+  p.router_bias = layer->router_bias;
+  p.packed = static_cast<const uint8_t*>(layer->packed);
+  p.expert_stride = P.expert_stride;
+  p.gu_bytes = P.gu_bytes;
+  p.logits = w.at<float>(w.L.logits);
+  p.topk_idx = w.at<int32_t>(w.L.topk_idx);
+  p.topk_w = w.at<float>(w.L.topk_w);
+  p.partials = w.at<float>(w.L.dec_part);
+  p.y = y;
+  p.hdr = w.at<WsHeader>(w.L.header);
+  p.d = d.d;
+  p.E = d.n_experts;
+  p.k = d.top_k;
+  p.inter = d.inter;
+  if (launch_decode(p, stream, events, mode) != cudaSuccess) return MOE_ERR_CUDA;
+  if (!out) return MOE_OK;
+  st = copy_out(out->logits, p.logits, (size_t)d.n_experts * 4, stream);
+  st |= copy_out(out->topk_idx, p.topk_idx, (size_t)d.top_k * 4, stream);
+  st |= copy_out(out->topk_w, p.topk_w, (size_t)d.top_k * 4, stream);
+  return st ? MOE_ERR_CUDA : MOE_OK;
+}
 }  // namespace
 
 extern "C" {
@@ -347,39 +383,16 @@ int moe_prefill(const moe_layer* layer, const uint16_t* x, int32_t T, uint16_t* 
 
 int moe_decode_timed(const moe_layer* layer, const uint16_t* x, uint16_t* y, moe_route_out* out, void* ws,
                      size_t ws_bytes, moe_stream_t stream, void* const* events) {
-  int st = check_layer(layer, true);
-  if (st) return st;
-  if (!x || !y) return MOE_ERR_INVALID_ARG;
-  if (!aligned(x, 16) || !aligned(y, 16)) return MOE_ERR_MISALIGNED;
-  if (layer->dims.d > kDecodeMaxD) return MOE_ERR_UNSUPPORTED_SHAPE;
-  if ((st = check_out(out)) || (st = check_ws(ws, ws_bytes, layer->dims, 1))) return st;
-  const moe_dims& d = layer->dims;
-  Ws w{static_cast<uint8_t*>(ws), ws_layout(d, 1)};
-  const PackedLayout P = packed_layout(d);
-  DecodeParams p;
-  p.x = x;
-  p.router_w = layer->router_w;
-  p.router_bias = layer->router_bias;
-  p.packed = static_cast<const uint8_t*>(layer->packed);
-  p.expert_stride = P.expert_stride;
-  p.gu_bytes = P.gu_bytes;
-  p.logits = w.at<float>(w.L.logits);
-  p.topk_idx = w.at<int32_t>(w.L.topk_idx);
-  p.topk_w = w.at<float>(w.L.topk_w);
-  p.partials = w.at<float>(w.L.dec_part);
-  p.y = y;
-  p.hdr = w.at<WsHeader>(w.L.header);
-  p.d = d.d;
-  p.E = d.n_experts;
-  p.k = d.top_k;
-  p.inter = d.inter;
-  if (launch_decode(p, stream, events) != cudaSuccess) return MOE_ERR_CUDA;
-  if (!out) return MOE_OK;
-  st = copy_out(out->logits, p.logits, (size_t)d.n_experts * 4, stream);
-  st |= copy_out(out->topk_idx, p.topk_idx, (size_t)d.top_k * 4, stream);
-  st |= copy_out(out->topk_w, p.topk_w, (size_t)d.top_k * 4, stream);
-  return st ? MOE_ERR_CUDA : MOE_OK;
+  return decode_common(layer, x, y, out, ws, ws_bytes, stream, events, 0);
 }
+
+int moe_decode_diag(const moe_layer* layer, const uint16_t* x, uint16_t* y, void* ws, size_t ws_bytes, int mode,
+                    moe_stream_t stream) {
+  if (mode != MOE_DECODE_DIAG_NO_MATH && mode != MOE_DECODE_DIAG_READ_ONLY) return MOE_ERR_INVALID_ARG;
+  return decode_common(layer, x, y, nullptr, ws, ws_bytes, stream, nullptr,
+                       mode == MOE_DECODE_DIAG_NO_MATH ? kDecodeDiagNoMath : kDecodeDiagReadOnly);
+}
+
 
 int moe_decode(const moe_layer* layer, const uint16_t* x, uint16_t* y, moe_route_out* out, void* ws, size_t ws_bytes,
                moe_stream_t stream) {

@@ -162,6 +162,12 @@ __host__ __device__ inline XSmem x_smem(int d) {
   return L;
 }
 
+// kMode 0: the decode expert kernel. Diagnostics (the ablations the pages use to locate the
+// decode bound, section "What didn't work"): kMode 1 deletes the GEMV arithmetic (same copies,
+// waits and stores; the partial rows are zeros); kMode 2 is a read-only probe of the same access
+// pattern (each CTA copies the pieces it would copy for expert `slot` (< k) or the shared expert,
+// waits for them and exits; launched alone).
+template <int kMode>
 __global__ void __launch_bounds__(kXThreads, 1) decode_expert_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) uint8_t xs[];
   const XSmem L = x_smem(p.d);
@@ -203,6 +209,14 @@ __global__ void __launch_bounds__(kXThreads, 1) decode_expert_kernel(const Decod
     }
   };
 
+  if constexpr (kMode == 2) {
+    if (warp == 0) issue(shared ? p.E : min(slot, p.E - 1));
+    bool ok = true;
+    for (int i = 0; i <= NGU && ok; ++i) ok = mbar_wait(bars + 8u * i, 0, s_abort);
+    __syncthreads();
+    if (tid == 0 && *s_abort) set_device_status(p.hdr, MOE_ERR_DEVICE_TIMEOUT);
+    return;
+  }
   if (shared && warp == 0) issue(p.E);  // static weights: before waiting on the router
   pdl_launch_dependents();
   pdl_wait();
@@ -265,6 +279,7 @@ __global__ void __launch_bounds__(kXThreads, 1) decode_expert_kernel(const Decod
     int chunk = 0;
     while (kb >= (chunk + 1) * KB / NGU) ++chunk;
     if (!mbar_wait(bars + 8u * chunk, 0, s_abort)) break;
+    if constexpr (kMode == 1) continue;  // arithmetic deleted
     const uint8_t* st = xs + L.gu + kb * kGUStage;
     // B: x for the columns of this lane's two code words (tig and tig + 4): 4 consecutive pairs each
     uint4 xa = make_uint4(0u, 0u, 0u, 0u), xb = xa;
@@ -360,17 +375,24 @@ __global__ void __launch_bounds__(kXThreads, 1) decode_expert_kernel(const Decod
     if (i < ntw) {
       const int tile = warp + i * kXWarps, mm = tile >> 3, R0 = (tile & 7) * 16 + g, R1 = R0 + 8;
       float d[4] = {0.f, 0.f, 0.f, 0.f};
-      mma16816(d, q_pair_offset(c0[i], 0), q_pair_offset(c1[i], 0), q_pair_offset(c0[i], 4),
-               q_pair_offset(c1[i], 4), hb.x, hb.y);
-      mma16816(d, q_pair_offset(c0[i], 8), q_pair_offset(c1[i], 8), q_pair_offset(c0[i], 12),
-               q_pair_offset(c1[i], 12), hb.z, hb.w);
+      if constexpr (kMode == 0) {
+        mma16816(d, q_pair_offset(c0[i], 0), q_pair_offset(c1[i], 0), q_pair_offset(c0[i], 4),
+                 q_pair_offset(c1[i], 4), hb.x, hb.y);
+        mma16816(d, q_pair_offset(c0[i], 8), q_pair_offset(c1[i], 8), q_pair_offset(c0[i], 12),
+                 q_pair_offset(c1[i], 12), hb.z, hb.w);
+      }
       if (tig == 0) {
         const uint8_t* dsb = xs + L.dn + DM * kHalfBytes + mm * kSBBytes;
         const uint32_t sb0 = *reinterpret_cast<const uint32_t*>(dsb + R0 * 4);
         const uint32_t sb1 = *reinterpret_cast<const uint32_t*>(dsb + R1 * 4);
         // d = sum (1024 + q) h over the 32 columns: s*q + b weights give s*d + (b - 1024 s) * sum(h)
-        gout[mm * kBlockRows + R0] = bf16lo(sb0) * (d[0] + d[1]) + (bf16hi(sb0) - 1024.f * bf16lo(sb0)) * hs;
-        gout[mm * kBlockRows + R1] = bf16lo(sb1) * (d[2] + d[3]) + (bf16hi(sb1) - 1024.f * bf16lo(sb1)) * hs;
+        if constexpr (kMode == 0) {
+          gout[mm * kBlockRows + R0] = bf16lo(sb0) * (d[0] + d[1]) + (bf16hi(sb0) - 1024.f * bf16lo(sb0)) * hs;
+          gout[mm * kBlockRows + R1] = bf16lo(sb1) * (d[2] + d[3]) + (bf16hi(sb1) - 1024.f * bf16lo(sb1)) * hs;
+        } else {
+          gout[mm * kBlockRows + R0] = 0.f;
+          gout[mm * kBlockRows + R1] = 0.f;
+        }
       }
     }
   }
@@ -408,7 +430,7 @@ __global__ void __launch_bounds__(kYThreads) decode_reduce_kernel(const DecodePa
 
 }  // namespace
 
-cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s, void* const* events) {
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s, void* const* events, int mode) {
   const moe_dims dims = {p.d, p.E, p.k, p.inter, p.inter, kGroup};
   const int n_parts = decode_parts(dims);
   const int smem = x_smem(p.d).total;
@@ -416,8 +438,10 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s, void* const* ev
   // they run on can take an expert-kernel CTA (~160 KB of shared memory) as soon as PDL lets it
   // start, instead of waiting for the SM to drain and change its L1/shared split.
   static cudaError_t attr = [] {
-    cudaError_t e = cudaFuncSetAttribute(decode_expert_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         x_smem(kDecodeMaxD).total);
+    cudaError_t e = cudaSuccess;
+    for (auto kernel : {decode_expert_kernel<0>, decode_expert_kernel<1>, decode_expert_kernel<2>})
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, x_smem(kDecodeMaxD).total);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(decode_router_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                cudaSharedmemCarveoutMaxShared);
@@ -427,11 +451,17 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s, void* const* ev
     return e;
   }();
   if (attr != cudaSuccess) return attr;
+  if (mode == kDecodeDiagReadOnly) {  // the expert kernel's weight copies alone, no chain
+    decode_expert_kernel<2><<<n_parts, kXThreads, (size_t)smem, s>>>(p);
+    return cudaGetLastError();
+  }
   cudaError_t err = record_event(events, 0, s);
   if (err != cudaSuccess) return err;
   if ((err = launch_pdl(decode_router_kernel, (p.E + 1) / 2, kRThreads, 0, 1, s, p)) != cudaSuccess) return err;
   if ((err = record_event(events, 1, s)) != cudaSuccess) return err;
-  if ((err = launch_pdl(decode_expert_kernel, n_parts, kXThreads, (size_t)smem, 1, s, p)) != cudaSuccess) return err;
+  err = mode == kDecodeDiagNoMath ? launch_pdl(decode_expert_kernel<1>, n_parts, kXThreads, (size_t)smem, 1, s, p)
+                                  : launch_pdl(decode_expert_kernel<0>, n_parts, kXThreads, (size_t)smem, 1, s, p);
+  if (err != cudaSuccess) return err;
   if ((err = record_event(events, 2, s)) != cudaSuccess) return err;
   if ((err = launch_pdl(decode_reduce_kernel, p.d / kYRows, kYThreads, 0, 1, s, p, n_parts)) != cudaSuccess)
     return err;

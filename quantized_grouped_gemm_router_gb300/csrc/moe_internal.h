@@ -230,7 +230,10 @@ int gemm_kb_per_stage(int mode);  // K blocks that one activation copy covers
 int gemm_kw_per_stage(int mode);  // K blocks that one weight stage covers
 int gemm_out_rows(int mode);      // output rows of one work item (gate/up: 64 features)
 cudaError_t launch_cast(const float* yacc, uint16_t* y, size_t n, cudaStream_t s);
-cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s, void* const* events);
+// mode: 0 the decode path; kDecodeDiagNoMath the same chain with the GEMV arithmetic deleted
+// (partial rows of zeros); kDecodeDiagReadOnly the expert kernel's weight copies alone.
+constexpr int kDecodeDiagNoMath = 1, kDecodeDiagReadOnly = 2;
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s, void* const* events, int mode = 0);
 
 // Records events[i] (if the array and the entry are non-NULL) on the stream; capturable.
 inline cudaError_t record_event(void* const* events, int i, cudaStream_t s) {

@@ -75,5 +75,7 @@ def test_argument_errors_before_launch(m):
     assert lib.moe_route(ctypes.byref(layer), None, None, 16, None, A, ws_need, None) == 1
     assert lib.moe_decode(ctypes.byref(layer), A, None, None, A, ws_need, None) == 1
     assert lib.moe_decode(ctypes.byref(layer), A, A, None, A, 16, None) == 4
+    assert lib.moe_decode_diag(ctypes.byref(layer), A, A, A, ws_need, 3, None) == 1  # unknown mode
+    assert lib.moe_decode_diag(ctypes.byref(layer), A, A, A, 16, 1, None) == 4      # workspace too small
     assert lib.moe_workspace_init(None, 256, None) == 1
     assert lib.moe_read_device_status(None, None) == 1

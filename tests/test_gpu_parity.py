@@ -253,6 +253,27 @@ def test_decode(m, shape, bias, seed):
         C.check_y(y, ref["y"])
 
 
+
+def test_decode_diagnostics(m):
+    """moe_decode_diag: the arithmetic-deleted chain gives zeros, the read-only probe only reads;
+    neither disturbs the workspace for the next regular decode."""
+    layer = dev_layer(m, FULL)
+    ws = m.workspace(layer.dims, 1)
+    x = make_tokens(1, FULL.d, seed=21)
+    xd = to_dev(x)
+    y = m.decode_diag(layer, xd, ws, m.DECODE_DIAG_NO_MATH)
+    torch.cuda.synchronize()
+    assert m.read_device_status(ws) == 0
+    assert not bool((y.view(torch.int16) & 0x7FFF).any()), "no-math decode must give zeros"
+    m.decode_diag(layer, xd, ws, m.DECODE_DIAG_READ_ONLY)
+    torch.cuda.synchronize()
+    assert m.read_device_status(ws) == 0
+    with pytest.raises(m.MoeError):
+        m.decode_diag(layer, xd, ws, 3)
+    y = m.decode(layer, xd, ws)
+    torch.cuda.synchronize()
+    C.check_y(C.bf16_bits_f64(y), O.moe_forward(x, _np_layer(FULL, 0, None), tile_rows=m.tile_rows())["y"], "decode after diagnostics")
+
 def test_decode_matches_prefill_T1(m):
     shape = FULL
     layer = dev_layer(m, shape)
