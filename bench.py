@@ -48,7 +48,7 @@ def parse_args(argv=None):
     ap.add_argument("--skip-check", action="store_true",
                     help="accepted for older command lines; the sampled oracle check of this launch "
                          "configuration is tests/test_gpu_bench_config.py")
-    ap.add_argument("--skip-diag", action="store_true", help="skip the decode diagnostics (after the timed region)")
+    ap.add_argument("--skip-diag", action="store_true", help="skip the diagnostics that run after the timed region (decode split, small batches, chunked prefill)")
     ap.add_argument("--oracle-child", default=None, help=argparse.SUPPRESS)
     return ap.parse_args(argv)
 
@@ -504,6 +504,10 @@ def run_ours(args, config: dict) -> None:
                       "calls) through the Python binding, outputs copied back, per step"}
 
     diag = decode_diagnostics(W) if S and not args.skip_diag else None
+    small = chunked = None
+    if T and not args.skip_diag:
+        small = small_batch_diagnostics(W, None if diag is None else diag["decode_us_per_layer"])
+        chunked = chunked_prefill_diagnostics(W)
 
     red = reduce_over_ranks({"pre": pre_ms, "dec": dec_ms, "wall": wall_s}, "max")
     kavg = {n: ksum[n] / kcnt[n] for n in ksum if kcnt[n]}
@@ -546,6 +550,7 @@ def run_ours(args, config: dict) -> None:
         "prefill_us_per_layer": 1e3 * red["pre"] / (args.steps * L) if T else None,
         "roofline": dict(rooflines[0]) if rooflines else None, "rooflines": rooflines,
         "cpu_baseline": cpu, "e2e": e2e, "decode_diagnostics": diag,
+        "small_batch_diagnostics": small, "chunked_prefill_diagnostics": chunked,
         "gpu_launches": W.launches_per_step() * args.steps,
         "clocks": clk, "wall_s_timed": red["wall"], "graphs": not args.no_graph,
     }
@@ -558,7 +563,6 @@ def decode_diagnostics(W, steps: int = 8) -> dict:
     weight copies alone, each captured in a CUDA graph over the stack's layers like the timed
     decode. The fraction is the decode's weight-read rate over the probe's (the page reports 90.3%
     for its GEMV); the arithmetic share is the time the arithmetic adds to the chain."""
-    import torch
     L, S = len(W.layers), W.args.decode_steps
     m = W.m
 
@@ -570,21 +574,7 @@ def decode_diagnostics(W, steps: int = 8) -> dict:
                         m.decode(layer, W.xd[s % S, l], W.ws_d, y=W.yd[s % S, l])
                     else:
                         m.decode_diag(layer, W.xd[s % S, l], W.ws_d, mode, y=W.yd[s % S, l])
-        body()
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            body()
-        g.replay()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ts = []
-        for _ in range(3):
-            a.record()
-            g.replay()
-            b.record()
-            b.synchronize()
-            ts.append(a.elapsed_time(b) * 1e3 / (steps * L))
-        return min(ts)
+        return _graph_time_ms(body) * 1e3 / (steps * L)
 
     t_dec, t_nomath, t_read = one(0), one(m.DECODE_DIAG_NO_MATH), one(m.DECODE_DIAG_READ_ONLY)
     if m.read_device_status(W.ws_d):
@@ -597,6 +587,87 @@ def decode_diagnostics(W, steps: int = 8) -> dict:
             "arithmetic_share": 1.0 - t_nomath / t_dec,
             "how": f"{L} layers x {steps} steps per CUDA graph, best of 3 replays; read-only probe: the "
                    "expert kernel's weight copies for experts 0..k-1 and the shared expert, launched alone"}
+
+
+def _graph_time_ms(body, reps: int = 3) -> float:
+    """Best of `reps` replays of a CUDA graph captured from body() (after one eager run and one
+    untimed replay), in milliseconds."""
+    import torch
+    body()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        body()
+    g.replay()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ts = []
+    for _ in range(reps):
+        a.record()
+        g.replay()
+        b.record()
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    return min(ts)
+
+
+def small_batch_diagnostics(W, decode_us: float | None, sizes=(1, 2, 3, 4, 5, 8)) -> dict:
+    """Prefill on T = 1..8 token rows (the shape of verifying a few draft tokens at once, which the
+    page's section "What didn't work" found awkward) against T batch-1 decodes: per-layer time of
+    the prefill path over the stack in a CUDA graph, and the distinct experts the T rows select,
+    i.e. the expert bytes one such step must read."""
+    import torch
+    m, L, sh = W.m, len(W.layers), W.shape
+    eb = expert_bytes(sh.d, sh.inter)
+    one_expert = eb["gate_up"] + eb["down"]
+    rows = []
+    for T in sizes:
+        if T > W.xp.shape[1]:
+            break
+        ys = torch.empty((L, T, sh.d), dtype=torch.int16, device=W.xp.device)
+
+        def body():
+            for l, layer in enumerate(W.layers):
+                m.prefill(layer, W.xp[l, :T], W.ws_p, y=ys[l])
+        us = 1e3 * _graph_time_ms(body) / L
+        distinct = 0
+        for l, layer in enumerate(W.layers):
+            out = m.route(layer, W.xp[l, :T], T, W.ws_p, out=m.route_out_tensors(W.dims, T, W.xp.device,
+                                                                                  want=("counts",)))
+            distinct += int((out["counts"] > 0).sum())
+        distinct /= L
+        nbytes = (distinct + 1) * one_expert + sh.n_experts * sh.d * 2
+        rows.append({"T": T, "prefill_us_per_layer": us,
+                     "T_decodes_us_per_layer": None if decode_us is None else T * decode_us,
+                     "distinct_experts": distinct, "weight_MB": nbytes / 1e6, "weight_GBps": nbytes / (us * 1e3)})
+    if m.read_device_status(W.ws_p):
+        raise RuntimeError("device status set during the small-batch diagnostics")
+    return {"rows": rows, "how": f"moe_prefill on the first T rows of each layer's prefill input, {L} layers per "
+                                 "CUDA graph, best of 3 replays; T_decodes = T x the batch-1 decode time per layer"}
+
+
+def chunked_prefill_diagnostics(W, prompt_chunks: int = 4, chunks=(512, 1024, 2048, 4096)) -> dict:
+    """Bounded-chunk prefill (moe_prefill_chunked) of one long prompt per layer, made of
+    `prompt_chunks` layers' prefill inputs back to back, with a workspace sized for the largest
+    chunk only: per-layer time and token rate for several chunk sizes."""
+    import torch
+    m, L, sh = W.m, len(W.layers), W.shape
+    T0 = W.xp.shape[1]
+    n = min(prompt_chunks, L) * T0
+    x = W.xp.view(-1, sh.d)[:n]
+    y = torch.empty_like(x)
+    chunks = [c for c in chunks if c <= T0]
+    rows = []
+    for c in chunks:
+        def body():
+            for layer in W.layers:
+                m.prefill_chunked(layer, x, W.ws_p, c, y=y)
+        us = 1e3 * _graph_time_ms(body) / L
+        rows.append({"chunk_tokens": c, "us_per_layer": us, "tok_per_s_per_layer": n / (us * 1e-6),
+                     "workspace_MB": m.workspace_bytes(W.dims, c) / 1e6})
+    if m.read_device_status(W.ws_p):
+        raise RuntimeError("device status set during the chunked prefill diagnostics")
+    return {"prompt_tokens": n, "single_call_workspace_MB": m.workspace_bytes(W.dims, n) / 1e6, "rows": rows,
+            "how": f"{L} layers per CUDA graph, each prefilling the same {n}-token prompt in chunks, best of 3 replays"}
 
 
 def main(argv=None):

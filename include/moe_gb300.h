@@ -192,6 +192,23 @@ MOE_API int moe_prefill(const moe_layer* layer, const uint16_t* x, int32_t T, ui
                 moe_route_out* out, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /*
+ * Bounded-chunk prefill (section "Prefill: keep routing on the GPU, dequantize in flight":
+ * long prompts run in chunks of bounded size so that temporary activations stay small next to
+ * the weights): moe_prefill on rows [c, c + chunk_tokens) of x for c = 0, chunk_tokens, ...,
+ * the last chunk ragged, all queued on `stream` in order. Every token's output depends only on
+ * its own row, so y is the single-call result for any chunking (up to the combine's fp32
+ * rounding order). Only the workspace of one chunk is needed, however long the prompt:
+ * ws_bytes >= moe_workspace_bytes(dims, min(chunk_tokens, T)); T may exceed the single-call
+ * limit of 65536 tokens.
+ * x: bf16 [T, d]; y: bf16 [T, d] (may not alias x). chunk_tokens: 1..65536.
+ * Errors (returned before anything is queued): INVALID_ARG for T < 1, chunk_tokens < 1 or a NULL
+ * pointer; UNSUPPORTED_SHAPE for chunk_tokens > 65536; the argument errors of moe_prefill.
+ * A launch failure in a later chunk returns MOE_ERR_CUDA with the earlier chunks queued.
+ */
+MOE_API int moe_prefill_chunked(const moe_layer* layer, const uint16_t* x, int64_t T, uint16_t* y,
+                                int32_t chunk_tokens, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
  * Batch-1 decode forward (sections "Prefill and decode are different problems" and
  * "Decode: minimize bytes per token"): router GEMV and top-k, then Q4 GEMVs that stream only
  * the top_k selected experts and the shared expert, gate activation fused into the input

@@ -19,6 +19,7 @@ from .binding import (  # noqa: F401
     pack_weights,
     packed_bytes,
     prefill,
+    prefill_chunked,
     read_device_status,
     route,
     route_out_tensors,

@@ -74,6 +74,9 @@ def lib() -> ctypes.CDLL:
         L.moe_prefill.argtypes = [P(MoeLayer), c_void_p, c_int32, c_void_p, P(RouteOut), c_void_p, c_size_t,
                                   c_void_p]
         L.moe_prefill.restype = ctypes.c_int
+        L.moe_prefill_chunked.argtypes = [P(MoeLayer), c_void_p, ctypes.c_int64, c_void_p, c_int32, c_void_p,
+                                          c_size_t, c_void_p]
+        L.moe_prefill_chunked.restype = ctypes.c_int
         L.moe_decode.argtypes = [P(MoeLayer), c_void_p, c_void_p, P(RouteOut), c_void_p, c_size_t, c_void_p]
         L.moe_decode.restype = ctypes.c_int
         L.moe_prefill_timed.argtypes = L.moe_prefill.argtypes + [ctypes.POINTER(c_void_p)]
@@ -229,6 +232,17 @@ def prefill(layer: Layer, x: torch.Tensor, ws: torch.Tensor, y: torch.Tensor | N
         _check(lib().moe_prefill(*args), "moe_prefill")
     else:
         _check(lib().moe_prefill_timed(*args, _events(events, 6)), "moe_prefill_timed")
+    return y
+
+
+def prefill_chunked(layer: Layer, x: torch.Tensor, ws: torch.Tensor, chunk_tokens: int,
+                    y: torch.Tensor | None = None) -> torch.Tensor:
+    """moe_prefill_chunked: prefill of all rows of x in chunks of at most chunk_tokens rows, with
+    a workspace sized for one chunk."""
+    _check_dev(x, torch.int16, "x")
+    y = y if y is not None else torch.empty_like(x)
+    _check(lib().moe_prefill_chunked(ctypes.byref(layer.c), x.data_ptr(), x.shape[0], y.data_ptr(), int(chunk_tokens),
+                                     ws.data_ptr(), ws.numel(), _stream()), "moe_prefill_chunked")
     return y
 
 

@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "moe_internal.h"
@@ -379,6 +380,24 @@ int moe_prefill_timed(const moe_layer* layer, const uint16_t* x, int32_t T, uint
 int moe_prefill(const moe_layer* layer, const uint16_t* x, int32_t T, uint16_t* y, moe_route_out* out, void* ws,
                 size_t ws_bytes, moe_stream_t stream) {
   return moe_prefill_timed(layer, x, T, y, out, ws, ws_bytes, stream, nullptr);
+}
+
+int moe_prefill_chunked(const moe_layer* layer, const uint16_t* x, int64_t T, uint16_t* y, int32_t chunk_tokens,
+                        void* ws, size_t ws_bytes, moe_stream_t stream) {
+  int st = check_layer(layer, true);
+  if (st) return st;
+  if (T < 1 || chunk_tokens < 1 || !x || !y) return MOE_ERR_INVALID_ARG;
+  if (chunk_tokens > kMaxTokens) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(x, 16) || !aligned(y, 16)) return MOE_ERR_MISALIGNED;
+  const int32_t chunk = (int32_t)std::min<int64_t>(chunk_tokens, T);
+  // Workspaces only grow with the token count, so the first (largest) chunk's check covers all.
+  if ((st = check_ws(ws, ws_bytes, layer->dims, chunk))) return st;
+  const size_t d = (size_t)layer->dims.d;
+  for (int64_t c = 0; c < T; c += chunk) {
+    const int32_t n = (int32_t)std::min<int64_t>(chunk, T - c);
+    if ((st = moe_prefill_timed(layer, x + c * d, n, y + c * d, nullptr, ws, ws_bytes, stream, nullptr))) return st;
+  }
+  return MOE_OK;
 }
 
 int moe_decode_timed(const moe_layer* layer, const uint16_t* x, uint16_t* y, moe_route_out* out, void* ws,

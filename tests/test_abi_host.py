@@ -77,5 +77,13 @@ def test_argument_errors_before_launch(m):
     assert lib.moe_decode(ctypes.byref(layer), A, A, None, A, 16, None) == 4
     assert lib.moe_decode_diag(ctypes.byref(layer), A, A, A, ws_need, 3, None) == 1  # unknown mode
     assert lib.moe_decode_diag(ctypes.byref(layer), A, A, A, 16, 1, None) == 4      # workspace too small
+    chunked = lambda x, T, y, chunk, n: lib.moe_prefill_chunked(ctypes.byref(layer), x, T, y, chunk, A, n, None)  # noqa: E731
+    assert chunked(A, 0, A, 16, ws_need) == 1                             # T < 1
+    assert chunked(A, 100000, A, 0, ws_need) == 1                         # chunk < 1
+    assert chunked(None, 100000, A, 16, ws_need) == 1                     # null x
+    assert chunked(A, 100000, A, 70000, ws_need) == 2                     # chunk above the single-call limit
+    assert chunked(A, 100000, A + 2, 16, ws_need) == 3                    # misaligned y
+    assert chunked(A, 100000, A, 32, ws_need) == 4                        # workspace smaller than one chunk
+    assert chunked(A, 100000, A, 16, ws_need - 1) == 4
     assert lib.moe_workspace_init(None, 256, None) == 1
     assert lib.moe_read_device_status(None, None) == 1

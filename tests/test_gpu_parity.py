@@ -214,7 +214,7 @@ def test_prefill_full_replays_identical(m):
     def run(i):
         out = m.route_out_tensors(layers[i].dims, T, "cuda", want=("n_tiles", "hidden"), hidden=True)
         y = m.prefill(layers[i], xs[i], ws, out=out)
-        return out["hidden"].clone(), y.float()
+        return out["hidden"].clone(), y.view(torch.bfloat16).float()
 
     first = [run(0), run(1)]
     for rep in range(12):
@@ -226,6 +226,86 @@ def test_prefill_full_replays_identical(m):
             assert not bool(bad.any()), f"replay {rep} layer {i}: {int(bad.sum())} outputs differ"
     torch.cuda.synchronize()
     assert m.read_device_status(ws) == 0
+
+# ------------------------------------------------------------------------------ bounded-chunk prefill
+def _oracle_rows(m, layer, npl, shape, x):
+    """Oracle y for the token rows x; where the oracle's k-th and (k+1)-th logits lie within the
+    logit tolerance, the selection follows the GPU's own logits (from moe_route on the same rows)."""
+    g = run_route(m, layer, x.shape[0], x=x)
+    ref_logits = O.router_logits(x, npl["router_w"], npl["router_bias"])
+    tol = C.logit_tolerance(x, npl["router_w"]) + 1e-6 * np.abs(ref_logits)
+    diff, ok = C.selection_with_near_ties(g["logits"], ref_logits, tol, shape.top_k)
+    assert ok, f"tokens {diff} select different experts without a near tie"
+    routing = None
+    if diff:
+        idx = g["topk_idx"]
+        sel = np.take_along_axis(ref_logits.astype(np.float64), idx.astype(np.int64), axis=1)
+        w = np.exp(sel - sel.max(1, keepdims=True))
+        routing = (idx, w / w.sum(1, keepdims=True))
+    return O.moe_forward(x, npl, tile_rows=m.tile_rows(), routing=routing)["y"]
+
+
+def _same_up_to_combine_order(y, y0):
+    """bf16 outputs equal up to the rounding order of the fp32 combine (one bf16 unit)."""
+    a = torch.as_tensor(y).view(torch.bfloat16).float()
+    b = torch.as_tensor(y0).view(torch.bfloat16).float()
+    bad = (a - b).abs() > 2.0 ** -7 * torch.clamp(b.abs(), min=1e-3) + 1e-6
+    return int(bad.sum())
+
+
+@pytest.mark.parametrize("T,chunk", [(300, 64), (5, 1), (37, 100), (192 * 3 + 1, 192)])
+def test_prefill_chunked_tiny(m, T, chunk):
+    """Chunks of 64 rows (4 whole + a ragged 44), one row per chunk, a chunk larger than the
+    prompt, and chunks of exactly one block-map tile: y against the oracle on every row and
+    against a single moe_prefill call."""
+    npl, layer = _np_layer(TINY, 0, None), dev_layer(m, TINY)
+    x = make_tokens(T, TINY.d, seed=200 + T)
+    ws = m.workspace(layer.dims, min(chunk, T))
+    y = m.prefill_chunked(layer, to_dev(x), ws, chunk)
+    torch.cuda.synchronize()
+    assert m.read_device_status(ws) == 0
+    C.check_y(y, _oracle_rows(m, layer, npl, TINY, x))
+    y1 = m.prefill(layer, to_dev(x), m.workspace(layer.dims, T))
+    assert _same_up_to_combine_order(y, y1) == 0
+
+
+def test_prefill_chunked_full(m):
+    """Full-size layer, 5000 tokens in chunks of 2048 (two whole chunks + a ragged 904): equal to one
+    moe_prefill call up to the combine's rounding order, and sampled rows (every chunk's first and
+    last row among them) against the oracle."""
+    T, chunk = 5000, 2048
+    npl, layer = _np_layer(FULL, 0, None), dev_layer(m, FULL)
+    x = make_tokens(T, FULL.d, seed=301)
+    xd = to_dev(x)
+    ws = m.workspace(layer.dims, chunk)
+    y = m.prefill_chunked(layer, xd, ws, chunk)
+    torch.cuda.synchronize()
+    assert m.read_device_status(ws) == 0
+    y1 = m.prefill(layer, xd, m.workspace(layer.dims, T))
+    assert _same_up_to_combine_order(y, y1) == 0
+    rng = np.random.default_rng(7)
+    rows = np.unique(np.concatenate([[0, chunk - 1, chunk, 2 * chunk - 1, 2 * chunk, T - 1],
+                                     rng.choice(T, 26, replace=False)]))
+    C.check_y(y[torch.as_tensor(rows, device=y.device)], _oracle_rows(m, layer, npl, FULL, x[rows]))
+
+
+def test_prefill_chunked_beyond_single_call_limit(m):
+    """70001 tokens (over the 65536 of one moe_prefill call) with a workspace for 32768: every row
+    finite, sampled rows (the chunk edges among them) against the oracle."""
+    T, chunk = 70001, 32768
+    npl, layer = _np_layer(TINY, 0, None), dev_layer(m, TINY)
+    x = make_tokens(T, TINY.d, seed=302)
+    ws = m.workspace(layer.dims, chunk)
+    y = m.prefill_chunked(layer, to_dev(x), ws, chunk)
+    torch.cuda.synchronize()
+    assert m.read_device_status(ws) == 0
+    yf = C.bf16_bits_f64(y)
+    assert np.all(np.isfinite(yf))
+    rng = np.random.default_rng(8)
+    rows = np.unique(np.concatenate([[0, chunk - 1, chunk, 2 * chunk - 1, 2 * chunk, T - 1],
+                                     rng.choice(T, 58, replace=False)]))
+    C.check_y(yf[rows], _oracle_rows(m, layer, npl, TINY, x[rows]))
+
 
 # ------------------------------------------------------------------------------ decode
 @pytest.mark.parametrize("shape,bias,seed", [(TINY, None, 0), (FULL, None, 0), (FULL, None, 1),
