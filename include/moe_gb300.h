@@ -196,8 +196,9 @@ MOE_API int moe_prefill(const moe_layer* layer, const uint16_t* x, int32_t T, ui
  * long prompts run in chunks of bounded size so that temporary activations stay small next to
  * the weights): moe_prefill on rows [c, c + chunk_tokens) of x for c = 0, chunk_tokens, ...,
  * the last chunk ragged, all queued on `stream` in order. Every token's output depends only on
- * its own row, so y is the single-call result for any chunking (up to the combine's fp32
- * rounding order). Only the workspace of one chunk is needed, however long the prompt:
+ * its own row, so y is the single-call result for any chunking, up to fp32 summation order (the
+ * expert tiles, and with them the order of the GEMMs' K sums, follow the chunk's routing). Only
+ * the workspace of one chunk is needed, however long the prompt:
  * ws_bytes >= moe_workspace_bytes(dims, min(chunk_tokens, T)); T may exceed the single-call
  * limit of 65536 tokens.
  * x: bf16 [T, d]; y: bf16 [T, d] (may not alias x). chunk_tokens: 1..65536.

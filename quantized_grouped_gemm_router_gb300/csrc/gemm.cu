@@ -33,7 +33,9 @@
 //   warp 1       activation producer: the tile's contiguous rows (expert-sorted fp16 x, hidden
 //                rows of both planes, or token rows) for kSB K blocks in one tensor copy
 //   warps 2, 11  MMA issuers (whole warp runs the loop, one elected lane issues), each for one
-//                half of the tile's rows; warp 2 also owns the TMEM allocation
+//                half of the tile's rows, or for tiles of at most 96 rows, each for one of a
+//                stage's two K blocks into its own half of the accumulator buffer (the epilogue
+//                adds the halves); warp 2 also owns the TMEM allocation
 //   warps 3-10   dequantize nibbles into fp16 A tiles in tensor memory (each warp writes the 32
 //                TMEM lanes its index may access)
 //   warps 12-19  epilogue (two warps per TMEM lane quadrant, alternate 16-column chunks) from
@@ -346,10 +348,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int buf = n & 1;
         if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(acc_empty(buf), ((n >> 1) & 1) ^ 1, s_abort)))) break;
         tc_fence_after();
+        // A tile of at most half a buffer (96 rows) splits the K blocks instead of the rows:
+        // issuer i takes K block i of every stage over all of the tile's rows, into its own half of
+        // the buffer, and the epilogue adds the halves. Each tcgen05.mma costs its issuing thread
+        // tens of cycles however narrow the tile, so a narrow tile left to one issuer would bound
+        // the kernel (K blocks per stage: kSB = 2, and every K extent here is a multiple of 128).
+        const bool split_k = C::kIssuers == 2 && it.n16 <= S::kAccCols / 2;
         const int half16 = C::kIssuers == 2 ? 16 * ((it.n16 / 16 + 1) / 2) : it.n16;
-        const int c0 = issuer == 0 ? 0 : half16, ncols = issuer == 0 ? half16 : it.n16 - half16;
+        const int c0 = split_k || issuer == 0 ? 0 : half16;
+        const int ncols = split_k ? it.n16 : issuer == 0 ? half16 : it.n16 - half16;
         const uint32_t idesc = idesc_f16(kBlockRows, ncols > 0 ? ncols : 16, C::kFp16);
-        const uint32_t acc = tmem_base + buf * S::kAccCols + c0;
+        const uint32_t acc = tmem_base + buf * S::kAccCols + (split_k ? issuer * (S::kAccCols / 2) : c0);
         int kb = 0;  // K block of this item
         for (int s0 = 0; s0 < KB && ok; s0 += C::kSB, ++gb) {
           const int nkb = min(C::kSB, KB - s0);
@@ -369,14 +378,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            if (ncols > 0) {
+            if (ncols > 0 && (!split_k || j == issuer)) {
+              const int kfirst = split_k ? s0 : kb;  // 0 on this issuer's first K block of the item
 #pragma unroll
               for (int ks = 0; ks < kGroup / 16; ++ks) {
 #pragma unroll
                 for (int b = 0; b < C::kPlanes; ++b) {
                   const uint32_t btile = b_stage(sb) + ((j * C::kPlanes + b) * it.n16 + c0) * 128;
                   const uint64_t bdesc = sw128_desc(btile + ks * 32);
-                  const uint32_t accumulate = (kb | ks | b) != 0;
+                  const uint32_t accumulate = (kfirst | ks | b) != 0;
                   if constexpr (C::kQ4)
                     umma_f16_ts_elect(acc, a_tmem(tmem_base, sa) + j * 32 + ks * 8, bdesc, idesc, accumulate);
                   else
@@ -510,10 +520,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(acc_full(buf), (n >> 1) & 1, s_abort)))) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + lane_addr + buf * S::kAccCols;
+      const bool split_k = C::kIssuers == 2 && it.n16 <= S::kAccCols / 2;  // the MMA issuers' K split
       for (int j0 = 16 * half; j0 < it.n16 && ok; j0 += 32) {
         uint32_t acc[16];
         tmem_ld16(taddr + j0, acc);
         tmem_wait_ld();
+        if (split_k) {  // the second issuer's partial sums over the other K blocks
+          uint32_t acc2[16];
+          tmem_ld16(taddr + S::kAccCols / 2 + j0, acc2);
+          tmem_wait_ld();
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) acc[jj] = __float_as_uint(__uint_as_float(acc[jj]) + __uint_as_float(acc2[jj]));
+        }
         if (MODE == kModeGateUp) {
           const int sl = u & 1;
           float* xs = xbuf + sl * 16 * 32;

@@ -245,11 +245,15 @@ def _oracle_rows(m, layer, npl, shape, x):
     return O.moe_forward(x, npl, tile_rows=m.tile_rows(), routing=routing)["y"]
 
 
-def _same_up_to_combine_order(y, y0):
-    """bf16 outputs equal up to the rounding order of the fp32 combine (one bf16 unit)."""
+def _same_up_to_summation_order(y, y0):
+    """bf16 outputs of the same rows prefilled in different chunks. A row's expert tiles differ in
+    size between chunkings, and a tile of at most 96 rows sums its K blocks in another order, so
+    the hidden rows and the combine may round differently in fp32: one bf16 unit plus an absolute
+    2^-12 of the output's rms (fp32 reordering of sums whose terms reach the output's size)."""
     a = torch.as_tensor(y).view(torch.bfloat16).float()
     b = torch.as_tensor(y0).view(torch.bfloat16).float()
-    bad = (a - b).abs() > 2.0 ** -7 * torch.clamp(b.abs(), min=1e-3) + 1e-6
+    rms = float(b.pow(2).mean().sqrt())
+    bad = (a - b).abs() > 2.0 ** -7 * b.abs() + 2.0 ** -12 * rms
     return int(bad.sum())
 
 
@@ -266,13 +270,13 @@ def test_prefill_chunked_tiny(m, T, chunk):
     assert m.read_device_status(ws) == 0
     C.check_y(y, _oracle_rows(m, layer, npl, TINY, x))
     y1 = m.prefill(layer, to_dev(x), m.workspace(layer.dims, T))
-    assert _same_up_to_combine_order(y, y1) == 0
+    assert _same_up_to_summation_order(y, y1) == 0
 
 
 def test_prefill_chunked_full(m):
     """Full-size layer, 5000 tokens in chunks of 2048 (two whole chunks + a ragged 904): equal to one
-    moe_prefill call up to the combine's rounding order, and sampled rows (every chunk's first and
-    last row among them) against the oracle."""
+    moe_prefill call up to fp32 summation order, and sampled rows (every chunk's first and last
+    row among them) against the oracle."""
     T, chunk = 5000, 2048
     npl, layer = _np_layer(FULL, 0, None), dev_layer(m, FULL)
     x = make_tokens(T, FULL.d, seed=301)
@@ -282,7 +286,7 @@ def test_prefill_chunked_full(m):
     torch.cuda.synchronize()
     assert m.read_device_status(ws) == 0
     y1 = m.prefill(layer, xd, m.workspace(layer.dims, T))
-    assert _same_up_to_combine_order(y, y1) == 0
+    assert _same_up_to_summation_order(y, y1) == 0
     rng = np.random.default_rng(7)
     rows = np.unique(np.concatenate([[0, chunk - 1, chunk, 2 * chunk - 1, 2 * chunk, T - 1],
                                      rng.choice(T, 26, replace=False)]))
