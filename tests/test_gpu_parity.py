@@ -178,6 +178,63 @@ def test_prefill_forced_tile_edges(m):
         assert np.all(g["counts"][: shape.top_k] == T)
 
 
+def integer_layer(shape, seed, force_top=False):
+    """Every weight of every expert is scale 1, bias -8, so w = q - 8 is an integer in -8..7
+    (the packed codes stay random); optionally a router bias that sends every token to experts
+    0..k-1."""
+    npl = dict(_np_layer(shape, seed, None))
+    for mat in ("gate", "up", "down", "sh_gate", "sh_up", "sh_down"):
+        q = dict(npl[mat])
+        q["scale"] = np.full_like(q["scale"], 0x3F80)  # bf16 1.0
+        q["bias"] = np.full_like(q["bias"], 0xC100)    # bf16 -8.0
+        npl[mat] = q
+    if force_top:
+        rb = np.zeros(shape.n_experts, dtype=np.float32)
+        rb[: shape.top_k] = 100.0
+        npl["router_bias"] = rb
+    return npl
+
+
+def sparse_sign_tokens(T, d, nnz, seed):
+    """x = +-1 on nnz random features of each row, 0 elsewhere (bf16 bits): with w in -8..7,
+    |g|, |u| <= 8 nnz, far below 2^24, so every partial sum is an exact integer in fp32."""
+    rng = np.random.default_rng(seed)
+    x = np.zeros((T, d), dtype=np.float32)
+    for t in range(T):
+        cols = rng.choice(d, nnz, replace=False)
+        x[t, cols] = rng.choice(np.array([-1.0, 1.0], dtype=np.float32), nnz)
+    return (x.view(np.uint32) >> 16).astype(np.uint16)
+
+
+@pytest.mark.parametrize("T,force_top", [(600, False), (400, True)], ids=["narrow_tiles", "wide_tiles"])
+def test_prefill_integer_weights_exact_hidden(m, T, force_top):
+    """Integer-valued case of the expert GEMMs: g and u are exact integers on both sides whatever
+    the order of the K sums (narrow tiles split K over the two MMA issuers, wide tiles split
+    rows: 600 tokens give ~19 rows per expert; forcing every token onto experts 0..k-1 gives
+    tiles of 192 rows and a ragged 16). The SwiGLU rows must then equal the oracle's up to the
+    rounding of silu and of the fp16 pair: 1e-5 relative + 1e-7 absolute, where one unit of
+    error in g or u moves h by at least ~1/|g| > 1e-3 relative."""
+    shape = FULL
+    npl = integer_layer(shape, 21, force_top)
+    layer = m.upload_layer(npl)
+    x = sparse_sign_tokens(T, shape.d, 32, seed=T)
+    ws = m.workspace(layer.dims, T)
+    out = m.route_out_tensors(layer.dims, T, "cuda", hidden=True)
+    m.prefill(layer, to_dev(x), ws, out=out)
+    torch.cuda.synchronize()
+    assert m.read_device_status(ws) == 0
+    g = C.to_np({k: v for k, v in out.items() if k != "hidden"})
+    C.check_routing_exact(g, g["logits"], shape.n_experts, shape.top_k, m.tile_rows())
+    if force_top:
+        assert np.all(g["counts"][: shape.top_k] == T)
+    grouping = O.group_assignments(g["topk_idx"], shape.n_experts, m.tile_rows())
+    H = O.hidden_sorted(x, npl, grouping)
+    planes = out["hidden"].cpu().numpy().view(np.float16).astype(np.float64)
+    err = np.abs(planes[0] + planes[1] - H)
+    worst = float(np.max(err / (1e-5 * np.abs(H) + 1e-7)))
+    assert worst <= 1.0, f"hidden rows off by {worst:.2f} x tolerance"
+
+
 def test_prefill_out_of_range_sets_status(m):
     """x beyond the fp16 operand range is reported on the device instead of silently saturating."""
     layer = dev_layer(m, TINY)
