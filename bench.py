@@ -180,18 +180,23 @@ KERNEL_SOURCES = {
 }
 
 
-def measured_traffic() -> dict:
+def measured_traffic(prefill_tokens: int, router_bias: str, path: str | None = None) -> dict:
     """DRAM bytes per launch from the committed ncu summary (profiles/dram_traffic.md), kept only
-    for kernels whose sources still hash to the value recorded at capture time."""
+    for kernels whose sources still hash to the value recorded at capture time and whose captured
+    workload is this run's: prefill rows name their tokens per layer and router bias
+    (`T=4096 bias=none`), decode rows (`decode`) hold for any prefill setting."""
     out = {}
     try:
-        lines = open(os.path.join(ROOT, "profiles", "dram_traffic.md")).read().splitlines()
+        lines = open(path or os.path.join(ROOT, "profiles", "dram_traffic.md")).read().splitlines()
     except OSError:
         return out
+    here = f"T={prefill_tokens} bias={router_bias}"
     for ln in lines:
-        m = re.match(r"\| `(\w+)` \| [^|]+ \| (\d+) \| (\w+) \|", ln)
-        if m and m.group(1) in KERNEL_SOURCES and src_sha(*KERNEL_SOURCES[m.group(1)]) == m.group(3):
-            out[m.group(1)] = int(m.group(2))
+        m = re.match(r"\| `(\w+)` \| ([^|]+?) \| [^|]+ \| (\d+) \| (\w+) \|", ln)
+        if not m or m.group(1) not in KERNEL_SOURCES or m.group(2) not in ("decode", here):
+            continue
+        if src_sha(*KERNEL_SOURCES[m.group(1)]) == m.group(4):
+            out[m.group(1)] = int(m.group(3))
     return out
 
 
@@ -518,7 +523,7 @@ def run_ours(args, config: dict) -> None:
     per_step_launches = {n: L for n in names_pre}
     per_step_launches.update({n: L * S for n in names_dec})
     rooflines = []
-    traffic = measured_traffic()
+    traffic = measured_traffic(T, args.router_bias)
     for n, ms in kavg.items():
         w = work.get(n)
         if not w:
