@@ -20,6 +20,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -49,6 +50,9 @@ def parse_args(argv=None):
                     help="accepted for older command lines; the sampled oracle check of this launch "
                          "configuration is tests/test_gpu_bench_config.py")
     ap.add_argument("--skip-diag", action="store_true", help="skip the diagnostics that run after the timed region (decode split, small batches, chunked prefill)")
+    ap.add_argument("--clocks-csv", default=None,
+                    help="keep the nvidia-smi clock samples of the timed region in this file ({rank} is "
+                         "replaced by the rank; default: a temporary file)")
     ap.add_argument("--oracle-child", default=None, help=argparse.SUPPRESS)
     return ap.parse_args(argv)
 
@@ -448,10 +452,13 @@ def run_ours(args, config: dict) -> None:
     except Exception:
         pass
     clocks = ClockSampler(uuid)
-    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+    clocks_csv = args.clocks_csv.replace("{rank}", str(rank)) if args.clocks_csv else \
+        os.path.join(tempfile.gettempdir(), f"moe_bench_clocks_{os.getpid()}_r{rank}.csv")
+    if os.path.dirname(clocks_csv):
+        os.makedirs(os.path.dirname(clocks_csv), exist_ok=True)
     barrier()
     torch.cuda.synchronize()
-    clocks.start(os.path.join(ROOT, "gpurun_out", f"bench_clocks_r{rank}.csv"))
+    clocks.start(clocks_csv)
     wall0 = time.perf_counter()
     pre_ms = dec_ms = 0.0
     for _ in range(args.steps):
