@@ -184,6 +184,17 @@ KERNEL_SOURCES = {
 }
 
 
+def device_info(device) -> dict:
+    """The GPU the numbers were taken on (name, SM count, compute capability, memory)."""
+    try:
+        import torch
+        p = torch.cuda.get_device_properties(device)
+        return {"name": p.name, "sms": p.multi_processor_count, "cc": f"{p.major}.{p.minor}",
+                "hbm_gib": round(p.total_memory / 2**30, 1)}
+    except Exception as e:  # informational only: never fail the run for it
+        return {"error": str(e)[:120]}
+
+
 def measured_traffic(prefill_tokens: int, router_bias: str, path: str | None = None) -> dict:
     """DRAM bytes per launch from the committed ncu summary (profiles/dram_traffic.md), kept only
     for kernels whose sources still hash to the value recorded at capture time and whose captured
@@ -565,6 +576,7 @@ def run_ours(args, config: dict) -> None:
         "small_batch_diagnostics": small, "chunked_prefill_diagnostics": chunked,
         "gpu_launches": W.launches_per_step() * args.steps,
         "clocks": clk, "wall_s_timed": red["wall"], "graphs": not args.no_graph,
+        "device": device_info(device), "sources": {k: src_sha(*v) for k, v in KERNEL_SOURCES.items()},
     }
     print(json.dumps(line), flush=True)
 

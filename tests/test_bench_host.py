@@ -50,3 +50,14 @@ def test_algorithmic_work_per_launch():
     assert w["prefill_router_gemm"]["flop"] == 2.0 * 4096 * 256 * 2048
     eb = bench.expert_bytes(2048, 512)
     assert eb["gate_up"] + eb["down"] == 1769472
+
+
+def test_device_info_never_raises():
+    """The device record is informational: without a usable GPU it reports the error instead of
+    failing the run."""
+    import torch
+    info = bench.device_info(torch.device("cuda", 0))
+    if torch.cuda.is_available():
+        assert {"name", "sms", "cc", "hbm_gib"} <= set(info)
+    else:
+        assert set(info) == {"error"}

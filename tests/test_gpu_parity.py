@@ -112,6 +112,33 @@ def test_route_nonfinite_sets_status(m):
     assert m.read_device_status(ws) == 0
 
 
+# ------------------------------------------------------------------------------ packing
+@pytest.mark.parametrize("shape", [TINY, FULL], ids=["tiny", "full"])
+def test_pack_deterministic_permutation(m, shape):
+    """moe_pack_weights is a pure re-layout: packing the same canonical weights twice gives the
+    same bytes (same SHA-256), and the packed buffer holds exactly the input's nibbles (codes
+    permuted inside their words, scales and biases copied), nothing added or lost."""
+    import hashlib
+    npl = _np_layer(shape, 0, None)
+    names = ("gate", "up", "down", "sh_gate", "sh_up", "sh_down")
+    dev = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a).view(dt)).cuda()  # noqa: E731
+    mats = {n: (dev(npl[n]["q"], np.int32), dev(npl[n]["scale"], np.int16), dev(npl[n]["bias"], np.int16))
+            for n in names}
+    dims = m.dims_of(shape)
+    a = m.pack_weights(dims, mats)
+    b = m.pack_weights(dims, mats)
+    torch.cuda.synchronize()
+    pa, pb = a.cpu().numpy(), b.cpu().numpy()
+    assert hashlib.sha256(pa.tobytes()).hexdigest() == hashlib.sha256(pb.tobytes()).hexdigest()
+    src = np.concatenate([np.ascontiguousarray(npl[n][f]).view(np.uint8).ravel()
+                          for n in names for f in ("q", "scale", "bias")])
+    assert pa.size == src.size == m.packed_bytes(dims)
+
+    def nibbles(v):
+        return np.bincount(v & 15, minlength=16) + np.bincount(v >> 4, minlength=16)
+    np.testing.assert_array_equal(nibbles(pa), nibbles(src))
+
+
 # ------------------------------------------------------------------------------ prefill
 def prefill_and_check(m, shape, T, seed=0, bias=None, npl=None, layer=None, hidden=False):
     npl = npl if npl is not None else _np_layer(shape, seed, bias)
