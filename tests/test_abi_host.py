@@ -87,3 +87,16 @@ def test_argument_errors_before_launch(m):
     assert chunked(A, 100000, A, 16, ws_need - 1) == 4
     assert lib.moe_workspace_init(None, 256, None) == 1
     assert lib.moe_read_device_status(None, None) == 1
+
+
+def test_workspace_grows_with_tokens(m):
+    """moe_prefill_chunked checks the workspace against its first (largest) chunk only: that is
+    sound because a workspace for T tokens also serves every smaller T. Pinned over every T up to
+    4096 and a spread of larger T, for the full and tiny shapes."""
+    from synthetic import FULL, TINY
+    for shape in (FULL, TINY):
+        dims = m.dims_of(shape)
+        ts = list(range(1, 4097)) + [5000, 8191, 8192, 16384, 32768, 65535, 65536]
+        sizes = [m.workspace_bytes(dims, t) for t in ts]
+        assert all(b > 0 for b in sizes)
+        assert all(a <= b for a, b in zip(sizes, sizes[1:])), shape
