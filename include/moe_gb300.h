@@ -285,6 +285,16 @@ MOE_API int moe_decode_timed(const moe_layer* layer, const uint16_t* x, uint16_t
 MOE_API int moe_decode_diag(const moe_layer* layer, const uint16_t* x, uint16_t* y, void* ws, size_t ws_bytes,
                             int mode, moe_stream_t stream);
 
+/*
+ * Failure-detection self-test: launches one thread block whose bounded mbarrier wait (the routine
+ * the prefill GEMM and decode kernels wait with) is never satisfied. It gives up after about 2e9 SM cycles
+ * (roughly one second), records MOE_ERR_DEVICE_TIMEOUT in the sticky status word of `ws`
+ * (read it with moe_read_device_status) and returns: no fault, trap or hang, and the context
+ * stays usable. ws: at least 256 bytes, 128-byte aligned. Returns INVALID_ARG, MISALIGNED or
+ * CUDA synchronously.
+ */
+MOE_API int moe_selftest_wait_timeout(void* ws, size_t ws_bytes, moe_stream_t stream);
+
 /* Synchronises `stream`, returns the sticky device status of `ws` (MOE_OK or a device error
  * code) and clears it. */
 MOE_API int moe_read_device_status(void* ws, moe_stream_t stream);

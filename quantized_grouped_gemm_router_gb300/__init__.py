@@ -23,6 +23,7 @@ from .binding import (  # noqa: F401
     read_device_status,
     route,
     route_out_tensors,
+    selftest_wait_timeout,
     status_string,
     tile_rows,
     upload_layer,

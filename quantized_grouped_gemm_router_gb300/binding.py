@@ -88,6 +88,8 @@ def lib() -> ctypes.CDLL:
         L.moe_decode_noalloc.argtypes = [P(MoeLayer), c_void_p, c_void_p, c_void_p]
         L.moe_decode_noalloc.restype = ctypes.c_int
         L.moe_read_device_status.argtypes = [c_void_p, c_void_p]
+        L.moe_selftest_wait_timeout.argtypes = [c_void_p, c_size_t, c_void_p]
+        L.moe_selftest_wait_timeout.restype = ctypes.c_int
         L.moe_read_device_status.restype = ctypes.c_int
         L.moe_status_string.argtypes = [ctypes.c_int]
         L.moe_status_string.restype = ctypes.c_char_p
@@ -281,6 +283,12 @@ def decode_noalloc(layer: Layer, x: torch.Tensor, y: torch.Tensor) -> torch.Tens
     _check(lib().moe_decode_noalloc(ctypes.byref(layer.c), x.data_ptr(), y.data_ptr(), _stream()),
            "moe_decode_noalloc")
     return y
+
+
+def selftest_wait_timeout(ws: torch.Tensor) -> None:
+    """moe_selftest_wait_timeout: a bounded device wait that is never satisfied gives up (about a
+    second) and records MOE_ERR_DEVICE_TIMEOUT in ws; read it with read_device_status."""
+    _check(lib().moe_selftest_wait_timeout(ws.data_ptr(), ws.numel(), _stream()), "moe_selftest_wait_timeout")
 
 
 def read_device_status(ws: torch.Tensor) -> int:

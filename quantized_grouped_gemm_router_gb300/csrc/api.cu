@@ -418,6 +418,12 @@ int moe_decode(const moe_layer* layer, const uint16_t* x, uint16_t* y, moe_route
   return moe_decode_timed(layer, x, y, out, ws, ws_bytes, stream, nullptr);
 }
 
+int moe_selftest_wait_timeout(void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!ws || ws_bytes < sizeof(WsHeader)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(ws, 128)) return MOE_ERR_MISALIGNED;
+  return launch_wait_timeout_selftest(static_cast<WsHeader*>(ws), stream) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 int moe_read_device_status(void* ws, moe_stream_t stream) {
   if (!ws) return MOE_ERR_INVALID_ARG;
   if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;

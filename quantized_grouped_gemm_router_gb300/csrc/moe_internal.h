@@ -209,6 +209,7 @@ struct DecodeParams {
 };
 
 // Launchers (each returns cudaGetLastError()).
+cudaError_t launch_wait_timeout_selftest(WsHeader* hdr, cudaStream_t s);
 cudaError_t launch_pack(const moe_dims& d, const moe_q4_view* views, uint8_t* packed, cudaStream_t s);
 cudaError_t launch_route(const RouteParams& p, cudaStream_t s);
 // Tensor maps of the prefill GEMMs.

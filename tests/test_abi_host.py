@@ -85,6 +85,9 @@ def test_argument_errors_before_launch(m):
     assert chunked(A, 100000, A + 2, 16, ws_need) == 3                    # misaligned y
     assert chunked(A, 100000, A, 32, ws_need) == 4                        # workspace smaller than one chunk
     assert chunked(A, 100000, A, 16, ws_need - 1) == 4
+    assert lib.moe_selftest_wait_timeout(None, 256, None) == 1
+    assert lib.moe_selftest_wait_timeout(A, 16, None) == 1                # smaller than the status header
+    assert lib.moe_selftest_wait_timeout(A + 64, 256, None) == 3
     assert lib.moe_workspace_init(None, 256, None) == 1
     assert lib.moe_read_device_status(None, None) == 1
 

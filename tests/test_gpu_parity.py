@@ -422,6 +422,26 @@ def test_decode(m, shape, bias, seed):
 
 
 
+def test_bounded_wait_gives_up_and_reports(m):
+    """Failure detection without a GPU fault: a bounded mbarrier wait that nothing satisfies (the
+    wait routine of the GEMM and decode kernels) gives up after about a second and records
+    MOE_ERR_DEVICE_TIMEOUT, which the host reads once and which is then cleared; the context stays
+    usable (a decode right after matches the oracle)."""
+    import time
+    layer = dev_layer(m, TINY)
+    ws = m.workspace(layer.dims, 1)
+    t0 = time.perf_counter()
+    m.selftest_wait_timeout(ws)
+    assert m.read_device_status(ws) == 7
+    assert 0.2 < time.perf_counter() - t0 < 60
+    assert m.read_device_status(ws) == 0
+    x = make_tokens(1, TINY.d, seed=0, stream=1)
+    y = m.decode(layer, to_dev(x), ws)
+    torch.cuda.synchronize()
+    assert m.read_device_status(ws) == 0
+    C.check_y(y, O.moe_forward(x, _np_layer(TINY, 0, None), tile_rows=m.tile_rows())["y"])
+
+
 def test_decode_diagnostics(m):
     """moe_decode_diag: the arithmetic-deleted chain gives zeros, the read-only probe only reads;
     neither disturbs the workspace for the next regular decode."""
