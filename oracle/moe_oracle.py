@@ -68,7 +68,8 @@ def dequant(mat: dict, group: int = 64) -> np.ndarray:
 
 
 def silu(z):
-    """silu(z) = z / (1 + exp(-z)), the gate activation of SwiGLU."""
+    """silu(z) = z / (1 + exp(-z)), the gate activation of SwiGLU (section "Decode: minimize bytes
+    per token" names the experts' gate activation; SwiGLU is the reading taken)."""
     z = np.asarray(z, dtype=np.float64)
     with np.errstate(over="ignore"):
         return z / (1.0 + np.exp(-z))
@@ -163,7 +164,11 @@ def _expert_mats(layer: dict, e):
 
 
 def expert_ffn(x64, gate: dict, up: dict, down: dict, group: int = 64, return_hidden: bool = False):
-    """One expert on rows x64 [n, d]: h = silu(W_g x) * (W_u x); out = W_d h (all fp64)."""
+    """One expert on rows x64 [n, d]: h = silu(W_g x) * (W_u x); out = W_d h (all fp64).
+
+    Section "Decode: minimize bytes per token" (fusion list): the input projections feed the gate
+    activation, whose output goes through the output projection.
+    """
     g = x64 @ dequant(gate, group).T
     u = x64 @ dequant(up, group).T
     h = silu(g) * u
@@ -194,6 +199,10 @@ def hidden_sorted(x_bits, layer: dict, grouping: dict) -> np.ndarray:
 
 def moe_forward(x_bits, layer: dict, tile_rows: int = 128, routing=None) -> dict:
     """The whole layer: y[t] = sum_j w[t,j] * FFN_{e(t,j)}(x_t) + FFN_shared(x_t).
+
+    Section "Why Qwen3.6-35B-A3B is a weird workload": the router picks 8 of 256 experts per
+    token and one shared expert sees every token (added with weight 1, the reading taken);
+    section "Decode: minimize bytes per token": the routing scores weight the output projection.
 
     ``routing`` = (topk_idx, topk_w) overrides the oracle's own selection (used when the
     comparison must follow a selection taken on another path's logits).
