@@ -50,6 +50,11 @@ def parse_args(argv=None):
                     help="accepted for older command lines; the sampled oracle check of this launch "
                          "configuration is tests/test_gpu_bench_config.py")
     ap.add_argument("--skip-diag", action="store_true", help="skip the diagnostics that run after the timed region (decode split, small batches, chunked prefill)")
+    ap.add_argument("--skip-configs", action="store_true",
+                    help="skip the per-workload sub-results after the timed region (single-layer cold "
+                         "decode, 512-token prefill, skewed 2048-token prefill)")
+    ap.add_argument("--rank-check", action="store_true",
+                    help="only start the ranks, all-reduce one value and print the world size (rank 0)")
     ap.add_argument("--clocks-csv", default=None,
                     help="keep the nvidia-smi clock samples of the timed region in this file ({rank} is "
                          "replaced by the rank; default: a temporary file)")
@@ -501,32 +506,20 @@ def run_ours(args, config: dict) -> None:
     # end-to-end: host inputs in pinned memory, copies inside the timed region, eager calls
     e2e = None
     if not args.skip_e2e:
-        stream = torch.cuda.current_stream()
-        e2e_pre = e2e_dec = 0.0
-        for _ in range(args.steps):
-            e0.record()
-            if T:
-                W.xp.copy_(W.xp_host, non_blocking=True)
-                W.prefill_all()
-                W.yp_host.copy_(W.yp, non_blocking=True)
-            e1.record()
-            if S:
-                W.xd.copy_(W.xd_host, non_blocking=True)
-                W.decode_all()
-                W.yd_host.copy_(W.yd, non_blocking=True)
-            e2.record()
-            stream.synchronize()
-            e2e_pre += e0.elapsed_time(e1)
-            e2e_dec += e1.elapsed_time(e2)
+        e2e_pre, e2e_dec = end_to_end(W, args, e0, e1, e2)
         red = reduce_over_ranks({"pre": e2e_pre, "dec": e2e_dec}, "max")
         h2d = (W.xp_host.numel() * 2 if T else 0) + (W.xd_host.numel() * 2 if S else 0)
         e2e = {"value": world * L * T * args.steps / (red["pre"] / 1e3) if T else None, "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": h2d,
                "decode_us_per_layer": 1e3 * red["dec"] / (args.steps * max(1, S * L)) if S else None,
-               "how": "pinned host inputs copied in, 40 eager moe_prefill calls (and 256x40 eager moe_decode "
-                      "calls) through the Python binding, outputs copied back, per step"}
+               "how": "prefill: per layer, pinned host x copied in on a copy stream, an eager moe_prefill call "
+                      "through the Python binding on the compute stream once its input has landed, y copied "
+                      "back on a second copy stream, so layer l's copies overlap the neighbouring layers' "
+                      "compute; decode: all inputs copied in, 256x40 eager moe_decode calls, outputs copied "
+                      "back, per step"}
 
     diag = decode_diagnostics(W) if S and not args.skip_diag else None
+    configs = None if args.skip_configs else config_results(W, load_peaks())
     small = chunked = None
     if T and not args.skip_diag:
         small = small_batch_diagnostics(W, None if diag is None else diag["decode_us_per_layer"])
@@ -572,7 +565,7 @@ def run_ours(args, config: dict) -> None:
         "decode_us_per_layer": 1e3 * red["dec"] / (args.steps * S * L) if S else None,
         "prefill_us_per_layer": 1e3 * red["pre"] / (args.steps * L) if T else None,
         "roofline": dict(rooflines[0]) if rooflines else None, "rooflines": rooflines,
-        "cpu_baseline": cpu, "e2e": e2e, "decode_diagnostics": diag,
+        "cpu_baseline": cpu, "e2e": e2e, "configs": configs, "decode_diagnostics": diag,
         "small_batch_diagnostics": small, "chunked_prefill_diagnostics": chunked,
         "gpu_launches": W.launches_per_step() * args.steps,
         "clocks": clk, "wall_s_timed": red["wall"], "graphs": not args.no_graph,
@@ -694,10 +687,203 @@ def chunked_prefill_diagnostics(W, prompt_chunks: int = 4, chunks=(512, 1024, 20
             "how": f"{L} layers per CUDA graph, each prefilling the same {n}-token prompt in chunks, best of 3 replays"}
 
 
+def end_to_end(W, args, e0, e1, e2):
+    """The same workload through the public binding with host buffers: (prefill ms, decode ms)
+    summed over args.steps steps. Prefill overlaps each layer's host copies with the neighbouring
+    layers' compute (copy-in stream, compute stream, copy-out stream); decode copies all inputs in,
+    runs the eager calls and copies all outputs back."""
+    import torch
+    L, T, S = args.layers, args.prefill_tokens, args.decode_steps
+    compute = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(L)]
+    ev_done = [torch.cuda.Event() for _ in range(L)]
+    pre = dec = 0.0
+    for _ in range(args.steps):
+        e0.record(compute)
+        if T:
+            s_in.wait_stream(compute)      # the copies belong to the timed region
+            s_out.wait_stream(compute)
+            for l, layer in enumerate(W.layers):
+                with torch.cuda.stream(s_in):
+                    W.xp[l].copy_(W.xp_host[l], non_blocking=True)
+                    ev_in[l].record(s_in)
+                compute.wait_event(ev_in[l])
+                W.m.prefill(layer, W.xp[l], W.ws_p, y=W.yp[l])
+                ev_done[l].record(compute)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(ev_done[l])
+                    W.yp_host[l].copy_(W.yp[l], non_blocking=True)
+            compute.wait_stream(s_out)
+        e1.record(compute)
+        if S:
+            W.xd.copy_(W.xd_host, non_blocking=True)
+            W.decode_all()
+            W.yd_host.copy_(W.yd, non_blocking=True)
+        e2.record(compute)
+        compute.synchronize()
+        pre += e0.elapsed_time(e1)
+        dec += e1.elapsed_time(e2)
+    return pre, dec
+
+
+def _l2_bytes(device) -> int:
+    import torch
+    try:
+        return int(torch.cuda.get_device_properties(device).L2_cache_size)
+    except Exception:
+        return 128 << 20
+
+
+def config_results(W, peaks: dict, reps: int = 8) -> dict:
+    """Per-workload sub-results on this GPU, after the timed region, each with its roofline:
+      decode      single-layer batch-1 decode with a cold L2 (a buffer of twice the L2 size is
+                  written before every call, the layer and x change every call): HBM fraction of
+                  the router + k+1 active experts' bytes;
+      prefill512  512-token prefill, near-uniform routing (all experts hit), layers rotated so no
+                  weights stay in L2: HBM fraction of the bytes one layer must read, and the tensor
+                  fraction of the expert GEMMs;
+      skew2048    2048-token prefill with the Zipf router bias (a few experts with hundreds of rows,
+                  most with few or none), eight layers rotated: tensor fraction of the grouped
+                  gate/up + down GEMMs (the target the pages' design is held to) and of the layer.
+    Kernel times come from events recorded by the library at its kernel boundaries inside a CUDA
+    graph (the timed launch configuration). Peaks: the burst figures (kernels timed alone)."""
+    import numpy as np
+    import torch
+    from synthetic import make_tokens, zipf_router_bias
+    m, sh, dev = W.m, W.shape, W.xp.device if W.xp is not None else W.xd.device
+    d, E, k, I = sh.d, sh.n_experts, sh.top_k, sh.inter
+    eb = expert_bytes(d, I)
+    one_expert = eb["gate_up"] + eb["down"]
+    hbm, tf = peaks["hbm_gbs"], peaks["bf16_tflops"]
+    out = {}
+
+    # ---- single-layer decode, cold L2
+    nl = min(len(W.layers), 8)
+    flush = torch.empty(2 * _l2_bytes(dev), dtype=torch.uint8, device=dev)
+    x1 = torch.from_numpy(make_tokens(reps, d, seed=77, stream=5).view(np.int16)).to(dev)
+    y1 = torch.empty_like(x1)
+    ws1 = m.workspace(W.dims, 1, dev)
+    ev = [_new_events(2) for _ in range(reps)]
+
+    def dec_body():
+        for r in range(reps):
+            flush.fill_(r & 0x7F)
+            m.decode(W.layers[r % nl], x1[r], ws1, y=y1[r], events=[ev[r][0], None, None, ev[r][1]])
+    _graph_time_ms(dec_body, reps=1)
+    us = statistics.median(1e3 * a.elapsed_time(b) for a, b in ev)
+    nbytes = algorithmic_work(d, E, k, I, 1)["decode_layer"]["bytes"]
+    out["decode"] = {"workload": "single MoE layer, batch-1 decode (T=1), cold L2", "us_per_layer": us,
+                     "roofline": {"bound": "hbm", "achieved": nbytes / (us * 1e3), "peak": hbm, "unit": "GB/s",
+                                  "frac": nbytes / (us * 1e3) / hbm, "per_launch_bytes": nbytes}}
+
+    def prefill_config(T, layers, seed_stream):
+        xs = [torch.from_numpy(make_tokens(T, d, seed=i, stream=seed_stream).view(np.int16)).to(dev)
+              for i in range(len(layers))]
+        ys = [torch.empty_like(x) for x in xs]
+        ws = m.workspace(W.dims, T, dev)
+        evs = [[_new_events(6) for _ in layers] for _ in range(reps)]
+
+        def body():
+            for r in range(reps):
+                for i, layer in enumerate(layers):
+                    m.prefill(layer, xs[i], ws, y=ys[i], events=evs[r][i])
+        _graph_time_ms(body, reps=1)
+        names = ["router", "route", "gate_up", "down", "cast"]
+        per = {n: statistics.mean(1e3 * e[j].elapsed_time(e[j + 1]) for row in evs for e in row)
+               for j, n in enumerate(names)}
+        layer_us = statistics.mean(1e3 * e[0].elapsed_time(e[5]) for row in evs for e in row)
+        hit = []
+        for i, layer in enumerate(layers):
+            o = m.route(layer, xs[i], T, ws, out=m.route_out_tensors(W.dims, T, dev, want=("counts",)))
+            hit.append(int((o["counts"] > 0).sum()))
+        if m.read_device_status(ws):
+            raise RuntimeError("device status set during the per-workload sub-results")
+        return layer_us, per, statistics.mean(hit)
+
+    def gemm_flop(T):
+        return 2.0 * (T * k + T) * 3 * I * d
+
+    # ---- 512-token prefill, near-uniform routing
+    lay = W.layers[:min(len(W.layers), 4)]
+    T = 512
+    layer_us, per, hit = prefill_config(T, lay, 3)
+    nbytes = (hit + 1) * one_expert + E * d * 2 + 2 * T * d * 2
+    gemm_us = per["gate_up"] + per["down"]
+    out["prefill512"] = {
+        "workload": "512-token prefill, one layer, near-uniform routing", "us_per_layer": layer_us,
+        "tok_per_s": T / (layer_us * 1e-6), "kernels_us": per, "experts_hit": hit,
+        "roofline": {"bound": "hbm", "achieved": nbytes / (layer_us * 1e3), "peak": hbm, "unit": "GB/s",
+                     "frac": nbytes / (layer_us * 1e3) / hbm, "per_launch_bytes": nbytes},
+        "gemm_tensor_frac": gemm_flop(T) / (gemm_us * 1e-6) / 1e12 / tf}
+
+    # ---- 2048-token prefill, Zipf router bias
+    rb = torch.from_numpy(zipf_router_bias(E)).to(dev)
+    lay = [m.Layer(W.dims, L.router_w, rb, L.packed) for L in W.layers[:min(len(W.layers), 8)]]
+    T = 2048
+    layer_us, per, hit = prefill_config(T, lay, 4)
+    gemm_us = per["gate_up"] + per["down"]
+    ach = gemm_flop(T) / (gemm_us * 1e-6) / 1e12
+    out["skew2048"] = {
+        "workload": "2048-token prefill, one layer, Zipf(1.1) router bias", "us_per_layer": layer_us,
+        "tok_per_s": T / (layer_us * 1e-6), "kernels_us": per, "experts_hit": hit,
+        "roofline": {"bound": "tensor", "kernel": "grouped gate/up + down GEMMs", "achieved": ach, "peak": tf,
+                     "unit": "TFLOP/s", "frac": ach / tf, "frac_of_sustained": ach / peaks["bf16_tflops_sustained"],
+                     "per_launch_flop": gemm_flop(T)},
+        "layer_tensor_frac": (gemm_flop(T) + 2.0 * T * E * d) / (layer_us * 1e-6) / 1e12 / tf}
+    out["how"] = (f"CUDA graphs of {reps} repetitions; events recorded by moe_decode_timed / moe_prefill_timed "
+                  f"at the kernel boundaries; peaks: {peaks['source']} burst (HBM copy, bf16 dense = fp16 dense)")
+    return out
+
+
+def spawn_ranks(args, argv) -> None:
+    """`--gpus N` (N > 1) outside a launcher: re-executes this command under torch.distributed.run
+    with N ranks on this node (rendezvous on 127.0.0.1). Inside a launcher the world size must be N."""
+    import socket
+    if "WORLD_SIZE" in os.environ:
+        world = int(os.environ["WORLD_SIZE"])
+        if world != args.gpus:
+            print(json.dumps({"error": f"--gpus {args.gpus} but WORLD_SIZE={world}"}), flush=True)
+            sys.exit(2)
+        return
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={args.gpus}",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__), *argv]
+    sys.stdout.flush()
+    os.execv(sys.executable, cmd)
+
+
+def rank_check() -> None:
+    """Starts the process group (NCCL with GPUs, gloo without), sums one value over the ranks and
+    prints the world size from rank 0."""
+    import torch
+    import torch.distributed as dist
+    rank, world, local = dist_env()
+    backend = "gloo"
+    if world > 1:
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+            backend = "nccl"
+        dist.init_process_group(backend)
+    total = reduce_over_ranks({"one": 1.0}, "sum")["one"]
+    if rank == 0:
+        print(json.dumps({"rank_check": True, "world": world, "ranks_summed": total, "backend": backend}), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def main(argv=None):
+    argv = sys.argv[1:] if argv is None else list(argv)
     args = parse_args(argv)
     if args.oracle_child is not None:
         _oracle_child(args.oracle_child)
+        return
+    if args.gpus > 1:
+        spawn_ranks(args, argv)
+    if args.rank_check:
+        rank_check()
         return
     config = {"workload": f"layer stack: {args.layers} independent MoE layers x ({args.prefill_tokens}-token "
                           f"prefill + {args.decode_steps} batch-1 decode steps)",

@@ -31,18 +31,24 @@
  *   - Argument errors are returned before anything is launched (MOE_ERR_INVALID_ARG,
  *     MOE_ERR_UNSUPPORTED_SHAPE, MOE_ERR_MISALIGNED, MOE_ERR_WORKSPACE_TOO_SMALL). A failed
  *     launch returns MOE_ERR_CUDA. Errors detected on the device (non-finite router logits,
- *     an activation outside the fp16 operand range, a bounded wait that gave up) are ORed into
- *     a sticky status word inside `ws`; read them with moe_read_device_status.
- *   - Numerics of prefill: the expert GEMMs take fp16 operands with fp32 accumulation. Every
- *     dequantized weight scale*q + bias whose exact value has at most 11 significant bits
- *     (e.g. bias = -8*scale) is exact in fp16, x converts exactly from bf16 within the fp16
- *     range, and the SwiGLU output reaches the down projection as an fp16 pair (about 22
- *     significant bits). Routing weights and the combine are fp32; y is rounded once to bf16.
+ *     a value outside the fp16 operand range, a bounded wait that gave up) are ORed into a
+ *     sticky status word inside `ws`; read them with moe_read_device_status. After
+ *     MOE_ERR_DEVICE_TIMEOUT the call's outputs are undefined.
+ *   - Numerics of prefill: the expert GEMMs take fp16 operands with fp32 accumulation. A
+ *     dequantized weight scale*q + bias is one fused multiply-add rounded once to fp16, exact
+ *     whenever its exact value has at most 11 significant bits (e.g. bias = -8*scale). bf16 x
+ *     converts to fp16 exactly for 2^-14 <= |x| <= 65504 and for zero; smaller magnitudes round
+ *     to fp16 subnormals (absolute error at most 2^-25). The SwiGLU output reaches the down
+ *     projection as an fp16 pair (about 22 significant bits). Routing weights and the combine are
+ *     fp32; y is rounded once to bf16. Decode keeps the weights exact (scale and bias applied in
+ *     fp32) and x, h in fp16 operands (h as a leading part and remainder).
  *   - Supported shapes: group == 64, d % 128 == 0, inter % 128 == 0, shared_inter == inter,
  *     1 <= top_k <= 16, top_k <= n_experts <= 1024, 1 <= T <= 65536 (MOE_ERR_UNSUPPORTED_SHAPE).
- *   - The library keeps no state across calls beyond a per-process cache of the driver entry
- *     point used to encode TMA descriptors; calls on different streams with different
- *     workspaces may run concurrently.
+ *   - State kept across calls: per-process caches set once (the driver entry point that encodes
+ *     TMA descriptors, the SM count of the device, the kernels' shared-memory attributes) and,
+ *     for moe_decode_noalloc only, a fixed device array; no call result depends on an earlier
+ *     call. Calls on different streams with different workspaces may run concurrently
+ *     (moe_decode_noalloc excepted: see there).
  */
 #ifndef MOE_GB300_H
 #define MOE_GB300_H
@@ -72,8 +78,10 @@ enum moe_status {
   MOE_ERR_CUDA = 5,               /* a CUDA launch or copy failed                           */
   MOE_ERR_NONFINITE = 6,          /* device: a router logit was NaN or infinite             */
   MOE_ERR_DEVICE_TIMEOUT = 7,     /* device: a bounded wait inside a kernel gave up         */
-  MOE_ERR_OUT_OF_RANGE = 8        /* device: an activation (x or a SwiGLU output) exceeded the
-                                     fp16 operand range (|v| > 65504) of the expert GEMMs    */
+  MOE_ERR_OUT_OF_RANGE = 8        /* device: a value outside what the fp16 operands of the expert
+                                     GEMMs hold: an activation (x or a SwiGLU output) with
+                                     |v| > 65504, or (prefill) a nonzero scale or bias below
+                                     2^-14 in magnitude or with 15*|scale| + |bias| > 65504  */
 };
 
 /* Layer dimensions. `group` is the quantization group along the input dimension (64). */
@@ -243,8 +251,11 @@ MOE_API int moe_decode(const moe_layer* layer, const uint16_t* x, uint16_t* y, m
  *   - Every call uses the same array, which keeps the last call's contents; each call writes
  *     everything it later reads, so nothing has to start at zero. Calls that overlap on the GPU
  *     (other streams or host threads) race on the array: serialise them.
- *   - Device-side errors (e.g. non-finite logits) are not reported by this variant: it has no
- *     status word the caller can read. Argument errors are returned as for moe_decode.
+ *   - Device-side errors (non-finite logits, an activation outside the fp16 range, a bounded
+ *     wait that gave up) are not reported by this variant: it has no status word the caller can
+ *     read, and y may then be non-finite or wrong. Callers that need these errors use
+ *     moe_decode with a workspace and moe_read_device_status. Argument errors are returned as
+ *     for moe_decode.
  */
 MOE_API int moe_decode_noalloc(const moe_layer* layer, const uint16_t* x, uint16_t* y, moe_stream_t stream);
 

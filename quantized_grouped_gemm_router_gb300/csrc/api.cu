@@ -9,9 +9,28 @@
 #include "moe_internal.h"
 
 namespace moe {
-size_t decode_smem_gateup(int d);
-size_t decode_smem_down(int k, int inter);
 int router_tile_rows();
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_dims(const moe_dims* d) {
+  if (!d) return MOE_ERR_INVALID_ARG;
+  if (d->group != kGroup || d->d < kBlockRows || d->d % kBlockRows || d->d > 16384 || d->inter < kBlockRows ||
+      d->inter % kBlockRows || d->inter > 16384 || d->shared_inter != d->inter || d->top_k < 1 ||
+      d->top_k > kMaxTopK || d->n_experts < d->top_k || d->n_experts > kMaxExperts)
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  return MOE_OK;
+}
+
+int check_layer(const moe_layer* L, bool need_router) {
+  if (!L) return MOE_ERR_INVALID_ARG;
+  int st = check_dims(&L->dims);
+  if (st) return st;
+  if (!L->packed || (need_router && !L->router_w)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(L->packed, 128) || !aligned(L->router_w, 16) || !aligned(L->router_bias, 16)) return MOE_ERR_MISALIGNED;
+  return MOE_OK;
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -95,26 +114,6 @@ bool make_down_weight_maps(GemmMaps* g, const uint8_t* packed, const PackedLayou
   const cuuint32_t sbox[4] = {kSBBytes / 8, 1, kb, 1};
   return encode(&g->a, CU_TENSOR_MAP_DATA_TYPE_UINT64, 4, codes, cdims, cstr, cbox, CU_TENSOR_MAP_SWIZZLE_NONE) &&
          encode(&g->a2, CU_TENSOR_MAP_DATA_TYPE_UINT64, 4, sb, sdims, sstr, sbox, CU_TENSOR_MAP_SWIZZLE_NONE);
-}
-
-bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
-int check_dims(const moe_dims* d) {
-  if (!d) return MOE_ERR_INVALID_ARG;
-  if (d->group != kGroup || d->d < kBlockRows || d->d % kBlockRows || d->d > 16384 || d->inter < kBlockRows ||
-      d->inter % kBlockRows || d->inter > 16384 || d->shared_inter != d->inter || d->top_k < 1 ||
-      d->top_k > kMaxTopK || d->n_experts < d->top_k || d->n_experts > kMaxExperts)
-    return MOE_ERR_UNSUPPORTED_SHAPE;
-  return MOE_OK;
-}
-
-int check_layer(const moe_layer* L, bool need_router) {
-  if (!L) return MOE_ERR_INVALID_ARG;
-  int st = check_dims(&L->dims);
-  if (st) return st;
-  if (!L->packed || (need_router && !L->router_w)) return MOE_ERR_INVALID_ARG;
-  if (!aligned(L->packed, 128) || !aligned(L->router_w, 16) || !aligned(L->router_bias, 16)) return MOE_ERR_MISALIGNED;
-  return MOE_OK;
 }
 
 int check_ws(void* ws, size_t ws_bytes, const moe_dims& d, int T) {
@@ -341,10 +340,7 @@ int moe_prefill_timed(const moe_layer* layer, const uint16_t* x, int32_t T, uint
   p.tile_map = w.at<int32_t>(w.L.tile_map);
   p.tile_row0 = w.at<int32_t>(w.L.tile_row0);
   p.n_tiles = w.at<int32_t>(w.L.n_tiles);
-  p.offsets = w.at<int32_t>(w.L.offsets);
-  p.perm = w.at<int32_t>(w.L.perm);
   p.row_tw = w.at<int2>(w.L.row_tw);
-  p.topk_w = w.at<float>(w.L.topk_w);
   p.hidden = hidden;
   p.yacc = yacc;
   p.hdr = w.at<WsHeader>(w.L.header);

@@ -152,7 +152,15 @@ __device__ __forceinline__ uint4 dequant8(uint32_t w, __half2 s2, __half2 b2) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// bf16 (scale, bias) pair -> two fp16x2 broadcasts (exact inside the fp16 range).
+// A (scale, bias) pair the fp16 dequantization cannot carry exactly: a nonzero scale or bias below
+// the normal fp16 range (2^-14, where fp16 starts losing significant bits), or a weight
+// scale * q + bias that could exceed 65504 (q <= 15); NaN and infinity included.
+__device__ __forceinline__ bool sb_out_of_range(uint32_t sbw) {
+  const float as = fabsf(__uint_as_float(sbw << 16)), ab = fabsf(__uint_as_float(sbw & 0xFFFF0000u));
+  return !((as == 0.f || as >= 0x1p-14f) && (ab == 0.f || ab >= 0x1p-14f) && 15.f * as + ab <= 65504.f);
+}
+
+// bf16 (scale, bias) pair -> two fp16x2 broadcasts (exact inside the range sb_out_of_range checks).
 __device__ __forceinline__ void scale_bias(uint32_t sbw, __half2& s2, __half2& b2) {
   const __half sh = __float2half_rn(__uint_as_float(sbw << 16));
   const __half bh = __float2half_rn(__uint_as_float(sbw & 0xFFFF0000u));
@@ -205,16 +213,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = smem_raw + (base - raw_u32);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---------------------------------------------------------------- work list
-  int n_routed = 0, n_tile_total;
-  if (MODE == kModeRouter) {
-    n_tile_total = (p.T + kRouterRows - 1) / kRouterRows;
-  } else {
-    n_routed = *p.n_tiles;
-    n_tile_total = n_routed + (p.T + kTileRows - 1) / kTileRows;  // routed tiles, then shared
-  }
-  const int n_items = n_tile_total * p.m_tiles;
-  if ((int)blockIdx.x >= n_items) return;  // nothing for this CTA (uniform: before any set-up)
   const int KB = p.k_blocks;
 
   const uint32_t bars = base + S::bar_off;
@@ -272,6 +270,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
+
+  // ---------------------------------------------------------------- work list
+  // Everything above touched only this CTA's shared and tensor memory, so it overlaps the
+  // predecessor kernel (programmatic dependent launch); the tile count and every activation are
+  // read after it has completed. A CTA past the end of the work list runs empty loops.
+  pdl_wait();
+  pdl_launch_dependents();
+  int n_routed = 0, n_tile_total;
+  if (MODE == kModeRouter) {
+    n_tile_total = (p.T + kRouterRows - 1) / kRouterRows;
+  } else {
+    n_routed = *p.n_tiles;
+    n_tile_total = n_routed + (p.T + kTileRows - 1) / kTileRows;  // routed tiles, then shared
+  }
+  const int n_items = n_tile_total * p.m_tiles;
 
   if (warp == kWarpW) {
     // ------------------------------------------------------------ weight producer
@@ -418,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int r = quad * 32 + lane;  // A row
       const uint32_t lanes = (uint32_t)(quad * 32) << 16;
       uint32_t ga = 0, gw = 0;
-      bool ok = true;
+      bool ok = true, sb_bad = false;
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
         for (int kb0 = 0; kb0 < KB && ok; kb0 += C::kSW, ++gw) {
           const int nk = min(C::kSW, KB - kb0);  // even: KB and kSW are
@@ -447,6 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int t = 0; t < kAK; ++t) {
               __half2 s2, b2;
+              sb_bad |= sb_out_of_range(sbw[t]);
               scale_bias(sbw[t], s2, b2);
               const uint32_t words[4] = {cw[t].x, cw[t].y, cw[t].z, cw[t].w};
               uint32_t v[16];
@@ -471,6 +485,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      // scales or biases the fp16 operands cannot hold exactly are reported, not hidden
+      if (__any_sync(0xFFFFFFFFu, sb_bad) && lane == 0) set_device_status(p.hdr, MOE_ERR_OUT_OF_RANGE);
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -616,8 +632,7 @@ cudaError_t launch_mode(const GemmParams& p, const GemmMaps* maps, int max_items
                                                  Smem<MODE>::alloc);
   if (attr != cudaSuccess) return attr;
   const int grid = max_items < num_sms() ? max_items : num_sms();  // persistent: one CTA per SM
-  moe_gemm_kernel<MODE><<<grid, kThreads, Smem<MODE>::alloc, s>>>(p, *maps);
-  return cudaGetLastError();
+  return launch_pdl(moe_gemm_kernel<MODE>, grid, kThreads, (size_t)Smem<MODE>::alloc, 1, s, p, *maps);
 }
 
 }  // namespace

@@ -178,10 +178,7 @@ struct GemmParams {
   const int32_t* tile_map;    // [max_tiles, 3]
   const int32_t* tile_row0;   // [max_tiles]
   const int32_t* n_tiles;     // device count of routed tiles
-  const int32_t* offsets;     // [E + 1]
-  const int32_t* perm;        // [A]
   const int2* row_tw;         // [A] (token, routing weight bits) of each expert-sorted row
-  const float* topk_w;        // [A]
   // activations
   uint16_t* hidden;           // [2, A + T, I] fp16: leading part, then remainder (gate/up writes,
                               // down reads both planes via TMA)
@@ -207,6 +204,12 @@ struct DecodeParams {
   WsHeader* hdr;
   int d, E, k, inter;
 };
+
+// Argument checks shared by every entry point (csrc/api.cu): supported dims, and a layer's
+// pointers (non-NULL where required, 128-byte aligned packed weights, 16-byte aligned router).
+bool aligned(const void* p, size_t a);
+int check_dims(const moe_dims* d);
+int check_layer(const moe_layer* L, bool need_router);
 
 // Launchers (each returns cudaGetLastError()).
 cudaError_t launch_wait_timeout_selftest(WsHeader* hdr, cudaStream_t s);

@@ -65,29 +65,19 @@ cudaError_t scratch_address(void** out) {
   return cudaSuccess;
 }
 
-int check_dims_noalloc(const moe_dims& d) {
-  if (d.group != kGroup || d.d < kBlockRows || d.d % kBlockRows || d.d > 16384 || d.inter < kBlockRows ||
-      d.inter % kBlockRows || d.inter > 16384 || d.shared_inter != d.inter || d.top_k < 1 || d.top_k > kMaxTopK ||
-      d.n_experts < d.top_k || d.n_experts > kMaxExperts || d.d > kDecodeMaxD)
-    return MOE_ERR_UNSUPPORTED_SHAPE;
-  return MOE_OK;
-}
-
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 }  // namespace
 }  // namespace moe
 
 using namespace moe;
 
 extern "C" int moe_decode_noalloc(const moe_layer* layer, const uint16_t* x, uint16_t* y, moe_stream_t stream) {
-  if (!layer || !x || !y || !layer->packed || !layer->router_w) return MOE_ERR_INVALID_ARG;
-  const moe_dims& d = layer->dims;
-  int st = check_dims_noalloc(d);
+  // the same checks as moe_decode, then the limits of this variant
+  int st = check_layer(layer, true);
   if (st) return st;
-  if ((reinterpret_cast<uintptr_t>(layer->packed) & 127u) || !aligned16(layer->router_w) ||
-      !aligned16(layer->router_bias) || !aligned16(x) || !aligned16(y))
-    return MOE_ERR_MISALIGNED;
+  if (!x || !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(y, 16)) return MOE_ERR_MISALIGNED;
+  const moe_dims& d = layer->dims;
+  if (d.d > kDecodeMaxD) return MOE_ERR_UNSUPPORTED_SHAPE;
   const ScratchLayout L = scratch_layout(d);
   if (L.total > kNoAllocScratchBytes) return MOE_ERR_UNSUPPORTED_SHAPE;  // shape needs more scratch
   void* base = nullptr;

@@ -3,7 +3,8 @@
 // selection, histogram, prefix scan, scatter and block map run on the GPU with no host round
 // trip). Three launches (four in prefill):
 //   route_topk_kernel    16 tokens per CTA: warp top-k on order-preserving logit keys (ties to
-//                        the lower index), renormalised softmax weights; the fp16 copy of x and
+//                        the lower index; a threshold from the lanes' maxima, then exact ranks of
+//                        the few experts above it), renormalised softmax weights; the fp16 copy of x and
 //                        the zeroing of the combine accumulator rows
 //   route_hist_kernel    one CTA per 64-token chunk: histogram in shared memory; the last CTA to
 //                        finish (ticket) scans the chunk histograms into counts, offsets,
@@ -59,18 +60,20 @@ __device__ int block_exclusive_scan4(const int (&v)[4], int* s_warp, int* total)
 // x and of the zeroing of the combine accumulator (wide grid: this is the launch that moves
 // the bytes).
 __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const RouteParams p) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int E = p.E, k = p.k;
   const int t_begin = blockIdx.x * kTopkTokens;
   const int t_end = min(p.T, t_begin + kTopkTokens);
   for (int t = t_begin + warp; t < t_end; t += kTopkThreads / 32) {
-    int my_e;
+    int rank, my_e;
     float my_w;
-    const bool bad = warp_topk_softmax(p.logits + (size_t)t * E, E, k, &my_e, &my_w);
+    const bool bad = warp_select_topk(p.logits + (size_t)t * E, E, k, &rank, &my_e, &my_w);
     if (bad && lane == 0) set_device_status(p.hdr, MOE_ERR_NONFINITE);
-    if (lane < k) {
-      p.topk_idx[(size_t)t * k + lane] = my_e;
-      p.topk_w[(size_t)t * k + lane] = my_w;
+    if (rank >= 0) {
+      p.topk_idx[(size_t)t * k + rank] = my_e;
+      p.topk_w[(size_t)t * k + rank] = my_w;
     }
   }
   const int n8 = (t_end - t_begin) * p.d / 8;  // 8-element chunks of this CTA's rows
@@ -105,6 +108,8 @@ __global__ void __launch_bounds__(kTopkThreads) route_hist_kernel(const RoutePar
   __shared__ int s_counts[kMaxExperts];
   __shared__ int s_warp[32];
   __shared__ int s_last;
+  pdl_wait();
+  pdl_launch_dependents();
   const int tid = threadIdx.x;
   const int c = blockIdx.x;
   const int E = p.E, k = p.k;
@@ -182,6 +187,8 @@ __global__ void __launch_bounds__(kTopkThreads) route_hist_kernel(const RoutePar
 constexpr int kScatterWarps = 8;
 __global__ void __launch_bounds__(kScatterWarps * 32) route_scatter_kernel(const RouteParams p) {
   __shared__ int s_run[kScatterWarps][kMaxExperts];  // counts, then first free positions
+  pdl_wait();
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int c = blockIdx.x;
   const int E = p.E;
@@ -233,6 +240,8 @@ __global__ void __launch_bounds__(kScatterWarps * 32) route_scatter_kernel(const
 
 // One warp per sorted row: x16[pos] = x16[A + perm[pos] / k] (16-byte copies, d/8 per row).
 __global__ void __launch_bounds__(256) route_rows_kernel(const RouteParams p) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int A = p.T * p.k, n16 = p.d / 8;
   const int warps = gridDim.x * (blockDim.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -245,6 +254,8 @@ __global__ void __launch_bounds__(256) route_rows_kernel(const RouteParams p) {
 }
 
 __global__ void __launch_bounds__(256) cast_kernel(const float* __restrict__ yacc, uint16_t* __restrict__ y, size_t n8) {
+  pdl_wait();
+  pdl_launch_dependents();
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
     const float4 a = reinterpret_cast<const float4*>(yacc)[2 * i];
     const float4 b = reinterpret_cast<const float4*>(yacc)[2 * i + 1];
@@ -261,25 +272,23 @@ __global__ void __launch_bounds__(256) cast_kernel(const float* __restrict__ yac
 
 }  // namespace
 
+// Every launch is chained to its predecessor with programmatic dependent launch: it starts while
+// the predecessor finishes and waits for it (pdl_wait) before touching any data.
 cudaError_t launch_route(const RouteParams& p, cudaStream_t s) {
-  route_topk_kernel<<<(p.T + kTopkTokens - 1) / kTopkTokens, kTopkThreads, 0, s>>>(p);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err = launch_pdl(route_topk_kernel, (p.T + kTopkTokens - 1) / kTopkTokens, kTopkThreads, 0, 1, s, p);
   if (err != cudaSuccess) return err;
-  route_hist_kernel<<<p.n_chunks, kTopkThreads, 0, s>>>(p);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  route_scatter_kernel<<<p.n_chunks, kScatterWarps * 32, 0, s>>>(p);
-  if ((err = cudaGetLastError()) != cudaSuccess || !p.x) return err;
+  if ((err = launch_pdl(route_hist_kernel, p.n_chunks, kTopkThreads, 0, 1, s, p)) != cudaSuccess) return err;
+  if ((err = launch_pdl(route_scatter_kernel, p.n_chunks, kScatterWarps * 32, 0, 1, s, p)) != cudaSuccess || !p.x)
+    return err;
   const int rows = p.T * p.k, per_cta = 8;  // 8 warps of 256 threads
   const int blocks = (rows + per_cta - 1) / per_cta < 152 * 8 ? (rows + per_cta - 1) / per_cta : 152 * 8;
-  route_rows_kernel<<<blocks, 256, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(route_rows_kernel, blocks, 256, 0, 1, s, p);
 }
 
 cudaError_t launch_cast(const float* yacc, uint16_t* y, size_t n, cudaStream_t s) {
   const size_t n8 = n / 8;
   const int blocks = (int)((n8 + 255) / 256 < 1216 ? (n8 + 255) / 256 : 1216);
-  cast_kernel<<<blocks > 0 ? blocks : 1, 256, 0, s>>>(yacc, y, n8);
-  return cudaGetLastError();
+  return launch_pdl(cast_kernel, blocks > 0 ? blocks : 1, 256, 0, 1, s, yacc, y, n8);
 }
 
 }  // namespace moe

@@ -48,3 +48,23 @@ def test_replica_reduction_gloo():
 def test_single_process_is_identity():
     import bench
     assert bench.reduce_over_ranks({"a": 3.0}, "max") == {"a": 3.0}
+
+
+def test_bench_gpus_flag_starts_the_ranks():
+    """`bench.py --gpus 2` outside a launcher starts two ranks itself (torch.distributed.run on
+    127.0.0.1; gloo here without GPUs) and they form one group; inside a launcher whose world size
+    differs from --gpus it refuses to run."""
+    import json
+    import subprocess
+    import sys
+    import bench
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_PORT")}
+    res = subprocess.run([sys.executable, os.path.join(bench.ROOT, "bench.py"), "--gpus", "2", "--rank-check"],
+                         capture_output=True, text=True, timeout=180, env=env)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [json.loads(ln) for ln in res.stdout.splitlines() if ln.startswith("{")]
+    assert lines == [{"rank_check": True, "world": 2, "ranks_summed": 2.0, "backend": lines[0]["backend"]}]
+    env["WORLD_SIZE"] = "3"
+    res = subprocess.run([sys.executable, os.path.join(bench.ROOT, "bench.py"), "--gpus", "2", "--rank-check"],
+                         capture_output=True, text=True, timeout=60, env=env)
+    assert res.returncode == 2

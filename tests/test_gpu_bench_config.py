@@ -1,7 +1,8 @@
-"""Full-size parity in the launch configuration bench.py times: the layer-stack workload's
-layers at T=4096 and batch-1 decode, replayed from CUDA graphs, checked against the oracle on
-sampled tokens (each token's output depends only on that token, so the oracle computes the
-sampled rows alone)."""
+"""Full-size parity in the launch configuration bench.py times: the whole layer-stack workload
+(40 layers at T=4096, 256 batch-1 decode steps through the 40 layers), replayed from CUDA graphs,
+checked against the oracle on layers 0, 19 and 39 (sampled prefill tokens; decode steps 0, 127
+and 255). Each token's output depends only on that token, so the oracle computes the sampled
+rows alone."""
 import numpy as np
 import pytest
 
@@ -16,7 +17,7 @@ pytestmark = pytest.mark.gpu
 
 
 def test_bench_launch_configuration_sampled():
-    args = bench.parse_args(["--layers", "2", "--prefill-tokens", "4096", "--decode-steps", "3"])
+    args = bench.parse_args(["--layers", "40", "--prefill-tokens", "4096", "--decode-steps", "256"])
     from quantized_grouped_gemm_router_gb300 import build as B
     B.build()
     W = bench.Workload(args, torch.device("cuda", 0))
@@ -27,7 +28,9 @@ def test_bench_launch_configuration_sampled():
     torch.cuda.synchronize()
     assert W.m.read_device_status(W.ws_p) == 0 and W.m.read_device_status(W.ws_d) == 0
     rng = np.random.default_rng(0)
-    for l in range(args.layers):
+    xd = make_tokens(args.decode_steps * args.layers, FULL.d, seed=0, stream=2).reshape(
+        args.decode_steps, args.layers, FULL.d)
+    for l in (0, 19, 39):
         npl = make_layer(FULL, seed=l)
         xp = make_tokens(4096, FULL.d, seed=l, stream=1)
         rows = np.sort(rng.choice(4096, size=24, replace=False))
@@ -35,8 +38,6 @@ def test_bench_launch_configuration_sampled():
         ref = O.moe_forward(xp[rows], npl, tile_rows=256)["y"]
         got = C.bf16_bits_f64(W.yp[l][torch.as_tensor(rows, device="cuda")])
         C.check_y(got, ref, f"prefill layer {l}")
-        xd = make_tokens(args.decode_steps * args.layers, FULL.d, seed=0, stream=2).reshape(
-            args.decode_steps, args.layers, FULL.d)
-        for s in range(args.decode_steps):
+        for s in (0, 127, 255):
             ref = O.moe_forward(xd[s, l][None], npl, tile_rows=256)["y"]
             C.check_y(C.bf16_bits_f64(W.yd[s, l][None]), ref, f"decode step {s} layer {l}")
