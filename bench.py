@@ -181,11 +181,12 @@ def src_sha(*rel_paths) -> str:
 
 
 _CSRC = "quantized_grouped_gemm_router_gb300/csrc/"
+# the kernels' own device sources (the DRAM traffic of a capture holds while these are unchanged)
 KERNEL_SOURCES = {
-    "prefill_gate_up_gemm": (_CSRC + "gemm.cu", _CSRC + "ptx.cuh", _CSRC + "moe_internal.h"),
-    "prefill_down_gemm": (_CSRC + "gemm.cu", _CSRC + "ptx.cuh", _CSRC + "moe_internal.h"),
-    "prefill_router_gemm": (_CSRC + "gemm.cu", _CSRC + "ptx.cuh", _CSRC + "moe_internal.h"),
-    "decode_layer": (_CSRC + "decode.cu", _CSRC + "topk.cuh", _CSRC + "ptx.cuh", _CSRC + "moe_internal.h"),
+    "prefill_gate_up_gemm": (_CSRC + "gemm.cu", _CSRC + "ptx.cuh"),
+    "prefill_down_gemm": (_CSRC + "gemm.cu", _CSRC + "ptx.cuh"),
+    "prefill_router_gemm": (_CSRC + "gemm.cu", _CSRC + "ptx.cuh"),
+    "decode_layer": (_CSRC + "decode.cu", _CSRC + "topk.cuh", _CSRC + "ptx.cuh"),
 }
 
 
@@ -392,7 +393,9 @@ class Workload:
 
     def launches_per_step(self) -> int:
         a = self.args
-        return (6 * a.layers if a.prefill_tokens else 0) + 3 * a.layers * a.decode_steps
+        # prefill: router GEMM, top-k, histogram, scatter, row placement, gate/up, down, cast;
+        # decode: router GEMV, expert kernel (with the combine)
+        return (8 * a.layers if a.prefill_tokens else 0) + 2 * a.layers * a.decode_steps
 
 
 def capture(W: Workload, ev_pre=None, ev_dec=None, graphs: bool = True):
@@ -436,9 +439,10 @@ def run_ours(args, config: dict) -> None:
     W = Workload(args, device, seed_offset=1000 * rank)
     L, T, S = args.layers, args.prefill_tokens, args.decode_steps
 
-    # events inside the timed region: per kernel for every prefill layer; around every 16th
-    # 40-layer decode step (decode kernels overlap through PDL, so the unit is the layer)
-    ev_pre = {l: _new_events(6) for l in range(L)} if T else {}
+    # events inside the timed region: per kernel on every 8th prefill layer; around every 16th
+    # 40-layer decode step (kernels overlap through PDL, which an event between two kernels stops,
+    # so most layers run without them and the decode unit is the whole layer)
+    ev_pre = {l: _new_events(6) for l in range(0, L, 8)} if T else {}
     ev_dec = {s: tuple(_new_events(2)) for s in range(0, S, 16)}
     for _ in range(2):                     # eager warm-up (also initialises the library)
         if T:
@@ -531,7 +535,7 @@ def run_ours(args, config: dict) -> None:
         return
     peaks = load_peaks()
     work = algorithmic_work(W.shape.d, W.shape.n_experts, W.shape.top_k, W.shape.inter, T)
-    per_step_launches = {n: L for n in names_pre}
+    per_step_launches = {n: L for n in names_pre}  # the sampled layers' averages stand for all
     per_step_launches.update({n: L * S for n in names_dec})
     rooflines = []
     traffic = measured_traffic(T, args.router_bias)
@@ -606,11 +610,13 @@ def decode_diagnostics(W, steps: int = 8) -> dict:
                    "expert kernel's weight copies for experts 0..k-1 and the shared expert, launched alone"}
 
 
-def _graph_time_ms(body, reps: int = 3) -> float:
-    """Best of `reps` replays of a CUDA graph captured from body() (after one eager run and one
-    untimed replay), in milliseconds."""
+def _graph_time_ms(body, reps: int = 3, eager: bool = True) -> float:
+    """Best of `reps` replays of a CUDA graph captured from body() (after one eager run, unless
+    `eager` is false, and one untimed replay), in milliseconds. A body that hands events to the
+    library records them as graph nodes, so it is only captured, never run eagerly."""
     import torch
-    body()
+    if eager:
+        body()
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
@@ -770,14 +776,14 @@ def config_results(W, peaks: dict, reps: int = 8) -> dict:
         for r in range(reps):
             flush.fill_(r & 0x7F)
             m.decode(W.layers[r % nl], x1[r], ws1, y=y1[r], events=[ev[r][0], None, None, ev[r][1]])
-    _graph_time_ms(dec_body, reps=1)
+    _graph_time_ms(dec_body, reps=1, eager=False)
     us = statistics.median(1e3 * a.elapsed_time(b) for a, b in ev)
     nbytes = algorithmic_work(d, E, k, I, 1)["decode_layer"]["bytes"]
     out["decode"] = {"workload": "single MoE layer, batch-1 decode (T=1), cold L2", "us_per_layer": us,
                      "roofline": {"bound": "hbm", "achieved": nbytes / (us * 1e3), "peak": hbm, "unit": "GB/s",
                                   "frac": nbytes / (us * 1e3) / hbm, "per_launch_bytes": nbytes}}
 
-    def prefill_config(T, layers, seed_stream):
+    def prefill_config(T, layers, seed_stream, arms):
         xs = [torch.from_numpy(make_tokens(T, d, seed=i, stream=seed_stream).view(np.int16)).to(dev)
               for i in range(len(layers))]
         ys = [torch.empty_like(x) for x in xs]
@@ -788,7 +794,10 @@ def config_results(W, peaks: dict, reps: int = 8) -> dict:
             for r in range(reps):
                 for i, layer in enumerate(layers):
                     m.prefill(layer, xs[i], ws, y=ys[i], events=evs[r][i])
-        _graph_time_ms(body, reps=1)
+        _graph_time_ms(body, reps=1, eager=False)
+        abl = {}
+        for arm in arms:
+            abl[arm] = prefill_ablation_arm(m, arm, layers, xs, ys, ws, reps)
         names = ["router", "route", "gate_up", "down", "cast"]
         per = {n: statistics.mean(1e3 * e[j].elapsed_time(e[j + 1]) for row in evs for e in row)
                for j, n in enumerate(names)}
@@ -799,7 +808,7 @@ def config_results(W, peaks: dict, reps: int = 8) -> dict:
             hit.append(int((o["counts"] > 0).sum()))
         if m.read_device_status(ws):
             raise RuntimeError("device status set during the per-workload sub-results")
-        return layer_us, per, statistics.mean(hit)
+        return layer_us, per, statistics.mean(hit), abl
 
     def gemm_flop(T):
         return 2.0 * (T * k + T) * 3 * I * d
@@ -807,7 +816,7 @@ def config_results(W, peaks: dict, reps: int = 8) -> dict:
     # ---- 512-token prefill, near-uniform routing
     lay = W.layers[:min(len(W.layers), 4)]
     T = 512
-    layer_us, per, hit = prefill_config(T, lay, 3)
+    layer_us, per, hit, abl = prefill_config(T, lay, 3, ("host_routing", "dense"))
     nbytes = (hit + 1) * one_expert + E * d * 2 + 2 * T * d * 2
     gemm_us = per["gate_up"] + per["down"]
     out["prefill512"] = {
@@ -815,13 +824,13 @@ def config_results(W, peaks: dict, reps: int = 8) -> dict:
         "tok_per_s": T / (layer_us * 1e-6), "kernels_us": per, "experts_hit": hit,
         "roofline": {"bound": "hbm", "achieved": nbytes / (layer_us * 1e3), "peak": hbm, "unit": "GB/s",
                      "frac": nbytes / (layer_us * 1e3) / hbm, "per_launch_bytes": nbytes},
-        "gemm_tensor_frac": gemm_flop(T) / (gemm_us * 1e-6) / 1e12 / tf}
+        "gemm_tensor_frac": gemm_flop(T) / (gemm_us * 1e-6) / 1e12 / tf, "ablations": abl}
 
     # ---- 2048-token prefill, Zipf router bias
     rb = torch.from_numpy(zipf_router_bias(E)).to(dev)
     lay = [m.Layer(W.dims, L.router_w, rb, L.packed) for L in W.layers[:min(len(W.layers), 8)]]
     T = 2048
-    layer_us, per, hit = prefill_config(T, lay, 4)
+    layer_us, per, hit, abl = prefill_config(T, lay, 4, ("host_routing", "tile32"))
     gemm_us = per["gate_up"] + per["down"]
     ach = gemm_flop(T) / (gemm_us * 1e-6) / 1e12
     out["skew2048"] = {
@@ -830,10 +839,58 @@ def config_results(W, peaks: dict, reps: int = 8) -> dict:
         "roofline": {"bound": "tensor", "kernel": "grouped gate/up + down GEMMs", "achieved": ach, "peak": tf,
                      "unit": "TFLOP/s", "frac": ach / tf, "frac_of_sustained": ach / peaks["bf16_tflops_sustained"],
                      "per_launch_flop": gemm_flop(T)},
-        "layer_tensor_frac": (gemm_flop(T) + 2.0 * T * E * d) / (layer_us * 1e-6) / 1e12 / tf}
+        "layer_tensor_frac": (gemm_flop(T) + 2.0 * T * E * d) / (layer_us * 1e-6) / 1e12 / tf, "ablations": abl}
     out["how"] = (f"CUDA graphs of {reps} repetitions; events recorded by moe_decode_timed / moe_prefill_timed "
                   f"at the kernel boundaries; peaks: {peaks['source']} burst (HBM copy, bf16 dense = fp16 dense)")
     return out
+
+
+def prefill_ablation_arm(m, arm: str, layers, xs, ys, ws, reps: int) -> dict:
+    """One ablation arm of the page's prefill design against the product path, on the same layers
+    and inputs (section "Prefill: keep routing on the GPU, dequantize in flight"):
+      host_routing  the block map built on the host after a stream synchronisation, against the
+                    GPU-resident routing: both called eagerly and timed per call on the host clock
+                    (the arm cannot be graph-captured); `speedup` = arm time / product time, the
+                    page's "+89%" at 512 tokens is a speedup of 1.89;
+      tile32        32-row block-map tiles against tiles of up to moe_tile_rows() rows, both replayed
+                    from CUDA graphs; `speedup` = arm time / product time (the page: +13.2% for its
+                    32-row tiles over 16-row ones at 2K tokens);
+      dense         the selected experts' weights expanded to fp16 in a buffer first, then dense
+                    GEMMs, against in-tile dequantization, both from CUDA graphs (the page: +77.4%
+                    at 512 tokens for in-tile dequantization over materialised bf16 weights)."""
+    import torch
+    n = len(layers)
+    aux = None
+    if arm == "host_routing":
+        def wall(fn):
+            fn(0)
+            torch.cuda.synchronize()
+            ts = []
+            for r in range(reps):
+                for i in range(n):
+                    t0 = time.perf_counter()
+                    fn(i)
+                    torch.cuda.synchronize()
+                    ts.append(time.perf_counter() - t0)
+            return 1e6 * statistics.median(ts)
+        base = wall(lambda i: m.prefill(layers[i], xs[i], ws, y=ys[i]))
+        t = wall(lambda i: m.prefill_ablation(layers[i], xs[i], ws, m.PREFILL_ARM_HOST_ROUTING, y=ys[i]))
+        how = "eager calls, host clock per call with a synchronize, median"
+    else:
+        def graph(fn):
+            def body():
+                for _ in range(reps):
+                    for i in range(n):
+                        fn(i)
+            return 1e3 * _graph_time_ms(body) / (reps * n)
+        code = m.PREFILL_ARM_TILE32 if arm == "tile32" else m.PREFILL_ARM_DENSE
+        n_aux = m.ablation_aux_bytes(layers[0].dims, code)
+        aux = torch.empty(n_aux, dtype=torch.uint8, device=xs[0].device) if n_aux else None
+        base = graph(lambda i: m.prefill(layers[i], xs[i], ws, y=ys[i]))
+        t = graph(lambda i: m.prefill_ablation(layers[i], xs[i], ws, code, y=ys[i], aux=aux))
+        how = "CUDA graphs over the rotated layers, best of 3 replays"
+    del aux
+    return {"arm_us_per_layer": t, "product_us_per_layer": base, "speedup": t / base, "how": how}
 
 
 def spawn_ranks(args, argv) -> None:

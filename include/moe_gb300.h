@@ -218,6 +218,39 @@ MOE_API int moe_prefill_chunked(const moe_layer* layer, const uint16_t* x, int64
                                 int32_t chunk_tokens, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /*
+ * Prefill ablations: the three design choices the page measures one at a time (section "Prefill:
+ * keep routing on the GPU, dequantize in flight": in-tile dequantization +77.4% and GPU-resident
+ * routing +89% at 512 tokens, 32-row tiles +13.2% at 2K tokens), each undone in an otherwise
+ * unchanged moe_prefill, so that the benchmark can time what each buys on this GPU. Arguments,
+ * checks and results as moe_prefill (no routing outputs); `arm`:
+ *   MOE_PREFILL_ARM_HOST_ROUTING  after the top-k kernel the selection is copied to the host and
+ *                                 the stream is synchronised; the host computes the histogram,
+ *                                 scan, stable scatter and block map and copies them back (the
+ *                                 round trip the GPU-resident routing removes). This arm
+ *                                 synchronises `stream` and allocates host memory; it cannot be
+ *                                 captured in a CUDA graph.
+ *   MOE_PREFILL_ARM_TILE32        block-map tiles of 32 rows instead of moe_tile_rows() (fixed
+ *                                 narrow tiles, as on the page, instead of tiles as tall as the
+ *                                 expert's rows allow); the workspace of moe_workspace_bytes
+ *                                 holds either tiling.
+ *   MOE_PREFILL_ARM_DENSE         materialised dequantization: the weights of every selected
+ *                                 expert and of the shared expert are first expanded to fp16
+ *                                 (scale * q + bias rounded once, the values the in-tile path
+ *                                 computes) into `aux`, then the grouped GEMMs read those dense
+ *                                 weights instead of the packed codes. aux: device buffer of at
+ *                                 least moe_prefill_ablation_aux_bytes(dims, arm) bytes, 128-byte
+ *                                 aligned (NULL and 0 for the other arms).
+ * MOE_ERR_INVALID_ARG for another arm or a missing aux buffer, MOE_ERR_WORKSPACE_TOO_SMALL for a
+ * short one.
+ */
+#define MOE_PREFILL_ARM_HOST_ROUTING 1
+#define MOE_PREFILL_ARM_TILE32 2
+#define MOE_PREFILL_ARM_DENSE 3
+MOE_API size_t moe_prefill_ablation_aux_bytes(const moe_dims* dims, int arm);
+MOE_API int moe_prefill_ablation(const moe_layer* layer, const uint16_t* x, int32_t T, uint16_t* y, int arm,
+                                 void* ws, size_t ws_bytes, void* aux, size_t aux_bytes, moe_stream_t stream);
+
+/*
  * Batch-1 decode forward (sections "Prefill and decode are different problems" and
  * "Decode: minimize bytes per token"): router GEMV and top-k, then Q4 GEMVs that stream only
  * the top_k selected experts and the shared expert, gate activation fused into the input
@@ -231,6 +264,21 @@ MOE_API int moe_prefill_chunked(const moe_layer* layer, const uint16_t* x, int64
  */
 MOE_API int moe_decode(const moe_layer* layer, const uint16_t* x, uint16_t* y, moe_route_out* out,
                void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * Small-batch decode of T = 1..8 tokens at once (page, section "What didn't work": verifying 2 to
+ * 5 draft tokens at once, whose rows route to different experts): the router and the selection
+ * of every token, then one pass over the union of the experts the T tokens selected (each
+ * distinct expert's weights are streamed once and applied to every token that chose it, the
+ * tokens filling the columns of the MMAs), the shared expert likewise, and a fixed-order combine
+ * per token. Each token's y equals what moe_decode gives for it alone, up to fp32 summation order.
+ * x, y: bf16 [T, d]. ws: at least moe_workspace_bytes(dims, T). `out` may be NULL; it receives
+ * logits [T, E], topk_idx [T, k] and topk_w [T, k].
+ * Supports d <= 2048 and T <= 8 (MOE_ERR_UNSUPPORTED_SHAPE otherwise); INVALID_ARG for T < 1.
+ * Kernels chained by programmatic dependent launch, as moe_decode.
+ */
+MOE_API int moe_decode_batch(const moe_layer* layer, const uint16_t* x, int32_t T, uint16_t* y,
+                             moe_route_out* out, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /*
  * Allocation-free batch-1 decode. The paper has no counterpart to this call; it exists for
@@ -267,8 +315,8 @@ MOE_API int moe_decode_noalloc(const moe_layer* layer, const uint16_t* x, uint16
  *   prefill: events[0] before the router GEMM, [1] before the routing kernels (top-k and
  *            scatter), [2] before the gate/up GEMM, [3] before the down GEMM, [4] before the
  *            output cast, [5] after it (6 entries).
- *   decode:  events[0] before the router GEMV + top-k, [1] before the expert kernel (gate/up
- *            GEMV + SwiGLU + this block's down partial), [2] before the combine of the partial
+ *   decode:  events[0] before the router GEMV, [1] before the expert kernel (top-k, gate/up
+ *            GEMV + SwiGLU, each block's down partial), [2] before the combine of the partial
  *            outputs, [3] after it (4 entries). Events between the kernels also stop them from
  *            overlapping through programmatic dependent launch.
  */

@@ -10,6 +10,7 @@ from .binding import (  # noqa: F401
     MoeDims,
     MoeError,
     decode,
+    decode_batch,
     decode_noalloc,
     decode_diag,
     DECODE_DIAG_NO_MATH,
@@ -19,6 +20,11 @@ from .binding import (  # noqa: F401
     pack_weights,
     packed_bytes,
     prefill,
+    prefill_ablation,
+    PREFILL_ARM_HOST_ROUTING,
+    PREFILL_ARM_TILE32,
+    PREFILL_ARM_DENSE,
+    ablation_aux_bytes,
     prefill_chunked,
     read_device_status,
     route,

@@ -85,6 +85,14 @@ def lib() -> ctypes.CDLL:
         L.moe_decode_timed.restype = ctypes.c_int
         L.moe_decode_diag.argtypes = [P(MoeLayer), c_void_p, c_void_p, c_void_p, c_size_t, ctypes.c_int, c_void_p]
         L.moe_decode_diag.restype = ctypes.c_int
+        L.moe_decode_batch.argtypes = [P(MoeLayer), c_void_p, c_int32, c_void_p, P(RouteOut), c_void_p, c_size_t,
+                                       c_void_p]
+        L.moe_decode_batch.restype = ctypes.c_int
+        L.moe_prefill_ablation.argtypes = [P(MoeLayer), c_void_p, c_int32, c_void_p, ctypes.c_int, c_void_p, c_size_t,
+                                           c_void_p, c_size_t, c_void_p]
+        L.moe_prefill_ablation.restype = ctypes.c_int
+        L.moe_prefill_ablation_aux_bytes.argtypes = [P(MoeDims), ctypes.c_int]
+        L.moe_prefill_ablation_aux_bytes.restype = c_size_t
         L.moe_decode_noalloc.argtypes = [P(MoeLayer), c_void_p, c_void_p, c_void_p]
         L.moe_decode_noalloc.restype = ctypes.c_int
         L.moe_read_device_status.argtypes = [c_void_p, c_void_p]
@@ -237,6 +245,26 @@ def prefill(layer: Layer, x: torch.Tensor, ws: torch.Tensor, y: torch.Tensor | N
     return y
 
 
+PREFILL_ARM_HOST_ROUTING, PREFILL_ARM_TILE32, PREFILL_ARM_DENSE = 1, 2, 3
+
+
+def ablation_aux_bytes(dims: MoeDims, arm: int) -> int:
+    return int(lib().moe_prefill_ablation_aux_bytes(ctypes.byref(dims), int(arm)))
+
+
+def prefill_ablation(layer: Layer, x: torch.Tensor, ws: torch.Tensor, arm: int,
+                     y: torch.Tensor | None = None, aux: torch.Tensor | None = None) -> torch.Tensor:
+    """moe_prefill_ablation: moe_prefill with the block map built on the host after a stream
+    synchronisation (arm 1), with 32-row block-map tiles (arm 2), or on weights expanded to fp16
+    into `aux` first (arm 3; aux of ablation_aux_bytes(dims, 3) bytes)."""
+    _check_dev(x, torch.int16, "x")
+    y = y if y is not None else torch.empty_like(x)
+    _check(lib().moe_prefill_ablation(ctypes.byref(layer.c), x.data_ptr(), x.shape[0], y.data_ptr(), int(arm),
+                                      ws.data_ptr(), ws.numel(), _ptr(aux), 0 if aux is None else aux.numel(),
+                                      _stream()), "moe_prefill_ablation")
+    return y
+
+
 def prefill_chunked(layer: Layer, x: torch.Tensor, ws: torch.Tensor, chunk_tokens: int,
                     y: torch.Tensor | None = None) -> torch.Tensor:
     """moe_prefill_chunked: prefill of all rows of x in chunks of at most chunk_tokens rows, with
@@ -260,6 +288,18 @@ def decode(layer: Layer, x: torch.Tensor, ws: torch.Tensor, y: torch.Tensor | No
         _check(lib().moe_decode(*args), "moe_decode")
     else:
         _check(lib().moe_decode_timed(*args, _events(events, 4)), "moe_decode_timed")
+    return y
+
+
+def decode_batch(layer: Layer, x: torch.Tensor, ws: torch.Tensor, y: torch.Tensor | None = None,
+                 out: dict | None = None) -> torch.Tensor:
+    """moe_decode_batch: decode of the T = x.shape[0] <= 8 token rows of x at once."""
+    _check_dev(x, torch.int16, "x")
+    y = y if y is not None else torch.empty_like(x)
+    ro = _route_struct(out)
+    _check(lib().moe_decode_batch(ctypes.byref(layer.c), x.data_ptr(), x.shape[0], y.data_ptr(),
+                                  ctypes.byref(ro) if ro is not None else None, ws.data_ptr(), ws.numel(),
+                                  _stream()), "moe_decode_batch")
     return y
 
 

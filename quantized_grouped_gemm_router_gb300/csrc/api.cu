@@ -4,7 +4,9 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "moe_internal.h"
 
@@ -144,11 +146,8 @@ int copy_out(void* dst, const void* src, size_t bytes, cudaStream_t s) {
   return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
-// Routing on top of logits already in the workspace (or caller-given): top-k, histogram, scan,
-// scatter and block map. `yacc` non-NULL also zeroes the combine accumulator rows.
-// `x` non-NULL also writes its fp16 copy (the expert GEMMs' operand) into the workspace.
-int run_route(const moe_dims& d, const float* logits, int T, const Ws& w, float* yacc, const uint16_t* x,
-              cudaStream_t s) {
+RouteParams route_params(const moe_dims& d, const float* logits, int T, const Ws& w, float* yacc, const uint16_t* x,
+                         int tile_rows) {
   RouteParams p;
   p.logits = logits;
   p.topk_idx = w.at<int32_t>(w.L.topk_idx);
@@ -163,6 +162,7 @@ int run_route(const moe_dims& d, const float* logits, int T, const Ws& w, float*
   p.tile_map = w.at<int32_t>(w.L.tile_map);
   p.tile_row0 = w.at<int32_t>(w.L.tile_row0);
   p.n_tiles = w.at<int32_t>(w.L.n_tiles);
+  p.tile_rows = tile_rows;
   p.yacc = yacc;
   p.x = x;
   p.x16 = w.at<uint16_t>(w.L.x16);
@@ -172,7 +172,63 @@ int run_route(const moe_dims& d, const float* logits, int T, const Ws& w, float*
   p.k = d.top_k;
   p.d = d.d;
   p.n_chunks = w.L.n_chunks;
-  return launch_route(p, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  return p;
+}
+
+// Routing on top of logits already in the workspace (or caller-given): top-k, histogram, scan,
+// scatter and block map. `yacc` non-NULL also zeroes the combine accumulator rows.
+// `x` non-NULL also writes its fp16 copy (the expert GEMMs' operand) into the workspace.
+int run_route(const moe_dims& d, const float* logits, int T, const Ws& w, float* yacc, const uint16_t* x,
+              cudaStream_t s, int tile_rows = kTileRows) {
+  return launch_route(route_params(d, logits, T, w, yacc, x, tile_rows), s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// The host round trip the GPU-resident routing removes (ablation): after the top-k kernel, the
+// selection is copied to the host and the stream synchronised; the host computes the histogram,
+// the exclusive scan, the stable scatter and the block map exactly as the device kernels define
+// them and copies them back; then the fp16 rows are placed as usual.
+int run_route_host(const moe_dims& d, const float* logits, int T, const Ws& w, float* yacc, const uint16_t* x,
+                   cudaStream_t s) {
+  const RouteParams p = route_params(d, logits, T, w, yacc, x, kTileRows);
+  if (launch_route_topk(p, s) != cudaSuccess) return MOE_ERR_CUDA;
+  const int E = d.n_experts, k = d.top_k, A = T * k;
+  std::vector<int32_t> idx(A), counts(E, 0), offsets(E + 1, 0), perm(A), inv(A), tile_map, tile_row0;
+  std::vector<float> wt(A);
+  std::vector<int2> row_tw(A);
+  if (cudaMemcpyAsync(idx.data(), p.topk_idx, (size_t)A * 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaMemcpyAsync(wt.data(), p.topk_w, (size_t)A * 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  for (int a = 0; a < A; ++a) ++counts[std::min(std::max(idx[a], 0), E - 1)];
+  for (int e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+  std::vector<int32_t> next(offsets.begin(), offsets.end() - 1);
+  for (int a = 0; a < A; ++a) {  // stable: ascending assignment within each expert
+    const int pos = next[std::min(std::max(idx[a], 0), E - 1)]++;
+    perm[pos] = a;
+    inv[a] = pos;
+    int32_t wbits;
+    std::memcpy(&wbits, &wt[a], 4);
+    row_tw[pos] = make_int2(a / k, wbits);
+  }
+  for (int e = 0; e < E; ++e)
+    for (int r = 0; r < counts[e]; r += kTileRows) {
+      tile_map.insert(tile_map.end(), {e, r, std::min(kTileRows, counts[e] - r)});
+      tile_row0.push_back(offsets[e] + r);
+    }
+  const int32_t n_tiles = (int32_t)tile_row0.size();
+  int st = cudaMemcpyAsync(p.counts, counts.data(), (size_t)E * 4, cudaMemcpyHostToDevice, s) |
+           cudaMemcpyAsync(p.offsets, offsets.data(), (size_t)(E + 1) * 4, cudaMemcpyHostToDevice, s) |
+           cudaMemcpyAsync(p.perm, perm.data(), (size_t)A * 4, cudaMemcpyHostToDevice, s) |
+           cudaMemcpyAsync(p.inv_perm, inv.data(), (size_t)A * 4, cudaMemcpyHostToDevice, s) |
+           cudaMemcpyAsync(p.row_tw, row_tw.data(), (size_t)A * 8, cudaMemcpyHostToDevice, s) |
+           cudaMemcpyAsync(p.n_tiles, &n_tiles, 4, cudaMemcpyHostToDevice, s);
+  if (n_tiles)
+    st |= cudaMemcpyAsync(p.tile_map, tile_map.data(), tile_map.size() * 4, cudaMemcpyHostToDevice, s) |
+          cudaMemcpyAsync(p.tile_row0, tile_row0.data(), tile_row0.size() * 4, cudaMemcpyHostToDevice, s);
+  if (st != cudaSuccess) return MOE_ERR_CUDA;
+  // pageable host buffers: wait for the copies before the vectors go out of scope
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  return launch_route_rows(p, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 int run_router_gemm(const moe_layer* L, const uint16_t* x, int T, const Ws& w, cudaStream_t s) {
@@ -208,7 +264,7 @@ int copy_route_out(const moe_dims& d, int T, const Ws& w, const moe_route_out* o
   st |= copy_out(o->offsets, w.base + w.L.offsets, (E + 1) * 4, s);
   st |= copy_out(o->perm, w.base + w.L.perm, A * 4, s);
   st |= copy_out(o->inv_perm, w.base + w.L.inv_perm, A * 4, s);
-  st |= copy_out(o->tile_map, w.base + w.L.tile_map, (size_t)w.L.max_tiles * 12, s);
+  st |= copy_out(o->tile_map, w.base + w.L.tile_map, (size_t)max_routed_tiles(T, d.top_k, d.n_experts) * 12, s);
   st |= copy_out(o->n_tiles, w.base + w.L.n_tiles, 4, s);
   return st ? MOE_ERR_CUDA : MOE_OK;
 }
@@ -242,6 +298,7 @@ int decode_common(const moe_layer* layer, const uint16_t* x, uint16_t* y, moe_ro
   p.E = d.n_experts;
   p.k = d.top_k;
   p.inter = d.inter;
+  p.T = 1;
   if (launch_decode(p, stream, events, mode) != cudaSuccess) return MOE_ERR_CUDA;
   if (!out) return MOE_OK;
   st = copy_out(out->logits, p.logits, (size_t)d.n_experts * 4, stream);
@@ -307,8 +364,12 @@ int moe_route(const moe_layer* layer, const uint16_t* x, const float* logits_in,
   return copy_route_out(d, T, w, out, stream);
 }
 
-int moe_prefill_timed(const moe_layer* layer, const uint16_t* x, int32_t T, uint16_t* y, moe_route_out* out,
-                      void* ws, size_t ws_bytes, moe_stream_t stream, void* const* events) {
+// The prefill sequence. arm: 0 the product path; MOE_PREFILL_ARM_HOST_ROUTING the block map built
+// on the host after a synchronisation; MOE_PREFILL_ARM_TILE32 block-map tiles of 32 rows;
+// MOE_PREFILL_ARM_DENSE the selected experts' weights expanded into `aux` first.
+static int prefill_impl(const moe_layer* layer, const uint16_t* x, int32_t T, uint16_t* y, moe_route_out* out,
+                        void* ws, size_t ws_bytes, moe_stream_t stream, void* const* events, int arm,
+                        void* aux = nullptr) {
   int st = check_layer(layer, true);
   if (st) return st;
   if (T < 1 || !x || !y) return MOE_ERR_INVALID_ARG;
@@ -326,7 +387,12 @@ int moe_prefill_timed(const moe_layer* layer, const uint16_t* x, int32_t T, uint
   if (record_event(events, 0, stream) != cudaSuccess) return MOE_ERR_CUDA;
   if ((st = run_router_gemm(layer, x, T, w, stream))) return st;
   if (record_event(events, 1, stream) != cudaSuccess) return MOE_ERR_CUDA;
-  if ((st = run_route(d, w.at<float>(w.L.logits), T, w, yacc, x, stream))) return st;
+  const int tile_rows = arm == MOE_PREFILL_ARM_TILE32 ? kMinTileRows : kTileRows;
+  if (arm == MOE_PREFILL_ARM_HOST_ROUTING) {
+    if ((st = run_route_host(d, w.at<float>(w.L.logits), T, w, yacc, x, stream))) return st;
+  } else if ((st = run_route(d, w.at<float>(w.L.logits), T, w, yacc, x, stream, tile_rows))) {
+    return st;
+  }
 
   // 3. gate|up grouped GEMM + SwiGLU -> hidden; 4. down grouped GEMM + weighted combine -> yacc
   GemmMaps x_maps, h_maps;
@@ -350,19 +416,34 @@ int moe_prefill_timed(const moe_layer* layer, const uint16_t* x, int32_t T, uint
   p.d = d.d;
   p.inter = d.inter;
   p.hidden_rows = A + T;
-  const int tiles = w.L.max_tiles + (T + kTileRows - 1) / kTileRows;
+  p.tile_rows = tile_rows;
+  const int tiles = max_routed_tiles(T, d.top_k, d.n_experts, tile_rows) + (T + tile_rows - 1) / tile_rows;
 
+  int mode_gu = kModeGateUp, mode_dn = kModeDown;
+  if (arm == MOE_PREFILL_ARM_DENSE) {  // expand the selected experts' weights, then dense GEMMs on them
+    uint16_t* dgu = static_cast<uint16_t*>(aux);
+    uint16_t* ddn = dgu + dense_gu_bytes(d) / 2;
+    mode_gu = kModeGateUpDense;
+    mode_dn = kModeDownDense;
+    if (launch_dense_dequant(d, p.packed, w.at<int32_t>(w.L.counts), dgu, ddn, stream) != cudaSuccess ||
+        !make_gemm_planes(&h_maps, hidden, (uint64_t)A + T, d.inter, gemm_kb_per_stage(kModeDownDense)) ||
+        !make_rows_map(&x_maps.a, dgu, (uint64_t)(d.n_experts + 1) * 2 * d.inter, d.d, kBlockRows,
+                       gemm_kw_per_stage(kModeGateUpDense), true) ||
+        !make_rows_map(&h_maps.a, ddn, (uint64_t)(d.n_experts + 1) * d.d, d.inter, kBlockRows,
+                       gemm_kw_per_stage(kModeDownDense), true))
+      return MOE_ERR_CUDA;
+  }
   p.region_offset = 0;
-  p.m_tiles = d.inter / gemm_out_rows(kModeGateUp);
+  p.m_tiles = d.inter / gemm_out_rows(mode_gu);
   p.k_blocks = d.d / kGroup;
   if (record_event(events, 2, stream) != cudaSuccess) return MOE_ERR_CUDA;
-  if (launch_gemm(kModeGateUp, p, &x_maps, tiles * p.m_tiles, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_gemm(mode_gu, p, &x_maps, tiles * p.m_tiles, stream) != cudaSuccess) return MOE_ERR_CUDA;
 
   p.region_offset = P.gu_bytes;
   p.m_tiles = d.d / kBlockRows;
   p.k_blocks = d.inter / kGroup;
   if (record_event(events, 3, stream) != cudaSuccess) return MOE_ERR_CUDA;
-  if (launch_gemm(kModeDown, p, &h_maps, tiles * p.m_tiles, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_gemm(mode_dn, p, &h_maps, tiles * p.m_tiles, stream) != cudaSuccess) return MOE_ERR_CUDA;
 
   // 5. fp32 accumulator -> bf16 output
   if (record_event(events, 4, stream) != cudaSuccess) return MOE_ERR_CUDA;
@@ -373,9 +454,33 @@ int moe_prefill_timed(const moe_layer* layer, const uint16_t* x, int32_t T, uint
   return MOE_OK;
 }
 
+int moe_prefill_timed(const moe_layer* layer, const uint16_t* x, int32_t T, uint16_t* y, moe_route_out* out,
+                      void* ws, size_t ws_bytes, moe_stream_t stream, void* const* events) {
+  return prefill_impl(layer, x, T, y, out, ws, ws_bytes, stream, events, 0);
+}
+
 int moe_prefill(const moe_layer* layer, const uint16_t* x, int32_t T, uint16_t* y, moe_route_out* out, void* ws,
                 size_t ws_bytes, moe_stream_t stream) {
-  return moe_prefill_timed(layer, x, T, y, out, ws, ws_bytes, stream, nullptr);
+  return prefill_impl(layer, x, T, y, out, ws, ws_bytes, stream, nullptr, 0);
+}
+
+size_t moe_prefill_ablation_aux_bytes(const moe_dims* dims, int arm) {
+  if (check_dims(dims) != MOE_OK || arm != MOE_PREFILL_ARM_DENSE) return 0;
+  return dense_gu_bytes(*dims) + dense_dn_bytes(*dims);
+}
+
+int moe_prefill_ablation(const moe_layer* layer, const uint16_t* x, int32_t T, uint16_t* y, int arm, void* ws,
+                         size_t ws_bytes, void* aux, size_t aux_bytes, moe_stream_t stream) {
+  if (arm != MOE_PREFILL_ARM_HOST_ROUTING && arm != MOE_PREFILL_ARM_TILE32 && arm != MOE_PREFILL_ARM_DENSE)
+    return MOE_ERR_INVALID_ARG;
+  if (arm == MOE_PREFILL_ARM_DENSE) {
+    int st = check_layer(layer, true);
+    if (st) return st;
+    if (!aux) return MOE_ERR_INVALID_ARG;
+    if (!aligned(aux, 128)) return MOE_ERR_MISALIGNED;
+    if (aux_bytes < moe_prefill_ablation_aux_bytes(&layer->dims, arm)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  }
+  return prefill_impl(layer, x, T, y, nullptr, ws, ws_bytes, stream, nullptr, arm, aux);
 }
 
 int moe_prefill_chunked(const moe_layer* layer, const uint16_t* x, int64_t T, uint16_t* y, int32_t chunk_tokens,
@@ -391,9 +496,46 @@ int moe_prefill_chunked(const moe_layer* layer, const uint16_t* x, int64_t T, ui
   const size_t d = (size_t)layer->dims.d;
   for (int64_t c = 0; c < T; c += chunk) {
     const int32_t n = (int32_t)std::min<int64_t>(chunk, T - c);
-    if ((st = moe_prefill_timed(layer, x + c * d, n, y + c * d, nullptr, ws, ws_bytes, stream, nullptr))) return st;
+    if ((st = prefill_impl(layer, x + c * d, n, y + c * d, nullptr, ws, ws_bytes, stream, nullptr, 0))) return st;
   }
   return MOE_OK;
+}
+
+int moe_decode_batch(const moe_layer* layer, const uint16_t* x, int32_t T, uint16_t* y, moe_route_out* out, void* ws,
+                     size_t ws_bytes, moe_stream_t stream) {
+  int st = check_layer(layer, true);
+  if (st) return st;
+  if (!x || !y || T < 1) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(y, 16)) return MOE_ERR_MISALIGNED;
+  const moe_dims& d = layer->dims;
+  if (T > kMaxDecodeBatch || d.d > kBatchMaxD) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if ((st = check_out(out)) || (st = check_ws(ws, ws_bytes, d, T))) return st;
+  Ws w{static_cast<uint8_t*>(ws), ws_layout(d, T)};
+  const PackedLayout P = packed_layout(d);
+  DecodeParams p;
+  p.x = x;
+  p.router_w = layer->router_w;
+  p.router_bias = layer->router_bias;
+  p.packed = static_cast<const uint8_t*>(layer->packed);
+  p.expert_stride = P.expert_stride;
+  p.gu_bytes = P.gu_bytes;
+  p.logits = w.at<float>(w.L.logits);
+  p.topk_idx = w.at<int32_t>(w.L.topk_idx);
+  p.topk_w = w.at<float>(w.L.topk_w);   // followed by room for the distinct-expert list (T*k + 1 ints)
+  p.partials = w.at<float>(w.L.dec_part);
+  p.y = y;
+  p.hdr = w.at<WsHeader>(w.L.header);
+  p.d = d.d;
+  p.E = d.n_experts;
+  p.k = d.top_k;
+  p.inter = d.inter;
+  p.T = T;
+  if (launch_decode_batch(p, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  if (!out) return MOE_OK;
+  st = copy_out(out->logits, p.logits, (size_t)T * d.n_experts * 4, stream);
+  st |= copy_out(out->topk_idx, p.topk_idx, (size_t)T * d.top_k * 4, stream);
+  st |= copy_out(out->topk_w, p.topk_w, (size_t)T * d.top_k * 4, stream);
+  return st ? MOE_ERR_CUDA : MOE_OK;
 }
 
 int moe_decode_timed(const moe_layer* layer, const uint16_t* x, uint16_t* y, moe_route_out* out, void* ws,

@@ -9,7 +9,9 @@
 //
 // Three launches chained with programmatic dependent launch (PDL): each kernel lets its
 // successor start at once, and does everything that does not depend on its predecessor's
-// results (loading static weights) before waiting for it.
+// results (loading static weights) before waiting for it. (Folding the router or the combine into
+// the expert kernel behind an in-kernel release/acquire handshake was measured slower: each
+// handshake costs more than the hand-off between two dependent launches.)
 //   decode_router_kernel  two experts per CTA: logit = W_r[e] . x (+ b_e); the router weight
 //                         slice is loaded before the wait
 //   decode_expert_kernel  one CTA per (selected or shared expert, 32 intermediate rows): routed
@@ -21,7 +23,7 @@
 //                         is known); gate/up + SwiGLU, scaled by the routing weight, then this
 //                         slice's contribution to every output row (split-K over the intermediate
 //                         dimension), written as the CTA's partial row
-//   decode_reduce_kernel  y = sum of the partial rows in a fixed order -> bf16
+//   decode_reduce_kernel  y of every token = sum of its partial rows in a fixed order -> bf16
 // The GEMV inner products run on the tensor cores (mma.sync m16n8k16, fp16 in, fp32
 // accumulate): the packed nibble pairs of a row map directly onto the MMA fragment layout, so
 // the weights cost about one ALU operation per two values instead of an fp32 FMA each, which on
@@ -82,7 +84,7 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 }
 
 __global__ void __launch_bounds__(kRThreads) decode_router_kernel(const DecodeParams p) {
-  __shared__ float s_part[kRThreads / 32];
+  __shared__ float s_part[kMaxDecodeBatch][kRThreads / 32];
   const int half = threadIdx.x >> 7, t = threadIdx.x & 127, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x * 2 + half;
   const int nch = p.d >> 3;  // 8-element chunks per row
@@ -94,27 +96,30 @@ __global__ void __launch_bounds__(kRThreads) decode_router_kernel(const DecodePa
   }
   pdl_launch_dependents();
   pdl_wait();
-  float acc = 0.f;
+  for (int tok = 0; tok < p.T; ++tok) {  // the same weights against every token of the call
+    const uint4* xt = reinterpret_cast<const uint4*>(p.x + (size_t)tok * p.d);
+    float acc = 0.f;
 #pragma unroll
-  for (int i = 0; i < kRMaxChunks; ++i) {
-    const int c = t + 128 * i;
-    if (e < p.E && c < nch) {
-      const uint4 xv = __ldcg(reinterpret_cast<const uint4*>(p.x) + c);
-      const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w}, wa[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+    for (int i = 0; i < kRMaxChunks; ++i) {
+      const int c = t + 128 * i;
+      if (e < p.E && c < nch) {
+        const uint4 xv = __ldcg(xt + c);
+        const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w}, wa[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        acc = fmaf(bf16lo(xa[j]), bf16lo(wa[j]), acc);
-        acc = fmaf(bf16hi(xa[j]), bf16hi(wa[j]), acc);
+        for (int j = 0; j < 4; ++j) {
+          acc = fmaf(bf16lo(xa[j]), bf16lo(wa[j]), acc);
+          acc = fmaf(bf16hi(xa[j]), bf16hi(wa[j]), acc);
+        }
       }
     }
-  }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
-  if (lane == 0) s_part[warp] = acc;
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+    if (lane == 0) s_part[tok][warp] = acc;
+  }
   __syncthreads();
-  if (t == 0 && e < p.E) {
-    const float* sp = s_part + 4 * half;
-    p.logits[e] = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + (p.router_bias ? p.router_bias[e] : 0.f);
+  if (t < p.T && e < p.E) {  // thread t of each half writes token t's logit of its expert
+    const float* sp = s_part[t] + 4 * half;
+    p.logits[(size_t)t * p.E + e] = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + (p.router_bias ? p.router_bias[e] : 0.f);
   }
 }
 
@@ -124,10 +129,15 @@ struct XSmem {
 };
 __host__ __device__ inline int up16(int v) { return (v + 15) & ~15; }
 
-// The routing of this call as warp 0 selected it: slot j's expert and weight.
-struct SelSmem {
-  int e[kMaxTopK];
+// Block-wide top-k scratch: the 16-lane groups' largest keys, the threshold, per-warp candidate
+// counts, the candidate keys, the selected keys and weights.
+struct TopkSmem {
+  unsigned long long gmax[kXThreads / 16];
+  unsigned long long tau;
+  int wcnt[kXWarps];
+  unsigned long long sel[kMaxTopK];
   float w[kMaxTopK];
+  unsigned long long cand[kMaxExperts];
 };
 
 __host__ __device__ inline XSmem x_smem(int d) {
@@ -140,10 +150,106 @@ __host__ __device__ inline XSmem x_smem(int d) {
   L.red = up16(L.xsum + KB * 8);                      // [warp][gate/up][32 rows] partial dots
   L.h = up16(L.red + kXWarps * 2 * kDecPartRows * 4); // h leading part, remainder (fp16), two sums
   L.topk = up16(L.h + 2 * kDecPartRows * 2 + 16);
-  L.misc = up16(L.topk + (int)sizeof(SelSmem));       // abort flag
+  L.misc = up16(L.topk + (int)sizeof(TopkSmem));      // abort flag
   L.bars = up16(L.misc + 16);
-  L.total = L.bars + (kXMaxGUChunks + 1) * 8;
+  L.total = L.bars + (kXMaxGUChunks + 1) * 8;         // gate/up pieces, down
   return L;
+}
+
+// Top k (k <= 16) of the E <= 1024 router logits, by all kXThreads threads of the block, with
+// the same selection as warp_topk_softmax (largest logit first, equal logits to the lower
+// index). Every expert has the unique key (orderable logit << 32) | ~index. Thread t reads the
+// logits t and t + 512 (coalesced); the largest keys of the 32 groups of 16 consecutive threads
+// belong to different experts, so the k-th largest key overall is at least tau, the k-th largest
+// of those group maxima (once k groups hold experts; tau = 0 otherwise). Only the experts with a
+// key >= tau (about k + 2 for Gaussian logits; all of them when the logits tie) are gathered,
+// without atomics (per-warp counts and a prefix over the warps), and ranked by counting the
+// larger candidate keys. Leaves the selected keys in s->sel[0..k) in slot order. Returns true on
+// every thread if a logit was NaN or infinite (the selection is then meaningless but stays within
+// [0, E)). Contains barriers: the whole block calls it.
+__device__ bool block_select_topk(const float* logits, int E, int k, TopkSmem* s) {
+  static_assert(kXWarps == 16 && kXThreads * 2 == kMaxExperts, "two experts per thread");
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int kPer = kMaxExperts / kXThreads;
+  unsigned long long u[kPer];
+  bool bad = false;
+  unsigned long long best = 0ull;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = tid + kXThreads * i;
+    u[i] = 0ull;  // below every real key
+    if (e < E) {
+      const float v = __ldcg(logits + e);
+      bad |= !isfinite(v);
+      u[i] = ((unsigned long long)max(orderable_f32(v), 1u) << 32) | (uint32_t)~(uint32_t)e;
+    }
+    best = u[i] > best ? u[i] : best;
+  }
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) {  // the largest key of these 16 lanes
+    const unsigned long long b = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+    best = b > best ? b : best;
+  }
+  if ((lane & 15) == 0) s->gmax[tid >> 4] = best;
+  __syncthreads();
+  if (warp == 0) {  // tau: the k-th largest group maximum (0 if fewer than k groups hold experts)
+    const unsigned long long v = s->gmax[lane];
+    int r = 0;
+#pragma unroll 8
+    for (int j = 0; j < kXThreads / 16; ++j) r += s->gmax[j] > v ? 1 : 0;
+    const unsigned nz = __ballot_sync(0xFFFFFFFFu, v != 0ull);
+    const unsigned hit = __ballot_sync(0xFFFFFFFFu, v != 0ull && r == k - 1);
+    const unsigned long long tv = __shfl_sync(0xFFFFFFFFu, v, hit ? __ffs(hit) - 1 : 0);
+    if (lane == 0) s->tau = (k <= __popc(nz) && hit) ? tv : 0ull;
+  }
+  __syncthreads();
+  const unsigned long long tau = s->tau;
+  unsigned bal[kPer];
+  int cnt = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    bal[i] = __ballot_sync(0xFFFFFFFFu, u[i] != 0ull && u[i] >= tau);
+    cnt += __popc(bal[i]);
+  }
+  if (lane == 0) s->wcnt[warp] = cnt;
+  __syncthreads();
+  int base = 0, n = 0;
+#pragma unroll
+  for (int w = 0; w < kXWarps; ++w) {
+    const int c = s->wcnt[w];
+    base += w < warp ? c : 0;
+    n += c;
+  }
+  const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    if ((bal[i] >> lane) & 1u) s->cand[base + __popc(bal[i] & lt)] = u[i];
+    base += __popc(bal[i]);
+  }
+  __syncthreads();
+  for (int c = tid; c < n; c += kXThreads) {
+    const unsigned long long K = s->cand[c];
+    int rank = 0;
+#pragma unroll 4
+    for (int j = 0; j < n; ++j) rank += s->cand[j] > K ? 1 : 0;
+    if (rank < k) s->sel[rank] = K;
+  }
+  return __syncthreads_or(bad) != 0;
+}
+
+// Softmax restricted to the selected experts (slot 0 holds the largest logit), by one warp, in
+// the same arithmetic as warp_topk_softmax. Lane j < k returns slot j's expert and weight.
+__device__ __forceinline__ void warp_selected_softmax(const TopkSmem* s, int E, int k, int* e_out, float* w_out) {
+  const int lane = threadIdx.x & 31;
+  const unsigned long long K = lane < k ? s->sel[lane] : s->sel[0];
+  const float my_v = from_orderable_f32((uint32_t)(K >> 32));
+  const float vmax = __shfl_sync(0xFFFFFFFFu, my_v, 0);
+  const float ex = lane < k ? expf(my_v - vmax) : 0.f;
+  float sum = ex;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+  *e_out = min(max((int)~(uint32_t)K, 0), E - 1);
+  *w_out = ex / sum;
 }
 
 // The four nibble pairs of a packed word (columns 2i, 2i+1 of its eight are nibbles i and i+4) as
@@ -173,9 +279,7 @@ __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
 // waits and stores; the partial rows are zeros); kMode 2 is a read-only probe of the same access
 // pattern (each CTA copies the pieces it would copy for expert `slot` (< k) or the shared expert,
 // waits for them and exits; launched alone).
-// kSlots: router logits per lane of the top-k warp (8 for up to 256 experts, 32 for up to 1024),
-// a template parameter so the common shapes keep the register footprint of the 8-slot selection.
-template <int kMode, int kSlots>
+template <int kMode>
 __global__ void __launch_bounds__(kXThreads, 1) decode_expert_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) uint8_t xs[];
   const XSmem L = x_smem(p.d);
@@ -188,7 +292,7 @@ __global__ void __launch_bounds__(kXThreads, 1) decode_expert_kernel(const Decod
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t bars = smem_u32(xs + L.bars);
   volatile int* s_abort = reinterpret_cast<volatile int*>(xs + L.misc);
-  SelSmem* sel = reinterpret_cast<SelSmem*>(xs + L.topk);
+  TopkSmem* tk = reinterpret_cast<TopkSmem*>(xs + L.topk);
   const int NGU = min(kXMaxGUChunks, KB);  // barriers 0..NGU-1: gate/up pieces; NGU: down
   if (tid == 0) {
     for (int i = 0; i <= NGU; ++i) mbar_init(bars + 8u * i, 1);
@@ -202,19 +306,32 @@ __global__ void __launch_bounds__(kXThreads, 1) decode_expert_kernel(const Decod
   // gate and up rows for every column block (KB * 2304 bytes, in NGU pieces), then its 32-column
   // half of every down row block (DM * 2048 bytes of codes) and the matching scale/bias rows.
   auto issue = [&](int expert) {
+    // lanes 0..NGU-1: the gate/up pieces; lane NGU: the down codes; lane NGU+1: the down scale/bias
+    // rows (both on the down barrier, whose expected bytes lane NGU announces). Every copy goes out
+    // in the same instruction.
     const uint8_t* eb = p.packed + (size_t)expert * p.expert_stride;
-    if (lane < NGU) {
-      const uint8_t* gu = eb + gu_offset(m, part % (kBlockRows / kDecPartRows), 0, KB);
-      const int c = lane, kb0 = c * KB / NGU, kb1 = (c + 1) * KB / NGU;
-      const uint32_t bytes = (uint32_t)(kb1 - kb0) * kGUStage;
-      mbar_arrive_expect_tx(bars + 8u * c, bytes);
-      tma_bulk_g2s(smem_u32(xs + L.gu + kb0 * kGUStage), gu + (size_t)kb0 * kGUStage, bytes, bars + 8u * c);
-    } else if (lane == NGU) {
-      const uint8_t* dn = eb + p.gu_bytes;
-      mbar_arrive_expect_tx(bars + 8u * NGU, (uint32_t)(DM * (kHalfBytes + kSBBytes)));
-      tma_bulk_g2s(smem_u32(xs + L.dn), dn + dn_code_offset(kbd, hd, 0, DM), DM * kHalfBytes, bars + 8u * NGU);
-      tma_bulk_g2s(smem_u32(xs + L.dn + DM * kHalfBytes), dn + dn_sb_offset(kbd, 0, DM, KBI), DM * kSBBytes,
-                   bars + 8u * NGU);
+    if (lane <= NGU + 1) {
+      uint32_t dst, bytes, bar;
+      const uint8_t* src;
+      if (lane < NGU) {
+        const int kb0 = lane * KB / NGU, kb1 = (lane + 1) * KB / NGU;
+        bytes = (uint32_t)(kb1 - kb0) * kGUStage;
+        dst = smem_u32(xs + L.gu + kb0 * kGUStage);
+        src = eb + gu_offset(m, part % (kBlockRows / kDecPartRows), 0, KB) + (size_t)kb0 * kGUStage;
+        bar = bars + 8u * lane;
+      } else if (lane == NGU) {
+        bytes = DM * kHalfBytes;
+        dst = smem_u32(xs + L.dn);
+        src = eb + p.gu_bytes + dn_code_offset(kbd, hd, 0, DM);
+        bar = bars + 8u * NGU;
+      } else {
+        bytes = DM * kSBBytes;
+        dst = smem_u32(xs + L.dn + DM * kHalfBytes);
+        src = eb + p.gu_bytes + dn_sb_offset(kbd, 0, DM, KBI);
+        bar = bars + 8u * NGU;
+      }
+      if (lane <= NGU) mbar_arrive_expect_tx(bar, lane < NGU ? bytes : (uint32_t)(DM * (kHalfBytes + kSBBytes)));
+      tma_bulk_g2s(dst, src, bytes, bar);
     }
   };
 
@@ -233,65 +350,63 @@ __global__ void __launch_bounds__(kXThreads, 1) decode_expert_kernel(const Decod
   pdl_launch_dependents();
   pdl_wait();
 
-  if (warp == 0) {
-    // Routed blocks select the top k themselves from the router's logits (every block gets the
-    // same, deterministic answer), then issue this block's copies at once; block 0 also publishes
-    // the routing.
-    if (!shared || blockIdx.x == 0) {
-      int rank, my_e;
+  // x (one 8-value chunk per thread of warps 2..15) is loaded before the selection so both loads
+  // overlap.
+  static_assert(kDecodeMaxD / 8 <= kXThreads - 64, "warps 2..15 hold one 8-value chunk of x each");
+  const int nch = p.d / 8, cx = tid - 64;
+  const uint4 xv = cx >= 0 && cx < nch ? __ldcg(reinterpret_cast<const uint4*>(p.x) + cx) : make_uint4(0u, 0u, 0u, 0u);
+  // Routed blocks select the top k themselves from the router's logits (every block gets the same,
+  // deterministic answer); then warp 0 issues this block's copies at once while warp 1 computes the
+  // routing weights (block 0 also publishes the routing) and the other warps stage x. The branch
+  // is uniform over the block.
+  if (!shared || blockIdx.x == 0) {
+    const bool bad = block_select_topk(p.logits, p.E, p.k, tk);
+    if (warp == 0 && !shared) issue((int)~(uint32_t)tk->sel[slot]);
+    if (warp == 1) {
+      int my_e;
       float my_w;
-      const bool bad = warp_select_topk<kSlots>(p.logits, p.E, p.k, &rank, &my_e, &my_w);
-      if (rank >= 0) {
-        sel->e[rank] = my_e;
-        sel->w[rank] = my_w;
-      }
-      __syncwarp();
-      if (!shared) issue(sel->e[slot]);
+      warp_selected_softmax(tk, p.E, p.k, &my_e, &my_w);
+      if (lane < p.k) tk->w[lane] = my_w;
       if (blockIdx.x == 0) {
-        if (rank >= 0) {
-          p.topk_idx[rank] = my_e;
-          p.topk_w[rank] = my_w;
+        if (lane < p.k) {
+          p.topk_idx[lane] = my_e;
+          p.topk_w[lane] = my_w;
         }
         if (bad && lane == 0) set_device_status(p.hdr, MOE_ERR_NONFINITE);
       }
     }
-  } else {
-    // Meanwhile the other warps stage x as fp16 pairs, and per 64-column group the sums of x over
-    // the columns whose codes enter the MMA with base 1024 (columns 0,1,4,5 of every 8) and base 64
-    // (columns 2,3,6,7); x must lie in the fp16 operand range (block 0 reports it once per call).
+  }
+  if (warp >= 2) {
+    // x as fp16 pairs, and per 64-column group the sums of x over the columns whose codes enter
+    // the MMA with base 1024 (columns 0,1,4,5 of every 8) and base 64 (columns 2,3,6,7); x must lie
+    // in the fp16 operand range (block 0 reports it once per call).
     uint32_t* x2w = reinterpret_cast<uint32_t*>(xs + L.x16);
     float* xsw = reinterpret_cast<float*>(xs + L.xsum);
-    const int nch = p.d / 8, t = tid - 32, nt = kXThreads - 32;
+    const uint32_t in[4] = {xv.x, xv.y, xv.z, xv.w};
+    float sa = 0.f, sb = 0.f;
     bool over = false;
-    for (int base = 0; base < nch; base += nt) {
-      const int c = base + t;
-      float sa = 0.f, sb = 0.f;
-      if (c < nch) {
-        const uint4 v = __ldcg(reinterpret_cast<const uint4*>(p.x) + c);
-        const uint32_t in[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float lo = bf16lo(in[j]), hi = bf16hi(in[j]);
-          over |= !(fabsf(lo) <= 65504.f) || !(fabsf(hi) <= 65504.f);
-          if (j == 0 || j == 2) sa += lo + hi; else sb += lo + hi;
-          const __half2 h2 = __floats2half2_rn(lo, hi);
-          x2w[4 * c + j] = *reinterpret_cast<const uint32_t*>(&h2);
-        }
-      }
-#pragma unroll
-      for (int o = 1; o < 8; o <<= 1) {
-        sa += __shfl_xor_sync(0xFFFFFFFFu, sa, o);
-        sb += __shfl_xor_sync(0xFFFFFFFFu, sb, o);
-      }
-      if (c < nch && (c & 7) == 0) {
-        xsw[2 * (c >> 3)] = sa;
-        xsw[2 * (c >> 3) + 1] = sb;
-      }
+    for (int j = 0; j < 4; ++j) {
+      const float lo = bf16lo(in[j]), hi = bf16hi(in[j]);
+      over |= !(fabsf(lo) <= 65504.f) || !(fabsf(hi) <= 65504.f);
+      if (j == 0 || j == 2) sa += lo + hi; else sb += lo + hi;
+      const __half2 h2 = __floats2half2_rn(lo, hi);
+      if (cx < nch) x2w[4 * cx + j] = *reinterpret_cast<const uint32_t*>(&h2);
     }
-    if (blockIdx.x == 0 && __any_sync(0xFFFFFFFFu, over) && lane == 0) set_device_status(p.hdr, MOE_ERR_OUT_OF_RANGE);
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+      sa += __shfl_xor_sync(0xFFFFFFFFu, sa, o);
+      sb += __shfl_xor_sync(0xFFFFFFFFu, sb, o);
+    }
+    if (cx < nch && (cx & 7) == 0) {
+      xsw[2 * (cx >> 3)] = sa;
+      xsw[2 * (cx >> 3) + 1] = sb;
+    }
+    if (blockIdx.x == 0 && __any_sync(0xFFFFFFFFu, over && cx < nch) && lane == 0)
+      set_device_status(p.hdr, MOE_ERR_OUT_OF_RANGE);
   }
   __syncthreads();
-  const float wslot = shared ? 1.f : sel->w[slot];
+  const float wslot = shared ? 1.f : tk->w[slot];
   const uint32_t* x2 = reinterpret_cast<const uint32_t*>(xs + L.x16);
   const float* xsum = reinterpret_cast<const float*>(xs + L.xsum);
 
@@ -408,36 +523,47 @@ __global__ void __launch_bounds__(kXThreads, 1) decode_expert_kernel(const Decod
       c1[i] = *reinterpret_cast<const uint32_t*>(ds + (R0 + 8) * 16 + 4 * tig);
     }
   }
+  // all of this warp's MMAs first (independent, so they pipeline), then the epilogue of the rows
+  // (lanes with tig == 0 hold columns 0 and 1: the leading part and the remainder of h)
+  float dd[kMaxTilesPerWarp][4];
 #pragma unroll
   for (int i = 0; i < kMaxTilesPerWarp; ++i) {
-    if (ok && i < ntw) {
-      const int tile = warp + i * kXWarps, mm = tile >> 3, R0 = (tile & 7) * 16 + g, R1 = R0 + 8;
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
-      if constexpr (kMode == 0) {
+    dd[i][0] = dd[i][1] = dd[i][2] = dd[i][3] = 0.f;
+    if constexpr (kMode == 0) {
+      if (ok && i < ntw) {
         uint32_t q0[4], q1[4];
         q_pairs(c0[i], q0);
         q_pairs(c1[i], q1);
-        mma16816(d, q0[0], q1[0], q0[1], q1[1], hb.x, hb.y);
-        mma16816(d, q0[2], q1[2], q0[3], q1[3], hb.z, hb.w);
+        mma16816(dd[i], q0[0], q1[0], q0[1], q1[1], hb.x, hb.y);
+        mma16816(dd[i], q0[2], q1[2], q0[3], q1[3], hb.z, hb.w);
       }
-      if (tig == 0) {
+    }
+  }
+  // the row results go to a shared-memory copy of the partial row (the gate/up stage area, free
+  // once every block of it has been consumed), then out as coalesced 16-byte stores
+  float* prow = reinterpret_cast<float*>(xs + L.gu);
+  if (tig == 0) {
+#pragma unroll
+    for (int i = 0; i < kMaxTilesPerWarp; ++i) {
+      if (ok && i < ntw) {
+        const int tile = warp + i * kXWarps, mm = tile >> 3, R0 = (tile & 7) * 16 + g, R1 = R0 + 8;
         const uint8_t* dsb = xs + L.dn + DM * kHalfBytes + mm * kSBBytes;
         const uint32_t sb0 = *reinterpret_cast<const uint32_t*>(dsb + R0 * 4);
         const uint32_t sb1 = *reinterpret_cast<const uint32_t*>(dsb + R1 * 4);
         // d = sum (base + q) h over the 32 columns: s*q + b weights give
-        // s*d + (b - 1024 s) * (sum of h over base-1024 columns) + (b - 64 s) * (the others)
-        if constexpr (kMode == 0) {
-          gout[mm * kBlockRows + R0] = bf16lo(sb0) * (d[0] + d[1]) + (bf16hi(sb0) - 1024.f * bf16lo(sb0)) * ha +
-                                       (bf16hi(sb0) - 64.f * bf16lo(sb0)) * hb64;
-          gout[mm * kBlockRows + R1] = bf16lo(sb1) * (d[2] + d[3]) + (bf16hi(sb1) - 1024.f * bf16lo(sb1)) * ha +
-                                       (bf16hi(sb1) - 64.f * bf16lo(sb1)) * hb64;
-        } else {
-          gout[mm * kBlockRows + R0] = 0.f;
-          gout[mm * kBlockRows + R1] = 0.f;
-        }
+        // s*d + (b - 1024 s) * (sum of h over base-1024 columns) + (b - 64 s) * (the others);
+        // with the arithmetic deleted (kMode 1) the partial row is zeros
+        const float s0 = kMode == 0 ? bf16lo(sb0) : 0.f, s1 = kMode == 0 ? bf16lo(sb1) : 0.f;
+        const float b0 = kMode == 0 ? bf16hi(sb0) : 0.f, b1 = kMode == 0 ? bf16hi(sb1) : 0.f;
+        prow[mm * kBlockRows + R0] = s0 * (dd[i][0] + dd[i][1]) + (b0 - 1024.f * s0) * ha + (b0 - 64.f * s0) * hb64;
+        prow[mm * kBlockRows + R1] = s1 * (dd[i][2] + dd[i][3]) + (b1 - 1024.f * s1) * ha + (b1 - 64.f * s1) * hb64;
       }
     }
   }
+  __syncthreads();
+  if (ok)
+    for (int i = tid; i < p.d / 4; i += kXThreads)
+      reinterpret_cast<float4*>(gout)[i] = reinterpret_cast<const float4*>(prow)[i];
   if (!down_ok && tid == 0) *s_abort = 1;
   __syncthreads();
   if (tid == 0 && *s_abort) {  // outputs are undefined; let this CTA's copies land before exiting
@@ -446,32 +572,362 @@ __global__ void __launch_bounds__(kXThreads, 1) decode_expert_kernel(const Decod
   }
 }
 
-// y[i] = sum over the expert-kernel CTAs c (ascending) of partials[c][i], rounded to bf16.
-// Thread (row r, group q) sums a contiguous range of c with batched loads; the 32 group sums of
-// a row are then added in group order, so the result does not depend on timing.
+// ------------------------------------------------------------------------------------------
+// Small-batch decode (2..8 tokens, e.g. checking a few draft tokens at once): the tokens route
+// to different experts (page, section "What didn't work": 2 to 5 draft rows touch different
+// experts), so the union of their selected experts is streamed once, each distinct expert's
+// CTAs serving every token that chose it; the tokens fill the columns of the MMAs' B operand.
+// ------------------------------------------------------------------------------------------
+
+// Selection of every token (warp t = token t), then the distinct selected experts in ascending
+// order: dexp[0..n_distinct).
+__global__ void __launch_bounds__(kMaxDecodeBatch * 32) decode_batch_select_kernel(const DecodeParams p,
+                                                                                    int32_t* dexp,
+                                                                                    int32_t* n_distinct) {
+  __shared__ uint32_t bitmap[kMaxExperts / 32];
+  pdl_launch_dependents();
+  pdl_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x < kMaxExperts / 32) bitmap[threadIdx.x] = 0u;
+  __syncthreads();
+  if (warp < p.T) {
+    int e;
+    float w;
+    const bool bad = warp_topk_softmax(p.logits + (size_t)warp * p.E, p.E, p.k, &e, &w);
+    if (lane < p.k) {
+      p.topk_idx[warp * p.k + lane] = e;
+      p.topk_w[warp * p.k + lane] = w;
+      atomicOr(&bitmap[e >> 5], 1u << (e & 31));
+    }
+    if (bad && lane == 0) set_device_status(p.hdr, MOE_ERR_NONFINITE);
+  }
+  __syncthreads();
+  if (warp == 0) {  // lane l owns experts 32 l .. 32 l + 31
+    uint32_t bits = bitmap[lane];
+    int before = __popc(bits);
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, before, o);
+      if (lane >= o) before += v;
+    }
+    const int total = __shfl_sync(0xFFFFFFFFu, before, 31);
+    before -= __popc(bits);
+    while (bits) {
+      const int b = __ffs(bits) - 1;
+      dexp[before++] = 32 * lane + b;
+      bits &= bits - 1;
+    }
+    if (lane == 0) *n_distinct = total;
+  }
+}
+
+// Shared memory of the batch expert kernel.
+struct BSmem {
+  int gu, dn, x16, xsum, red, h, hsum, tok, misc, bars, total;
+};
+__host__ __device__ inline BSmem b_smem(int d) {
+  const int KB = d / kGroup, DM = d / kBlockRows;
+  BSmem L;
+  L.gu = 0;
+  L.dn = L.gu + KB * kGUStage;
+  L.x16 = up16(L.dn + DM * kDnStage);                                       // [token][d] fp16
+  L.xsum = up16(L.x16 + kMaxDecodeBatch * d * 2);                           // [token][KB][2]
+  L.red = up16(L.xsum + kMaxDecodeBatch * KB * 8);                          // [warp][mat][row][token]
+  L.h = up16(L.red + kXWarps * 2 * kDecPartRows * kMaxDecodeBatch * 4);     // [plane][token][32] fp16
+  L.hsum = up16(L.h + 2 * kMaxDecodeBatch * kDecPartRows * 2);              // [token][2]
+  L.tok = up16(L.hsum + kMaxDecodeBatch * 8);                               // weight[8], slot[8]
+  L.misc = up16(L.tok + kMaxDecodeBatch * 8);                               // abort flag, expert
+  L.bars = up16(L.misc + 16);
+  L.total = L.bars + (kXMaxGUChunks + 1) * 8;
+  return L;
+}
+
+// One CTA per (distinct selected expert, or the shared expert) x 32 intermediate rows, for every
+// token of the call at once. Slots beyond the call's distinct experts exit at once. Token t's
+// contribution from its slot j goes to partial row [t][j][part] (the shared expert to [t][k]).
+__global__ void __launch_bounds__(kXThreads, 1) decode_batch_expert_kernel(const DecodeParams p,
+                                                                           const int32_t* dexp,
+                                                                           const int32_t* n_distinct) {
+  extern __shared__ __align__(128) uint8_t xs[];
+  const BSmem L = b_smem(p.d);
+  const int KB = p.d / kGroup, DM = p.d / kBlockRows, KBI = p.inter / kGroup;
+  const int parts = p.inter / kDecPartRows, T = p.T, k = p.k;
+  const int slot = blockIdx.x / parts, part = blockIdx.x % parts;
+  const bool shared = slot == T * k;
+  const int m = part / (kBlockRows / kDecPartRows);
+  const int kbd = part / 2, hd = part % 2;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t bars = smem_u32(xs + L.bars);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(xs + L.misc);
+  int* s_expert = reinterpret_cast<int*>(xs + L.misc + 4);
+  float* s_w = reinterpret_cast<float*>(xs + L.tok);
+  int* s_slot = reinterpret_cast<int*>(xs + L.tok + kMaxDecodeBatch * 4);
+  const int NGU = min(kXMaxGUChunks, KB);
+  if (tid == 0) {
+    for (int i = 0; i <= NGU; ++i) mbar_init(bars + 8u * i, 1);
+    *s_abort = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  auto issue = [&](int expert) {  // the same pieces as the batch-1 expert kernel
+    const uint8_t* eb = p.packed + (size_t)expert * p.expert_stride;
+    if (lane < NGU) {
+      const uint8_t* gu = eb + gu_offset(m, part % (kBlockRows / kDecPartRows), 0, KB);
+      const int c = lane, kb0 = c * KB / NGU, kb1 = (c + 1) * KB / NGU;
+      const uint32_t bytes = (uint32_t)(kb1 - kb0) * kGUStage;
+      mbar_arrive_expect_tx(bars + 8u * c, bytes);
+      tma_bulk_g2s(smem_u32(xs + L.gu + kb0 * kGUStage), gu + (size_t)kb0 * kGUStage, bytes, bars + 8u * c);
+    } else if (lane == NGU) {
+      const uint8_t* dn = eb + p.gu_bytes;
+      mbar_arrive_expect_tx(bars + 8u * NGU, (uint32_t)(DM * (kHalfBytes + kSBBytes)));
+      tma_bulk_g2s(smem_u32(xs + L.dn), dn + dn_code_offset(kbd, hd, 0, DM), DM * kHalfBytes, bars + 8u * NGU);
+      tma_bulk_g2s(smem_u32(xs + L.dn + DM * kHalfBytes), dn + dn_sb_offset(kbd, 0, DM, KBI), DM * kSBBytes,
+                   bars + 8u * NGU);
+    }
+  };
+  if (shared && warp == 0) issue(p.E);  // static weights: before waiting on the selection
+  pdl_launch_dependents();
+  pdl_wait();
+  if (tid == 0) *s_expert = shared ? p.E : (slot < __ldcg(n_distinct) ? __ldcg(dexp + slot) : -1);
+  __syncthreads();
+  const int expert = *s_expert;
+  if (expert < 0) return;  // fewer distinct experts than slots (uniform; nothing was issued)
+  if (!shared && warp == 0) issue(expert);
+  if (tid < kMaxDecodeBatch) {  // this expert's weight and slot for every token (0 and -1: not chosen)
+    float w = 0.f;
+    int j = -1;
+    if (tid < T) {
+      if (shared) {
+        w = 1.f;
+        j = k;
+      } else {
+        for (int jj = 0; jj < k; ++jj)
+          if (__ldcg(p.topk_idx + tid * k + jj) == expert) {
+            w = __ldcg(p.topk_w + tid * k + jj);
+            j = jj;
+          }
+      }
+    }
+    s_w[tid] = w;
+    s_slot[tid] = j;
+  }
+  {
+    // x of every token as fp16 pairs, and per token and 64-column group the sums of x over the
+    // base-1024 columns (0,1,4,5 of every 8) and the base-64 columns (2,3,6,7)
+    uint32_t* x2w = reinterpret_cast<uint32_t*>(xs + L.x16);
+    float* xsw = reinterpret_cast<float*>(xs + L.xsum);
+    const int nch = p.d / 8;
+    bool over = false;
+    for (int base = 0; base < kMaxDecodeBatch * nch; base += kXThreads) {
+      const int i = base + tid, t = i / nch, c = i % nch;
+      float sa = 0.f, sb = 0.f;
+      uint32_t o[4] = {0u, 0u, 0u, 0u};
+      if (t < T) {
+        const uint4 v = __ldcg(reinterpret_cast<const uint4*>(p.x + (size_t)t * p.d) + c);
+        const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float lo = bf16lo(in[j]), hi = bf16hi(in[j]);
+          over |= !(fabsf(lo) <= 65504.f) || !(fabsf(hi) <= 65504.f);
+          if (j == 0 || j == 2) sa += lo + hi; else sb += lo + hi;
+          const __half2 h2 = __floats2half2_rn(lo, hi);
+          o[j] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+      }
+      if (t < kMaxDecodeBatch) *reinterpret_cast<uint4*>(x2w + (size_t)t * (p.d / 2) + 4 * c) = make_uint4(o[0], o[1], o[2], o[3]);
+#pragma unroll
+      for (int q = 1; q < 8; q <<= 1) {
+        sa += __shfl_xor_sync(0xFFFFFFFFu, sa, q);
+        sb += __shfl_xor_sync(0xFFFFFFFFu, sb, q);
+      }
+      if (t < kMaxDecodeBatch && (c & 7) == 0) {
+        xsw[(t * KB + (c >> 3)) * 2] = sa;
+        xsw[(t * KB + (c >> 3)) * 2 + 1] = sb;
+      }
+    }
+    if (slot == 0 && part == 0 && __any_sync(0xFFFFFFFFu, over) && lane == 0)
+      set_device_status(p.hdr, MOE_ERR_OUT_OF_RANGE);
+  }
+  __syncthreads();
+  const uint32_t* x2 = reinterpret_cast<const uint32_t*>(xs + L.x16);
+  const float* xsum = reinterpret_cast<const float*>(xs + L.xsum);
+
+  // ---- gate/up: warp w takes K blocks w, w+16, ...; the tokens are the 8 columns of B
+  const int g = lane >> 2, tig = lane & 3;
+  float acc[2][2][4] = {};  // [gate/up][row tile][(row g, tokens 2tig, 2tig+1), (row g+8, ...)]
+  bool gu_ok = true;
+  for (int kb = warp; kb < KB; kb += kXWarps) {
+    int chunk = 0;
+    while (kb >= (chunk + 1) * KB / NGU) ++chunk;
+    if (!(gu_ok = mbar_wait(bars + 8u * chunk, 0, s_abort))) break;
+    const uint8_t* st = xs + L.gu + kb * kGUStage;
+    // B: token g's x for the columns of this lane's two code words (tig and tig + 4)
+    const uint4 xa = *reinterpret_cast<const uint4*>(x2 + (size_t)g * (p.d / 2) + kb * (kGroup / 2) + 4 * tig);
+    const uint4 xb = *reinterpret_cast<const uint4*>(x2 + (size_t)g * (p.d / 2) + kb * (kGroup / 2) + 16 + 4 * tig);
+    const float sa0 = xsum[((2 * tig) * KB + kb) * 2], sb0 = xsum[((2 * tig) * KB + kb) * 2 + 1];
+    const float sa1 = xsum[((2 * tig + 1) * KB + kb) * 2], sb1 = xsum[((2 * tig + 1) * KB + kb) * 2 + 1];
+#pragma unroll
+    for (int mat = 0; mat < 2; ++mat) {
+      const uint8_t* ms = st + mat * (kGUStage / 2);
+#pragma unroll
+      for (int rt = 0; rt < 2; ++rt) {
+        const int R0 = rt * 16 + g, R1 = R0 + 8;
+        uint32_t a0[4], a1[4], b0[4], b1[4];
+        q_pairs(*reinterpret_cast<const uint32_t*>(ms + R0 * 16 + 4 * tig), a0);
+        q_pairs(*reinterpret_cast<const uint32_t*>(ms + R1 * 16 + 4 * tig), a1);
+        q_pairs(*reinterpret_cast<const uint32_t*>(ms + kDecPartRows * 16 + R0 * 16 + 4 * tig), b0);
+        q_pairs(*reinterpret_cast<const uint32_t*>(ms + kDecPartRows * 16 + R1 * 16 + 4 * tig), b1);
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        mma16816(d, a0[0], a1[0], a0[1], a1[1], xa.x, xa.y);
+        mma16816(d, a0[2], a1[2], a0[3], a1[3], xa.z, xa.w);
+        mma16816(d, b0[0], b1[0], b0[1], b1[1], xb.x, xb.y);
+        mma16816(d, b0[2], b1[2], b0[3], b1[3], xb.z, xb.w);
+        const uint32_t sbw0 = *reinterpret_cast<const uint32_t*>(ms + 2 * kDecPartRows * 16 + R0 * 4);
+        const uint32_t sbw1 = *reinterpret_cast<const uint32_t*>(ms + 2 * kDecPartRows * 16 + R1 * 4);
+        const float s0 = bf16lo(sbw0), c0a = bf16hi(sbw0) - 1024.f * s0, c0b = bf16hi(sbw0) - 64.f * s0;
+        const float s1 = bf16lo(sbw1), c1a = bf16hi(sbw1) - 1024.f * s1, c1b = bf16hi(sbw1) - 64.f * s1;
+        acc[mat][rt][0] += s0 * d[0] + c0a * sa0 + c0b * sb0;
+        acc[mat][rt][1] += s0 * d[1] + c0a * sa1 + c0b * sb1;
+        acc[mat][rt][2] += s1 * d[2] + c1a * sa0 + c1b * sb0;
+        acc[mat][rt][3] += s1 * d[3] + c1a * sa1 + c1b * sb1;
+      }
+    }
+  }
+  gu_ok = __all_sync(0xFFFFFFFFu, gu_ok);
+  float* red = reinterpret_cast<float*>(xs + L.red);  // [warp][mat][row][token]
+#pragma unroll
+  for (int mat = 0; mat < 2; ++mat)
+#pragma unroll
+    for (int rt = 0; rt < 2; ++rt)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int row = rt * 16 + g + 8 * (q >> 1), tok = 2 * tig + (q & 1);
+        red[((warp * 2 + mat) * kDecPartRows + row) * kMaxDecodeBatch + tok] = acc[mat][rt][q];
+      }
+  __syncthreads();
+  __half* hh = reinterpret_cast<__half*>(xs + L.h);            // [token][32] leading part
+  __half* hl = hh + kMaxDecodeBatch * kDecPartRows;            // [token][32] remainder
+  float* hsum = reinterpret_cast<float*>(xs + L.hsum);         // [token][2]
+  if (warp < kMaxDecodeBatch) {  // warp t: SwiGLU of token t's 32 rows, scaled by its routing weight
+    const int t = warp;
+    float gs = 0.f, us = 0.f;
+    for (int w = 0; w < kXWarps; ++w) {
+      gs += red[((w * 2 + 0) * kDecPartRows + lane) * kMaxDecodeBatch + t];
+      us += red[((w * 2 + 1) * kDecPartRows + lane) * kMaxDecodeBatch + t];
+    }
+    const float wt = s_w[t];
+    const float h = wt != 0.f ? gs / (1.f + expf(-gs)) * us * wt : 0.f;
+    const __half hi = __float2half_rn(h);
+    hh[t * kDecPartRows + lane] = hi;
+    hl[t * kDecPartRows + lane] = __float2half_rn(h - __half2float(hi));
+    const bool base1024 = (lane & 2) == 0;
+    float ta = base1024 ? h : 0.f, tb = base1024 ? 0.f : h;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      ta += __shfl_xor_sync(0xFFFFFFFFu, ta, o);
+      tb += __shfl_xor_sync(0xFFFFFFFFu, tb, o);
+    }
+    if (lane == 0) {
+      hsum[2 * t] = ta;
+      hsum[2 * t + 1] = tb;
+    }
+    if (__any_sync(0xFFFFFFFFu, !(fabsf(h) <= 65504.f)) && lane == 0) set_device_status(p.hdr, MOE_ERR_OUT_OF_RANGE);
+  }
+  __syncthreads();
+
+  // ---- down: this CTA's 32 columns of W_down against every output row, 4 tokens per MMA (the
+  // leading part and remainder of token t's h in columns 2t, 2t + 1 of B)
+  const bool down_ok = mbar_wait(bars + 8u * NGU, 0, s_abort);
+  const bool ok = !*s_abort && down_ok && gu_ok;
+  const int nsets = (T + 3) / 4;
+  uint4 hbv[2];
+#pragma unroll
+  for (int set = 0; set < 2; ++set) {
+    const int tok = 4 * set + (g >> 1);
+    const __half* src = (g & 1) ? hl : hh;
+    hbv[set] = *reinterpret_cast<const uint4*>(src + tok * kDecPartRows + 8 * tig);
+  }
+  constexpr int kMaxTilesPerWarp = kBatchMaxD / 16 / kXWarps;
+  const int ntw = DM * 8 / kXWarps;
+  uint32_t c0[kMaxTilesPerWarp], c1[kMaxTilesPerWarp];
+#pragma unroll
+  for (int i = 0; i < kMaxTilesPerWarp; ++i) {
+    if (ok && i < ntw) {
+      const int tile = warp + i * kXWarps, mm = tile >> 3, R0 = (tile & 7) * 16 + g;
+      const uint8_t* ds = xs + L.dn + mm * kHalfBytes;
+      c0[i] = *reinterpret_cast<const uint32_t*>(ds + R0 * 16 + 4 * tig);
+      c1[i] = *reinterpret_cast<const uint32_t*>(ds + (R0 + 8) * 16 + 4 * tig);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kMaxTilesPerWarp; ++i) {
+    if (ok && i < ntw) {
+      const int tile = warp + i * kXWarps, mm = tile >> 3, R0 = (tile & 7) * 16 + g, R1 = R0 + 8;
+      uint32_t q0[4], q1[4];
+      q_pairs(c0[i], q0);
+      q_pairs(c1[i], q1);
+      const uint8_t* dsb = xs + L.dn + DM * kHalfBytes + mm * kSBBytes;
+      const uint32_t sbw0 = *reinterpret_cast<const uint32_t*>(dsb + R0 * 4);
+      const uint32_t sbw1 = *reinterpret_cast<const uint32_t*>(dsb + R1 * 4);
+      const float s0 = bf16lo(sbw0), s1 = bf16lo(sbw1);
+#pragma unroll
+      for (int set = 0; set < 2; ++set) {
+        if (set < nsets) {
+          float d[4] = {0.f, 0.f, 0.f, 0.f};
+          mma16816(d, q0[0], q1[0], q0[1], q1[1], hbv[set].x, hbv[set].y);
+          mma16816(d, q0[2], q1[2], q0[3], q1[3], hbv[set].z, hbv[set].w);
+          const int tok = 4 * set + tig;  // columns 2 tig, 2 tig + 1: this token's two planes
+          const int j = tok < T ? s_slot[tok] : -1;
+          if (j >= 0) {
+            const float ha = hsum[2 * tok], hb = hsum[2 * tok + 1];
+            float* gout = p.partials + (((size_t)tok * (k + 1) + j) * parts + part) * p.d;
+            gout[mm * kBlockRows + R0] = s0 * (d[0] + d[1]) + (bf16hi(sbw0) - 1024.f * s0) * ha + (bf16hi(sbw0) - 64.f * s0) * hb;
+            gout[mm * kBlockRows + R1] = s1 * (d[2] + d[3]) + (bf16hi(sbw1) - 1024.f * s1) * ha + (bf16hi(sbw1) - 64.f * s1) * hb;
+          }
+        }
+      }
+    }
+  }
+  if (!down_ok && tid == 0) *s_abort = 1;
+  __syncthreads();
+  if (tid == 0 && *s_abort) {
+    for (int i = 0; i <= NGU; ++i) mbar_drain(bars + 8u * i, 0);
+    set_device_status(p.hdr, MOE_ERR_DEVICE_TIMEOUT);
+  }
+}
+
+// y[t][i] = the sum of partials[t][c][i] over c, rounded to bf16, for token t = blockIdx.y (c runs
+// over the n_parts partial rows of one token: every (expert slot, 32-row part)). Thread (row r,
+// group q) sums the rows c = q, q + 32, ... (loads of 16 consecutive floats per group); warp r
+// then adds the 32 group sums of row r by a butterfly. The order is fixed, so the result does
+// not depend on timing.
 __global__ void __launch_bounds__(kYThreads) decode_reduce_kernel(const DecodeParams p, int n_parts) {
   constexpr int kGroups = kYThreads / kYRows;
-  __shared__ float s[kGroups][kYRows];
+  static_assert(kGroups == 32 && kYRows == kYThreads / 32, "one warp per output row for the butterfly");
+  __shared__ float s[kYRows][kGroups + 1];
   pdl_launch_dependents();
   pdl_wait();
   const int r = threadIdx.x % kYRows, q = threadIdx.x / kYRows;
   const int row = blockIdx.x * kYRows + r;
-  const int per = (n_parts + kGroups - 1) / kGroups, c_end = min(n_parts, (q + 1) * per);
+  const float* part = p.partials + (size_t)blockIdx.y * n_parts * p.d;
   float acc = 0.f;
-  for (int c0 = q * per; c0 < c_end; c0 += 8) {
+  for (int c0 = q; c0 < n_parts; c0 += 8 * kGroups) {
     float v[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = (c0 + j < c_end) ? __ldcg(p.partials + (size_t)(c0 + j) * p.d + row) : 0.f;
+    for (int j = 0; j < 8; ++j) {
+      const int c = c0 + j * kGroups;
+      v[j] = c < n_parts ? __ldcg(part + (size_t)c * p.d + row) : 0.f;
+    }
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc += v[j];
   }
-  s[q][r] = acc;
+  s[r][q] = acc;
   __syncthreads();
-  if (q == 0) {
-    float y = 0.f;
-    for (int i = 0; i < kGroups; ++i) y += s[i][r];
-    p.y[row] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
-  }
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float y = s[w][lane];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) y += __shfl_xor_sync(0xFFFFFFFFu, y, o);
+  if (lane == 0) p.y[(size_t)blockIdx.y * p.d + blockIdx.x * kYRows + w] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
 }
 
 }  // namespace
@@ -481,12 +937,11 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s, void* const* ev
   const int n_parts = decode_parts(dims);
   const int smem = x_smem(p.d).total;
   // The router and reduce kernels ask for the largest shared-memory carveout, so that the SMs
-  // they run on can take an expert-kernel CTA (~160 KB of shared memory) as soon as PDL lets it
+  // they run on can take an expert-kernel CTA (~130 KB of shared memory) as soon as PDL lets it
   // start, instead of waiting for the SM to drain and change its L1/shared split.
   static cudaError_t attr = [] {
     cudaError_t e = cudaSuccess;
-    for (auto kernel : {decode_expert_kernel<0, 8>, decode_expert_kernel<1, 8>, decode_expert_kernel<2, 8>,
-                        decode_expert_kernel<0, 32>, decode_expert_kernel<1, 32>})
+    for (auto kernel : {decode_expert_kernel<0>, decode_expert_kernel<1>, decode_expert_kernel<2>})
       if (e == cudaSuccess)
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, x_smem(kDecodeMaxD).total);
     if (e == cudaSuccess)
@@ -499,24 +954,40 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s, void* const* ev
   }();
   if (attr != cudaSuccess) return attr;
   if (mode == kDecodeDiagReadOnly) {  // the expert kernel's weight copies alone, no chain
-    decode_expert_kernel<2, 8><<<n_parts, kXThreads, (size_t)smem, s>>>(p);
+    decode_expert_kernel<2><<<n_parts, kXThreads, (size_t)smem, s>>>(p);
     return cudaGetLastError();
   }
   cudaError_t err = record_event(events, 0, s);
   if (err != cudaSuccess) return err;
   if ((err = launch_pdl(decode_router_kernel, (p.E + 1) / 2, kRThreads, 0, 1, s, p)) != cudaSuccess) return err;
   if ((err = record_event(events, 1, s)) != cudaSuccess) return err;
-  if (p.E <= 256)
-    err = mode == kDecodeDiagNoMath ? launch_pdl(decode_expert_kernel<1, 8>, n_parts, kXThreads, (size_t)smem, 1, s, p)
-                                    : launch_pdl(decode_expert_kernel<0, 8>, n_parts, kXThreads, (size_t)smem, 1, s, p);
-  else
-    err = mode == kDecodeDiagNoMath ? launch_pdl(decode_expert_kernel<1, 32>, n_parts, kXThreads, (size_t)smem, 1, s, p)
-                                    : launch_pdl(decode_expert_kernel<0, 32>, n_parts, kXThreads, (size_t)smem, 1, s, p);
+  err = mode == kDecodeDiagNoMath ? launch_pdl(decode_expert_kernel<1>, n_parts, kXThreads, (size_t)smem, 1, s, p)
+                                  : launch_pdl(decode_expert_kernel<0>, n_parts, kXThreads, (size_t)smem, 1, s, p);
   if (err != cudaSuccess) return err;
   if ((err = record_event(events, 2, s)) != cudaSuccess) return err;
   if ((err = launch_pdl(decode_reduce_kernel, p.d / kYRows, kYThreads, 0, 1, s, p, n_parts)) != cudaSuccess)
     return err;
   return record_event(events, 3, s);
+}
+
+cudaError_t launch_decode_batch(const DecodeParams& p, cudaStream_t s) {
+  const moe_dims dims = {p.d, p.E, p.k, p.inter, p.inter, kGroup};
+  const int parts = p.inter / kDecPartRows, n_parts = decode_parts(dims);
+  const int smem = b_smem(p.d).total;
+  static cudaError_t attr = cudaFuncSetAttribute(decode_batch_expert_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 b_smem(kBatchMaxD).total);
+  if (attr != cudaSuccess) return attr;
+  // the distinct-expert list lives in the routing part of the workspace: after topk_w
+  int32_t* dexp = reinterpret_cast<int32_t*>(p.topk_w + (size_t)p.T * p.k);
+  int32_t* n_distinct = dexp + p.T * p.k;
+  cudaError_t err = launch_pdl(decode_router_kernel, (p.E + 1) / 2, kRThreads, 0, 1, s, p);
+  if (err != cudaSuccess) return err;
+  err = launch_pdl(decode_batch_select_kernel, 1, kMaxDecodeBatch * 32, 0, 1, s, p, dexp, n_distinct);
+  if (err != cudaSuccess) return err;
+  if ((err = launch_pdl(decode_batch_expert_kernel, (p.T * p.k + 1) * parts, kXThreads, (size_t)smem, 1, s, p,
+                        (const int32_t*)dexp, (const int32_t*)n_distinct)) != cudaSuccess)
+    return err;
+  return launch_pdl(decode_reduce_kernel, dim3(p.d / kYRows, p.T), kYThreads, 0, 1, s, p, n_parts);
 }
 
 }  // namespace moe

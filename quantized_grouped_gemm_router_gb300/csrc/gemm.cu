@@ -71,12 +71,15 @@ constexpr int kATileBytes = kBlockRows * 128;              // 128 rows x 64 16-b
 // rows); kRows: maximum tile rows (MMA N); kMRows: output rows of one work item.
 template <int MODE>
 struct Cfg;
+// kEpi: the work list and epilogue the mode shares (the dense ablation modes reuse the gate/up and
+// down ones; only their A operand differs).
 template <>
 struct Cfg<kModeGateUp> {
   static constexpr int kIssuers = 2, kSW = 4, kSB = 2, kStagesW = 3, kStagesB = 3, kStagesA = 2, kPlanes = 1;
   static constexpr int kRows = kTileRows, kMRows = 64;             // 64 features: gate rows over up rows
   static constexpr int kWStage = 2 * kSW * kGUQuarter;            // two row quarters x kSW blocks
   static constexpr bool kFp16 = true, kQ4 = true;
+  static constexpr int kEpi = kModeGateUp;
 };
 template <>
 struct Cfg<kModeDown> {
@@ -84,6 +87,7 @@ struct Cfg<kModeDown> {
   static constexpr int kRows = kTileRows, kMRows = kBlockRows;
   static constexpr int kWStage = kSW * kBlockBytes;                // codes (2 kSW halves), then kSW sb
   static constexpr bool kFp16 = true, kQ4 = true;
+  static constexpr int kEpi = kModeDown;
 };
 template <>
 struct Cfg<kModeRouter> {
@@ -91,6 +95,25 @@ struct Cfg<kModeRouter> {
   static constexpr int kRows = kRouterRows, kMRows = kBlockRows;
   static constexpr int kWStage = kSW * kATileBytes;                // bf16 A tiles, read by the MMA
   static constexpr bool kFp16 = false, kQ4 = false;
+  static constexpr int kEpi = kModeRouter;
+};
+// Materialised-dequantization ablation: fp16 weight tiles from the dense buffer, read by the MMA
+// from shared memory like the router's.
+template <>
+struct Cfg<kModeGateUpDense> {
+  static constexpr int kIssuers = 2, kSW = 2, kSB = 2, kStagesW = 3, kStagesB = 2, kStagesA = 0, kPlanes = 1;
+  static constexpr int kRows = kTileRows, kMRows = 64;
+  static constexpr int kWStage = kSW * kATileBytes;
+  static constexpr bool kFp16 = true, kQ4 = false;
+  static constexpr int kEpi = kModeGateUp;
+};
+template <>
+struct Cfg<kModeDownDense> {
+  static constexpr int kIssuers = 2, kSW = 2, kSB = 1, kStagesW = 3, kStagesB = 2, kStagesA = 0, kPlanes = 2;
+  static constexpr int kRows = kTileRows, kMRows = kBlockRows;
+  static constexpr int kWStage = kSW * kATileBytes;
+  static constexpr bool kFp16 = true, kQ4 = false;
+  static constexpr int kEpi = kModeDown;
 };
 
 constexpr int tmem_cols_for(int cols) {
@@ -112,8 +135,8 @@ struct Smem {
   static constexpr int kTmemCols = tmem_cols_for(kTmemNeed);
   static_assert(kTmemNeed <= 512, "tensor memory budget");
   // down: each epilogue warp keeps the (token, weight) list of its own chunks (half the rows)
-  static constexpr int kListRows = MODE == kModeDown ? C::kRows / 2 : 0;
-  static constexpr int kXBytes = MODE == kModeGateUp ? kXPairs * kXSlots * 16 * 32 * 4 : 0;
+  static constexpr int kListRows = C::kEpi == kModeDown ? C::kRows / 2 : 0;
+  static constexpr int kXBytes = C::kEpi == kModeGateUp ? kXPairs * kXSlots * 16 * 32 * 4 : 0;
   static constexpr int w_off = 0;
   static constexpr int b_off = w_off + C::kStagesW * C::kWStage;
   static constexpr int x_off = b_off + C::kStagesB * kBStage;
@@ -192,10 +215,10 @@ __device__ __forceinline__ Item decode_item(const GemmParams& p, int item, int n
     it.nrows = p.tile_map[3 * tile + 2];
     it.row0 = p.tile_row0[tile];  // no dependent load: the router stored offsets[expert] + r0
   } else {
-    it.r0 = (tile - n_routed) * kTileRows;
+    it.r0 = (tile - n_routed) * p.tile_rows;
     it.expert = p.E;
     it.shared = true;
-    it.nrows = min(kTileRows, p.T - it.r0);
+    it.nrows = min(p.tile_rows, p.T - it.r0);
     it.row0 = p.T * p.k + it.r0;
   }
   it.n16 = (it.nrows + 15) & ~15;
@@ -282,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     n_tile_total = (p.T + kRouterRows - 1) / kRouterRows;
   } else {
     n_routed = *p.n_tiles;
-    n_tile_total = n_routed + (p.T + kTileRows - 1) / kTileRows;  // routed tiles, then shared
+    n_tile_total = n_routed + (p.T + p.tile_rows - 1) / p.tile_rows;  // routed tiles, then shared
   }
   const int n_items = n_tile_total * p.m_tiles;
 
@@ -314,8 +337,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_4d(dst, &maps.a, 0, it.m, 2 * kb0, it.expert, full_w(s));
             tma_load_4d(dst + 2 * C::kSW * kHalfBytes, &maps.a2, 0, it.m, kb0, it.expert, full_w(s));
           } else {
+            // 16-bit A tiles by one 3-D tensor copy: the router weight, or the dense weights of the
+            // materialised-dequantization ablation ([expert][item][128 rows] / [expert][d rows])
+            const int row0 = MODE == kModeRouter       ? it.m * kBlockRows
+                             : MODE == kModeGateUpDense ? (it.expert * p.m_tiles + it.m) * kBlockRows
+                                                        : it.expert * p.d + it.m * kBlockRows;
             mbar_arrive_expect_tx(full_w(s), (uint32_t)C::kWStage);
-            tma_load_3d(dst, &maps.a, 0, it.m * kBlockRows, kb0, full_w(s));
+            tma_load_3d(dst, &maps.a, 0, row0, kb0, full_w(s));
           }
         }
       }
@@ -366,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the buffer, and the epilogue adds the halves. Each tcgen05.mma costs its issuing thread
         // tens of cycles however narrow the tile, so a narrow tile left to one issuer would bound
         // the kernel (K blocks per stage: kSB = 2, and every K extent here is a multiple of 128).
-        const bool split_k = C::kIssuers == 2 && it.n16 <= S::kAccCols / 2;
+        const bool split_k = C::kIssuers == 2 && C::kSB == 2 && it.n16 <= S::kAccCols / 2;
         const int half16 = C::kIssuers == 2 ? 16 * ((it.n16 / 16 + 1) / 2) : it.n16;
         const int c0 = split_k || issuer == 0 ? 0 : half16;
         const int ncols = split_k ? it.n16 : issuer == 0 ? half16 : it.n16 - half16;
@@ -510,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Item it = nxt;
       if (item + (int)gridDim.x < n_items) nxt = decode_item<MODE>(p, item + gridDim.x, n_routed);
       const int buf = n & 1;
-      if (MODE == kModeDown) {  // this warp's (token, routing weight) list, read before the wait
+      if (C::kEpi == kModeDown) {  // this warp's (token, routing weight) list, read before the wait
         constexpr int kPer = (C::kRows + 31) / 32;
         int2 tw[kPer];
 #pragma unroll
@@ -536,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(acc_full(buf), (n >> 1) & 1, s_abort)))) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + lane_addr + buf * S::kAccCols;
-      const bool split_k = C::kIssuers == 2 && it.n16 <= S::kAccCols / 2;  // the MMA issuers' K split
+      const bool split_k = C::kIssuers == 2 && C::kSB == 2 && it.n16 <= S::kAccCols / 2;  // the MMA issuers' K split
       for (int j0 = 16 * half; j0 < it.n16 && ok; j0 += 32) {
         uint32_t acc[16];
         tmem_ld16(taddr + j0, acc);
@@ -548,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) acc[jj] = __float_as_uint(__uint_as_float(acc[jj]) + __uint_as_float(acc2[jj]));
         }
-        if (MODE == kModeGateUp) {
+        if (C::kEpi == kModeGateUp) {
           const int sl = u & 1;
           float* xs = xbuf + sl * 16 * 32;
           if (!gate_warp) {  // hand the up values to the gate warp
@@ -587,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int j = j0 + jj;
             if (j < it.nrows) {
               const float v = __uint_as_float(acc[jj]);
-              if (MODE == kModeDown) {
+              if (C::kEpi == kModeDown) {
                 const int li = ((j >> 5) << 4) | jj;
                 atomicAdd(p.yacc + (size_t)tok[li] * p.d + orow, v * wgt[li]);
               } else if (orow < p.E) {
@@ -601,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(acc_empty(buf));  // the accumulator buffer is free again
     }
-    if (MODE == kModeGateUp && __any_sync(0xFFFFFFFFu, over) && lane == 0)
+    if (C::kEpi == kModeGateUp && __any_sync(0xFFFFFFFFu, over) && lane == 0)
       set_device_status(p.hdr, MOE_ERR_OUT_OF_RANGE);
   }
 
@@ -644,22 +672,27 @@ cudaError_t launch_gemm(int mode, const GemmParams& p, const GemmMaps* maps, int
   switch (mode) {
     case kModeRouter: return launch_mode<kModeRouter>(p, maps, grid, s);
     case kModeGateUp: return launch_mode<kModeGateUp>(p, maps, grid, s);
+    case kModeGateUpDense: return launch_mode<kModeGateUpDense>(p, maps, grid, s);
+    case kModeDownDense: return launch_mode<kModeDownDense>(p, maps, grid, s);
     default: return launch_mode<kModeDown>(p, maps, grid, s);
   }
 }
 
-int gemm_kb_per_stage(int mode) {
-  return mode == kModeRouter ? Cfg<kModeRouter>::kSB : mode == kModeGateUp ? Cfg<kModeGateUp>::kSB : Cfg<kModeDown>::kSB;
+template <int F>
+int cfg_value(int mode) {
+  switch (mode) {
+    case kModeRouter: return F == 0 ? Cfg<kModeRouter>::kSB : F == 1 ? Cfg<kModeRouter>::kSW : Cfg<kModeRouter>::kMRows;
+    case kModeGateUp: return F == 0 ? Cfg<kModeGateUp>::kSB : F == 1 ? Cfg<kModeGateUp>::kSW : Cfg<kModeGateUp>::kMRows;
+    case kModeGateUpDense:
+      return F == 0 ? Cfg<kModeGateUpDense>::kSB : F == 1 ? Cfg<kModeGateUpDense>::kSW : Cfg<kModeGateUpDense>::kMRows;
+    case kModeDownDense:
+      return F == 0 ? Cfg<kModeDownDense>::kSB : F == 1 ? Cfg<kModeDownDense>::kSW : Cfg<kModeDownDense>::kMRows;
+    default: return F == 0 ? Cfg<kModeDown>::kSB : F == 1 ? Cfg<kModeDown>::kSW : Cfg<kModeDown>::kMRows;
+  }
 }
-
-int gemm_kw_per_stage(int mode) {
-  return mode == kModeRouter ? Cfg<kModeRouter>::kSW : mode == kModeGateUp ? Cfg<kModeGateUp>::kSW : Cfg<kModeDown>::kSW;
-}
-
-int gemm_out_rows(int mode) {
-  return mode == kModeRouter ? Cfg<kModeRouter>::kMRows : mode == kModeGateUp ? Cfg<kModeGateUp>::kMRows
-                                                                               : Cfg<kModeDown>::kMRows;
-}
+int gemm_kb_per_stage(int mode) { return cfg_value<0>(mode); }
+int gemm_kw_per_stage(int mode) { return cfg_value<1>(mode); }
+int gemm_out_rows(int mode) { return cfg_value<2>(mode); }
 
 int router_tile_rows() { return kRouterRows; }
 

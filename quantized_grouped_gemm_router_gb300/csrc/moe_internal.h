@@ -43,6 +43,7 @@ constexpr int kGUMat = 2 * kQuarterRows * 16 + kQuarterRows * 4;  // 1152: one m
 constexpr int kGUQuarter = 2 * kGUMat;                             // 2304: gate + up quarter
 constexpr int kSBBytes = kBlockRows * 4;                           // 512
 constexpr int kTileRows = 192;      // block-map tile height (max MMA N of the prefill GEMMs)
+constexpr int kMinTileRows = 32;    // smallest tile height a call may ask for (fixed-tile ablation)
 constexpr int kMaxTopK = 16;
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTokens = 65536;
@@ -82,9 +83,8 @@ constexpr int kRouteChunk = 64;     // tokens per routing chunk (one CTA of the 
 
 struct WsHeader {
   int status;        // sticky device status (moe_status codes ORed as bits 1 << code)
-  unsigned ticket;   // last-CTA ticket of the top-k kernel
-  unsigned dticket;  // last-CTA ticket of the decode router
-  int pad[61];
+  unsigned ticket;   // last-CTA ticket of the routing histogram kernel
+  int pad[62];
 };
 static_assert(sizeof(WsHeader) == 256, "header size");
 
@@ -100,25 +100,29 @@ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 // writes a partial output row of d floats that the combine kernel sums in a fixed order.
 constexpr int kDecPartRows = 32;
 constexpr int kDecodeMaxD = 3072;   // the expert kernel keeps all its weight slices in smem
+constexpr int kMaxDecodeBatch = 8;  // tokens of one moe_decode_batch call (the MMA's 8 columns)
+constexpr int kBatchMaxD = 2048;    // the batch expert kernel also keeps 8 tokens' x in smem
 inline int decode_parts(const moe_dims& d) { return (d.top_k + 1) * (d.inter / kDecPartRows); }
 inline size_t decode_partial_bytes(const moe_dims& d) { return (size_t)decode_parts(d) * d.d * 4; }
 
-inline int max_routed_tiles(int T, int k, int E) {
+// Upper bound on the routed block-map tiles of T tokens with tiles of tile_rows rows: every hit
+// expert has a ragged last tile, and the whole tiles are at most A / tile_rows.
+inline int max_routed_tiles(int T, int k, int E, int tile_rows = kTileRows) {
   long long A = (long long)T * k;
-  return (int)((A < E ? A : E) + A / kTileRows);
+  return (int)((A < E ? A : E) + A / tile_rows);
 }
 
 inline WsLayout ws_layout(const moe_dims& d, int T) {
   WsLayout L;
   const size_t A = (size_t)T * d.top_k, E = (size_t)d.n_experts;
   L.n_chunks = (T + kRouteChunk - 1) / kRouteChunk;
-  L.max_tiles = max_routed_tiles(T, d.top_k, d.n_experts);
+  L.max_tiles = max_routed_tiles(T, d.top_k, d.n_experts, kMinTileRows);  // room for any tile height
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t r = o; o = align256(o + bytes); return r; };
   L.header = take(sizeof(WsHeader));
   L.logits = take((size_t)T * E * 4);
   L.topk_idx = take(A * 4);
-  L.topk_w = take(A * 4);
+  L.topk_w = take(A * 4 + (A + 1) * 4);  // + the batch decode's distinct-expert list
   L.chunk_counts = take((size_t)L.n_chunks * E * 4);
   L.chunk_base = take((size_t)L.n_chunks * E * 4);
   L.counts = take(E * 4);
@@ -132,7 +136,7 @@ inline WsLayout ws_layout(const moe_dims& d, int T) {
   L.x16 = take((A + T) * (size_t)d.d * 2);             // fp16 x: A expert-sorted rows, then T token rows
   L.hidden = take(2 * (A + T) * (size_t)d.inter * 2);  // SwiGLU rows: fp16 leading part, fp16 remainder
   L.yacc = take((size_t)T * d.d * 4);
-  L.dec_part = take(decode_partial_bytes(d));
+  L.dec_part = take(decode_partial_bytes(d) * (size_t)(T < kMaxDecodeBatch ? T : kMaxDecodeBatch));
   L.total = o;
   return L;
 }
@@ -157,6 +161,7 @@ struct RouteParams {
   int32_t* tile_map;     // [max_tiles, 3]
   int32_t* tile_row0;    // [max_tiles] sorted row of each tile's first row (offsets[expert] + row)
   int32_t* n_tiles;      // [1]
+  int tile_rows;         // block-map tile height (kTileRows, or smaller for the fixed-tile ablation)
   float* yacc;           // [T, d] zeroed by the top-k kernel (NULL: skip)
   const uint16_t* x;     // [T, d] bf16 input (NULL: no conversion)
   uint16_t* x16;         // [A + T, d] fp16 x: rows A.. in token order (top-k kernel), rows 0..A-1 in
@@ -165,7 +170,10 @@ struct RouteParams {
   int T, E, k, d, n_chunks;
 };
 
-enum GemmMode { kModeRouter = 0, kModeGateUp = 1, kModeDown = 2 };
+// kModeGateUpDense / kModeDownDense: the materialised-dequantization ablation, the same GEMMs on
+// fp16 weights expanded beforehand into a dense buffer (gate/up: [E + 1][I / 64][128 rows: 64 gate
+// then the same 64 features' up][d]; down: [E + 1][d][I]).
+enum GemmMode { kModeRouter = 0, kModeGateUp = 1, kModeDown = 2, kModeGateUpDense = 3, kModeDownDense = 4 };
 
 struct GemmParams {
   // weights
@@ -187,22 +195,24 @@ struct GemmParams {
   const float* router_bias;   // [E] or NULL (router)
   WsHeader* hdr;
   int T, k, E, d, inter;
+  int tile_rows;              // block-map tile height (shared-expert tiles use the same)
   int hidden_rows;            // A + T: row offset of the remainder plane of `hidden`
 };
 
 struct DecodeParams {
-  const uint16_t* x;          // [d] bf16
+  const uint16_t* x;          // [T, d] bf16
   const uint16_t* router_w;   // [E, d] bf16
   const float* router_bias;   // [E] or NULL
   const uint8_t* packed;
   size_t expert_stride, gu_bytes;
-  float* logits;              // [E]
-  int32_t* topk_idx;          // [k]
-  float* topk_w;              // [k]
-  float* partials;            // [(k + 1) * I / 32, d] fp32 per-CTA partial outputs
-  uint16_t* y;                // [d] bf16
+  float* logits;              // [T, E]
+  int32_t* topk_idx;          // [T, k]
+  float* topk_w;              // [T, k]
+  float* partials;            // [T, k + 1, I / 32, d] fp32 partial outputs (T = 1: one per expert-kernel CTA)
+  uint16_t* y;                // [T, d] bf16
   WsHeader* hdr;
   int d, E, k, inter;
+  int T;                      // tokens: 1 (moe_decode), up to kMaxDecodeBatch (moe_decode_batch)
 };
 
 // Argument checks shared by every entry point (csrc/api.cu): supported dims, and a layer's
@@ -214,7 +224,16 @@ int check_layer(const moe_layer* L, bool need_router);
 // Launchers (each returns cudaGetLastError()).
 cudaError_t launch_wait_timeout_selftest(WsHeader* hdr, cudaStream_t s);
 cudaError_t launch_pack(const moe_dims& d, const moe_q4_view* views, uint8_t* packed, cudaStream_t s);
-cudaError_t launch_route(const RouteParams& p, cudaStream_t s);
+// Expands the packed weights of the experts with counts[e] > 0 and of the shared expert into the
+// dense fp16 layouts of the materialised-dequantization ablation (see GemmMode).
+size_t dense_gu_bytes(const moe_dims& d);
+size_t dense_dn_bytes(const moe_dims& d);
+cudaError_t launch_dense_dequant(const moe_dims& d, const uint8_t* packed, const int32_t* counts, uint16_t* dense_gu,
+                                 uint16_t* dense_dn, cudaStream_t s);
+cudaError_t launch_route(const RouteParams& p, cudaStream_t s);        // all of the routing below
+cudaError_t launch_route_topk(const RouteParams& p, cudaStream_t s);   // top-k (+ fp16 x, zero Yacc)
+cudaError_t launch_route_group(const RouteParams& p, cudaStream_t s);  // histogram, scan, block map, scatter
+cudaError_t launch_route_rows(const RouteParams& p, cudaStream_t s);   // expert-sorted fp16 x rows
 // Tensor maps of the prefill GEMMs.
 //   rows[i]: the activation operand for tiles of 16 (i + 1) rows, box = 64 columns x 16 (i + 1)
 //            rows x kSB column blocks: gate/up and router see a row-major [rows, cols] 16-bit
@@ -238,6 +257,8 @@ cudaError_t launch_cast(const float* yacc, uint16_t* y, size_t n, cudaStream_t s
 // (partial rows of zeros); kDecodeDiagReadOnly the expert kernel's weight copies alone.
 constexpr int kDecodeDiagNoMath = 1, kDecodeDiagReadOnly = 2;
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s, void* const* events, int mode = 0);
+// p.T tokens (2..kMaxDecodeBatch): the union of their selected experts is read once.
+cudaError_t launch_decode_batch(const DecodeParams& p, cudaStream_t s);
 
 // Records events[i] (if the array and the entry are non-NULL) on the stream; capturable.
 inline cudaError_t record_event(void* const* events, int i, cudaStream_t s) {

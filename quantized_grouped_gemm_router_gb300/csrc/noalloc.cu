@@ -104,5 +104,6 @@ extern "C" int moe_decode_noalloc(const moe_layer* layer, const uint16_t* x, uin
   p.E = d.n_experts;
   p.k = d.top_k;
   p.inter = d.inter;
+  p.T = 1;
   return launch_decode(p, stream, nullptr) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -1,6 +1,10 @@
 // Canonical MLX-style Q4 matrices -> the library's packed expert layout (a pure re-layout:
 // codes are permuted inside each 32-bit word and scales/biases are interleaved; no value
 // changes). Layout: see PackedLayout in moe_internal.h.
+#include <cuda_fp16.h>
+
+#include <algorithm>
+
 #include "moe_internal.h"
 
 namespace moe {
@@ -86,6 +90,75 @@ cudaError_t launch_pack(const moe_dims& d, const moe_q4_view* v, uint8_t* packed
   a.n_experts = d.n_experts;
   const int blocks = 2 * (d.inter / kBlockRows) * (d.d / kGroup) + (d.d / kBlockRows) * (d.inter / kGroup);
   pack_kernel<<<dim3(blocks, d.n_experts + 1), 128, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------------------------
+// Materialised dequantization (ablation): each thread expands one packed word (8 codes) of one
+// expert into 8 fp16 weights, scale * q + bias rounded once to fp16 exactly as the in-tile path
+// does; experts no token selected are skipped.
+// ------------------------------------------------------------------------------------------
+size_t dense_gu_bytes(const moe_dims& d) { return (size_t)(d.n_experts + 1) * 2 * d.inter * d.d * 2; }
+size_t dense_dn_bytes(const moe_dims& d) { return (size_t)(d.n_experts + 1) * d.d * d.inter * 2; }
+
+namespace {
+
+__device__ __forceinline__ uint4 expand8(uint32_t w, uint32_t sbw) {
+  const __half s = __float2half_rn(__uint_as_float(sbw << 16));
+  const __half b = __float2half_rn(__uint_as_float(sbw & 0xFFFF0000u));
+  uint32_t o[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {  // columns 2j, 2j+1 sit in nibble slots j and j + 4
+    const __half lo = __hfma(__ushort2half_rn((w >> (4 * j)) & 0xF), s, b);
+    const __half hi = __hfma(__ushort2half_rn((w >> (4 * j + 16)) & 0xF), s, b);
+    o[j] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__global__ void __launch_bounds__(256) dense_dequant_kernel(const uint8_t* __restrict__ packed, const int32_t* counts,
+                                                            uint16_t* dense_gu, uint16_t* dense_dn, int d, int E,
+                                                            int inter, size_t expert_stride, size_t gu_bytes) {
+  const int e = blockIdx.y;
+  if (e < E && __ldcg(counts + e) == 0) return;  // unselected expert (the shared expert, e == E, always runs)
+  const int KB = d / kGroup, DM = d / kBlockRows, KBI = inter / kGroup;
+  const uint8_t* eb = packed + (size_t)e * expert_stride;
+  const size_t gu_words = (size_t)2 * inter * d / 8, dn_words = (size_t)d * inter / 8;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < gu_words + dn_words;
+       i += (size_t)gridDim.x * blockDim.x) {
+    if (i < gu_words) {  // dense gate/up row r of item h, columns 8 cw .. 8 cw + 7
+      const int cw = (int)(i % (d / 8));
+      const size_t rowi = i / (d / 8);
+      const int r = (int)(rowi % 128), h = (int)(rowi / 128);
+      const int f = 64 * h + (r & 63), mat = r >> 6;
+      const int m = f / kBlockRows, q = (f % kBlockRows) / kQuarterRows, rr = f % kQuarterRows;
+      const int c = 8 * cw, kb = c / kGroup, half = (c % kGroup) / 32, w = (c % 32) / 8;
+      const uint8_t* blk = eb + gu_offset(m, q, kb, KB) + mat * kGUMat;
+      const uint32_t word = *reinterpret_cast<const uint32_t*>(blk + half * kQuarterRows * 16 + rr * 16 + 4 * w);
+      const uint32_t sbw = *reinterpret_cast<const uint32_t*>(blk + 2 * kQuarterRows * 16 + rr * 4);
+      reinterpret_cast<uint4*>(dense_gu + (size_t)e * 2 * inter * d)[i] = expand8(word, sbw);
+    } else {  // dense down row o, columns 8 cw .. 8 cw + 7 of I
+      const size_t j = i - gu_words;
+      const int cw = (int)(j % (inter / 8)), o = (int)(j / (inter / 8));
+      const int mm = o / kBlockRows, r = o % kBlockRows;
+      const int c = 8 * cw, kbd = c / kGroup, hd = (c % kGroup) / 32, w = (c % 32) / 8;
+      const uint8_t* dn = eb + gu_bytes;
+      const uint32_t word = *reinterpret_cast<const uint32_t*>(dn + dn_code_offset(kbd, hd, mm, DM) + r * 16 + 4 * w);
+      const uint32_t sbw = *reinterpret_cast<const uint32_t*>(dn + dn_sb_offset(kbd, mm, DM, KBI) + r * 4);
+      reinterpret_cast<uint4*>(dense_dn + (size_t)e * d * inter)[j] = expand8(word, sbw);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_dense_dequant(const moe_dims& d, const uint8_t* packed, const int32_t* counts, uint16_t* dense_gu,
+                                 uint16_t* dense_dn, cudaStream_t s) {
+  const PackedLayout P = packed_layout(d);
+  const size_t words = (size_t)3 * d.inter * d.d / 8;
+  const int blocks = (int)std::min<size_t>((words + 255) / 256, 4096);
+  dense_dequant_kernel<<<dim3(blocks, d.n_experts + 1), 256, 0, s>>>(packed, counts, dense_gu, dense_dn, d.d,
+                                                                      d.n_experts, d.inter, P.expert_stride, P.gu_bytes);
   return cudaGetLastError();
 }
 

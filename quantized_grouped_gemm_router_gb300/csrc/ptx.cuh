@@ -178,9 +178,9 @@ __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepc
 
 // Host: launch with programmatic dependent launch (and an optional thread-block cluster size).
 template <class Kernel, class... Args>
-cudaError_t launch_pdl(Kernel kernel, int grid, int block, size_t smem, int cluster, cudaStream_t s, Args... args) {
+cudaError_t launch_pdl(Kernel kernel, dim3 grid, int block, size_t smem, int cluster, cudaStream_t s, Args... args) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
+  cfg.gridDim = grid;
   cfg.blockDim = dim3(block);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -199,6 +199,5 @@ cudaError_t launch_pdl(Kernel kernel, int grid, int block, size_t smem, int clus
   cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
-
 
 }  // namespace moe

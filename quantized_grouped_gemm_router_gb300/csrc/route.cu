@@ -3,8 +3,7 @@
 // selection, histogram, prefix scan, scatter and block map run on the GPU with no host round
 // trip). Three launches (four in prefill):
 //   route_topk_kernel    16 tokens per CTA: warp top-k on order-preserving logit keys (ties to
-//                        the lower index; a threshold from the lanes' maxima, then exact ranks of
-//                        the few experts above it), renormalised softmax weights; the fp16 copy of x and
+//                        the lower index), renormalised softmax weights; the fp16 copy of x and
 //                        the zeroing of the combine accumulator rows
 //   route_hist_kernel    one CTA per 64-token chunk: histogram in shared memory; the last CTA to
 //                        finish (ticket) scans the chunk histograms into counts, offsets,
@@ -67,13 +66,13 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const RoutePar
   const int t_begin = blockIdx.x * kTopkTokens;
   const int t_end = min(p.T, t_begin + kTopkTokens);
   for (int t = t_begin + warp; t < t_end; t += kTopkThreads / 32) {
-    int rank, my_e;
+    int my_e;
     float my_w;
-    const bool bad = warp_select_topk(p.logits + (size_t)t * E, E, k, &rank, &my_e, &my_w);
+    const bool bad = warp_topk_softmax(p.logits + (size_t)t * E, E, k, &my_e, &my_w);
     if (bad && lane == 0) set_device_status(p.hdr, MOE_ERR_NONFINITE);
-    if (rank >= 0) {
-      p.topk_idx[(size_t)t * k + rank] = my_e;
-      p.topk_w[(size_t)t * k + rank] = my_w;
+    if (lane < k) {
+      p.topk_idx[(size_t)t * k + lane] = my_e;
+      p.topk_w[(size_t)t * k + lane] = my_w;
     }
   }
   const int n8 = (t_end - t_begin) * p.d / 8;  // 8-element chunks of this CTA's rows
@@ -149,7 +148,7 @@ __global__ void __launch_bounds__(kTopkThreads) route_hist_kernel(const RoutePar
   for (int i = 0; i < 4; ++i) {
     const int e = 4 * tid + i;
     cnt[i] = e < E ? s_counts[e] : 0;
-    tiles[i] = (cnt[i] + kTileRows - 1) / kTileRows;
+    tiles[i] = (cnt[i] + p.tile_rows - 1) / p.tile_rows;
   }
   int total_rows, total_tiles;
   const int off0 = block_exclusive_scan4(cnt, s_warp, &total_rows);
@@ -164,9 +163,9 @@ __global__ void __launch_bounds__(kTopkThreads) route_hist_kernel(const RoutePar
       for (int r = 0; r < tiles[i]; ++r) {
         int32_t* tm = p.tile_map + 3 * (size_t)(tl + r);
         tm[0] = e;
-        tm[1] = r * kTileRows;
-        tm[2] = min(kTileRows, cnt[i] - r * kTileRows);
-        p.tile_row0[tl + r] = off + r * kTileRows;
+        tm[1] = r * p.tile_rows;
+        tm[2] = min(p.tile_rows, cnt[i] - r * p.tile_rows);
+        p.tile_row0[tl + r] = off + r * p.tile_rows;
       }
     }
     off += cnt[i];
@@ -274,15 +273,27 @@ __global__ void __launch_bounds__(256) cast_kernel(const float* __restrict__ yac
 
 // Every launch is chained to its predecessor with programmatic dependent launch: it starts while
 // the predecessor finishes and waits for it (pdl_wait) before touching any data.
-cudaError_t launch_route(const RouteParams& p, cudaStream_t s) {
-  cudaError_t err = launch_pdl(route_topk_kernel, (p.T + kTopkTokens - 1) / kTopkTokens, kTopkThreads, 0, 1, s, p);
+cudaError_t launch_route_topk(const RouteParams& p, cudaStream_t s) {
+  return launch_pdl(route_topk_kernel, (p.T + kTopkTokens - 1) / kTopkTokens, kTopkThreads, 0, 1, s, p);
+}
+
+cudaError_t launch_route_group(const RouteParams& p, cudaStream_t s) {
+  cudaError_t err = launch_pdl(route_hist_kernel, p.n_chunks, kTopkThreads, 0, 1, s, p);
   if (err != cudaSuccess) return err;
-  if ((err = launch_pdl(route_hist_kernel, p.n_chunks, kTopkThreads, 0, 1, s, p)) != cudaSuccess) return err;
-  if ((err = launch_pdl(route_scatter_kernel, p.n_chunks, kScatterWarps * 32, 0, 1, s, p)) != cudaSuccess || !p.x)
-    return err;
+  return launch_pdl(route_scatter_kernel, p.n_chunks, kScatterWarps * 32, 0, 1, s, p);
+}
+
+cudaError_t launch_route_rows(const RouteParams& p, cudaStream_t s) {
   const int rows = p.T * p.k, per_cta = 8;  // 8 warps of 256 threads
   const int blocks = (rows + per_cta - 1) / per_cta < 152 * 8 ? (rows + per_cta - 1) / per_cta : 152 * 8;
   return launch_pdl(route_rows_kernel, blocks, 256, 0, 1, s, p);
+}
+
+cudaError_t launch_route(const RouteParams& p, cudaStream_t s) {
+  cudaError_t err = launch_route_topk(p, s);
+  if (err != cudaSuccess) return err;
+  if ((err = launch_route_group(p, s)) != cudaSuccess || !p.x) return err;
+  return launch_route_rows(p, s);
 }
 
 cudaError_t launch_cast(const float* yacc, uint16_t* y, size_t n, cudaStream_t s) {

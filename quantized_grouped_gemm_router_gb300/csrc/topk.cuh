@@ -86,87 +86,76 @@ __device__ __forceinline__ bool warp_topk_softmax(const float* row, int E, int k
   return __any_sync(0xFFFFFFFFu, bad);
 }
 
-// Whole warp, E <= 32 * SLOTS, k <= 16: the same selection and weights as warp_topk_softmax,
-// computed by a threshold and exact ranks instead of k serial rounds. Every expert has the unique
-// key (orderable logit << 32) | ~index. Each lane's largest key belongs to a different expert, so
-// the k-th largest key overall is at least tau, the k-th largest of the 32 lane maxima; only the
-// experts with a key >= tau (about k + 1 for Gaussian logits) are candidates. They are gathered
-// one per lane and ranked by counting the larger candidate keys. If more than 32 experts pass the
-// threshold (ties of the logits), the serial selection runs instead.
-// Returns true (on every lane) if a logit of the row was NaN or infinite. Lane l gets *rank_out =
-// the slot (0..k-1) of the expert it holds, with its expert and weight, or -1.
-template <int SLOTS>
-__device__ __forceinline__ bool warp_select_topk(const float* row, int E, int k, int* rank_out, int* e_out,
-                                                 float* w_out) {
+// Compare-exchange keeping a >= b (descending order).
+__device__ __forceinline__ void cx_desc(uint64_t& a, uint64_t& b) {
+  const uint64_t hi = a > b ? a : b, lo = a > b ? b : a;
+  a = hi;
+  b = lo;
+}
+// Sorts 8 keys descending (Batcher's odd-even merge network, 19 compare-exchanges).
+__device__ __forceinline__ void sort8_desc(uint64_t (&v)[8]) {
+  cx_desc(v[0], v[1]); cx_desc(v[2], v[3]); cx_desc(v[4], v[5]); cx_desc(v[6], v[7]);
+  cx_desc(v[0], v[2]); cx_desc(v[1], v[3]); cx_desc(v[4], v[6]); cx_desc(v[5], v[7]);
+  cx_desc(v[1], v[2]); cx_desc(v[5], v[6]);
+  cx_desc(v[0], v[4]); cx_desc(v[1], v[5]); cx_desc(v[2], v[6]); cx_desc(v[3], v[7]);
+  cx_desc(v[2], v[4]); cx_desc(v[3], v[5]);
+  cx_desc(v[1], v[2]); cx_desc(v[3], v[4]); cx_desc(v[5], v[6]);
+}
+
+// Whole warp, E <= 256, k <= 8: the same selection and weights as warp_topk_softmax<8>, with no
+// serial rounds. Every expert gets the unique key (orderable logit << 32) | ~index, so a larger
+// key is a larger logit, or an equal logit with a lower index. Each lane sorts its 8 keys; five
+// butterfly steps then merge the lane's sorted top 8 with its partner's (a bitonic merge keeps
+// the larger half), after which every lane holds the warp's top 8 in order.
+__device__ __forceinline__ bool warp_top8_softmax(const float* row, int E, int k, int* e_out, float* w_out) {
   const int lane = threadIdx.x & 31;
-  uint32_t key[SLOTS];
+  uint64_t v[8];
   bool bad = false;
-  uint32_t bk = 0u;
-  int bi = 0;
 #pragma unroll
-  for (int i = 0; i < SLOTS; ++i) {
+  for (int i = 0; i < 8; ++i) {
     const int e = lane + 32 * i;
-    key[i] = 0u;  // below every real key
+    v[i] = 0ull;  // below every real key
     if (e < E) {
-      const float v = __ldcg(row + e);
-      bad |= !isfinite(v);
-      key[i] = max(orderable_f32(v), 1u);
-    }
-    if (key[i] > bk) {  // strict: the lowest index wins among equal keys
-      bk = key[i];
-      bi = i;
+      const float x = __ldcg(row + e);
+      bad |= !isfinite(x);
+      v[i] = ((uint64_t)max(orderable_f32(x), 1u) << 32) | (uint32_t)~(uint32_t)e;
     }
   }
-  const unsigned long long lu = bk ? ((unsigned long long)bk << 32) | (uint32_t)~(uint32_t)(lane + 32 * bi) : 0ull;
-  int lr = 0;  // rank of this lane's maximum among the 32
-#pragma unroll 8
-  for (int j = 0; j < 32; ++j) lr += __shfl_sync(0xFFFFFFFFu, lu, j) > lu ? 1 : 0;
-  const int n_valid = __popc(__ballot_sync(0xFFFFFFFFu, bk != 0u));
-  unsigned long long tau = 0ull;
-  if (k <= n_valid) {
-    const unsigned src = __ballot_sync(0xFFFFFFFFu, lu != 0ull && lr == k - 1);
-    tau = __shfl_sync(0xFFFFFFFFu, lu, __ffs(src) - 1);
-  }
-  // gather the candidates (keys >= tau) one per lane, in (slot i, lane) order
-  unsigned long long cand = 0ull;
-  int n = 0;
+  sort8_desc(v);
 #pragma unroll
-  for (int i = 0; i < SLOTS; ++i) {
-    const int e = lane + 32 * i;
-    const unsigned long long u = ((unsigned long long)key[i] << 32) | (uint32_t)~(uint32_t)e;
-    const unsigned b = __ballot_sync(0xFFFFFFFFu, e < E && u >= tau);
-    const int c = lane - n;  // this lane's candidate slot, if it falls in this row
-    const int src = (c >= 0 && c < __popc(b)) ? __fns(b, 0, c + 1) : 0;
-    const unsigned long long got = __shfl_sync(0xFFFFFFFFu, u, src);
-    if (c >= 0 && c < __popc(b)) cand = got;
-    n += __popc(b);
+  for (int off = 1; off < 32; off <<= 1) {
+    uint64_t o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = __shfl_xor_sync(0xFFFFFFFFu, v[i], off);
+    // v descending, o descending: max(v[i], o[7-i]) is a bitonic sequence holding the top 8
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = v[i] > o[7 - i] ? v[i] : o[7 - i];
+    cx_desc(v[0], v[4]); cx_desc(v[1], v[5]); cx_desc(v[2], v[6]); cx_desc(v[3], v[7]);
+    cx_desc(v[0], v[2]); cx_desc(v[1], v[3]); cx_desc(v[4], v[6]); cx_desc(v[5], v[7]);
+    cx_desc(v[0], v[1]); cx_desc(v[2], v[3]); cx_desc(v[4], v[5]); cx_desc(v[6], v[7]);
   }
-  if (n > 32) {  // ties at the threshold: serial selection (lane j holds slot j)
-    const bool b2 = warp_topk_softmax<SLOTS>(row, E, k, e_out, w_out);
-    *rank_out = lane < k ? lane : -1;
-    return b2;
-  }
-  int rank = 0;
-  for (int j = 0; j < n; ++j) rank += __shfl_sync(0xFFFFFFFFu, cand, j) > cand ? 1 : 0;
-  const bool mine = lane < n && rank < k;
-  const float my_v = from_orderable_f32((uint32_t)(cand >> 32));
-  // Softmax restricted to the selected experts, relative to the largest logit (rank 0).
-  const float vmax = __shfl_sync(0xFFFFFFFFu, my_v, __ffs(__ballot_sync(0xFFFFFFFFu, mine && rank == 0)) - 1);
-  const float ex = mine ? expf(my_v - vmax) : 0.f;
+  uint64_t mine = v[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i)
+    if (lane == i) mine = v[i];
+  const int my_e = (int)~(uint32_t)mine;
+  const float my_v = from_orderable_f32((uint32_t)(mine >> 32));
+  // Softmax restricted to the selected experts; slot 0 holds the largest logit.
+  const float vmax = from_orderable_f32((uint32_t)(v[0] >> 32));
+  const float ex = lane < k ? expf(my_v - vmax) : 0.f;
   float sum = ex;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
-  *rank_out = mine ? rank : -1;
-  *e_out = min(max((int)~(uint32_t)cand, 0), E - 1);
+  *e_out = min(max(my_e, 0), E - 1);
   *w_out = ex / sum;
   return __any_sync(0xFFFFFFFFu, bad);
 }
 
-// Dispatch on the number of experts per lane.
-__device__ __forceinline__ bool warp_select_topk(const float* row, int E, int k, int* rank_out, int* e_out,
-                                                 float* w_out) {
-  if (E <= 256) return warp_select_topk<8>(row, E, k, rank_out, e_out, w_out);
-  return warp_select_topk<32>(row, E, k, rank_out, e_out, w_out);
+// Dispatch on the number of experts per lane and on k.
+__device__ __forceinline__ bool warp_topk_softmax(const float* row, int E, int k, int* e_out, float* w_out) {
+  if (E <= 256 && k <= 8) return warp_top8_softmax(row, E, k, e_out, w_out);
+  if (E <= 256) return warp_topk_softmax<8>(row, E, k, e_out, w_out);
+  return warp_topk_softmax<32>(row, E, k, e_out, w_out);
 }
 
 }  // namespace moe

@@ -90,6 +90,19 @@ def test_argument_errors_before_launch(m):
     assert lib.moe_selftest_wait_timeout(A + 64, 256, None) == 3
     assert lib.moe_workspace_init(None, 256, None) == 1
     assert lib.moe_read_device_status(None, None) == 1
+    abl = lambda x, T, arm, n, aux=None, na=0: lib.moe_prefill_ablation(  # noqa: E731
+        ctypes.byref(layer), x, T, A, arm, A, n, aux, na, None)
+    assert abl(A, 16, 0, ws_need) == 1                                    # unknown arm
+    assert abl(A, 16, 4, ws_need) == 1
+    assert abl(A, 16, 3, ws_need) == 1                                    # dense arm without its buffer
+    aux_need = lib.moe_prefill_ablation_aux_bytes(ctypes.byref(dims), 3)
+    assert aux_need == 257 * 3 * 512 * 2048 * 2                           # every expert's weights in fp16
+    assert lib.moe_prefill_ablation_aux_bytes(ctypes.byref(dims), 1) == 0
+    assert abl(A, 16, 3, ws_need, A + 64, aux_need) == 3                  # aux not 128-aligned
+    assert abl(A, 16, 3, ws_need, A, aux_need - 1) == 4
+    assert abl(None, 16, 1, ws_need) == 1                                 # null x
+    assert abl(A, 16, 2, ws_need - 1) == 4                                # workspace too small
+    assert abl(A, 70000, 1, ws_need) == 2
 
 
 def test_workspace_grows_with_tokens(m):

@@ -349,6 +349,30 @@ def test_prefill_full_replays_identical(m):
     torch.cuda.synchronize()
     assert m.read_device_status(ws) == 0
 
+# ------------------------------------------------------------------------------ prefill ablation arms
+@pytest.mark.parametrize("arm", [1, 2, 3], ids=["host_routing", "tile32", "dense"])
+@pytest.mark.parametrize("shape,T,bias", [(TINY, 300, None), (FULL, 512, None), (FULL, 2048, "zipf")],
+                         ids=["tiny300", "full512", "skew2048"])
+def test_prefill_ablation_arms(m, arm, shape, T, bias):
+    """Both ablation arms compute the same layer: against the oracle (sampled rows at full size)
+    and against moe_prefill up to the fp32 summation order of the combine and of K sums over
+    tiles of another width."""
+    npl, layer = _np_layer(shape, 0, bias), dev_layer(m, shape, 0, bias)
+    x = make_tokens(T, shape.d, seed=400 + T)
+    xd = to_dev(x)
+    ws = m.workspace(layer.dims, T)
+    n_aux = m.ablation_aux_bytes(layer.dims, arm)
+    aux = torch.empty(n_aux, dtype=torch.uint8, device="cuda") if n_aux else None
+    y = m.prefill_ablation(layer, xd, ws, arm, aux=aux)
+    torch.cuda.synchronize()
+    assert m.read_device_status(ws) == 0
+    y1 = m.prefill(layer, xd, ws)
+    torch.cuda.synchronize()
+    assert _same_up_to_summation_order(y, y1) == 0
+    rows = np.arange(T) if T <= 300 else np.unique(np.concatenate([[0, T - 1], np.random.default_rng(T).choice(T, 30)]))
+    C.check_y(y[torch.as_tensor(rows, device=y.device)], _oracle_rows(m, layer, npl, shape, x[rows]))
+
+
 # ------------------------------------------------------------------------------ bounded-chunk prefill
 def _oracle_rows(m, layer, npl, shape, x):
     """Oracle y for the token rows x; where the oracle's k-th and (k+1)-th logits lie within the
@@ -459,6 +483,54 @@ def test_decode(m, shape, bias, seed):
         ref = O.moe_forward(x, npl, tile_rows=m.tile_rows())
         C.check_y(y, ref["y"])
 
+
+
+@pytest.mark.parametrize("shape,T,force", [(FULL, 2, False), (FULL, 3, False), (FULL, 5, False), (FULL, 8, False),
+                                           (FULL, 8, True), (FULL, 1, False), (TINY, 4, False), (WIDE, 6, False)],
+                         ids=["full2", "full3", "full5", "full8", "full8_shared_experts", "full1", "tiny4",
+                              "E1024k16_6"])
+def test_decode_batch(m, shape, T, force):
+    """moe_decode_batch on T tokens: the routing of every token bit-exact against the oracle's
+    selection on the GPU's logits, every token's y within the output tolerance of the oracle and
+    equal to its own batch-1 moe_decode up to fp32 summation order; `force` sends every token to
+    experts 0..k-1 (one distinct expert set shared by all tokens)."""
+    npl = dict(_np_layer(shape, 5, None))
+    if force:
+        rb = np.zeros(shape.n_experts, dtype=np.float32)
+        rb[: shape.top_k] = 100.0
+        npl["router_bias"] = rb
+        layer = m.upload_layer(npl)
+    else:
+        layer = dev_layer(m, shape, 5, None)
+    x = make_tokens(T, shape.d, seed=600 + T)
+    ws = m.workspace(layer.dims, T)
+    out = m.route_out_tensors(layer.dims, T, "cuda", want=("logits", "topk_idx", "topk_w"))
+    y = m.decode_batch(layer, to_dev(x), ws, out=out)
+    torch.cuda.synchronize()
+    assert m.read_device_status(ws) == 0
+    g = C.to_np(out)
+    idx_ref, w_ref = O.select_experts(g["logits"], shape.top_k)
+    np.testing.assert_array_equal(g["topk_idx"], idx_ref)
+    assert np.max(np.abs(g["topk_w"] - w_ref)) <= C.W_TOL
+    if force:
+        assert np.all(np.sort(g["topk_idx"], axis=1) == np.arange(shape.top_k))
+    ref_logits = O.router_logits(x, npl["router_w"], npl["router_bias"])
+    tol = C.logit_tolerance(x, npl["router_w"]) + 1e-6 * np.abs(ref_logits)
+    assert np.all(np.abs(g["logits"] - ref_logits) <= tol)
+    diff, ok = C.selection_with_near_ties(g["logits"], ref_logits, tol, shape.top_k)
+    assert ok and not diff
+    C.check_y(y, O.moe_forward(x, npl, tile_rows=m.tile_rows())["y"])
+    ws1 = m.workspace(layer.dims, 1)
+    for t in range(T):
+        y1 = m.decode(layer, to_dev(x[t:t + 1]), ws1)
+        assert _same_up_to_summation_order(y[t:t + 1], y1) == 0, f"token {t}"
+
+
+def test_decode_batch_rejects_shapes(m):
+    layer = dev_layer(m, FULL)
+    ws = m.workspace(layer.dims, 16)
+    with pytest.raises(m.MoeError):
+        m.decode_batch(layer, to_dev(make_tokens(9, FULL.d, seed=1)), ws)   # more than 8 tokens
 
 
 def test_decode_out_of_range_sets_status(m):
