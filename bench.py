@@ -394,8 +394,8 @@ class Workload:
     def launches_per_step(self) -> int:
         a = self.args
         # prefill: router GEMM, top-k, histogram, scatter, row placement, gate/up, down, cast;
-        # decode: router GEMV, expert kernel (with the combine)
-        return (8 * a.layers if a.prefill_tokens else 0) + 2 * a.layers * a.decode_steps
+        # decode: router GEMV, expert kernel (top-k, gate/up, SwiGLU), down kernel (with the combine)
+        return (8 * a.layers if a.prefill_tokens else 0) + 3 * a.layers * a.decode_steps
 
 
 def capture(W: Workload, ev_pre=None, ev_dec=None, graphs: bool = True):

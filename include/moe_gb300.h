@@ -286,14 +286,14 @@ MOE_API int moe_decode_batch(const moe_layer* layer, const uint16_t* x, int32_t 
  * every device allocation and only lends it input and output buffers, and code that must not
  * allocate after start-up because cudaMalloc can synchronise the device and can fail under
  * memory pressure. It computes exactly what moe_decode computes, with the same kernels, but its
- * scratch (logits, selected experts and weights, per-block partial outputs, counters) lives in a
- * fixed 2 MiB device array inside the library instead of a caller workspace.
+ * scratch (logits, selected experts and weights, the expert kernel's per-block SwiGLU records,
+ * status) lives in a fixed 512 KiB device array inside the library instead of a caller workspace.
  *   - x, y: bf16 [1, d] device buffers owned by the caller, as for moe_decode.
  *   - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine.
- *   - The 2 MiB array is held on every device that loads the library until the process exits.
- *     Shapes whose scratch (256 + 4E + 8k + 4d(k+1)I/32 bytes, each part rounded up to 256)
- *     does not fit return MOE_ERR_UNSUPPORTED_SHAPE before anything is launched (d=2048,
- *     E=256, k=8, I=512 needs 1.13 MiB).
+ *   - The 512 KiB array is held on every device that loads the library until the process
+ *     exits. A shape needs 256 + 4E + 8k + 144(k+1)I/32 bytes of it (each part rounded up to
+ *     256; d=2048, E=256, k=8, I=512 needs 22 KiB); shapes whose scratch does not fit return
+ *     MOE_ERR_UNSUPPORTED_SHAPE before anything is launched.
  *   - The first call on a device looks up the array's device address (once per device, with
  *     that device current); make that first call before any stream capture.
  *   - Every call uses the same array, which keeps the last call's contents; each call writes
@@ -316,8 +316,8 @@ MOE_API int moe_decode_noalloc(const moe_layer* layer, const uint16_t* x, uint16
  *            scatter), [2] before the gate/up GEMM, [3] before the down GEMM, [4] before the
  *            output cast, [5] after it (6 entries).
  *   decode:  events[0] before the router GEMV, [1] before the expert kernel (top-k, gate/up
- *            GEMV + SwiGLU, each block's down partial), [2] before the combine of the partial
- *            outputs, [3] after it (4 entries). Events between the kernels also stop them from
+ *            GEMV + SwiGLU), [2] before the down kernel (down GEMVs and the weighted combine),
+ *            [3] after it (4 entries). Events between the kernels also stop them from
  *            overlapping through programmatic dependent launch.
  */
 MOE_API int moe_prefill_timed(const moe_layer* layer, const uint16_t* x, int32_t T, uint16_t* y,
@@ -332,10 +332,11 @@ MOE_API int moe_decode_timed(const moe_layer* layer, const uint16_t* x, uint16_t
  * pattern, and the effect of deleting its arithmetic). Arguments as for moe_decode (no routing
  * outputs); the same checks and error codes, plus MOE_ERR_INVALID_ARG for an unknown mode.
  *   MOE_DECODE_DIAG_NO_MATH    the full kernel chain with the GEMV arithmetic deleted: router,
- *                              top-k, the same weight copies and waits, zero partial rows, the
- *                              reduce; y becomes zeros.
- *   MOE_DECODE_DIAG_READ_ONLY  the expert kernel's weight copies alone (experts 0..k-1 and the
- *                              shared expert), each block waiting for its own; no router, no
+ *                              top-k, the same weight copies, prefetches, loads and waits; y
+ *                              becomes zeros.
+ *   MOE_DECODE_DIAG_READ_ONLY  one kernel that copies every expert weight byte the layer reads
+ *                              (gate/up and down of experts 0..k-1 and of the shared expert) into
+ *                              shared memory, each block waiting for its own; no router, no
  *                              chaining; x and y are not accessed (they must still be valid,
  *                              16-byte aligned pointers).
  */

@@ -118,6 +118,26 @@ bool make_down_weight_maps(GemmMaps* g, const uint8_t* packed, const PackedLayou
          encode(&g->a2, CU_TENSOR_MAP_DATA_TYPE_UINT64, 4, sb, sdims, sstr, sbox, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
+}  // namespace
+
+bool moe::make_decode_down_maps(DecodeMaps* m, const uint8_t* packed, const moe_dims& d) {
+  const PackedLayout P = packed_layout(d);
+  const uint64_t DM = d.d / kBlockRows, KBD = d.inter / kGroup, E1 = (uint64_t)d.n_experts + 1;
+  const uint32_t pieces = KBD * 2 < 16 ? (uint32_t)KBD * 2 : 16u;  // I is a multiple of 128: >= 4
+  const uint8_t* codes = packed + P.gu_bytes;
+  const uint8_t* sb = codes + dn_sb_offset(0, 0, (int)DM, (int)KBD);
+  const cuuint64_t cdims[4] = {kHalfBytes / 8, DM, 2 * KBD, E1};
+  const cuuint64_t cstr[3] = {kHalfBytes, DM * kHalfBytes, P.expert_stride};
+  const cuuint32_t cbox[4] = {16 * 16 / 8, 1, pieces, 1};
+  const cuuint64_t sdims[4] = {kSBBytes / 8, DM, KBD, E1};
+  const cuuint64_t sstr[3] = {kSBBytes, DM * kSBBytes, P.expert_stride};
+  const cuuint32_t sbox[4] = {16 * 4 / 8, 1, pieces / 2, 1};
+  return encode(&m->codes, CU_TENSOR_MAP_DATA_TYPE_UINT64, 4, codes, cdims, cstr, cbox, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+         encode(&m->sb, CU_TENSOR_MAP_DATA_TYPE_UINT64, 4, sb, sdims, sstr, sbox, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+namespace {
+
 int check_ws(void* ws, size_t ws_bytes, const moe_dims& d, int T) {
   if (!ws) return MOE_ERR_INVALID_ARG;
   if (!aligned(ws, 128)) return MOE_ERR_MISALIGNED;
@@ -291,7 +311,8 @@ int decode_common(const moe_layer* layer, const uint16_t* x, uint16_t* y, moe_ro
   p.logits = w.at<float>(w.L.logits);
   p.topk_idx = w.at<int32_t>(w.L.topk_idx);
   p.topk_w = w.at<float>(w.L.topk_w);
-  p.partials = w.at<float>(w.L.dec_part);
+  p.partials = nullptr;
+  p.hrec = w.at<uint8_t>(w.L.dec_part);
   p.y = y;
   p.hdr = w.at<WsHeader>(w.L.header);
   p.d = d.d;
@@ -299,7 +320,9 @@ int decode_common(const moe_layer* layer, const uint16_t* x, uint16_t* y, moe_ro
   p.k = d.top_k;
   p.inter = d.inter;
   p.T = 1;
-  if (launch_decode(p, stream, events, mode) != cudaSuccess) return MOE_ERR_CUDA;
+  DecodeMaps maps;
+  if (!make_decode_down_maps(&maps, p.packed, d)) return MOE_ERR_CUDA;
+  if (launch_decode(p, maps, stream, events, mode) != cudaSuccess) return MOE_ERR_CUDA;
   if (!out) return MOE_OK;
   st = copy_out(out->logits, p.logits, (size_t)d.n_experts * 4, stream);
   st |= copy_out(out->topk_idx, p.topk_idx, (size_t)d.top_k * 4, stream);
@@ -523,6 +546,7 @@ int moe_decode_batch(const moe_layer* layer, const uint16_t* x, int32_t T, uint1
   p.topk_idx = w.at<int32_t>(w.L.topk_idx);
   p.topk_w = w.at<float>(w.L.topk_w);   // followed by room for the distinct-expert list (T*k + 1 ints)
   p.partials = w.at<float>(w.L.dec_part);
+  p.hrec = nullptr;
   p.y = y;
   p.hdr = w.at<WsHeader>(w.L.header);
   p.d = d.d;

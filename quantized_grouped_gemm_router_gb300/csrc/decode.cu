@@ -16,14 +16,15 @@
 //                         slice is loaded before the wait
 //   decode_expert_kernel  one CTA per (selected or shared expert, 32 intermediate rows): routed
 //                         CTAs select the top k from the logits themselves (all 512 threads: a
-//                         threshold from the warp maxima, then exact ranks of the few experts
-//                         above it; ties to the lower index); all of a CTA's gate/up rows and its
-//                         32-column slice of the down projection are bulk-copied to shared memory
-//                         as soon as the expert is known (the shared expert's CTAs before routing
-//                         is known); gate/up + SwiGLU, scaled by the routing weight, then this
-//                         slice's contribution to every output row (split-K over the intermediate
-//                         dimension), written as the CTA's partial row
-//   decode_reduce_kernel  y of every token = sum of its partial rows in a fixed order -> bf16
+//                         threshold from the maxima of 16-thread groups, then exact ranks of the
+//                         few experts above it; ties to the lower index); each CTA bulk-copies its
+//                         gate/up rows to shared memory and prefetches its 32-column slice of the
+//                         down projection into L2 as soon as the expert is known (the shared
+//                         expert's CTAs before routing is known); gate/up GEMV + SwiGLU, scaled by
+//                         the routing weight, written as the CTA's h record
+//   decode_down_kernel    one CTA per 16 output rows: every (expert slot, 32-column part) piece of
+//                         W_down against its h record, the weights read from L2, summed in a
+//                         fixed order -> bf16 y (the combine needs no partial rows)
 // The GEMV inner products run on the tensor cores (mma.sync m16n8k16, fp16 in, fp32
 // accumulate): the packed nibble pairs of a row map directly onto the MMA fragment layout, so
 // the weights cost about one ALU operation per two values instead of an fp32 FMA each, which on
@@ -58,8 +59,16 @@ constexpr int kRThreads = 256;         // router: two experts per CTA, 128 threa
 constexpr int kRMaxChunks = kDecodeMaxD / 8 / 128;
 constexpr int kXThreads = 512;         // expert kernel: 16 warps to hide MMA and smem latency
 constexpr int kXWarps = kXThreads / 32;
-constexpr int kYThreads = 512;         // reduce: 16 output rows x 32 groups of partial rows
+constexpr int kYThreads = 512;         // reduce (small batch): 16 output rows x 32 groups of partial rows
 constexpr int kYRows = 16;
+constexpr int kDThreads = 512;         // down kernel: 16 warps, one 32-column part each
+constexpr int kDWarps = kDThreads / 32;
+constexpr int kDRows = 16;             // output rows per down-kernel CTA (the MMA's M)
+constexpr int kDPieceBytes = kDRows * 16;             // codes of one (part, 16 rows) piece
+constexpr int kDSBBytes = kDRows * 4;                 // scale/bias of 16 rows for one K block
+constexpr int kDCodeSlot = kDWarps * kDPieceBytes;    // one slot's codes for 16 parts
+constexpr int kDSBSlot = kDWarps / 2 * kDSBBytes;     // one slot's scale/bias for 8 K blocks
+constexpr int kDSlotBytes = kDCodeSlot + kDSBSlot + kDWarps * kHRecBytes;
 constexpr int kXMaxGUChunks = 4;       // gate/up run split into up to 4 copies (own barriers, own lanes)
 constexpr int kGUStage = 2 * (2 * kDecPartRows * 16 + kDecPartRows * 4);  // gate + up slice of one kb
 constexpr int kDnStage = kHalfBytes + kBlockRows * 4;                     // down half-block + sb
@@ -69,6 +78,18 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                : "l"(p));
+  return r;
+}
+// 16-byte asynchronous copy global -> shared through L2 only (data an earlier kernel of the chain
+// wrote), completed by cp_async_wait_all.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// Loads of data that an earlier kernel of the chain wrote: through L2 only.
+__device__ __forceinline__ int ld_cg_s32(const int* p) {
+  int r;
+  asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(r) : "l"(p));
   return r;
 }
 __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
@@ -81,6 +102,14 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%11,%12,%13};"
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(d[0]), "f"(d[1]), "f"(d[2]), "f"(d[3]));
+}
+
+// The same product accumulated into d, without volatile: the compiler may schedule it freely.
+__device__ __forceinline__ void mma16816_acc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 __global__ void __launch_bounds__(kRThreads) decode_router_kernel(const DecodeParams p) {
@@ -144,12 +173,11 @@ __host__ __device__ inline XSmem x_smem(int d) {
   const int KB = d / kGroup, DM = d / kBlockRows;
   XSmem L;
   L.gu = 0;                                           // KB entries of gate/up rows
-  L.dn = L.gu + KB * kGUStage;                        // DM code halves, then DM scale runs
+  L.dn = L.gu + KB * kGUStage;                        // read-only probe: DM code halves, DM scale runs
   L.x16 = up16(L.dn + DM * kDnStage);                 // x as fp16 pairs
   L.xsum = up16(L.x16 + d * 2);                       // per-64-group sums of x, two column classes
   L.red = up16(L.xsum + KB * 8);                      // [warp][gate/up][32 rows] partial dots
-  L.h = up16(L.red + kXWarps * 2 * kDecPartRows * 4); // h leading part, remainder (fp16), two sums
-  L.topk = up16(L.h + 2 * kDecPartRows * 2 + 16);
+  L.topk = up16(L.red + kXWarps * 2 * kDecPartRows * 4);
   L.misc = up16(L.topk + (int)sizeof(TopkSmem));      // abort flag
   L.bars = up16(L.misc + 16);
   L.total = L.bars + (kXMaxGUChunks + 1) * 8;         // gate/up pieces, down
@@ -301,37 +329,27 @@ __global__ void __launch_bounds__(kXThreads, 1) decode_expert_kernel(const Decod
   }
   __syncthreads();
 
-  // Lanes 0..NGU of warp 0 issue this CTA's copies, one piece each (a thread's TMA copies to
-  // different barriers are issued one after another, ~0.25 us apart): the contiguous run of its 32
-  // gate and up rows for every column block (KB * 2304 bytes, in NGU pieces), then its 32-column
-  // half of every down row block (DM * 2048 bytes of codes) and the matching scale/bias rows.
+  // Lanes of warp 0 issue this CTA's copies, one each (a thread's TMA copies to different barriers
+  // go out one after another, ~0.25 us apart): lanes 0..NGU-1 the contiguous run of its 32 gate
+  // and up rows for every column block (KB * 2304 bytes, in NGU pieces). The read-only probe also
+  // copies what the down kernel reads for this CTA's part, on the down barrier: lane NGU its
+  // 32-column half of every down row block (DM * 2048 bytes of codes), lane NGU + 1 the matching
+  // scale/bias rows.
   auto issue = [&](int expert) {
-    // lanes 0..NGU-1: the gate/up pieces; lane NGU: the down codes; lane NGU+1: the down scale/bias
-    // rows (both on the down barrier, whose expected bytes lane NGU announces). Every copy goes out
-    // in the same instruction.
     const uint8_t* eb = p.packed + (size_t)expert * p.expert_stride;
-    if (lane <= NGU + 1) {
-      uint32_t dst, bytes, bar;
-      const uint8_t* src;
-      if (lane < NGU) {
-        const int kb0 = lane * KB / NGU, kb1 = (lane + 1) * KB / NGU;
-        bytes = (uint32_t)(kb1 - kb0) * kGUStage;
-        dst = smem_u32(xs + L.gu + kb0 * kGUStage);
-        src = eb + gu_offset(m, part % (kBlockRows / kDecPartRows), 0, KB) + (size_t)kb0 * kGUStage;
-        bar = bars + 8u * lane;
-      } else if (lane == NGU) {
-        bytes = DM * kHalfBytes;
-        dst = smem_u32(xs + L.dn);
-        src = eb + p.gu_bytes + dn_code_offset(kbd, hd, 0, DM);
-        bar = bars + 8u * NGU;
-      } else {
-        bytes = DM * kSBBytes;
-        dst = smem_u32(xs + L.dn + DM * kHalfBytes);
-        src = eb + p.gu_bytes + dn_sb_offset(kbd, 0, DM, KBI);
-        bar = bars + 8u * NGU;
-      }
-      if (lane <= NGU) mbar_arrive_expect_tx(bar, lane < NGU ? bytes : (uint32_t)(DM * (kHalfBytes + kSBBytes)));
-      tma_bulk_g2s(dst, src, bytes, bar);
+    if (lane < NGU) {
+      const int kb0 = lane * KB / NGU, kb1 = (lane + 1) * KB / NGU;
+      const uint32_t bytes = (uint32_t)(kb1 - kb0) * kGUStage;
+      mbar_arrive_expect_tx(bars + 8u * lane, bytes);
+      tma_bulk_g2s(smem_u32(xs + L.gu + kb0 * kGUStage),
+                   eb + gu_offset(m, part % (kBlockRows / kDecPartRows), 0, KB) + (size_t)kb0 * kGUStage, bytes,
+                   bars + 8u * lane);
+    } else if (kMode == 2 && lane <= NGU + 1) {
+      const bool codes = lane == NGU;
+      const uint8_t* src = eb + p.gu_bytes + (codes ? dn_code_offset(kbd, hd, 0, DM) : dn_sb_offset(kbd, 0, DM, KBI));
+      if (codes) mbar_arrive_expect_tx(bars + 8u * NGU, (uint32_t)(DM * (kHalfBytes + kSBBytes)));
+      tma_bulk_g2s(smem_u32(xs + L.dn + (codes ? 0 : DM * kHalfBytes)), src, codes ? DM * kHalfBytes : DM * kSBBytes,
+                   bars + 8u * NGU);
     }
   };
 
@@ -347,8 +365,10 @@ __global__ void __launch_bounds__(kXThreads, 1) decode_expert_kernel(const Decod
     return;
   }
   if (shared && warp == 0) issue(p.E);  // static weights: before waiting on the router
-  pdl_launch_dependents();
   pdl_wait();
+  // The down kernel may start once every CTA of this kernel is past its wait: the router's logits,
+  // which it reads before its own wait, are complete by then.
+  pdl_launch_dependents();
 
   // x (one 8-value chunk per thread of warps 2..15) is loaded before the selection so both loads
   // overlap.
@@ -456,7 +476,6 @@ __global__ void __launch_bounds__(kXThreads, 1) decode_expert_kernel(const Decod
       }
     }
   }
-  gu_ok = __all_sync(0xFFFFFFFFu, gu_ok);
   float* red = reinterpret_cast<float*>(xs + L.red);
   if (tig == 0) {
 #pragma unroll
@@ -468,10 +487,10 @@ __global__ void __launch_bounds__(kXThreads, 1) decode_expert_kernel(const Decod
       }
   }
   __syncthreads();
-  __half* hh = reinterpret_cast<__half*>(xs + L.h);
-  __half* hl = hh + kDecPartRows;
-  float* hsum = reinterpret_cast<float*>(xs + L.h + 2 * kDecPartRows * 2);
-  if (warp == 0) {  // SwiGLU of this CTA's 32 rows, scaled by the routing weight
+  if (warp == 0 && !*s_abort) {
+    // SwiGLU of this CTA's 32 rows, scaled by the routing weight, into its h record: the fp16
+    // leading parts, the fp16 remainders, and the sums of h over the base-1024 columns (0,1,4,5 of
+    // every 8) and the base-64 columns of the down projection's codes
     float gs = 0.f, us = 0.f;
     for (int w = 0; w < kXWarps; ++w) {
       gs += red[(w * 2 + 0) * kDecPartRows + lane];
@@ -479,9 +498,9 @@ __global__ void __launch_bounds__(kXThreads, 1) decode_expert_kernel(const Decod
     }
     const float h = gs / (1.f + expf(-gs)) * us * wslot;
     const __half hi = __float2half_rn(h);
-    hh[lane] = hi;
-    hl[lane] = __float2half_rn(h - __half2float(hi));
-    // sums of h over the base-1024 columns (0,1,4,5 of every 8) and the base-64 columns
+    uint8_t* rec = p.hrec + (size_t)blockIdx.x * kHRecBytes;  // blockIdx.x = slot * parts + part
+    reinterpret_cast<__half*>(rec)[lane] = hi;
+    reinterpret_cast<__half*>(rec + 2 * kDecPartRows)[lane] = __float2half_rn(h - __half2float(hi));
     const bool base1024 = (lane & 2) == 0;
     float ta = base1024 ? h : 0.f, tb = base1024 ? 0.f : h;
 #pragma unroll
@@ -489,86 +508,151 @@ __global__ void __launch_bounds__(kXThreads, 1) decode_expert_kernel(const Decod
       ta += __shfl_xor_sync(0xFFFFFFFFu, ta, o);
       tb += __shfl_xor_sync(0xFFFFFFFFu, tb, o);
     }
-    if (lane == 0) {
-      hsum[0] = ta;
-      hsum[1] = tb;
-    }
+    if (lane == 0) *reinterpret_cast<float2*>(rec + 4 * kDecPartRows) = make_float2(ta, tb);
     if (__any_sync(0xFFFFFFFFu, !(fabsf(h) <= 65504.f)) && lane == 0) set_device_status(p.hdr, MOE_ERR_OUT_OF_RANGE);
   }
-  __syncthreads();
-
-  // ---- down: this CTA's 32 columns of W_down against every output row (split-K partial)
-  const bool down_ok = mbar_wait(bars + 8u * NGU, 0, s_abort);
-  const bool ok = !*s_abort && down_ok && gu_ok;  // after an abort nothing is computed or stored
-  const uint32_t* hh2 = reinterpret_cast<const uint32_t*>(hh);
-  const uint32_t* hl2 = reinterpret_cast<const uint32_t*>(hl);
-  // B: column 0 the leading part of h, column 1 its remainder, for this lane's code word (columns
-  // 8 tig..8 tig+7 of the CTA's 32): 4 consecutive pairs
-  uint4 hb = make_uint4(0u, 0u, 0u, 0u);
-  if (g < 2) hb = *reinterpret_cast<const uint4*>((g == 0 ? hh2 : hl2) + 4 * tig);
-  const float ha = hsum[0], hb64 = hsum[1];
-  // Each warp owns DM * 8 / 16 row tiles of 16; all of its code words are read first so the
-  // shared-memory latency overlaps, then the MMAs run back to back. Row results go straight to
-  // this CTA's partial row in global memory (16 consecutive floats per tile).
-  float* gout = p.partials + (size_t)blockIdx.x * p.d;
-  constexpr int kMaxTilesPerWarp = kDecodeMaxD / 16 / kXWarps;  // 12 for d = 3072
-  const int ntw = DM * 8 / kXWarps;                              // tiles per warp (exact: d % 128 == 0)
-  uint32_t c0[kMaxTilesPerWarp], c1[kMaxTilesPerWarp];
-#pragma unroll
-  for (int i = 0; i < kMaxTilesPerWarp; ++i) {
-    if (ok && i < ntw) {  // lane (g, tig): word tig of rows R0 and R0 + 8 of the tile
-      const int tile = warp + i * kXWarps, mm = tile >> 3, R0 = (tile & 7) * 16 + g;
-      const uint8_t* ds = xs + L.dn + mm * kHalfBytes;
-      c0[i] = *reinterpret_cast<const uint32_t*>(ds + R0 * 16 + 4 * tig);
-      c1[i] = *reinterpret_cast<const uint32_t*>(ds + (R0 + 8) * 16 + 4 * tig);
-    }
-  }
-  // all of this warp's MMAs first (independent, so they pipeline), then the epilogue of the rows
-  // (lanes with tig == 0 hold columns 0 and 1: the leading part and the remainder of h)
-  float dd[kMaxTilesPerWarp][4];
-#pragma unroll
-  for (int i = 0; i < kMaxTilesPerWarp; ++i) {
-    dd[i][0] = dd[i][1] = dd[i][2] = dd[i][3] = 0.f;
-    if constexpr (kMode == 0) {
-      if (ok && i < ntw) {
-        uint32_t q0[4], q1[4];
-        q_pairs(c0[i], q0);
-        q_pairs(c1[i], q1);
-        mma16816(dd[i], q0[0], q1[0], q0[1], q1[1], hb.x, hb.y);
-        mma16816(dd[i], q0[2], q1[2], q0[3], q1[3], hb.z, hb.w);
-      }
-    }
-  }
-  // the row results go to a shared-memory copy of the partial row (the gate/up stage area, free
-  // once every block of it has been consumed), then out as coalesced 16-byte stores
-  float* prow = reinterpret_cast<float*>(xs + L.gu);
-  if (tig == 0) {
-#pragma unroll
-    for (int i = 0; i < kMaxTilesPerWarp; ++i) {
-      if (ok && i < ntw) {
-        const int tile = warp + i * kXWarps, mm = tile >> 3, R0 = (tile & 7) * 16 + g, R1 = R0 + 8;
-        const uint8_t* dsb = xs + L.dn + DM * kHalfBytes + mm * kSBBytes;
-        const uint32_t sb0 = *reinterpret_cast<const uint32_t*>(dsb + R0 * 4);
-        const uint32_t sb1 = *reinterpret_cast<const uint32_t*>(dsb + R1 * 4);
-        // d = sum (base + q) h over the 32 columns: s*q + b weights give
-        // s*d + (b - 1024 s) * (sum of h over base-1024 columns) + (b - 64 s) * (the others);
-        // with the arithmetic deleted (kMode 1) the partial row is zeros
-        const float s0 = kMode == 0 ? bf16lo(sb0) : 0.f, s1 = kMode == 0 ? bf16lo(sb1) : 0.f;
-        const float b0 = kMode == 0 ? bf16hi(sb0) : 0.f, b1 = kMode == 0 ? bf16hi(sb1) : 0.f;
-        prow[mm * kBlockRows + R0] = s0 * (dd[i][0] + dd[i][1]) + (b0 - 1024.f * s0) * ha + (b0 - 64.f * s0) * hb64;
-        prow[mm * kBlockRows + R1] = s1 * (dd[i][2] + dd[i][3]) + (b1 - 1024.f * s1) * ha + (b1 - 64.f * s1) * hb64;
-      }
-    }
-  }
-  __syncthreads();
-  if (ok)
-    for (int i = tid; i < p.d / 4; i += kXThreads)
-      reinterpret_cast<float4*>(gout)[i] = reinterpret_cast<const float4*>(prow)[i];
-  if (!down_ok && tid == 0) *s_abort = 1;
-  __syncthreads();
   if (tid == 0 && *s_abort) {  // outputs are undefined; let this CTA's copies land before exiting
-    for (int i = 0; i <= NGU; ++i) mbar_drain(bars + 8u * i, 0);
+    for (int i = 0; i < NGU; ++i) mbar_drain(bars + 8u * i, 0);
     set_device_status(p.hdr, MOE_ERR_DEVICE_TIMEOUT);
+  }
+}
+
+// y[r0 .. r0 + 16) for r0 = 16 blockIdx.x: the sum over every (expert slot j <= k, 32-column part
+// pp) of W_down_e[rows, 32 pp .. 32 pp + 32) . h_{j,pp} (slot k: the shared expert; the routing
+// weights are already in h). The kernel starts once every expert-kernel CTA is past its own wait,
+// so the router's logits are complete: it selects the experts itself (the same deterministic
+// selection as the expert kernel) and, before waiting for the expert kernel, warp 0 issues two
+// tensor copies per slot for the first 16 parts (the CTA's 16 code rows of each part and their
+// scale/bias rows), which stream from HBM while the expert kernel runs. After the wait every
+// thread copies the parts' h records to shared memory. Each unit (slot, 64-column group: two
+// parts sharing their scale/bias rows) is four MMAs and one epilogue; every warp takes its units
+// in a fixed order, and the 16 warp sums are then added in warp order, so the result does not
+// depend on timing. kMode 1 (arithmetic deleted) makes the same copies and writes y = 0.
+template <int kMode>
+__global__ void __launch_bounds__(kDThreads, 2) decode_down_kernel(const DecodeParams p,
+                                                                   const __grid_constant__ DecodeMaps maps) {
+  static_assert(kDThreads == kXThreads, "the block-wide top-k runs on 512 threads");
+  extern __shared__ uint8_t ds_raw[];
+  uint8_t* ds = ds_raw + ((128u - (smem_u32(ds_raw) & 127u)) & 127u);  // tensor copies land 128-aligned
+  __shared__ float s_red[kDWarps][kDRows];
+  __shared__ TopkSmem s_tk;
+  __shared__ __align__(8) uint64_t s_bar;
+  __shared__ int s_abort;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, tig = lane & 3;
+  const int r0 = blockIdx.x * kDRows, mm = r0 / kBlockRows, ro = r0 % kBlockRows;
+  const int parts = p.inter / kDecPartRows, k1 = p.k + 1;
+  uint8_t* s_codes = ds;                               // [slot][16 parts][16 rows][16 B]
+  uint8_t* s_sb = ds + k1 * kDCodeSlot;                // [slot][8 K blocks][16 rows][4 B]
+  uint8_t* s_h = s_sb + k1 * kDSBSlot;                 // [slot][16 parts] h records
+  const uint32_t bar = smem_u32(&s_bar);
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    s_abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane < 2) prefetch_tmap(lane ? &maps.sb : &maps.codes);
+  __syncthreads();
+  block_select_topk(p.logits, p.E, p.k, &s_tk);  // non-finite logits are reported by the expert kernel
+  // lane j < k of warp 0: slot j's expert; lane k: the shared expert
+  const int e = lane < p.k ? min(max((int)~(uint32_t)s_tk.sel[lane], 0), p.E - 1) : p.E;
+  const int pieces = min(parts, kDWarps);
+  auto issue = [&](int pc) {  // warp 0: every slot's codes and scale/bias rows for parts pc .. pc + 15
+    if (warp == 0) {
+      if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(k1 * (pieces * kDPieceBytes + pieces / 2 * kDSBBytes)));
+      __syncwarp();
+      if (lane < k1) {
+        tma_load_4d(smem_u32(s_codes + lane * kDCodeSlot), &maps.codes, 2 * ro, mm, pc, e, bar);
+        tma_load_4d(smem_u32(s_sb + lane * kDSBSlot), &maps.sb, ro / 2, mm, pc / 2, e, bar);
+      }
+    }
+  };
+  issue(0);
+  pdl_launch_dependents();
+  pdl_wait();
+  float acc0 = 0.f, acc1 = 0.f;  // rows g and g + 8 (meaningful on tig == 0)
+  uint32_t phase = 0;
+  for (int pc = 0; pc < parts; pc += kDWarps, phase ^= 1u) {
+    if (pc > 0) issue(pc);
+    // the h records of parts pc .. pc + 15, every slot (k1 * 16 records of 9 16-byte words)
+    const int n16 = k1 * kDWarps * (kHRecBytes / 16);
+    for (int q = tid; q < n16; q += kDThreads) {
+      const int r = q / (kHRecBytes / 16), pq = pc + r % kDWarps;
+      if (pq < parts)
+        cp_async_16(smem_u32(s_h + (size_t)q * 16),
+                    p.hrec + (size_t)((r / kDWarps) * parts + pq) * kHRecBytes + (q % (kHRecBytes / 16)) * 16);
+    }
+    cp_async_wait_all();
+    mbar_wait(bar, phase, &s_abort);
+    __syncthreads();
+    if (s_abort) break;  // uniform: read after the barrier
+    if (kMode == 0) {
+      // units (slot j, column group kb) of this chunk: both 32-column halves of the group share its
+      // scale/bias rows, so one unit is four chained MMAs (K = 64) and one epilogue. Warp w takes
+      // column group w % npk and the slots w / npk, w / npk + 16 / npk, ... in order (warps past
+      // npk * (16 / npk) idle). The loop is bound by shared-memory and issue throughput, not by
+      // latency, so it is not unrolled.
+      const int npk = min(parts - pc, kDWarps) / 2, jstep = kDWarps / npk, kb = warp % npk;
+      const uint8_t* cw = s_codes + 2 * kb * kDPieceBytes + g * 16 + 4 * tig;
+      const uint8_t* sw = s_sb + kb * kDSBBytes + g * 4;
+      const uint8_t* rw = s_h + 2 * kb * kHRecBytes;
+      const int ho = 2 * kDecPartRows * (g & 1) + 16 * tig;
+#pragma unroll 1
+      for (int j = warp < npk * jstep ? warp / npk : k1; j < k1; j += jstep) {
+        // A: lane (g, tig) takes code word tig of rows g and g + 8 of both halves; B: column 0
+        // the leading part of h, column 1 its remainder, for that word's 8 columns (columns 2..7
+        // of B and of the product are not used)
+        const uint8_t* c = cw + j * kDCodeSlot;
+        const uint8_t* r = rw + j * (kDWarps * kHRecBytes);
+        const uint32_t c0a = *reinterpret_cast<const uint32_t*>(c);
+        const uint32_t c1a = *reinterpret_cast<const uint32_t*>(c + 8 * 16);
+        const uint32_t c0b = *reinterpret_cast<const uint32_t*>(c + kDPieceBytes);
+        const uint32_t c1b = *reinterpret_cast<const uint32_t*>(c + kDPieceBytes + 8 * 16);
+        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(sw + j * kDSBSlot);
+        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(sw + j * kDSBSlot + 8 * 4);
+        uint4 hva = make_uint4(0u, 0u, 0u, 0u), hvb = hva;
+        if (g < 2) {
+          hva = *reinterpret_cast<const uint4*>(r + ho);
+          hvb = *reinterpret_cast<const uint4*>(r + kHRecBytes + ho);
+        }
+        const float2 ha = *reinterpret_cast<const float2*>(r + 4 * kDecPartRows);
+        const float2 hb = *reinterpret_cast<const float2*>(r + kHRecBytes + 4 * kDecPartRows);
+        uint32_t qa0[4], qa1[4], qb0[4], qb1[4];
+        q_pairs(c0a, qa0);
+        q_pairs(c1a, qa1);
+        q_pairs(c0b, qb0);
+        q_pairs(c1b, qb1);
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        mma16816_acc(d, qa0[0], qa1[0], qa0[1], qa1[1], hva.x, hva.y);
+        mma16816_acc(d, qa0[2], qa1[2], qa0[3], qa1[3], hva.z, hva.w);
+        mma16816_acc(d, qb0[0], qb1[0], qb0[1], qb1[1], hvb.x, hvb.y);
+        mma16816_acc(d, qb0[2], qb1[2], qb0[3], qb1[3], hvb.z, hvb.w);
+        // d = sum (base + q) h over the 64 columns: s*q + b weights give
+        // s * (d - 1024 sa - 64 sb) + b * (sa + sb), with sa, sb the sums of h over the base-1024
+        // and base-64 columns
+        const float sa = ha.x + hb.x, sb = ha.y + hb.y, h0 = sa + sb, h1 = 1024.f * sa + 64.f * sb;
+        acc0 = fmaf(bf16lo(w0), (d[0] + d[1]) - h1, fmaf(bf16hi(w0), h0, acc0));
+        acc1 = fmaf(bf16lo(w1), (d[2] + d[3]) - h1, fmaf(bf16hi(w1), h0, acc1));
+      }
+    }
+    __syncthreads();  // before the next parts' copies overwrite shared memory
+  }
+  if (s_abort) {  // y is undefined; let this CTA's copies land before exiting
+    if (tid == 0) {
+      mbar_drain(bar, phase);
+      set_device_status(p.hdr, MOE_ERR_DEVICE_TIMEOUT);
+    }
+    return;
+  }
+  if (tig == 0) {
+    s_red[warp][g] = acc0;
+    s_red[warp][g + 8] = acc1;
+  }
+  __syncthreads();
+  if (tid < kDRows) {
+    float y = 0.f;
+#pragma unroll
+    for (int w = 0; w < kDWarps; ++w) y += s_red[w][tid];
+    p.y[r0 + tid] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
   }
 }
 
@@ -932,13 +1016,15 @@ __global__ void __launch_bounds__(kYThreads) decode_reduce_kernel(const DecodePa
 
 }  // namespace
 
-cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s, void* const* events, int mode) {
+cudaError_t launch_decode(const DecodeParams& p, const DecodeMaps& maps, cudaStream_t s, void* const* events,
+                          int mode) {
   const moe_dims dims = {p.d, p.E, p.k, p.inter, p.inter, kGroup};
   const int n_parts = decode_parts(dims);
   const int smem = x_smem(p.d).total;
-  // The router and reduce kernels ask for the largest shared-memory carveout, so that the SMs
-  // they run on can take an expert-kernel CTA (~130 KB of shared memory) as soon as PDL lets it
-  // start, instead of waiting for the SM to drain and change its L1/shared split.
+  const size_t down_smem = (size_t)(p.k + 1) * kDSlotBytes + 128;
+  // The router and down kernels ask for the largest shared-memory carveout, so that the SMs they
+  // run on can take an expert-kernel CTA (~120 KB of shared memory) as soon as PDL lets it start,
+  // instead of waiting for the SM to drain and change its L1/shared split.
   static cudaError_t attr = [] {
     cudaError_t e = cudaSuccess;
     for (auto kernel : {decode_expert_kernel<0>, decode_expert_kernel<1>, decode_expert_kernel<2>})
@@ -947,13 +1033,16 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s, void* const* ev
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(decode_router_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                cudaSharedmemCarveoutMaxShared);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(decode_reduce_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                               cudaSharedmemCarveoutMaxShared);
+    for (auto kernel : {decode_down_kernel<0>, decode_down_kernel<1>}) {
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (kMaxTopK + 1) * kDSlotBytes + 128);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    }
     return e;
   }();
   if (attr != cudaSuccess) return attr;
-  if (mode == kDecodeDiagReadOnly) {  // the expert kernel's weight copies alone, no chain
+  if (mode == kDecodeDiagReadOnly) {  // the layer's weight copies alone, no chain
     decode_expert_kernel<2><<<n_parts, kXThreads, (size_t)smem, s>>>(p);
     return cudaGetLastError();
   }
@@ -965,8 +1054,10 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s, void* const* ev
                                   : launch_pdl(decode_expert_kernel<0>, n_parts, kXThreads, (size_t)smem, 1, s, p);
   if (err != cudaSuccess) return err;
   if ((err = record_event(events, 2, s)) != cudaSuccess) return err;
-  if ((err = launch_pdl(decode_reduce_kernel, p.d / kYRows, kYThreads, 0, 1, s, p, n_parts)) != cudaSuccess)
-    return err;
+  err = mode == kDecodeDiagNoMath
+            ? launch_pdl(decode_down_kernel<1>, p.d / kDRows, kDThreads, down_smem, 1, s, p, maps)
+            : launch_pdl(decode_down_kernel<0>, p.d / kDRows, kDThreads, down_smem, 1, s, p, maps);
+  if (err != cudaSuccess) return err;
   return record_event(events, 3, s);
 }
 

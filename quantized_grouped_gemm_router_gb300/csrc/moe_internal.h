@@ -97,13 +97,17 @@ struct WsLayout {
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // Decode: one expert-kernel CTA per (selected or shared expert, 32 intermediate rows); each
-// writes a partial output row of d floats that the combine kernel sums in a fixed order.
+// writes an h record (the 32 SwiGLU values of its rows as fp16 leading parts and remainders, and
+// their sums over the two code-base column classes) that the down kernel reads. The small-batch
+// decode writes partial output rows of d floats instead, summed in a fixed order.
 constexpr int kDecPartRows = 32;
+constexpr int kHRecBytes = 144;     // 32 fp16 leading parts, 32 fp16 remainders, 2 floats, padding
 constexpr int kDecodeMaxD = 3072;   // the expert kernel keeps all its weight slices in smem
 constexpr int kMaxDecodeBatch = 8;  // tokens of one moe_decode_batch call (the MMA's 8 columns)
 constexpr int kBatchMaxD = 2048;    // the batch expert kernel also keeps 8 tokens' x in smem
 inline int decode_parts(const moe_dims& d) { return (d.top_k + 1) * (d.inter / kDecPartRows); }
 inline size_t decode_partial_bytes(const moe_dims& d) { return (size_t)decode_parts(d) * d.d * 4; }
+inline size_t decode_hrec_bytes(const moe_dims& d) { return (size_t)decode_parts(d) * kHRecBytes; }
 
 // Upper bound on the routed block-map tiles of T tokens with tiles of tile_rows rows: every hit
 // expert has a ragged last tile, and the whole tiles are at most A / tile_rows.
@@ -208,7 +212,8 @@ struct DecodeParams {
   float* logits;              // [T, E]
   int32_t* topk_idx;          // [T, k]
   float* topk_w;              // [T, k]
-  float* partials;            // [T, k + 1, I / 32, d] fp32 partial outputs (T = 1: one per expert-kernel CTA)
+  float* partials;            // [T, k + 1, I / 32, d] fp32 partial outputs (small-batch decode)
+  uint8_t* hrec;              // [k + 1, I / 32] h records of kHRecBytes (batch-1 decode)
   uint16_t* y;                // [T, d] bf16
   WsHeader* hdr;
   int d, E, k, inter;
@@ -254,9 +259,18 @@ int gemm_kw_per_stage(int mode);  // K blocks that one weight stage covers
 int gemm_out_rows(int mode);      // output rows of one work item (gate/up: 64 features)
 cudaError_t launch_cast(const float* yacc, uint16_t* y, size_t n, cudaStream_t s);
 // mode: 0 the decode path; kDecodeDiagNoMath the same chain with the GEMV arithmetic deleted
-// (partial rows of zeros); kDecodeDiagReadOnly the expert kernel's weight copies alone.
+// (y = 0); kDecodeDiagReadOnly one kernel that copies every weight the layer reads, alone.
 constexpr int kDecodeDiagNoMath = 1, kDecodeDiagReadOnly = 2;
-cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s, void* const* events, int mode = 0);
+// Tensor maps of the decode down kernel: the down codes of every expert as u64 words (256 words,
+// m block, 32-column part, expert), box = the 16 rows (32 words) of one m block for 16 parts; the
+// down scale/bias words (64 words, m block, K block, expert), box = the 16 rows (8 words) for 8 K
+// blocks.
+struct DecodeMaps {
+  CUtensorMap codes, sb;
+};
+bool make_decode_down_maps(DecodeMaps* m, const uint8_t* packed, const moe_dims& d);
+cudaError_t launch_decode(const DecodeParams& p, const DecodeMaps& maps, cudaStream_t s, void* const* events,
+                          int mode = 0);
 // p.T tokens (2..kMaxDecodeBatch): the union of their selected experts is read once.
 cudaError_t launch_decode_batch(const DecodeParams& p, cudaStream_t s);
 

@@ -5,7 +5,7 @@
 // forbids device allocation after start-up because cudaMalloc can synchronise the whole device
 // and can fail under memory pressure in the middle of serving. For them this entry point runs
 // the same decode kernels as moe_decode with its scratch (router logits, the selected experts and
-// weights, the per-block partial output rows and the kernels' counters) held in a fixed
+// weights, the expert kernel's per-block SwiGLU records and the status word) held in a fixed
 // file-scope device array.
 //
 // That array lives as long as the library stays loaded, on every device that loads it, and
@@ -21,15 +21,15 @@ namespace moe {
 namespace {
 
 // Largest scratch this entry point can use. A shape needs
-//   256 (counters, status) + 4 E + 8 k + 4 d (k + 1) I / 32 bytes, each part rounded up to 256;
-// d=2048, E=256, k=8, I=512 needs 1.13 MiB.
-constexpr size_t kNoAllocScratchBytes = 2 * 1024 * 1024;
+//   256 (status) + 4 E + 8 k + 144 (k + 1) I / 32 bytes, each part rounded up to 256;
+// d=2048, E=256, k=8, I=512 needs 22 KiB.
+constexpr size_t kNoAllocScratchBytes = 512 * 1024;
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
 
 struct ScratchLayout {
-  size_t header, logits, topk_idx, topk_w, partials, total;
+  size_t header, logits, topk_idx, topk_w, hrec, total;
 };
 
 ScratchLayout scratch_layout(const moe_dims& d) {
@@ -40,7 +40,7 @@ ScratchLayout scratch_layout(const moe_dims& d) {
   L.logits = take((size_t)d.n_experts * 4);
   L.topk_idx = take((size_t)d.top_k * 4);
   L.topk_w = take((size_t)d.top_k * 4);
-  L.partials = take(decode_partial_bytes(d));
+  L.hrec = take(decode_hrec_bytes(d));
   L.total = o;
   return L;
 }
@@ -84,7 +84,7 @@ extern "C" int moe_decode_noalloc(const moe_layer* layer, const uint16_t* x, uin
   if (scratch_address(&base) != cudaSuccess) return MOE_ERR_CUDA;
   uint8_t* s = static_cast<uint8_t*>(base);
   // Nothing in the scratch must start at zero: every call writes the logits, the routing and
-  // the partial rows before it reads them; the status word is written only on device errors.
+  // the SwiGLU records before it reads them; the status word is written only on device errors.
   WsHeader* hdr = reinterpret_cast<WsHeader*>(s + L.header);
   const PackedLayout P = packed_layout(d);
   DecodeParams p;
@@ -97,7 +97,8 @@ extern "C" int moe_decode_noalloc(const moe_layer* layer, const uint16_t* x, uin
   p.logits = reinterpret_cast<float*>(s + L.logits);
   p.topk_idx = reinterpret_cast<int32_t*>(s + L.topk_idx);
   p.topk_w = reinterpret_cast<float*>(s + L.topk_w);
-  p.partials = reinterpret_cast<float*>(s + L.partials);
+  p.partials = nullptr;
+  p.hrec = s + L.hrec;
   p.y = y;
   p.hdr = hdr;
   p.d = d.d;
@@ -105,5 +106,7 @@ extern "C" int moe_decode_noalloc(const moe_layer* layer, const uint16_t* x, uin
   p.k = d.top_k;
   p.inter = d.inter;
   p.T = 1;
-  return launch_decode(p, stream, nullptr) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  DecodeMaps maps;
+  if (!make_decode_down_maps(&maps, p.packed, d)) return MOE_ERR_CUDA;
+  return launch_decode(p, maps, stream, nullptr) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -55,8 +55,8 @@ def test_decode_noalloc_matches_decode(m, shape, seed):
 def test_decode_noalloc_rejects_oversized_shape(m):
     from quantized_grouped_gemm_router_gb300.binding import MoeLayer
     dims = m.dims_of(FULL)
-    dims.inter = 4096          # 4 d (k+1) I / 32 bytes of partial outputs exceed the fixed scratch
-    dims.shared_inter = 4096
+    dims.inter = 16384         # 144 (k+1) I / 32 bytes of SwiGLU records exceed the fixed scratch
+    dims.shared_inter = 16384
     A = 1 << 20                # never dereferenced: the shape check fails first
     layer = MoeLayer(dims, A, None, A)
     assert m.lib().moe_decode_noalloc(ctypes.byref(layer), A, A, None) == 2
