@@ -554,7 +554,7 @@ def run_ours(args, config: dict) -> None:
             peak = peaks["hbm_gbs"]
             r = {"kernel": n, "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
                  "per_launch": f"{w['bytes'] / 1e6:.3f} MB (router + k+1 active experts + x, y) per layer; "
-                               "router, expert and combine kernels overlap through PDL"}
+                               "router, expert and down (+ combine) kernels overlap through PDL"}
         r.update({"avg_launch_us": ms * 1e3, "ms_per_step": share_ms,
                   "peak_source": f"{peaks['source']} ({'sustained bf16 = fp16 dense' if 'flop' in w else 'HBM copy'})",
                   "traffic": traffic.get(n)})
