@@ -634,10 +634,11 @@ def _graph_time_ms(body, reps: int = 3, eager: bool = True) -> float:
 
 
 def small_batch_diagnostics(W, decode_us: float | None, sizes=(1, 2, 3, 4, 5, 8)) -> dict:
-    """Prefill on T = 1..8 token rows (the shape of verifying a few draft tokens at once, which the
-    page's section "What didn't work" found awkward) against T batch-1 decodes: per-layer time of
-    the prefill path over the stack in a CUDA graph, and the distinct experts the T rows select,
-    i.e. the expert bytes one such step must read."""
+    """T = 1..8 token rows at once (the shape of verifying a few draft tokens, which the page's
+    section "What didn't work" found awkward): per-layer time over the stack in a CUDA graph of the
+    small-batch decode (moe_decode_batch, which reads each distinct selected expert once) and of the
+    prefill path, against T batch-1 decodes; and the distinct experts the T rows select, i.e. the
+    expert bytes one such step must read."""
     import torch
     m, L, sh = W.m, len(W.layers), W.shape
     eb = expert_bytes(sh.d, sh.inter)
@@ -652,6 +653,11 @@ def small_batch_diagnostics(W, decode_us: float | None, sizes=(1, 2, 3, 4, 5, 8)
             for l, layer in enumerate(W.layers):
                 m.prefill(layer, W.xp[l, :T], W.ws_p, y=ys[l])
         us = 1e3 * _graph_time_ms(body) / L
+
+        def body_batch():
+            for l, layer in enumerate(W.layers):
+                m.decode_batch(layer, W.xp[l, :T], W.ws_p, y=ys[l])
+        us_b = 1e3 * _graph_time_ms(body_batch) / L
         distinct = 0
         for l, layer in enumerate(W.layers):
             out = m.route(layer, W.xp[l, :T], T, W.ws_p, out=m.route_out_tensors(W.dims, T, W.xp.device,
@@ -659,13 +665,15 @@ def small_batch_diagnostics(W, decode_us: float | None, sizes=(1, 2, 3, 4, 5, 8)
             distinct += int((out["counts"] > 0).sum())
         distinct /= L
         nbytes = (distinct + 1) * one_expert + sh.n_experts * sh.d * 2
-        rows.append({"T": T, "prefill_us_per_layer": us,
+        rows.append({"T": T, "decode_batch_us_per_layer": us_b, "prefill_us_per_layer": us,
                      "T_decodes_us_per_layer": None if decode_us is None else T * decode_us,
-                     "distinct_experts": distinct, "weight_MB": nbytes / 1e6, "weight_GBps": nbytes / (us * 1e3)})
+                     "distinct_experts": distinct, "weight_MB": nbytes / 1e6,
+                     "decode_batch_weight_GBps": nbytes / (us_b * 1e3), "prefill_weight_GBps": nbytes / (us * 1e3)})
     if m.read_device_status(W.ws_p):
         raise RuntimeError("device status set during the small-batch diagnostics")
-    return {"rows": rows, "how": f"moe_prefill on the first T rows of each layer's prefill input, {L} layers per "
-                                 "CUDA graph, best of 3 replays; T_decodes = T x the batch-1 decode time per layer"}
+    return {"rows": rows, "how": f"moe_decode_batch and moe_prefill on the first T rows of each layer's prefill "
+                                 f"input, {L} layers per CUDA graph, best of 3 replays; T_decodes = T x the batch-1 "
+                                 "decode time per layer"}
 
 
 def chunked_prefill_diagnostics(W, prompt_chunks: int = 4, chunks=(512, 1024, 2048, 4096)) -> dict:
