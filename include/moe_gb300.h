@@ -275,7 +275,8 @@ MOE_API int moe_decode(const moe_layer* layer, const uint16_t* x, uint16_t* y, m
  * x, y: bf16 [T, d]. ws: at least moe_workspace_bytes(dims, T). `out` may be NULL; it receives
  * logits [T, E], topk_idx [T, k] and topk_w [T, k].
  * Supports d <= 2048 and T <= 8 (MOE_ERR_UNSUPPORTED_SHAPE otherwise); INVALID_ARG for T < 1.
- * Kernels chained by programmatic dependent launch, as moe_decode.
+ * T = 1 runs moe_decode's kernels (bit-identical to it). Kernels chained by programmatic
+ * dependent launch, as moe_decode.
  */
 MOE_API int moe_decode_batch(const moe_layer* layer, const uint16_t* x, int32_t T, uint16_t* y,
                              moe_route_out* out, void* ws, size_t ws_bytes, moe_stream_t stream);

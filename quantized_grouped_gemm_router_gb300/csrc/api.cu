@@ -532,6 +532,7 @@ int moe_decode_batch(const moe_layer* layer, const uint16_t* x, int32_t T, uint1
   if (!aligned(x, 16) || !aligned(y, 16)) return MOE_ERR_MISALIGNED;
   const moe_dims& d = layer->dims;
   if (T > kMaxDecodeBatch || d.d > kBatchMaxD) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (T == 1) return decode_common(layer, x, y, out, ws, ws_bytes, stream, nullptr, 0);  // the batch-1 chain
   if ((st = check_out(out)) || (st = check_ws(ws, ws_bytes, d, T))) return st;
   Ws w{static_cast<uint8_t*>(ws), ws_layout(d, T)};
   const PackedLayout P = packed_layout(d);

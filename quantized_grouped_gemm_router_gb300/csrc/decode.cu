@@ -86,12 +86,6 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-// Loads of data that an earlier kernel of the chain wrote: through L2 only.
-__device__ __forceinline__ int ld_cg_s32(const int* p) {
-  int r;
-  asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(r) : "l"(p));
-  return r;
-}
 __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
@@ -932,11 +926,11 @@ __global__ void __launch_bounds__(kXThreads, 1) decode_batch_expert_kernel(const
     hbv[set] = *reinterpret_cast<const uint4*>(src + tok * kDecPartRows + 8 * tig);
   }
   constexpr int kMaxTilesPerWarp = kBatchMaxD / 16 / kXWarps;
-  const int ntw = DM * 8 / kXWarps;
+  const int ntiles = DM * 8;  // 16-row tiles of the d output rows (warp w: tiles w, w + 16, ...)
   uint32_t c0[kMaxTilesPerWarp], c1[kMaxTilesPerWarp];
 #pragma unroll
   for (int i = 0; i < kMaxTilesPerWarp; ++i) {
-    if (ok && i < ntw) {
+    if (ok && warp + i * kXWarps < ntiles) {
       const int tile = warp + i * kXWarps, mm = tile >> 3, R0 = (tile & 7) * 16 + g;
       const uint8_t* ds = xs + L.dn + mm * kHalfBytes;
       c0[i] = *reinterpret_cast<const uint32_t*>(ds + R0 * 16 + 4 * tig);
@@ -945,7 +939,7 @@ __global__ void __launch_bounds__(kXThreads, 1) decode_batch_expert_kernel(const
   }
 #pragma unroll
   for (int i = 0; i < kMaxTilesPerWarp; ++i) {
-    if (ok && i < ntw) {
+    if (ok && warp + i * kXWarps < ntiles) {
       const int tile = warp + i * kXWarps, mm = tile >> 3, R0 = (tile & 7) * 16 + g, R1 = R0 + 8;
       uint32_t q0[4], q1[4];
       q_pairs(c0[i], q0);

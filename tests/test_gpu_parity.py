@@ -19,6 +19,13 @@ pytestmark = pytest.mark.gpu
 # Shapes that take the general top-k paths (more than 8 experts per token, more than 256 experts).
 MID = LayerShape(d=256, n_experts=300, top_k=9, inter=128, shared_inter=128)
 WIDE = LayerShape(d=256, n_experts=1024, top_k=16, inter=128, shared_inter=128)
+# Shapes that take the decode down kernel's other work splits: 32 parts of 32 intermediate rows
+# (two chunks of 16 parts), 12 parts (six 64-column groups per chunk), and the widest decode
+# (d = 3072, 192 down blocks) with 20 parts (a last chunk of 4 parts whose copies run past the
+# end of the weights and read zeros there).
+LONGI = LayerShape(d=256, n_experts=16, top_k=2, inter=1024, shared_inter=1024)
+ODDI = LayerShape(d=384, n_experts=16, top_k=4, inter=384, shared_inter=384)
+BIGD = LayerShape(d=3072, n_experts=32, top_k=8, inter=640, shared_inter=640)
 
 
 @pytest.fixture(scope="module")
@@ -185,6 +192,11 @@ def prefill_and_check(m, shape, T, seed=0, bias=None, npl=None, layer=None, hidd
 @pytest.mark.parametrize("T", [1, 4, 37, 300])
 def test_prefill_tiny_shape(m, T):
     prefill_and_check(m, TINY, T, hidden=True)
+
+
+@pytest.mark.parametrize("shape,T", [(LONGI, 37), (ODDI, 37)], ids=["I1024", "d384I384"])
+def test_prefill_other_widths(m, shape, T):
+    prefill_and_check(m, shape, T, hidden=True)
 
 
 def test_prefill_config_tiny(m):
@@ -459,8 +471,10 @@ def test_prefill_chunked_beyond_single_call_limit(m):
 
 # ------------------------------------------------------------------------------ decode
 @pytest.mark.parametrize("shape,bias,seed", [(TINY, None, 0), (FULL, None, 0), (FULL, None, 1),
-                                             (FULL, "zipf", 2), (MID, None, 3), (WIDE, None, 4)],
-                         ids=["tiny", "full0", "full1", "zipf", "E300k9", "E1024k16"])
+                                             (FULL, "zipf", 2), (MID, None, 3), (WIDE, None, 4),
+                                             (LONGI, None, 5), (ODDI, None, 6), (BIGD, None, 7)],
+                         ids=["tiny", "full0", "full1", "zipf", "E300k9", "E1024k16", "I1024", "d384I384",
+                              "d3072I640"])
 def test_decode(m, shape, bias, seed):
     npl = _np_layer(shape, seed, bias)
     layer = dev_layer(m, shape, seed, bias)
@@ -486,9 +500,10 @@ def test_decode(m, shape, bias, seed):
 
 
 @pytest.mark.parametrize("shape,T,force", [(FULL, 2, False), (FULL, 3, False), (FULL, 5, False), (FULL, 8, False),
-                                           (FULL, 8, True), (FULL, 1, False), (TINY, 4, False), (WIDE, 6, False)],
+                                           (FULL, 8, True), (FULL, 1, False), (TINY, 4, False), (WIDE, 6, False),
+                                           (LONGI, 3, False), (ODDI, 5, False)],
                          ids=["full2", "full3", "full5", "full8", "full8_shared_experts", "full1", "tiny4",
-                              "E1024k16_6"])
+                              "E1024k16_6", "I1024_3", "d384I384_5"])
 def test_decode_batch(m, shape, T, force):
     """moe_decode_batch on T tokens: the routing of every token bit-exact against the oracle's
     selection on the GPU's logits, every token's y within the output tolerance of the oracle and
