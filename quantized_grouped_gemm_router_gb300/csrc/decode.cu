@@ -766,43 +766,44 @@ __global__ void __launch_bounds__(kXThreads, 1) decode_batch_expert_kernel(const
   if (shared && warp == 0) issue(p.E);  // static weights: before waiting on the selection
   pdl_launch_dependents();
   pdl_wait();
-  if (tid == 0) *s_expert = shared ? p.E : (slot < __ldcg(n_distinct) ? __ldcg(dexp + slot) : -1);
-  __syncthreads();
-  const int expert = *s_expert;
-  if (expert < 0) return;  // fewer distinct experts than slots (uniform; nothing was issued)
-  if (!shared && warp == 0) issue(expert);
-  if (tid < kMaxDecodeBatch) {  // this expert's weight and slot for every token (0 and -1: not chosen)
-    float w = 0.f;
-    int j = -1;
-    if (tid < T) {
-      if (shared) {
-        w = 1.f;
-        j = k;
-      } else {
-        for (int jj = 0; jj < k; ++jj)
-          if (__ldcg(p.topk_idx + tid * k + jj) == expert) {
-            w = __ldcg(p.topk_w + tid * k + jj);
-            j = jj;
-          }
-      }
+  // Warp 0 finds this block's expert and issues its copies at once, while warps 1..15 stage x (the
+  // copies' issue holds warp 0 up for a while).
+  if (warp == 0) {
+    int e = p.E;
+    if (lane == 0 && !shared) {  // both loads in flight at once (dexp holds T*k entries: in bounds)
+      const int nd = __ldcg(n_distinct), ex = __ldcg(dexp + slot);
+      e = slot < nd ? ex : -1;
     }
-    s_w[tid] = w;
-    s_slot[tid] = j;
-  }
-  {
+    e = __shfl_sync(0xFFFFFFFFu, e, 0);
+    if (lane == 0) *s_expert = e;
+    if (lane < kMaxDecodeBatch) {  // not chosen: weight 0, slot -1; the shared expert: every token
+      s_w[lane] = shared && lane < T ? 1.f : 0.f;
+      s_slot[lane] = shared && lane < T ? k : -1;
+    }
+    if (!shared && e >= 0) issue(e);
+  } else {
     // x of every token as fp16 pairs, and per token and 64-column group the sums of x over the
-    // base-1024 columns (0,1,4,5 of every 8) and the base-64 columns (2,3,6,7)
+    // base-1024 columns (0,1,4,5 of every 8) and the base-64 columns (2,3,6,7); chunk i of the
+    // T x d/8 chunks goes to thread 32 + (i mod 480), every thread's loads first so they overlap
+    constexpr int kStagers = kXThreads - 32;
+    constexpr int kXIter = (kMaxDecodeBatch * (kBatchMaxD / 8) + kStagers - 1) / kStagers;
     uint32_t* x2w = reinterpret_cast<uint32_t*>(xs + L.x16);
     float* xsw = reinterpret_cast<float*>(xs + L.xsum);
-    const int nch = p.d / 8;
+    const int nch = p.d / 8, st = tid - 32;
     bool over = false;
-    for (int base = 0; base < kMaxDecodeBatch * nch; base += kXThreads) {
-      const int i = base + tid, t = i / nch, c = i % nch;
+    uint4 xv[kXIter];
+#pragma unroll
+    for (int it = 0; it < kXIter; ++it) {
+      const int i = it * kStagers + st, t = i / nch, c = i % nch;
+      xv[it] = t < T ? __ldcg(reinterpret_cast<const uint4*>(p.x + (size_t)t * p.d) + c) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int it = 0; it < kXIter; ++it) {
+      const int i = it * kStagers + st, t = i / nch, c = i % nch;
       float sa = 0.f, sb = 0.f;
       uint32_t o[4] = {0u, 0u, 0u, 0u};
       if (t < T) {
-        const uint4 v = __ldcg(reinterpret_cast<const uint4*>(p.x + (size_t)t * p.d) + c);
-        const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+        const uint32_t in[4] = {xv[it].x, xv[it].y, xv[it].z, xv[it].w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const float lo = bf16lo(in[j]), hi = bf16hi(in[j]);
@@ -814,7 +815,7 @@ __global__ void __launch_bounds__(kXThreads, 1) decode_batch_expert_kernel(const
       }
       if (t < kMaxDecodeBatch) *reinterpret_cast<uint4*>(x2w + (size_t)t * (p.d / 2) + 4 * c) = make_uint4(o[0], o[1], o[2], o[3]);
 #pragma unroll
-      for (int q = 1; q < 8; q <<= 1) {
+      for (int q = 1; q < 8; q <<= 1) {  // 8 consecutive chunks (one 64-column group) per 8 lanes
         sa += __shfl_xor_sync(0xFFFFFFFFu, sa, q);
         sb += __shfl_xor_sync(0xFFFFFFFFu, sb, q);
       }
@@ -827,6 +828,16 @@ __global__ void __launch_bounds__(kXThreads, 1) decode_batch_expert_kernel(const
       set_device_status(p.hdr, MOE_ERR_OUT_OF_RANGE);
   }
   __syncthreads();
+  const int expert = *s_expert;
+  if (expert < 0) return;  // fewer distinct experts than slots (uniform; nothing was issued)
+  if (!shared && tid < T * k) {  // the T*k selections, one per thread (each token picks an expert once)
+    const int e = __ldcg(p.topk_idx + tid);
+    const float w = __ldcg(p.topk_w + tid);
+    if (e == expert) {  // read after the barrier that follows the gate/up loop
+      s_w[tid / k] = w;
+      s_slot[tid / k] = tid % k;
+    }
+  }
   const uint32_t* x2 = reinterpret_cast<const uint32_t*>(xs + L.x16);
   const float* xsum = reinterpret_cast<const float*>(xs + L.xsum);
 
