@@ -55,9 +55,10 @@ __device__ int block_exclusive_scan4(const int (&v)[4], int* s_warp, int* total)
   return before_warp + incl - mine;
 }
 
-// Top-k of kTopkTokens tokens per CTA (two per warp), then the CTA's share of the fp16 copy of
-// x and of the zeroing of the combine accumulator (wide grid: this is the launch that moves
-// the bytes).
+// The CTA's share of the fp16 copy of x and of the zeroing of the combine accumulator (wide grid:
+// this is the launch that moves the bytes), then the top-k of its kTopkTokens tokens (two per
+// warp). The copy goes first and keeps 8 loads in flight per thread, so the memory stream does not
+// wait for the (latency-bound) selections.
 __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const RouteParams p) {
   pdl_wait();
   pdl_launch_dependents();
@@ -65,6 +66,40 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const RoutePar
   const int E = p.E, k = p.k;
   const int t_begin = blockIdx.x * kTopkTokens;
   const int t_end = min(p.T, t_begin + kTopkTokens);
+  const int n8 = (t_end - t_begin) * p.d / 8;  // 8-element chunks of this CTA's rows
+  if (p.x) {  // fp16 operand copy of x for the expert GEMMs (exact inside the fp16 range)
+    constexpr int kU = 8;
+    const uint4* xs = reinterpret_cast<const uint4*>(p.x + (size_t)t_begin * p.d);
+    uint4* xd = reinterpret_cast<uint4*>(p.x16 + ((size_t)p.T * p.k + t_begin) * p.d);
+    bool over = false;
+    for (int i0 = tid; i0 < n8; i0 += kU * kTopkThreads) {
+      uint4 v[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = i0 + u * kTopkThreads;
+        v[u] = i < n8 ? xs[i] : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = i0 + u * kTopkThreads;
+        const uint32_t in[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float lo = __uint_as_float(in[j] << 16), hi = __uint_as_float(in[j] & 0xFFFF0000u);
+          over |= !(fabsf(lo) <= 65504.f) || !(fabsf(hi) <= 65504.f);
+          const __half2 h = __floats2half2_rn(lo, hi);
+          o[j] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        if (i < n8) xd[i] = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    }
+    if (__any_sync(0xFFFFFFFFu, over) && lane == 0) set_device_status(p.hdr, MOE_ERR_OUT_OF_RANGE);
+  }
+  if (p.yacc) {
+    float4* yrow = reinterpret_cast<float4*>(p.yacc + (size_t)t_begin * p.d);
+    for (int i = tid; i < 2 * n8; i += kTopkThreads) yrow[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   for (int t = t_begin + warp; t < t_end; t += kTopkThreads / 32) {
     int my_e;
     float my_w;
@@ -74,30 +109,6 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const RoutePar
       p.topk_idx[(size_t)t * k + lane] = my_e;
       p.topk_w[(size_t)t * k + lane] = my_w;
     }
-  }
-  const int n8 = (t_end - t_begin) * p.d / 8;  // 8-element chunks of this CTA's rows
-  if (p.x) {  // fp16 operand copy of x for the expert GEMMs (exact inside the fp16 range)
-    const uint4* xs = reinterpret_cast<const uint4*>(p.x + (size_t)t_begin * p.d);
-    uint4* xd = reinterpret_cast<uint4*>(p.x16 + ((size_t)p.T * p.k + t_begin) * p.d);
-    bool over = false;
-    for (int i = tid; i < n8; i += kTopkThreads) {
-      const uint4 v = xs[i];
-      const uint32_t in[4] = {v.x, v.y, v.z, v.w};
-      uint32_t o[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float lo = __uint_as_float(in[j] << 16), hi = __uint_as_float(in[j] & 0xFFFF0000u);
-        over |= !(fabsf(lo) <= 65504.f) || !(fabsf(hi) <= 65504.f);
-        const __half2 h = __floats2half2_rn(lo, hi);
-        o[j] = *reinterpret_cast<const uint32_t*>(&h);
-      }
-      xd[i] = make_uint4(o[0], o[1], o[2], o[3]);
-    }
-    if (__any_sync(0xFFFFFFFFu, over) && lane == 0) set_device_status(p.hdr, MOE_ERR_OUT_OF_RANGE);
-  }
-  if (p.yacc) {
-    float4* yrow = reinterpret_cast<float4*>(p.yacc + (size_t)t_begin * p.d);
-    for (int i = tid; i < 2 * n8; i += kTopkThreads) yrow[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 }
 
@@ -237,10 +248,12 @@ __global__ void __launch_bounds__(kScatterWarps * 32) route_scatter_kernel(const
   }
 }
 
-// One warp per sorted row: x16[pos] = x16[A + perm[pos] / k] (16-byte copies, d/8 per row).
+// One warp per sorted row: x16[pos] = x16[A + perm[pos] / k] (16-byte copies, d/8 per row; every
+// lane's loads of a row, up to 8, are in flight at once).
 __global__ void __launch_bounds__(256) route_rows_kernel(const RouteParams p) {
   pdl_wait();
   pdl_launch_dependents();
+  constexpr int kU = 8;
   const int A = p.T * p.k, n16 = p.d / 8;
   const int warps = gridDim.x * (blockDim.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -248,7 +261,14 @@ __global__ void __launch_bounds__(256) route_rows_kernel(const RouteParams p) {
     const int t = p.row_tw[pos].x;
     const uint4* src = reinterpret_cast<const uint4*>(p.x16 + ((size_t)A + t) * p.d);
     uint4* dst = reinterpret_cast<uint4*>(p.x16 + (size_t)pos * p.d);
-    for (int i = lane; i < n16; i += 32) dst[i] = src[i];
+    for (int i0 = lane; i0 < n16; i0 += kU * 32) {
+      uint4 v[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) v[u] = i0 + 32 * u < n16 ? src[i0 + 32 * u] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int u = 0; u < kU; ++u)
+        if (i0 + 32 * u < n16) dst[i0 + 32 * u] = v[u];
+    }
   }
 }
 
