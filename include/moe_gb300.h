@@ -258,9 +258,9 @@ MOE_API int moe_prefill_ablation(const moe_layer* layer, const uint16_t* x, int3
  * x: bf16 [1, d]; y: bf16 [1, d]. ws: at least moe_workspace_bytes(dims, 1). `out` may be NULL.
  * Decode supports d <= 3072 (MOE_ERR_UNSUPPORTED_SHAPE otherwise). The kernels are chained with
  * programmatic dependent launch: each loads the static weights it needs (router rows, the
- * shared expert) before waiting for the work that precedes it in the stream, so `layer`'s
- * weights must not be written by that preceding work. The result is deterministic (fixed
- * summation order).
+ * shared expert, and in the last kernel the selected experts' down rows) before waiting for the
+ * work that precedes it in the stream, so `layer`'s weights must not be written by that
+ * preceding work. The result is deterministic (fixed summation order).
  */
 MOE_API int moe_decode(const moe_layer* layer, const uint16_t* x, uint16_t* y, moe_route_out* out,
                void* ws, size_t ws_bytes, moe_stream_t stream);
