@@ -700,21 +700,26 @@ __global__ void __launch_bounds__(kMaxDecodeBatch * 32) decode_batch_select_kern
 }
 
 // Shared memory of the batch expert kernel.
+// Shared memory of the batch expert kernel, under half an SM's so that two blocks fit: the
+// gate/up stage area is reused, once the gate/up loop has consumed it, for the cross-warp
+// reduction of the gate/up dots and for the down slice (copied in only then).
 struct BSmem {
-  int gu, dn, x16, xsum, red, h, hsum, tok, misc, bars, total;
+  int gu, red, dn, x16, xsum, h, hsum, tok, misc, bars, total;
 };
 __host__ __device__ inline BSmem b_smem(int d) {
   const int KB = d / kGroup, DM = d / kBlockRows;
+  const int red_bytes = kXWarps * 2 * kDecPartRows * kMaxDecodeBatch * 4;          // [warp][mat][row][token]
+  const int area = max(KB * kGUStage, red_bytes + DM * kDnStage);
   BSmem L;
   L.gu = 0;
-  L.dn = L.gu + KB * kGUStage;
-  L.x16 = up16(L.dn + DM * kDnStage);                                       // [token][d] fp16
-  L.xsum = up16(L.x16 + kMaxDecodeBatch * d * 2);                           // [token][KB][2]
-  L.red = up16(L.xsum + kMaxDecodeBatch * KB * 8);                          // [warp][mat][row][token]
-  L.h = up16(L.red + kXWarps * 2 * kDecPartRows * kMaxDecodeBatch * 4);     // [plane][token][32] fp16
-  L.hsum = up16(L.h + 2 * kMaxDecodeBatch * kDecPartRows * 2);              // [token][2]
-  L.tok = up16(L.hsum + kMaxDecodeBatch * 8);                               // weight[8], slot[8]
-  L.misc = up16(L.tok + kMaxDecodeBatch * 8);                               // abort flag, expert
+  L.red = 0;                                                                  // after the gate/up loop
+  L.dn = red_bytes;                                                           // after the gate/up loop
+  L.x16 = up16(area);                                                         // [token][d] fp16
+  L.xsum = up16(L.x16 + kMaxDecodeBatch * d * 2);                             // [token][KB][2]
+  L.h = up16(L.xsum + kMaxDecodeBatch * KB * 8);                              // [plane][token][32] fp16
+  L.hsum = up16(L.h + 2 * kMaxDecodeBatch * kDecPartRows * 2);                // [token][2]
+  L.tok = up16(L.hsum + kMaxDecodeBatch * 8);                                 // weight[8], slot[8]
+  L.misc = up16(L.tok + kMaxDecodeBatch * 8);                                 // abort flag, expert
   L.bars = up16(L.misc + 16);
   L.total = L.bars + (kXMaxGUChunks + 1) * 8;
   return L;
@@ -723,7 +728,7 @@ __host__ __device__ inline BSmem b_smem(int d) {
 // One CTA per (distinct selected expert, or the shared expert) x 32 intermediate rows, for every
 // token of the call at once. Slots beyond the call's distinct experts exit at once. Token t's
 // contribution from its slot j goes to partial row [t][j][part] (the shared expert to [t][k]).
-__global__ void __launch_bounds__(kXThreads, 1) decode_batch_expert_kernel(const DecodeParams p,
+__global__ void __launch_bounds__(kXThreads, 2) decode_batch_expert_kernel(const DecodeParams p,
                                                                            const int32_t* dexp,
                                                                            const int32_t* n_distinct) {
   extern __shared__ __align__(128) uint8_t xs[];
@@ -747,7 +752,7 @@ __global__ void __launch_bounds__(kXThreads, 1) decode_batch_expert_kernel(const
     fence_barrier_init();
   }
   __syncthreads();
-  auto issue = [&](int expert) {  // the same pieces as the batch-1 expert kernel
+  auto issue = [&](int expert) {  // the gate/up pieces of the batch-1 expert kernel
     const uint8_t* eb = p.packed + (size_t)expert * p.expert_stride;
     if (lane < NGU) {
       const uint8_t* gu = eb + gu_offset(m, part % (kBlockRows / kDecPartRows), 0, KB);
@@ -755,13 +760,14 @@ __global__ void __launch_bounds__(kXThreads, 1) decode_batch_expert_kernel(const
       const uint32_t bytes = (uint32_t)(kb1 - kb0) * kGUStage;
       mbar_arrive_expect_tx(bars + 8u * c, bytes);
       tma_bulk_g2s(smem_u32(xs + L.gu + kb0 * kGUStage), gu + (size_t)kb0 * kGUStage, bytes, bars + 8u * c);
-    } else if (lane == NGU) {
-      const uint8_t* dn = eb + p.gu_bytes;
-      mbar_arrive_expect_tx(bars + 8u * NGU, (uint32_t)(DM * (kHalfBytes + kSBBytes)));
-      tma_bulk_g2s(smem_u32(xs + L.dn), dn + dn_code_offset(kbd, hd, 0, DM), DM * kHalfBytes, bars + 8u * NGU);
-      tma_bulk_g2s(smem_u32(xs + L.dn + DM * kHalfBytes), dn + dn_sb_offset(kbd, 0, DM, KBI), DM * kSBBytes,
-                   bars + 8u * NGU);
     }
+  };
+  auto issue_down = [&](int expert) {  // lane 0 of warp 0: the down slice, into the consumed gate/up area
+    const uint8_t* dn = p.packed + (size_t)expert * p.expert_stride + p.gu_bytes;
+    mbar_arrive_expect_tx(bars + 8u * NGU, (uint32_t)(DM * (kHalfBytes + kSBBytes)));
+    tma_bulk_g2s(smem_u32(xs + L.dn), dn + dn_code_offset(kbd, hd, 0, DM), DM * kHalfBytes, bars + 8u * NGU);
+    tma_bulk_g2s(smem_u32(xs + L.dn + DM * kHalfBytes), dn + dn_sb_offset(kbd, 0, DM, KBI), DM * kSBBytes,
+                 bars + 8u * NGU);
   };
   if (shared && warp == 0) issue(p.E);  // static weights: before waiting on the selection
   pdl_launch_dependents();
@@ -883,6 +889,10 @@ __global__ void __launch_bounds__(kXThreads, 1) decode_batch_expert_kernel(const
     }
   }
   gu_ok = __all_sync(0xFFFFFFFFu, gu_ok);
+  // every warp is done with the gate/up stages: the area now takes the reduction and the down slice
+  __syncthreads();
+  const bool down_issued = tid == 0 && !*s_abort;  // (meaningful on thread 0, which drains)
+  if (down_issued) issue_down(expert);
   float* red = reinterpret_cast<float*>(xs + L.red);  // [warp][mat][row][token]
 #pragma unroll
   for (int mat = 0; mat < 2; ++mat)
@@ -980,7 +990,8 @@ __global__ void __launch_bounds__(kXThreads, 1) decode_batch_expert_kernel(const
   if (!down_ok && tid == 0) *s_abort = 1;
   __syncthreads();
   if (tid == 0 && *s_abort) {
-    for (int i = 0; i <= NGU; ++i) mbar_drain(bars + 8u * i, 0);
+    for (int i = 0; i < NGU; ++i) mbar_drain(bars + 8u * i, 0);
+    if (down_issued) mbar_drain(bars + 8u * NGU, 0);
     set_device_status(p.hdr, MOE_ERR_DEVICE_TIMEOUT);
   }
 }
@@ -1070,8 +1081,14 @@ cudaError_t launch_decode_batch(const DecodeParams& p, cudaStream_t s) {
   const moe_dims dims = {p.d, p.E, p.k, p.inter, p.inter, kGroup};
   const int parts = p.inter / kDecPartRows, n_parts = decode_parts(dims);
   const int smem = b_smem(p.d).total;
-  static cudaError_t attr = cudaFuncSetAttribute(decode_batch_expert_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 b_smem(kBatchMaxD).total);
+  static cudaError_t attr = [] {  // two blocks per SM: the largest shared-memory carveout
+    cudaError_t e = cudaFuncSetAttribute(decode_batch_expert_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         b_smem(kBatchMaxD).total);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(decode_batch_expert_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
+    return e;
+  }();
   if (attr != cudaSuccess) return attr;
   // the distinct-expert list lives in the routing part of the workspace: after topk_w
   int32_t* dexp = reinterpret_cast<int32_t*>(p.topk_w + (size_t)p.T * p.k);
