@@ -186,7 +186,7 @@ KERNEL_SOURCES = {
     "prefill_gate_up_gemm": (_CSRC + "gemm.cu", _CSRC + "ptx.cuh"),
     "prefill_down_gemm": (_CSRC + "gemm.cu", _CSRC + "ptx.cuh"),
     "prefill_router_gemm": (_CSRC + "gemm.cu", _CSRC + "ptx.cuh"),
-    "decode_layer": (_CSRC + "decode.cu", _CSRC + "topk.cuh", _CSRC + "ptx.cuh"),
+    "decode_layer": (_CSRC + "decode.cu", _CSRC + "decode_common.cuh", _CSRC + "topk.cuh", _CSRC + "ptx.cuh"),
 }
 
 
