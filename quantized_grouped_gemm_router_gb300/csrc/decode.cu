@@ -12,19 +12,20 @@
 // results (loading static weights) before waiting for it. (Folding the router or the combine into
 // the expert kernel behind an in-kernel release/acquire handshake was measured slower: each
 // handshake costs more than the hand-off between two dependent launches.)
-//   decode_router_kernel  two experts per CTA: logit = W_r[e] . x (+ b_e); the router weight
-//                         slice is loaded before the wait
+//   decode_router_kernel  (decode_common.cuh) two experts per CTA: logit = W_r[e] . x (+ b_e);
+//                         the router weight slice is loaded before the wait
 //   decode_expert_kernel  one CTA per (selected or shared expert, 32 intermediate rows): routed
 //                         CTAs select the top k from the logits themselves (all 512 threads: a
 //                         threshold from the maxima of 16-thread groups, then exact ranks of the
 //                         few experts above it; ties to the lower index); each CTA bulk-copies its
-//                         gate/up rows to shared memory and prefetches its 32-column slice of the
-//                         down projection into L2 as soon as the expert is known (the shared
+//                         gate/up rows to shared memory as soon as the expert is known (the shared
 //                         expert's CTAs before routing is known); gate/up GEMV + SwiGLU, scaled by
 //                         the routing weight, written as the CTA's h record
-//   decode_down_kernel    one CTA per 16 output rows: every (expert slot, 32-column part) piece of
-//                         W_down against its h record, the weights read from L2, summed in a
-//                         fixed order -> bf16 y (the combine needs no partial rows)
+//   decode_down_kernel    one CTA per 16 output rows: started once the router is complete, it
+//                         selects the experts itself and copies its 16 down rows of every slot
+//                         before waiting for the expert kernel; then every (slot, 64-column group)
+//                         unit against the h records, summed in a fixed order -> bf16 y (the
+//                         combine needs no partial rows)
 // The GEMV inner products run on the tensor cores (mma.sync m16n8k16, fp16 in, fp32
 // accumulate): the packed nibble pairs of a row map directly onto the MMA fragment layout, so
 // the weights cost about one ALU operation per two values instead of an fp32 FMA each, which on
@@ -183,9 +184,10 @@ __device__ __forceinline__ void warp_selected_softmax(const TopkSmem* s, int E, 
 
 // kMode 0: the decode expert kernel. Diagnostics (the ablations the pages use to locate the
 // decode bound, section "What didn't work"): kMode 1 deletes the GEMV arithmetic (same copies,
-// waits and stores; the partial rows are zeros); kMode 2 is a read-only probe of the same access
-// pattern (each CTA copies the pieces it would copy for expert `slot` (< k) or the shared expert,
-// waits for them and exits; launched alone).
+// waits and stores; the h records are zeros, and the down kernel's kMode 1 writes y = 0); kMode 2
+// is a read-only probe of the layer's weight reads (each CTA copies its gate/up rows and the down
+// slice of its part, for expert `slot` (< k) or the shared expert, waits for them and exits;
+// launched alone).
 template <int kMode>
 __global__ void __launch_bounds__(kXThreads, 1) decode_expert_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) uint8_t xs[];

@@ -21,6 +21,9 @@
 namespace moe {
 namespace {
 
+constexpr int kYThreads = 512;  // reduce: 16 output rows x 32 groups of partial rows
+constexpr int kYRows = 16;
+
 // ------------------------------------------------------------------------------------------
 // Small-batch decode (2..8 tokens, e.g. checking a few draft tokens at once): the tokens route
 // to different experts (page, section "What didn't work": 2 to 5 draft rows touch different

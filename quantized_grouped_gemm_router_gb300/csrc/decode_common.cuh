@@ -17,8 +17,6 @@ constexpr int kRThreads = 256;         // router: two experts per CTA, 128 threa
 constexpr int kRMaxChunks = kDecodeMaxD / 8 / 128;
 constexpr int kXThreads = 512;         // expert kernel: 16 warps to hide MMA and smem latency
 constexpr int kXWarps = kXThreads / 32;
-constexpr int kYThreads = 512;         // reduce (small batch): 16 output rows x 32 groups of partial rows
-constexpr int kYRows = 16;
 constexpr int kDThreads = 512;         // down kernel: 16 warps, one 32-column part each
 constexpr int kDWarps = kDThreads / 32;
 constexpr int kDRows = 16;             // output rows per down-kernel CTA (the MMA's M)
