@@ -523,6 +523,16 @@ def run_ours(args, config: dict) -> None:
                       "back, per step"}
 
     diag = decode_diagnostics(W) if S and not args.skip_diag else None
+    probe = None
+    if T and not args.skip_diag:  # the layer-stack workload's GEMMs against their read-only probes
+        nl = min(L, 8)
+        probe = gemm_read_probe(W.m, W.layers[:nl], [W.xp[l] for l in range(nl)], [W.yp[l] for l in range(nl)],
+                                W.ws_p, {"gate_up": 1e3 * ksum["prefill_gate_up_gemm"] / kcnt["prefill_gate_up_gemm"],
+                                         "down": 1e3 * ksum["prefill_down_gemm"] / kcnt["prefill_down_gemm"]},
+                                W.shape.n_experts, expert_bytes(W.shape.d, W.shape.inter),
+                                load_peaks()["hbm_gbs"], 4)
+        if W.m.read_device_status(W.ws_p):
+            raise RuntimeError("device status set during the read-only probes")
     configs = None if args.skip_configs else config_results(W, load_peaks())
     small = chunked = None
     if T and not args.skip_diag:
@@ -570,7 +580,7 @@ def run_ours(args, config: dict) -> None:
         "prefill_us_per_layer": 1e3 * red["pre"] / (args.steps * L) if T else None,
         "roofline": dict(rooflines[0]) if rooflines else None, "rooflines": rooflines,
         "cpu_baseline": cpu, "e2e": e2e, "configs": configs, "decode_diagnostics": diag,
-        "small_batch_diagnostics": small, "chunked_prefill_diagnostics": chunked,
+        "small_batch_diagnostics": small, "chunked_prefill_diagnostics": chunked, "prefill_read_probe": probe,
         "gpu_launches": W.launches_per_step() * args.steps,
         "clocks": clk, "wall_s_timed": red["wall"], "graphs": not args.no_graph,
         "device": device_info(device), "sources": {k: src_sha(*v) for k, v in KERNEL_SOURCES.items()},
@@ -814,9 +824,10 @@ def config_results(W, peaks: dict, reps: int = 8) -> dict:
         for i, layer in enumerate(layers):
             o = m.route(layer, xs[i], T, ws, out=m.route_out_tensors(W.dims, T, dev, want=("counts",)))
             hit.append(int((o["counts"] > 0).sum()))
+        probe = gemm_read_probe(m, layers, xs, ys, ws, per, statistics.mean(hit), eb, hbm, reps)
         if m.read_device_status(ws):
             raise RuntimeError("device status set during the per-workload sub-results")
-        return layer_us, per, statistics.mean(hit), abl
+        return layer_us, per, statistics.mean(hit), abl, probe
 
     def gemm_flop(T):
         return 2.0 * (T * k + T) * 3 * I * d
@@ -824,7 +835,7 @@ def config_results(W, peaks: dict, reps: int = 8) -> dict:
     # ---- 512-token prefill, near-uniform routing
     lay = W.layers[:min(len(W.layers), 4)]
     T = 512
-    layer_us, per, hit, abl = prefill_config(T, lay, 3, ("host_routing", "dense"))
+    layer_us, per, hit, abl, probe = prefill_config(T, lay, 3, ("host_routing", "dense"))
     nbytes = (hit + 1) * one_expert + E * d * 2 + 2 * T * d * 2
     gemm_us = per["gate_up"] + per["down"]
     out["prefill512"] = {
@@ -832,13 +843,13 @@ def config_results(W, peaks: dict, reps: int = 8) -> dict:
         "tok_per_s": T / (layer_us * 1e-6), "kernels_us": per, "experts_hit": hit,
         "roofline": {"bound": "hbm", "achieved": nbytes / (layer_us * 1e3), "peak": hbm, "unit": "GB/s",
                      "frac": nbytes / (layer_us * 1e3) / hbm, "per_launch_bytes": nbytes},
-        "gemm_tensor_frac": gemm_flop(T) / (gemm_us * 1e-6) / 1e12 / tf, "ablations": abl}
+        "gemm_tensor_frac": gemm_flop(T) / (gemm_us * 1e-6) / 1e12 / tf, "ablations": abl, "read_probe": probe}
 
     # ---- 2048-token prefill, Zipf router bias
     rb = torch.from_numpy(zipf_router_bias(E)).to(dev)
     lay = [m.Layer(W.dims, L.router_w, rb, L.packed) for L in W.layers[:min(len(W.layers), 8)]]
     T = 2048
-    layer_us, per, hit, abl = prefill_config(T, lay, 4, ("host_routing", "tile32"))
+    layer_us, per, hit, abl, probe = prefill_config(T, lay, 4, ("host_routing", "tile32"))
     gemm_us = per["gate_up"] + per["down"]
     ach = gemm_flop(T) / (gemm_us * 1e-6) / 1e12
     out["skew2048"] = {
@@ -847,10 +858,36 @@ def config_results(W, peaks: dict, reps: int = 8) -> dict:
         "roofline": {"bound": "tensor", "kernel": "grouped gate/up + down GEMMs", "achieved": ach, "peak": tf,
                      "unit": "TFLOP/s", "frac": ach / tf, "frac_of_sustained": ach / peaks["bf16_tflops_sustained"],
                      "per_launch_flop": gemm_flop(T)},
-        "layer_tensor_frac": (gemm_flop(T) + 2.0 * T * E * d) / (layer_us * 1e-6) / 1e12 / tf, "ablations": abl}
+        "layer_tensor_frac": (gemm_flop(T) + 2.0 * T * E * d) / (layer_us * 1e-6) / 1e12 / tf, "ablations": abl,
+        "read_probe": probe}
     out["how"] = (f"CUDA graphs of {reps} repetitions; events recorded by moe_decode_timed / moe_prefill_timed "
                   f"at the kernel boundaries; peaks: {peaks['source']} burst (HBM copy, bf16 dense = fp16 dense)")
     return out
+
+
+def gemm_read_probe(m, layers, xs, ys, ws, per: dict, hit: float, eb: dict, hbm: float, reps: int) -> dict:
+    """The grouped GEMMs against their read-only probes (moe_prefill_diag: the same grid, work list,
+    copies and ring depths, no arithmetic), timed like the GEMMs (events at the kernel boundaries
+    in a CUDA graph of `reps` passes over the layers). per: the GEMMs' own times (us) on the same
+    inputs; hit: experts with at least one row. frac_of_read_ceiling = probe time / GEMM time,
+    i.e. the GEMM's read rate as a fraction of the fastest rate its own access pattern sustains;
+    probe_weight_gbs = packed weights of the hit experts and the shared expert / probe time."""
+    import torch
+    evp = [[_new_events(6) for _ in layers] for _ in range(reps)]
+
+    def body():
+        for r in range(reps):
+            for i, layer in enumerate(layers):
+                m.prefill_diag(layer, xs[i], ws, m.PREFILL_DIAG_READ_ONLY, y=ys[i], events=evp[r][i])
+    _graph_time_ms(body, reps=1, eager=False)
+    torch.cuda.synchronize()
+    res = {}
+    for j, n in ((2, "gate_up"), (3, "down")):
+        us = statistics.mean(1e3 * e[j].elapsed_time(e[j + 1]) for row in evp for e in row)
+        wb = (hit + 1) * eb[n]
+        res[n] = {"probe_us": us, "gemm_us": per[n], "frac_of_read_ceiling": us / per[n],
+                  "probe_weight_gbs": wb / (us * 1e3), "probe_weight_frac_of_hbm": wb / (us * 1e3) / hbm}
+    return res
 
 
 def prefill_ablation_arm(m, arm: str, layers, xs, ys, ws, reps: int) -> dict:

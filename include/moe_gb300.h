@@ -251,6 +251,22 @@ MOE_API int moe_prefill_ablation(const moe_layer* layer, const uint16_t* x, int3
                                  void* ws, size_t ws_bytes, void* aux, size_t aux_bytes, moe_stream_t stream);
 
 /*
+ * Prefill diagnostic: the read-rate ceiling of the two grouped GEMMs (section "What didn't work":
+ * a kernel's rate is placed against the fastest sustained read rate of its own access pattern).
+ *   MOE_PREFILL_DIAG_READ_ONLY  moe_prefill with each grouped GEMM replaced by its read-only probe:
+ *                               the same grid, work list (router GEMM and routing run as usual),
+ *                               packed-weight and activation copies, stage sizes and ring depths,
+ *                               every stage released as soon as it has landed; nothing is
+ *                               dequantized, multiplied or written, so the hidden rows are left
+ *                               as they were and y becomes zeros.
+ * Arguments, checks and errors as moe_prefill_timed (no routing outputs; `events` may be NULL, or 6
+ * entries recorded at the same kernel boundaries), plus MOE_ERR_INVALID_ARG for an unknown mode.
+ */
+#define MOE_PREFILL_DIAG_READ_ONLY 1
+MOE_API int moe_prefill_diag(const moe_layer* layer, const uint16_t* x, int32_t T, uint16_t* y, int mode,
+                             void* ws, size_t ws_bytes, moe_stream_t stream, void* const* events);
+
+/*
  * Batch-1 decode forward (sections "Prefill and decode are different problems" and
  * "Decode: minimize bytes per token"): router GEMV and top-k, then Q4 GEMVs that stream only
  * the top_k selected experts and the shared expert, gate activation fused into the input
@@ -309,9 +325,10 @@ MOE_API int moe_decode_batch(const moe_layer* layer, const uint16_t* x, int32_t 
 MOE_API int moe_decode_noalloc(const moe_layer* layer, const uint16_t* x, uint16_t* y, moe_stream_t stream);
 
 /*
- * Timed variants of moe_prefill and moe_decode for measurement: identical work, plus
- * cudaEventRecordWithFlags(events[i], stream, cudaEventRecordExternal) at each kernel boundary
- * so the events also become nodes of a CUDA graph captured from the call. `events` is a host
+ * Timed variants of moe_prefill and moe_decode for measurement: identical work, plus an event
+ * record at each kernel boundary: cudaEventRecordWithFlags(events[i], stream,
+ * cudaEventRecordExternal) while `stream` is being captured, so the events become nodes of the
+ * CUDA graph captured from the call, and a plain cudaEventRecord otherwise. `events` is a host
  * array of cudaEvent_t (created by the caller with timing enabled); any entry may be NULL.
  *   prefill: events[0] before the router GEMM, [1] before the routing kernels (top-k and
  *            scatter), [2] before the gate/up GEMM, [3] before the down GEMM, [4] before the

@@ -21,6 +21,8 @@ from .binding import (  # noqa: F401
     packed_bytes,
     prefill,
     prefill_ablation,
+    prefill_diag,
+    PREFILL_DIAG_READ_ONLY,
     PREFILL_ARM_HOST_ROUTING,
     PREFILL_ARM_TILE32,
     PREFILL_ARM_DENSE,

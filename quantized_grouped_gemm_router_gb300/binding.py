@@ -91,6 +91,9 @@ def lib() -> ctypes.CDLL:
         L.moe_prefill_ablation.argtypes = [P(MoeLayer), c_void_p, c_int32, c_void_p, ctypes.c_int, c_void_p, c_size_t,
                                            c_void_p, c_size_t, c_void_p]
         L.moe_prefill_ablation.restype = ctypes.c_int
+        L.moe_prefill_diag.argtypes = [P(MoeLayer), c_void_p, c_int32, c_void_p, ctypes.c_int, c_void_p, c_size_t,
+                                       c_void_p, ctypes.POINTER(c_void_p)]
+        L.moe_prefill_diag.restype = ctypes.c_int
         L.moe_prefill_ablation_aux_bytes.argtypes = [P(MoeDims), ctypes.c_int]
         L.moe_prefill_ablation_aux_bytes.restype = c_size_t
         L.moe_decode_noalloc.argtypes = [P(MoeLayer), c_void_p, c_void_p, c_void_p]
@@ -246,6 +249,19 @@ def prefill(layer: Layer, x: torch.Tensor, ws: torch.Tensor, y: torch.Tensor | N
 
 
 PREFILL_ARM_HOST_ROUTING, PREFILL_ARM_TILE32, PREFILL_ARM_DENSE = 1, 2, 3
+PREFILL_DIAG_READ_ONLY = 1
+
+
+def prefill_diag(layer: Layer, x: torch.Tensor, ws: torch.Tensor, mode: int, y: torch.Tensor | None = None,
+                 events=None) -> torch.Tensor:
+    """moe_prefill_diag: moe_prefill with the two grouped GEMMs replaced by their read-only probes
+    (mode 1; y becomes zeros). events: optional 6 events at the kernel boundaries, as for prefill."""
+    _check_dev(x, torch.int16, "x")
+    y = y if y is not None else torch.empty_like(x)
+    _check_dev(y, torch.int16, "y")
+    _check(lib().moe_prefill_diag(ctypes.byref(layer.c), x.data_ptr(), x.shape[0], y.data_ptr(), int(mode),
+                                  ws.data_ptr(), ws.numel(), _stream(), _events(events, 6)), "moe_prefill_diag")
+    return y
 
 
 def ablation_aux_bytes(dims: MoeDims, arm: int) -> int:

@@ -389,7 +389,10 @@ int moe_route(const moe_layer* layer, const uint16_t* x, const float* logits_in,
 
 // The prefill sequence. arm: 0 the product path; MOE_PREFILL_ARM_HOST_ROUTING the block map built
 // on the host after a synchronisation; MOE_PREFILL_ARM_TILE32 block-map tiles of 32 rows;
-// MOE_PREFILL_ARM_DENSE the selected experts' weights expanded into `aux` first.
+// MOE_PREFILL_ARM_DENSE the selected experts' weights expanded into `aux` first; kArmReadProbe the
+// read-only probes in place of the two grouped GEMMs (y = 0).
+constexpr int kArmReadProbe = 100;
+
 static int prefill_impl(const moe_layer* layer, const uint16_t* x, int32_t T, uint16_t* y, moe_route_out* out,
                         void* ws, size_t ws_bytes, moe_stream_t stream, void* const* events, int arm,
                         void* aux = nullptr) {
@@ -460,13 +463,18 @@ static int prefill_impl(const moe_layer* layer, const uint16_t* x, int32_t T, ui
   p.m_tiles = d.inter / gemm_out_rows(mode_gu);
   p.k_blocks = d.d / kGroup;
   if (record_event(events, 2, stream) != cudaSuccess) return MOE_ERR_CUDA;
-  if (launch_gemm(mode_gu, p, &x_maps, tiles * p.m_tiles, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  const bool probe = arm == kArmReadProbe;
+  if ((probe ? launch_gemm_read_probe(mode_gu, p, &x_maps, tiles * p.m_tiles, stream)
+             : launch_gemm(mode_gu, p, &x_maps, tiles * p.m_tiles, stream)) != cudaSuccess)
+    return MOE_ERR_CUDA;
 
   p.region_offset = P.gu_bytes;
   p.m_tiles = d.d / kBlockRows;
   p.k_blocks = d.inter / kGroup;
   if (record_event(events, 3, stream) != cudaSuccess) return MOE_ERR_CUDA;
-  if (launch_gemm(mode_dn, p, &h_maps, tiles * p.m_tiles, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  if ((probe ? launch_gemm_read_probe(mode_dn, p, &h_maps, tiles * p.m_tiles, stream)
+             : launch_gemm(mode_dn, p, &h_maps, tiles * p.m_tiles, stream)) != cudaSuccess)
+    return MOE_ERR_CUDA;
 
   // 5. fp32 accumulator -> bf16 output
   if (record_event(events, 4, stream) != cudaSuccess) return MOE_ERR_CUDA;
@@ -504,6 +512,12 @@ int moe_prefill_ablation(const moe_layer* layer, const uint16_t* x, int32_t T, u
     if (aux_bytes < moe_prefill_ablation_aux_bytes(&layer->dims, arm)) return MOE_ERR_WORKSPACE_TOO_SMALL;
   }
   return prefill_impl(layer, x, T, y, nullptr, ws, ws_bytes, stream, nullptr, arm, aux);
+}
+
+int moe_prefill_diag(const moe_layer* layer, const uint16_t* x, int32_t T, uint16_t* y, int mode, void* ws,
+                     size_t ws_bytes, moe_stream_t stream, void* const* events) {
+  if (mode != MOE_PREFILL_DIAG_READ_ONLY) return MOE_ERR_INVALID_ARG;
+  return prefill_impl(layer, x, T, y, nullptr, ws, ws_bytes, stream, events, kArmReadProbe);
 }
 
 int moe_prefill_chunked(const moe_layer* layer, const uint16_t* x, int64_t T, uint16_t* y, int32_t chunk_tokens,

@@ -225,7 +225,10 @@ __device__ __forceinline__ Item decode_item(const GemmParams& p, int item, int n
   return it;
 }
 
-template <int MODE>
+// RO: the read-only probe of the same access pattern. The two producers run unchanged (the same
+// work list, copies, stage sizes and ring depths); warps 2 and 11 release each weight / activation
+// stage as soon as it has landed; nothing is dequantized, multiplied or written.
+template <int MODE, bool RO = false>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
   using C = Cfg<MODE>;
@@ -260,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStagesW; ++s) {
       mbar_init(full_w(s), 1);
-      mbar_init(empty_w(s), C::kQ4 ? kDqThreads : C::kIssuers);
+      mbar_init(empty_w(s), RO ? 1 : C::kQ4 ? kDqThreads : C::kIssuers);
     }
     for (int s = 0; s < C::kStagesA; ++s) {
       mbar_init(full_a(s), kDqThreads);
@@ -268,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < C::kStagesB; ++s) {
       mbar_init(full_b(s), 1);
-      mbar_init(empty_b(s), C::kIssuers);
+      mbar_init(empty_b(s), RO ? 1 : C::kIssuers);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(acc_full(b), C::kIssuers);
@@ -371,6 +374,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(b_stage(s), map, 0, it.row0, kb0, full_b(s));
         }
       }
+    }
+  } else if constexpr (RO) {
+    // ------------------------------------------------------------ read-only probe: release stages
+    if ((warp == kWarpMMA || warp == kWarpMMA2) && lane == 0) {
+      const bool wring = warp == kWarpMMA;
+      const int per = wring ? C::kSW : C::kSB, stages = wring ? C::kStagesW : C::kStagesB;
+      uint32_t g = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x)
+        for (int kb0 = 0; kb0 < KB && ok; kb0 += per, ++g) {
+          const int s = g % stages;
+          if ((ok = mbar_wait(wring ? full_w(s) : full_b(s), (g / stages) & 1, s_abort)))
+            mbar_arrive(wring ? empty_w(s) : empty_b(s));
+        }
     }
   } else if (warp == kWarpMMA || warp == kWarpMMA2) {
     // ------------------------------------------------------------ MMA issuers
@@ -654,13 +671,13 @@ int num_sms() {
   return n;
 }
 
-template <int MODE>
+template <int MODE, bool RO = false>
 cudaError_t launch_mode(const GemmParams& p, const GemmMaps* maps, int max_items, cudaStream_t s) {
-  static cudaError_t attr = cudaFuncSetAttribute(moe_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 Smem<MODE>::alloc);
+  static cudaError_t attr = cudaFuncSetAttribute(moe_gemm_kernel<MODE, RO>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<MODE>::alloc);
   if (attr != cudaSuccess) return attr;
   const int grid = max_items < num_sms() ? max_items : num_sms();  // persistent: one CTA per SM
-  return launch_pdl(moe_gemm_kernel<MODE>, grid, kThreads, (size_t)Smem<MODE>::alloc, 1, s, p, *maps);
+  return launch_pdl(moe_gemm_kernel<MODE, RO>, grid, kThreads, (size_t)Smem<MODE>::alloc, 1, s, p, *maps);
 }
 
 }  // namespace
@@ -676,6 +693,13 @@ cudaError_t launch_gemm(int mode, const GemmParams& p, const GemmMaps* maps, int
     case kModeDownDense: return launch_mode<kModeDownDense>(p, maps, grid, s);
     default: return launch_mode<kModeDown>(p, maps, grid, s);
   }
+}
+
+cudaError_t launch_gemm_read_probe(int mode, const GemmParams& p, const GemmMaps* maps, int grid, cudaStream_t s) {
+  if (grid <= 0) return cudaSuccess;
+  if (mode == kModeGateUp) return launch_mode<kModeGateUp, true>(p, maps, grid, s);
+  if (mode == kModeDown) return launch_mode<kModeDown, true>(p, maps, grid, s);
+  return cudaErrorInvalidValue;
 }
 
 template <int F>

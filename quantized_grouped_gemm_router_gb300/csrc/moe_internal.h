@@ -254,6 +254,10 @@ struct GemmMaps {
   CUtensorMap a, a2;
 };
 cudaError_t launch_gemm(int mode, const GemmParams& p, const GemmMaps* maps, int grid, cudaStream_t s);
+// The read-only probe of a gate/up or down GEMM (kModeGateUp / kModeDown): the same grid, work list,
+// weight and activation copies and ring depths, each stage released as soon as it lands; no
+// dequantization, MMA or epilogue (hidden and yacc are not written).
+cudaError_t launch_gemm_read_probe(int mode, const GemmParams& p, const GemmMaps* maps, int grid, cudaStream_t s);
 int gemm_kb_per_stage(int mode);  // K blocks that one activation copy covers
 int gemm_kw_per_stage(int mode);  // K blocks that one weight stage covers
 int gemm_out_rows(int mode);      // output rows of one work item (gate/up: 64 features)
@@ -274,10 +278,17 @@ cudaError_t launch_decode(const DecodeParams& p, const DecodeMaps& maps, cudaStr
 // p.T tokens (2..kMaxDecodeBatch): the union of their selected experts is read once.
 cudaError_t launch_decode_batch(const DecodeParams& p, cudaStream_t s);
 
-// Records events[i] (if the array and the entry are non-NULL) on the stream; capturable.
+// Records events[i] (if the array and the entry are non-NULL) on the stream: as an external event
+// node while the stream is being captured (so the graph records it at replay), else a plain record
+// (the external flag is refused outside a capture).
 inline cudaError_t record_event(void* const* events, int i, cudaStream_t s) {
   if (!events || !events[i]) return cudaSuccess;
-  return cudaEventRecordWithFlags(static_cast<cudaEvent_t>(events[i]), s, cudaEventRecordExternal);
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  const cudaError_t e = cudaStreamIsCapturing(s, &cs);
+  if (e != cudaSuccess) return e;
+  const cudaEvent_t ev = static_cast<cudaEvent_t>(events[i]);
+  return cs == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal)
+                                             : cudaEventRecord(ev, s);
 }
 
 }  // namespace moe

@@ -600,6 +600,44 @@ def test_decode_diagnostics(m):
     torch.cuda.synchronize()
     C.check_y(C.bf16_bits_f64(y), O.moe_forward(x, _np_layer(FULL, 0, None), tile_rows=m.tile_rows())["y"], "decode after diagnostics")
 
+@pytest.mark.parametrize("shape,T,bias", [(FULL, 512, None), (FULL, 2048, "zipf"), (ODDI, 300, None),
+                                          (BIGD, 100, None)])
+def test_prefill_read_probe(m, shape, T, bias):
+    """moe_prefill_diag's read-only probes: no device error (every bounded wait was satisfied, so
+    every copy landed), y zeros (nothing accumulated), the events in kernel order; regular prefills
+    before and after give the same y up to the combine's summation order; an unknown mode is
+    refused."""
+    layer = dev_layer(m, shape, 0, bias)
+    xd = to_dev(make_tokens(T, shape.d, seed=610 + T))
+    ws = m.workspace(layer.dims, T)
+    y0 = m.prefill(layer, xd, ws)
+    y = torch.full_like(xd, 0x3C00)
+    m.prefill_diag(layer, xd, ws, m.PREFILL_DIAG_READ_ONLY, y=y)
+    torch.cuda.synchronize()
+    assert m.read_device_status(ws) == 0
+    assert not bool((y & 0x7FFF).any()), "the read-only probes accumulate nothing"
+    # events at the kernel boundaries, recorded eagerly and as nodes of a captured graph
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    for e in evs:
+        e.record()
+    m.prefill_diag(layer, xd, ws, m.PREFILL_DIAG_READ_ONLY, y=y, events=evs)
+    torch.cuda.synchronize()
+    assert all(evs[i].elapsed_time(evs[i + 1]) >= 0 for i in range(5))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        m.prefill_diag(layer, xd, ws, m.PREFILL_DIAG_READ_ONLY, y=y, events=evs)
+    g.replay()
+    torch.cuda.synchronize()
+    assert all(evs[i].elapsed_time(evs[i + 1]) >= 0 for i in range(5))
+    assert m.read_device_status(ws) == 0
+    with pytest.raises(m.MoeError):
+        m.prefill_diag(layer, xd, ws, 2)
+    y1 = m.prefill(layer, xd, ws)
+    torch.cuda.synchronize()
+    assert m.read_device_status(ws) == 0
+    assert _same_up_to_summation_order(y0, y1) == 0
+
+
 def test_decode_matches_prefill_T1(m):
     shape = FULL
     layer = dev_layer(m, shape)
