@@ -835,7 +835,7 @@ def config_results(W, peaks: dict, reps: int = 8) -> dict:
     # ---- 512-token prefill, near-uniform routing
     lay = W.layers[:min(len(W.layers), 4)]
     T = 512
-    layer_us, per, hit, abl, probe = prefill_config(T, lay, 3, ("host_routing", "dense"))
+    layer_us, per, hit, abl, probe = prefill_config(T, lay, 3, ("host_routing", "dense", "wide_cfg"))
     nbytes = (hit + 1) * one_expert + E * d * 2 + 2 * T * d * 2
     gemm_us = per["gate_up"] + per["down"]
     out["prefill512"] = {
@@ -849,7 +849,7 @@ def config_results(W, peaks: dict, reps: int = 8) -> dict:
     rb = torch.from_numpy(zipf_router_bias(E)).to(dev)
     lay = [m.Layer(W.dims, L.router_w, rb, L.packed) for L in W.layers[:min(len(W.layers), 8)]]
     T = 2048
-    layer_us, per, hit, abl, probe = prefill_config(T, lay, 4, ("host_routing", "tile32"))
+    layer_us, per, hit, abl, probe = prefill_config(T, lay, 4, ("host_routing", "tile32", "narrow_cfg"))
     gemm_us = per["gate_up"] + per["down"]
     ach = gemm_flop(T) / (gemm_us * 1e-6) / 1e12
     out["skew2048"] = {
@@ -902,7 +902,9 @@ def prefill_ablation_arm(m, arm: str, layers, xs, ys, ws, reps: int) -> dict:
                     32-row tiles over 16-row ones at 2K tokens);
       dense         the selected experts' weights expanded to fp16 in a buffer first, then dense
                     GEMMs, against in-tile dequantization, both from CUDA graphs (the page: +77.4%
-                    at 512 tokens for in-tile dequantization over materialised bf16 weights)."""
+                    at 512 tokens for in-tile dequantization over materialised bf16 weights);
+      wide_cfg / narrow_cfg  the GEMM configuration moe_prefill did not pick for this token count
+                    (tiles of up to 192 rows / 32-row tiles with deeper copy rings), forced."""
     import torch
     n = len(layers)
     aux = None
@@ -928,7 +930,8 @@ def prefill_ablation_arm(m, arm: str, layers, xs, ys, ws, reps: int) -> dict:
                     for i in range(n):
                         fn(i)
             return 1e3 * _graph_time_ms(body) / (reps * n)
-        code = m.PREFILL_ARM_TILE32 if arm == "tile32" else m.PREFILL_ARM_DENSE
+        code = {"tile32": m.PREFILL_ARM_TILE32, "dense": m.PREFILL_ARM_DENSE, "wide_cfg": m.PREFILL_ARM_WIDE_TILES,
+                "narrow_cfg": m.PREFILL_ARM_NARROW_TILES}[arm]
         n_aux = m.ablation_aux_bytes(layers[0].dims, code)
         aux = torch.empty(n_aux, dtype=torch.uint8, device=xs[0].device) if n_aux else None
         base = graph(lambda i: m.prefill(layers[i], xs[i], ws, y=ys[i]))

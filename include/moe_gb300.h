@@ -145,8 +145,8 @@ typedef struct moe_layer {
  *   perm     int32[A]         sorted position p -> assignment a (stable: ascending a within e)
  *   inv_perm int32[A]         assignment a -> sorted position p
  *   tile_map int32[max_tiles, 3] rows (expert, first row within the expert, rows), experts
- *                             ascending, tiles of moe_tile_rows() rows; max_tiles =
- *                             min(E, A) + A / moe_tile_rows()
+ *                             ascending, tiles of R = moe_prefill_tile_rows(dims, T) rows;
+ *                             max_tiles = min(E, A) + A / R
  *   n_tiles  int32[1]         number of valid tile_map rows
  *   hidden   fp16 [2, A + T, I] (prefill only) SwiGLU outputs h in sorted order as a pair of
  *                             fp16 planes, h = plane0 + plane1 (leading part and remainder);
@@ -176,8 +176,14 @@ MOE_API size_t moe_workspace_bytes(const moe_dims* dims, int32_t max_tokens);
 /* Zeroes the counters and the status word of a workspace (asynchronous on `stream`). */
 MOE_API int moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream);
 
-/* Height of a block-map tile (rows of one expert per tile), so a checker can rebuild tile_map. */
+/* Largest block-map tile height (rows of one expert per tile): 192. */
 MOE_API int32_t moe_tile_rows(void);
+
+/* Block-map tile height of a T-token moe_route / moe_prefill call, so a checker can rebuild
+ * tile_map: 32 while T * top_k <= 16 * n_experts (few rows per expert: the grouped GEMMs run
+ * their narrow configuration, with deeper copy rings), else moe_tile_rows(). 0 for unsupported
+ * dims or T < 1. */
+MOE_API int32_t moe_prefill_tile_rows(const moe_dims* dims, int32_t T);
 
 /*
  * Routing only (section "Prefill: keep routing on the GPU, dequantize in flight"):
@@ -221,22 +227,30 @@ MOE_API int moe_prefill_chunked(const moe_layer* layer, const uint16_t* x, int64
  * Prefill ablations: the three design choices the page measures one at a time (section "Prefill:
  * keep routing on the GPU, dequantize in flight": in-tile dequantization +77.4% and GPU-resident
  * routing +89% at 512 tokens, 32-row tiles +13.2% at 2K tokens), each undone in an otherwise
- * unchanged moe_prefill, so that the benchmark can time what each buys on this GPU. Arguments,
- * checks and results as moe_prefill (no routing outputs); `arm`:
+ * unchanged moe_prefill, so that the benchmark can time what each buys on this GPU, plus the two
+ * GEMM configurations moe_prefill chooses between, each forced. Arguments, checks and results as
+ * moe_prefill (no routing outputs); `arm`:
  *   MOE_PREFILL_ARM_HOST_ROUTING  after the top-k kernel the selection is copied to the host and
  *                                 the stream is synchronised; the host computes the histogram,
  *                                 scan, stable scatter and block map and copies them back (the
  *                                 round trip the GPU-resident routing removes). This arm
  *                                 synchronises `stream` and allocates host memory; it cannot be
  *                                 captured in a CUDA graph.
- *   MOE_PREFILL_ARM_TILE32        block-map tiles of 32 rows instead of moe_tile_rows() (fixed
- *                                 narrow tiles, as on the page, instead of tiles as tall as the
- *                                 expert's rows allow); the workspace of moe_workspace_bytes
- *                                 holds either tiling.
+ *   MOE_PREFILL_ARM_TILE32        block-map tiles of 32 rows in the wide GEMM configuration
+ *                                 (fixed narrow tiles, as on the page, instead of tiles as tall
+ *                                 as the expert's rows allow); the workspace of
+ *                                 moe_workspace_bytes holds any tiling.
+ *   MOE_PREFILL_ARM_WIDE_TILES    the wide GEMM configuration (tiles of up to moe_tile_rows()
+ *                                 rows) whatever the token count.
+ *   MOE_PREFILL_ARM_NARROW_TILES  the narrow GEMM configuration (32-row tiles, deeper weight,
+ *                                 activation and dequantized-operand rings) whatever the token
+ *                                 count. moe_prefill picks one of the two by
+ *                                 moe_prefill_tile_rows; these two arms time the other.
  *   MOE_PREFILL_ARM_DENSE         materialised dequantization: the weights of every selected
  *                                 expert and of the shared expert are first expanded to fp16
  *                                 (scale * q + bias rounded once, the values the in-tile path
- *                                 computes) into `aux`, then the grouped GEMMs read those dense
+ *                                 computes) into `aux`, then the grouped GEMMs (wide
+ *                                 configuration, moe_prefill's block map) read those dense
  *                                 weights instead of the packed codes. aux: device buffer of at
  *                                 least moe_prefill_ablation_aux_bytes(dims, arm) bytes, 128-byte
  *                                 aligned (NULL and 0 for the other arms).
@@ -246,6 +260,8 @@ MOE_API int moe_prefill_chunked(const moe_layer* layer, const uint16_t* x, int64
 #define MOE_PREFILL_ARM_HOST_ROUTING 1
 #define MOE_PREFILL_ARM_TILE32 2
 #define MOE_PREFILL_ARM_DENSE 3
+#define MOE_PREFILL_ARM_WIDE_TILES 4
+#define MOE_PREFILL_ARM_NARROW_TILES 5
 MOE_API size_t moe_prefill_ablation_aux_bytes(const moe_dims* dims, int arm);
 MOE_API int moe_prefill_ablation(const moe_layer* layer, const uint16_t* x, int32_t T, uint16_t* y, int arm,
                                  void* ws, size_t ws_bytes, void* aux, size_t aux_bytes, moe_stream_t stream);

@@ -26,6 +26,8 @@ from .binding import (  # noqa: F401
     PREFILL_ARM_HOST_ROUTING,
     PREFILL_ARM_TILE32,
     PREFILL_ARM_DENSE,
+    PREFILL_ARM_WIDE_TILES,
+    PREFILL_ARM_NARROW_TILES,
     ablation_aux_bytes,
     prefill_chunked,
     read_device_status,
@@ -34,6 +36,7 @@ from .binding import (  # noqa: F401
     selftest_wait_timeout,
     status_string,
     tile_rows,
+    prefill_tile_rows,
     upload_layer,
     workspace,
     workspace_bytes,

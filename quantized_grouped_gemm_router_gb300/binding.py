@@ -69,6 +69,8 @@ def lib() -> ctypes.CDLL:
         L.moe_workspace_init.restype = ctypes.c_int
         L.moe_tile_rows.argtypes = []
         L.moe_tile_rows.restype = c_int32
+        L.moe_prefill_tile_rows.argtypes = [P(MoeDims), c_int32]
+        L.moe_prefill_tile_rows.restype = c_int32
         L.moe_route.argtypes = [P(MoeLayer), c_void_p, c_void_p, c_int32, P(RouteOut), c_void_p, c_size_t, c_void_p]
         L.moe_route.restype = ctypes.c_int
         L.moe_prefill.argtypes = [P(MoeLayer), c_void_p, c_int32, c_void_p, P(RouteOut), c_void_p, c_size_t,
@@ -130,7 +132,13 @@ def dims_of(shape) -> MoeDims:
 
 
 def tile_rows() -> int:
+    """The largest block-map tile height."""
     return int(lib().moe_tile_rows())
+
+
+def prefill_tile_rows(dims: MoeDims, T: int) -> int:
+    """Block-map tile height of a T-token route / prefill call (32 or tile_rows())."""
+    return int(lib().moe_prefill_tile_rows(ctypes.byref(dims), int(T)))
 
 
 def packed_bytes(dims: MoeDims) -> int:
@@ -190,7 +198,7 @@ class Layer:
 def route_out_tensors(dims: MoeDims, T: int, device, want=ROUTE_FIELDS, hidden: bool = False) -> dict:
     """Allocates the requested routing outputs (see moe_route_out in include/moe_gb300.h)."""
     E, k, A = dims.n_experts, dims.top_k, T * dims.top_k
-    max_tiles = min(E, A) + A // tile_rows()
+    max_tiles = min(E, A) + A // prefill_tile_rows(dims, T)
     shapes = {"logits": ((T, E), torch.float32), "topk_idx": ((T, k), torch.int32),
               "topk_w": ((T, k), torch.float32), "counts": ((E,), torch.int32),
               "offsets": ((E + 1,), torch.int32), "perm": ((A,), torch.int32), "inv_perm": ((A,), torch.int32),
@@ -249,6 +257,7 @@ def prefill(layer: Layer, x: torch.Tensor, ws: torch.Tensor, y: torch.Tensor | N
 
 
 PREFILL_ARM_HOST_ROUTING, PREFILL_ARM_TILE32, PREFILL_ARM_DENSE = 1, 2, 3
+PREFILL_ARM_WIDE_TILES, PREFILL_ARM_NARROW_TILES = 4, 5
 PREFILL_DIAG_READ_ONLY = 1
 
 
@@ -271,8 +280,9 @@ def ablation_aux_bytes(dims: MoeDims, arm: int) -> int:
 def prefill_ablation(layer: Layer, x: torch.Tensor, ws: torch.Tensor, arm: int,
                      y: torch.Tensor | None = None, aux: torch.Tensor | None = None) -> torch.Tensor:
     """moe_prefill_ablation: moe_prefill with the block map built on the host after a stream
-    synchronisation (arm 1), with 32-row block-map tiles (arm 2), or on weights expanded to fp16
-    into `aux` first (arm 3; aux of ablation_aux_bytes(dims, 3) bytes)."""
+    synchronisation (arm 1), with 32-row block-map tiles in the wide GEMM configuration (arm 2), on
+    weights expanded to fp16 into `aux` first (arm 3; aux of ablation_aux_bytes(dims, 3) bytes), or
+    with the wide (arm 4) or narrow (arm 5) GEMM configuration forced."""
     _check_dev(x, torch.int16, "x")
     y = y if y is not None else torch.empty_like(x)
     _check(lib().moe_prefill_ablation(ctypes.byref(layer.c), x.data_ptr(), x.shape[0], y.data_ptr(), int(arm),

@@ -199,7 +199,7 @@ RouteParams route_params(const moe_dims& d, const float* logits, int T, const Ws
 // scatter and block map. `yacc` non-NULL also zeroes the combine accumulator rows.
 // `x` non-NULL also writes its fp16 copy (the expert GEMMs' operand) into the workspace.
 int run_route(const moe_dims& d, const float* logits, int T, const Ws& w, float* yacc, const uint16_t* x,
-              cudaStream_t s, int tile_rows = kTileRows) {
+              cudaStream_t s, int tile_rows) {
   return launch_route(route_params(d, logits, T, w, yacc, x, tile_rows), s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -208,8 +208,8 @@ int run_route(const moe_dims& d, const float* logits, int T, const Ws& w, float*
 // the exclusive scan, the stable scatter and the block map exactly as the device kernels define
 // them and copies them back; then the fp16 rows are placed as usual.
 int run_route_host(const moe_dims& d, const float* logits, int T, const Ws& w, float* yacc, const uint16_t* x,
-                   cudaStream_t s) {
-  const RouteParams p = route_params(d, logits, T, w, yacc, x, kTileRows);
+                   cudaStream_t s, int tile_rows) {
+  const RouteParams p = route_params(d, logits, T, w, yacc, x, tile_rows);
   if (launch_route_topk(p, s) != cudaSuccess) return MOE_ERR_CUDA;
   const int E = d.n_experts, k = d.top_k, A = T * k;
   std::vector<int32_t> idx(A), counts(E, 0), offsets(E + 1, 0), perm(A), inv(A), tile_map, tile_row0;
@@ -231,8 +231,8 @@ int run_route_host(const moe_dims& d, const float* logits, int T, const Ws& w, f
     row_tw[pos] = make_int2(a / k, wbits);
   }
   for (int e = 0; e < E; ++e)
-    for (int r = 0; r < counts[e]; r += kTileRows) {
-      tile_map.insert(tile_map.end(), {e, r, std::min(kTileRows, counts[e] - r)});
+    for (int r = 0; r < counts[e]; r += tile_rows) {
+      tile_map.insert(tile_map.end(), {e, r, std::min(tile_rows, counts[e] - r)});
       tile_row0.push_back(offsets[e] + r);
     }
   const int32_t n_tiles = (int32_t)tile_row0.size();
@@ -284,7 +284,8 @@ int copy_route_out(const moe_dims& d, int T, const Ws& w, const moe_route_out* o
   st |= copy_out(o->offsets, w.base + w.L.offsets, (E + 1) * 4, s);
   st |= copy_out(o->perm, w.base + w.L.perm, A * 4, s);
   st |= copy_out(o->inv_perm, w.base + w.L.inv_perm, A * 4, s);
-  st |= copy_out(o->tile_map, w.base + w.L.tile_map, (size_t)max_routed_tiles(T, d.top_k, d.n_experts) * 12, s);
+  st |= copy_out(o->tile_map, w.base + w.L.tile_map,
+                 (size_t)max_routed_tiles(T, d.top_k, d.n_experts, prefill_tile_rows(d, T)) * 12, s);
   st |= copy_out(o->n_tiles, w.base + w.L.n_tiles, 4, s);
   return st ? MOE_ERR_CUDA : MOE_OK;
 }
@@ -365,6 +366,11 @@ int moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream) {
 
 int32_t moe_tile_rows(void) { return kTileRows; }
 
+int32_t moe_prefill_tile_rows(const moe_dims* dims, int32_t T) {
+  if (check_dims(dims) != MOE_OK || T < 1) return 0;
+  return prefill_tile_rows(*dims, T);
+}
+
 int moe_route(const moe_layer* layer, const uint16_t* x, const float* logits_in, int32_t T, moe_route_out* out,
               void* ws, size_t ws_bytes, moe_stream_t stream) {
   int st = check_layer(layer, logits_in == nullptr);
@@ -383,14 +389,15 @@ int moe_route(const moe_layer* layer, const uint16_t* x, const float* logits_in,
   } else if ((st = run_router_gemm(layer, x, T, w, stream))) {
     return st;
   }
-  if ((st = run_route(d, logits, T, w, nullptr, nullptr, stream))) return st;
+  if ((st = run_route(d, logits, T, w, nullptr, nullptr, stream, prefill_tile_rows(d, T)))) return st;
   return copy_route_out(d, T, w, out, stream);
 }
 
 // The prefill sequence. arm: 0 the product path; MOE_PREFILL_ARM_HOST_ROUTING the block map built
-// on the host after a synchronisation; MOE_PREFILL_ARM_TILE32 block-map tiles of 32 rows;
-// MOE_PREFILL_ARM_DENSE the selected experts' weights expanded into `aux` first; kArmReadProbe the
-// read-only probes in place of the two grouped GEMMs (y = 0).
+// on the host after a synchronisation; MOE_PREFILL_ARM_TILE32 block-map tiles of 32 rows for the
+// wide GEMM configuration; MOE_PREFILL_ARM_DENSE the selected experts' weights expanded into `aux`
+// first; MOE_PREFILL_ARM_WIDE_TILES / MOE_PREFILL_ARM_NARROW_TILES one GEMM configuration at any
+// T; kArmReadProbe the read-only probes in place of the two grouped GEMMs (y = 0).
 constexpr int kArmReadProbe = 100;
 
 static int prefill_impl(const moe_layer* layer, const uint16_t* x, int32_t T, uint16_t* y, moe_route_out* out,
@@ -413,18 +420,25 @@ static int prefill_impl(const moe_layer* layer, const uint16_t* x, int32_t T, ui
   if (record_event(events, 0, stream) != cudaSuccess) return MOE_ERR_CUDA;
   if ((st = run_router_gemm(layer, x, T, w, stream))) return st;
   if (record_event(events, 1, stream) != cudaSuccess) return MOE_ERR_CUDA;
-  const int tile_rows = arm == MOE_PREFILL_ARM_TILE32 ? kMinTileRows : kTileRows;
+  // block-map tile height and GEMM configuration: narrow (32-row tiles, deeper rings) while the
+  // experts average few rows, else wide (tiles of up to 192 rows)
+  const int tile_rows = arm == MOE_PREFILL_ARM_TILE32        ? kMinTileRows
+                        : arm == MOE_PREFILL_ARM_WIDE_TILES   ? kTileRows
+                        : arm == MOE_PREFILL_ARM_NARROW_TILES ? kNarrowTileRows
+                                                              : prefill_tile_rows(d, T);
+  const bool narrow = tile_rows == kNarrowTileRows && arm != MOE_PREFILL_ARM_TILE32 && arm != MOE_PREFILL_ARM_DENSE;
   if (arm == MOE_PREFILL_ARM_HOST_ROUTING) {
-    if ((st = run_route_host(d, w.at<float>(w.L.logits), T, w, yacc, x, stream))) return st;
+    if ((st = run_route_host(d, w.at<float>(w.L.logits), T, w, yacc, x, stream, tile_rows))) return st;
   } else if ((st = run_route(d, w.at<float>(w.L.logits), T, w, yacc, x, stream, tile_rows))) {
     return st;
   }
 
   // 3. gate|up grouped GEMM + SwiGLU -> hidden; 4. down grouped GEMM + weighted combine -> yacc
+  int mode_gu = narrow ? kModeGateUpNarrow : kModeGateUp, mode_dn = narrow ? kModeDownNarrow : kModeDown;
   GemmMaps x_maps, h_maps;
-  if (!make_gemm_rows(&x_maps, w.at<uint16_t>(w.L.x16), (uint64_t)A + T, d.d, gemm_kb_per_stage(kModeGateUp), true) ||
-      !make_gemm_planes(&h_maps, hidden, (uint64_t)A + T, d.inter, gemm_kb_per_stage(kModeDown)) ||
-      !make_down_weight_maps(&h_maps, static_cast<const uint8_t*>(layer->packed), P, d, gemm_kw_per_stage(kModeDown)))
+  if (!make_gemm_rows(&x_maps, w.at<uint16_t>(w.L.x16), (uint64_t)A + T, d.d, gemm_kb_per_stage(mode_gu), true) ||
+      !make_gemm_planes(&h_maps, hidden, (uint64_t)A + T, d.inter, gemm_kb_per_stage(mode_dn)) ||
+      !make_down_weight_maps(&h_maps, static_cast<const uint8_t*>(layer->packed), P, d, gemm_kw_per_stage(mode_dn)))
     return MOE_ERR_CUDA;
   GemmParams p = {};
   p.packed = static_cast<const uint8_t*>(layer->packed);
@@ -445,7 +459,6 @@ static int prefill_impl(const moe_layer* layer, const uint16_t* x, int32_t T, ui
   p.tile_rows = tile_rows;
   const int tiles = max_routed_tiles(T, d.top_k, d.n_experts, tile_rows) + (T + tile_rows - 1) / tile_rows;
 
-  int mode_gu = kModeGateUp, mode_dn = kModeDown;
   if (arm == MOE_PREFILL_ARM_DENSE) {  // expand the selected experts' weights, then dense GEMMs on them
     uint16_t* dgu = static_cast<uint16_t*>(aux);
     uint16_t* ddn = dgu + dense_gu_bytes(d) / 2;
@@ -502,7 +515,8 @@ size_t moe_prefill_ablation_aux_bytes(const moe_dims* dims, int arm) {
 
 int moe_prefill_ablation(const moe_layer* layer, const uint16_t* x, int32_t T, uint16_t* y, int arm, void* ws,
                          size_t ws_bytes, void* aux, size_t aux_bytes, moe_stream_t stream) {
-  if (arm != MOE_PREFILL_ARM_HOST_ROUTING && arm != MOE_PREFILL_ARM_TILE32 && arm != MOE_PREFILL_ARM_DENSE)
+  if (arm != MOE_PREFILL_ARM_HOST_ROUTING && arm != MOE_PREFILL_ARM_TILE32 && arm != MOE_PREFILL_ARM_DENSE &&
+      arm != MOE_PREFILL_ARM_WIDE_TILES && arm != MOE_PREFILL_ARM_NARROW_TILES)
     return MOE_ERR_INVALID_ARG;
   if (arm == MOE_PREFILL_ARM_DENSE) {
     int st = check_layer(layer, true);

@@ -59,8 +59,6 @@ constexpr int kWarpW = 0, kWarpB = 1, kWarpMMA = 2, kWarpDq0 = 3, kNumDqWarps = 
 constexpr int kWarpMMA2 = kWarpDq0 + kNumDqWarps;          // second MMA issuer (warp 11)
 constexpr int kWarpEpi0 = kWarpMMA2 + 1, kNumEpiWarps = 8;  // warps 12-19
 constexpr int kThreads = (kWarpEpi0 + kNumEpiWarps) * 32;  // 640
-constexpr int kDqThreads = kNumDqWarps * 32;               // 256
-constexpr int kEpiThreads = kNumEpiWarps * 32;             // 256
 constexpr int kATileBytes = kBlockRows * 128;              // 128 rows x 64 16-bit values
 
 // kIssuers: MMA-issuing warps (each takes a column range of the one accumulator); kSW / kSB: K
@@ -68,52 +66,74 @@ constexpr int kATileBytes = kBlockRows * 128;              // 128 rows x 64 16-b
 // rings; kStagesA: TMEM A stages (kAK = 2 K blocks each, matching the activation stages, so the
 // MMA warps wait and commit once per 2 K blocks); kWStage: bytes of one weight stage;
 // kPlanes: B operand planes per K block (down: leading and remainder fp16 parts of the hidden
-// rows); kRows: maximum tile rows (MMA N); kMRows: output rows of one work item.
+// rows); kRows: maximum tile rows (MMA N); kMRows: output rows of one work item; kAcc: TMEM
+// columns of one accumulator buffer.
 template <int MODE>
 struct Cfg;
 // kEpi: the work list and epilogue the mode shares (the dense ablation modes reuse the gate/up and
-// down ones; only their A operand differs).
+// down ones; only their A operand differs); kW: the packed-weight layout the producer copies and
+// the dequant warps read (kModeGateUp / kModeDown for the Q4 modes, else the mode itself).
 template <>
 struct Cfg<kModeGateUp> {
   static constexpr int kIssuers = 2, kSW = 4, kSB = 2, kStagesW = 3, kStagesB = 3, kStagesA = 2, kPlanes = 1;
-  static constexpr int kRows = kTileRows, kMRows = 64;             // 64 features: gate rows over up rows
-  static constexpr int kWStage = 2 * kSW * kGUQuarter;            // two row quarters x kSW blocks
+  static constexpr int kRows = kTileRows, kMRows = 64, kAcc = kRows;  // 64 features: gate rows over up rows
+  static constexpr int kWStage = 2 * kSW * kGUQuarter;               // two row quarters x kSW blocks
   static constexpr bool kFp16 = true, kQ4 = true;
-  static constexpr int kEpi = kModeGateUp;
+  static constexpr int kEpi = kModeGateUp, kW = kModeGateUp;
 };
 template <>
 struct Cfg<kModeDown> {
   static constexpr int kIssuers = 2, kSW = 2, kSB = 2, kStagesW = 3, kStagesB = 2, kStagesA = 2, kPlanes = 2;
-  static constexpr int kRows = kTileRows, kMRows = kBlockRows;
+  static constexpr int kRows = kTileRows, kMRows = kBlockRows, kAcc = kRows;
   static constexpr int kWStage = kSW * kBlockBytes;                // codes (2 kSW halves), then kSW sb
   static constexpr bool kFp16 = true, kQ4 = true;
-  static constexpr int kEpi = kModeDown;
+  static constexpr int kEpi = kModeDown, kW = kModeDown;
+};
+// Narrow tiles (at most 32 rows: a short prompt spread over many experts): accumulator buffers of
+// 64 columns, so every tile splits its K blocks over the two issuers, and the room the 192-row
+// operands took goes to deeper rings: 8 (gate/up) or 7 (down) weight stages of 18 KB in flight
+// per SM instead of 3 x 18 KB / 3 x 9 KB, and 6 dequantized A stages instead of 2.
+template <>
+struct Cfg<kModeGateUpNarrow> {
+  static constexpr int kIssuers = 2, kSW = 4, kSB = 2, kStagesW = 8, kStagesB = 6, kStagesA = 6, kPlanes = 1;
+  static constexpr int kRows = kNarrowTileRows, kMRows = 64, kAcc = 2 * kRows;
+  static constexpr int kWStage = 2 * kSW * kGUQuarter;
+  static constexpr bool kFp16 = true, kQ4 = true;
+  static constexpr int kEpi = kModeGateUp, kW = kModeGateUp;
+};
+template <>
+struct Cfg<kModeDownNarrow> {
+  static constexpr int kIssuers = 2, kSW = 4, kSB = 2, kStagesW = 7, kStagesB = 6, kStagesA = 6, kPlanes = 2;
+  static constexpr int kRows = kNarrowTileRows, kMRows = kBlockRows, kAcc = 2 * kRows;
+  static constexpr int kWStage = kSW * kBlockBytes;
+  static constexpr bool kFp16 = true, kQ4 = true;
+  static constexpr int kEpi = kModeDown, kW = kModeDown;
 };
 template <>
 struct Cfg<kModeRouter> {
   static constexpr int kIssuers = 1, kSW = 4, kSB = 4, kStagesW = 2, kStagesB = 2, kStagesA = 0, kPlanes = 1;
-  static constexpr int kRows = kRouterRows, kMRows = kBlockRows;
+  static constexpr int kRows = kRouterRows, kMRows = kBlockRows, kAcc = kRows;
   static constexpr int kWStage = kSW * kATileBytes;                // bf16 A tiles, read by the MMA
   static constexpr bool kFp16 = false, kQ4 = false;
-  static constexpr int kEpi = kModeRouter;
+  static constexpr int kEpi = kModeRouter, kW = kModeRouter;
 };
 // Materialised-dequantization ablation: fp16 weight tiles from the dense buffer, read by the MMA
 // from shared memory like the router's.
 template <>
 struct Cfg<kModeGateUpDense> {
   static constexpr int kIssuers = 2, kSW = 2, kSB = 2, kStagesW = 3, kStagesB = 2, kStagesA = 0, kPlanes = 1;
-  static constexpr int kRows = kTileRows, kMRows = 64;
+  static constexpr int kRows = kTileRows, kMRows = 64, kAcc = kRows;
   static constexpr int kWStage = kSW * kATileBytes;
   static constexpr bool kFp16 = true, kQ4 = false;
-  static constexpr int kEpi = kModeGateUp;
+  static constexpr int kEpi = kModeGateUp, kW = kModeGateUpDense;
 };
 template <>
 struct Cfg<kModeDownDense> {
   static constexpr int kIssuers = 2, kSW = 2, kSB = 1, kStagesW = 3, kStagesB = 2, kStagesA = 0, kPlanes = 2;
-  static constexpr int kRows = kTileRows, kMRows = kBlockRows;
+  static constexpr int kRows = kTileRows, kMRows = kBlockRows, kAcc = kRows;
   static constexpr int kWStage = kSW * kATileBytes;
   static constexpr bool kFp16 = true, kQ4 = false;
-  static constexpr int kEpi = kModeDown;
+  static constexpr int kEpi = kModeDown, kW = kModeDownDense;
 };
 
 constexpr int tmem_cols_for(int cols) {
@@ -127,7 +147,7 @@ template <int MODE>
 struct Smem {
   using C = Cfg<MODE>;
   static constexpr int kBStage = C::kSB * C::kPlanes * C::kRows * 128;  // [kb][plane][rows][128 B]
-  static constexpr int kAccCols = C::kRows;                             // one accumulator buffer
+  static constexpr int kAccCols = C::kAcc;                              // one accumulator buffer
   // TMEM columns: two accumulator buffers, then (Q4 modes) the A tiles, 32 columns per 128x64 tile
   static constexpr int kACol = 2 * kAccCols;
   static constexpr int kTmemNeed = kACol + C::kStagesA * kAK * 32;
@@ -142,6 +162,7 @@ struct Smem {
   static constexpr int x_off = b_off + C::kStagesB * kBStage;
   static constexpr int tok_off = x_off + kXBytes;
   static constexpr int wgt_off = tok_off + kNumEpiWarps * kListRows * 4;
+  static_assert(tok_off % 16 == 0 && kListRows % 16 == 0, "16-byte loads of a chunk's list entries");
   static constexpr int bar_off = wgt_off + kNumEpiWarps * kListRows * 4;
   // full/empty per ring stage, acc_full[2], acc_empty[2], xfull/xempty[pairs][slots]
   static constexpr int n_bars = 2 * (C::kStagesW + C::kStagesA + C::kStagesB) + 4 + 2 * kXPairs * kXSlots;
@@ -263,10 +284,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStagesW; ++s) {
       mbar_init(full_w(s), 1);
-      mbar_init(empty_w(s), RO ? 1 : C::kQ4 ? kDqThreads : C::kIssuers);
+      mbar_init(empty_w(s), RO ? 1 : C::kQ4 ? kNumDqWarps : C::kIssuers);
     }
     for (int s = 0; s < C::kStagesA; ++s) {
-      mbar_init(full_a(s), kDqThreads);
+      mbar_init(full_a(s), kNumDqWarps);
       mbar_init(empty_a(s), C::kIssuers);
     }
     for (int s = 0; s < C::kStagesB; ++s) {
@@ -275,12 +296,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(acc_full(b), C::kIssuers);
-      mbar_init(acc_empty(b), kEpiThreads);
+      mbar_init(acc_empty(b), kNumEpiWarps);
     }
     for (int pr = 0; pr < kXPairs; ++pr)
       for (int sl = 0; sl < kXSlots; ++sl) {
-        mbar_init(xfull(pr, sl), 32);
-        mbar_init(xempty(pr, sl), 32);
+        mbar_init(xfull(pr, sl), 1);
+        mbar_init(xempty(pr, sl), 1);
       }
     *s_abort = 0;
     fence_barrier_init();
@@ -290,8 +311,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   if (warp == kWarpB && lane < 12) prefetch_tmap(&maps.rows[lane]);
-  if (warp == kWarpW && lane == 0 && MODE != kModeGateUp) prefetch_tmap(&maps.a);
-  if (warp == kWarpW && lane == 1 && MODE == kModeDown) prefetch_tmap(&maps.a2);
+  if (warp == kWarpW && lane == 0 && C::kW != kModeGateUp) prefetch_tmap(&maps.a);
+  if (warp == kWarpW && lane == 1 && C::kW == kModeDown) prefetch_tmap(&maps.a2);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -326,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s = gw % C::kStagesW;
           if (!(ok = mbar_wait(empty_w(s), ((gw / C::kStagesW) & 1) ^ 1, s_abort))) break;
           const uint32_t dst = smem_u32(w_stage(s));
-          if (MODE == kModeGateUp) {
+          if (C::kW == kModeGateUp) {
             // features 64h..64h+63 = quarters 2(h%2), 2(h%2)+1 of block h/2; K blocks kb0.. of a
             // quarter are contiguous, 2304 bytes each (gate then up)
             const int nk = min(C::kSW, KB - kb0), m = it.m >> 1, q0 = 2 * (it.m & 1);
@@ -334,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int qq = 0; qq < 2; ++qq)
               tma_bulk_g2s(dst + qq * C::kSW * kGUQuarter, ebase + gu_offset(m, q0 + qq, kb0, KB), nk * kGUQuarter,
                            full_w(s));
-          } else if (MODE == kModeDown) {
+          } else if (C::kW == kModeDown) {
             // codes of (K block, half) pieces kb0*2 .. kb0*2+2kSW-1 of block m, then their scale/bias
             mbar_arrive_expect_tx(full_w(s), (uint32_t)C::kWStage);
             tma_load_4d(dst, &maps.a, 0, it.m, 2 * kb0, it.expert, full_w(s));
@@ -491,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int t = 0; t < kAK; ++t) {
               const int j = j0 + t;
-              if constexpr (MODE == kModeGateUp) {
+              if constexpr (C::kW == kModeGateUp) {
                 const uint8_t* src = ws + ((quad & 1) * C::kSW + j) * kGUQuarter + (quad >> 1) * kGUMat;
                 cw[t] = *reinterpret_cast<const uint4*>(src + part * kQuarterRows * 16 + lane * 16);
                 sbw[t] = *reinterpret_cast<const uint32_t*>(src + 2 * kQuarterRows * 16 + lane * 4);
@@ -516,17 +537,22 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               tmem_st16(a_tmem(tmem_base, sa) + lanes + t * 32 + part * 16, v);
             }
-            // The weight stage is released only once its codes have been consumed (the values
-            // above depend on them). Arriving right after issuing the shared-memory loads let the
-            // next TMA copy overwrite the stage before every load had read it: the copy is an
-            // async-proxy write, which the barrier's release does not order after generic reads.
-            if (j0 + kAK >= nk) mbar_arrive(empty_w(sw));
+            // The weight stage is released only once every lane's codes have been consumed (the
+            // values above depend on them). Arriving right after issuing the shared-memory loads
+            // let the next TMA copy overwrite the stage before every load had read it: the copy is
+            // an async-proxy write, which the barrier's release does not order after generic
+            // reads. Barriers count warps: lane 0 arrives after the warp has synchronised (one
+            // arrival instead of 32 on the same shared-memory word).
+            if (j0 + kAK >= nk) {
+              __syncwarp();
+              if (lane == 0) mbar_arrive(empty_w(sw));
+            }
             tmem_wait_st();
             tc_fence_before();
             // the MMA warp waits only on full_a: make it imply this stage's activation rows too
             if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(full_b(ga % C::kStagesB), (ga / C::kStagesB) & 1, s_abort))))
               break;
-            mbar_arrive(full_a(sa));
+            if (lane == 0) mbar_arrive(full_a(sa));  // the vote above synchronised the warp
           }
         }
       }
@@ -539,6 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;                          // TMEM lane quadrant this warp may access
     const int half = (warp - kWarpEpi0) >> 2;        // this warp takes 16-column chunks half, half+2, ...
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+    // down: this warp's rows in chunk order, as output-row offsets (token x d) and routing weights
     int32_t* tok = reinterpret_cast<int32_t*>(smem + S::tok_off) + (warp - kWarpEpi0) * S::kListRows;
     float* wgt = reinterpret_cast<float*>(smem + S::wgt_off) + (warp - kWarpEpi0) * S::kListRows;
     // gate/up: the gate-lane warp (quadrants 0, 1) and the up-lane warp (quadrants 2, 3) of the
@@ -571,7 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int j = lane + 32 * i;
           if (j < it.nrows && ((j >> 4) & 1) == half) {
             const int li = ((j >> 5) << 4) | (j & 15);  // position among this warp's rows
-            tok[li] = tw[i].x;
+            tok[li] = tw[i].x * p.d;
             wgt[li] = __int_as_float(tw[i].y);
           }
         }
@@ -600,13 +627,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(xempty(pr, sl), ((u >> 1) & 1) ^ 1, s_abort)))) break;
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) xs[jj * 32 + lane] = __uint_as_float(acc[jj]);
-            mbar_arrive(xfull(pr, sl));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(xfull(pr, sl));
           } else {
             if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(xfull(pr, sl), (u >> 1) & 1, s_abort)))) break;
             float up[16];
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) up[jj] = xs[jj * 32 + lane];
-            mbar_arrive(xempty(pr, sl));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(xempty(pr, sl));
             const int f = it.m * 64 + (q & 1) * 32 + lane;  // feature
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
@@ -625,26 +654,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           ++u;
+        } else if constexpr (C::kEpi == kModeDown) {
+          // the chunk's 16 rows sit at 16 consecutive list positions: their offsets and weights
+          // come in as four 16-byte shared loads each, and every value is one multiply and one
+          // fp32 reduction into its token's output row
+          float* yrow = p.yacc + it.m * kBlockRows + q * 32 + lane;  // output feature of this lane
+          const int L0 = (j0 >> 5) << 4, nv = it.nrows - j0;
+          const int4* ro4 = reinterpret_cast<const int4*>(tok + L0);
+          const float4* w4 = reinterpret_cast<const float4*>(wgt + L0);
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const int4 ro = ro4[g];
+            const float4 w = w4[g];
+            const int o[4] = {ro.x, ro.y, ro.z, ro.w};
+            const float wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (4 * g + e < nv) atomicAdd(yrow + o[e], __uint_as_float(acc[4 * g + e]) * wv[e]);
+          }
         } else {
-          const int orow = it.m * kBlockRows + q * 32 + lane;  // output row (feature / expert)
+          const int orow = it.m * kBlockRows + q * 32 + lane;  // output row (expert)
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) {
             const int j = j0 + jj;
-            if (j < it.nrows) {
-              const float v = __uint_as_float(acc[jj]);
-              if (C::kEpi == kModeDown) {
-                const int li = ((j >> 5) << 4) | jj;
-                atomicAdd(p.yacc + (size_t)tok[li] * p.d + orow, v * wgt[li]);
-              } else if (orow < p.E) {
-                p.logits[(size_t)(it.r0 + j) * p.E + orow] = v + (p.router_bias ? p.router_bias[orow] : 0.f);
-              }
-            }
+            if (j < it.nrows && orow < p.E)
+              p.logits[(size_t)(it.r0 + j) * p.E + orow] =
+                  __uint_as_float(acc[jj]) + (p.router_bias ? p.router_bias[orow] : 0.f);
           }
         }
       }
       if (!ok) break;
       tc_fence_before();
-      mbar_arrive(acc_empty(buf));  // the accumulator buffer is free again
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty(buf));  // the accumulator buffer is free again
     }
     if (C::kEpi == kModeGateUp && __any_sync(0xFFFFFFFFu, over) && lane == 0)
       set_device_status(p.hdr, MOE_ERR_OUT_OF_RANGE);
@@ -691,6 +733,8 @@ cudaError_t launch_gemm(int mode, const GemmParams& p, const GemmMaps* maps, int
     case kModeGateUp: return launch_mode<kModeGateUp>(p, maps, grid, s);
     case kModeGateUpDense: return launch_mode<kModeGateUpDense>(p, maps, grid, s);
     case kModeDownDense: return launch_mode<kModeDownDense>(p, maps, grid, s);
+    case kModeGateUpNarrow: return launch_mode<kModeGateUpNarrow>(p, maps, grid, s);
+    case kModeDownNarrow: return launch_mode<kModeDownNarrow>(p, maps, grid, s);
     default: return launch_mode<kModeDown>(p, maps, grid, s);
   }
 }
@@ -699,12 +743,21 @@ cudaError_t launch_gemm_read_probe(int mode, const GemmParams& p, const GemmMaps
   if (grid <= 0) return cudaSuccess;
   if (mode == kModeGateUp) return launch_mode<kModeGateUp, true>(p, maps, grid, s);
   if (mode == kModeDown) return launch_mode<kModeDown, true>(p, maps, grid, s);
+  if (mode == kModeGateUpNarrow) return launch_mode<kModeGateUpNarrow, true>(p, maps, grid, s);
+  if (mode == kModeDownNarrow) return launch_mode<kModeDownNarrow, true>(p, maps, grid, s);
   return cudaErrorInvalidValue;
 }
 
+template <int F, int MODE>
+int cfg_field() {
+  using C = Cfg<MODE>;
+  return F == 0 ? C::kSB : F == 1 ? C::kSW : C::kMRows;
+}
 template <int F>
 int cfg_value(int mode) {
   switch (mode) {
+    case kModeGateUpNarrow: return cfg_field<F, kModeGateUpNarrow>();
+    case kModeDownNarrow: return cfg_field<F, kModeDownNarrow>();
     case kModeRouter: return F == 0 ? Cfg<kModeRouter>::kSB : F == 1 ? Cfg<kModeRouter>::kSW : Cfg<kModeRouter>::kMRows;
     case kModeGateUp: return F == 0 ? Cfg<kModeGateUp>::kSB : F == 1 ? Cfg<kModeGateUp>::kSW : Cfg<kModeGateUp>::kMRows;
     case kModeGateUpDense:

@@ -44,6 +44,8 @@ constexpr int kGUQuarter = 2 * kGUMat;                             // 2304: gate
 constexpr int kSBBytes = kBlockRows * 4;                           // 512
 constexpr int kTileRows = 192;      // block-map tile height (max MMA N of the prefill GEMMs)
 constexpr int kMinTileRows = 32;    // smallest tile height a call may ask for (fixed-tile ablation)
+constexpr int kNarrowTileRows = 32; // tile height of the narrow GEMM configuration (few rows per expert)
+constexpr int kNarrowMaxAvgRows = 16;  // narrow configuration while T * k <= this * E
 constexpr int kMaxTopK = 16;
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTokens = 65536;
@@ -116,6 +118,12 @@ inline int max_routed_tiles(int T, int k, int E, int tile_rows = kTileRows) {
   return (int)((A < E ? A : E) + A / tile_rows);
 }
 
+// Block-map tile height of a T-token prefill (and of moe_route): the narrow GEMM configuration's
+// 32-row tiles while the experts average at most kNarrowMaxAvgRows rows, else tiles of up to 192.
+inline int prefill_tile_rows(const moe_dims& d, int T) {
+  return (long long)T * d.top_k <= (long long)kNarrowMaxAvgRows * d.n_experts ? kNarrowTileRows : kTileRows;
+}
+
 inline WsLayout ws_layout(const moe_dims& d, int T) {
   WsLayout L;
   const size_t A = (size_t)T * d.top_k, E = (size_t)d.n_experts;
@@ -177,7 +185,18 @@ struct RouteParams {
 // kModeGateUpDense / kModeDownDense: the materialised-dequantization ablation, the same GEMMs on
 // fp16 weights expanded beforehand into a dense buffer (gate/up: [E + 1][I / 64][128 rows: 64 gate
 // then the same 64 features' up][d]; down: [E + 1][d][I]).
-enum GemmMode { kModeRouter = 0, kModeGateUp = 1, kModeDown = 2, kModeGateUpDense = 3, kModeDownDense = 4 };
+// kModeGateUpNarrow / kModeDownNarrow: the same GEMMs for tiles of at most kNarrowTileRows rows,
+// with the shared memory and tensor memory the wide tiles' operands take given to deeper weight,
+// activation and dequantized-operand rings.
+enum GemmMode {
+  kModeRouter = 0,
+  kModeGateUp = 1,
+  kModeDown = 2,
+  kModeGateUpDense = 3,
+  kModeDownDense = 4,
+  kModeGateUpNarrow = 5,
+  kModeDownNarrow = 6
+};
 
 struct GemmParams {
   // weights
@@ -254,7 +273,7 @@ struct GemmMaps {
   CUtensorMap a, a2;
 };
 cudaError_t launch_gemm(int mode, const GemmParams& p, const GemmMaps* maps, int grid, cudaStream_t s);
-// The read-only probe of a gate/up or down GEMM (kModeGateUp / kModeDown): the same grid, work list,
+// The read-only probe of a gate/up or down GEMM (the Q4 modes): the same grid, work list,
 // weight and activation copies and ring depths, each stage released as soon as it lands; no
 // dequantization, MMA or epilogue (hidden and yacc are not written).
 cudaError_t launch_gemm_read_probe(int mode, const GemmParams& p, const GemmMaps* maps, int grid, cudaStream_t s);

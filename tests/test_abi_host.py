@@ -36,6 +36,13 @@ def test_host_queries(m):
     from synthetic import FULL, TINY
     full = m.dims_of(FULL)
     assert m.tile_rows() == 192
+    # block-map tile height by token count: 32-row tiles while T * k <= 16 * E
+    assert m.prefill_tile_rows(full, 1) == 32 and m.prefill_tile_rows(full, 512) == 32
+    assert m.prefill_tile_rows(full, 513) == 192 and m.prefill_tile_rows(full, 4096) == 192
+    tiny = m.dims_of(TINY)
+    lim = 16 * tiny.n_experts // tiny.top_k
+    assert m.prefill_tile_rows(tiny, lim) == 32 and m.prefill_tile_rows(tiny, lim + 1) == 192
+    assert m.prefill_tile_rows(full, 0) == 0
     assert m.packed_bytes(full) == 257 * 1769472          # (E + 1) experts x 3*I*d*(1/2 + 4/64) bytes
     assert m.packed_bytes(m.dims_of(TINY)) == 17 * 3 * 128 * 256 * 9 // 16
     assert m.workspace_bytes(full, 1) > 0
@@ -47,6 +54,7 @@ def test_host_queries(m):
         for k, v in bad.items():
             setattr(dims, k, v)
         assert m.packed_bytes(dims) == 0 and m.workspace_bytes(dims, 16) == 0, bad
+        assert m.prefill_tile_rows(dims, 16) == 0, bad
     for code in range(8):
         assert m.status_string(code) and m.status_string(code) != "unknown status"
 
@@ -93,7 +101,11 @@ def test_argument_errors_before_launch(m):
     abl = lambda x, T, arm, n, aux=None, na=0: lib.moe_prefill_ablation(  # noqa: E731
         ctypes.byref(layer), x, T, A, arm, A, n, aux, na, None)
     assert abl(A, 16, 0, ws_need) == 1                                    # unknown arm
-    assert abl(A, 16, 4, ws_need) == 1
+    assert abl(A, 16, 6, ws_need) == 1
+    diag = lambda T, mode, n: lib.moe_prefill_diag(ctypes.byref(layer), A, T, A, mode, A, n, None, None)  # noqa: E731
+    assert diag(16, 2, ws_need) == 1                                      # unknown mode
+    assert diag(16, 1, ws_need - 1) == 4                                  # workspace too small
+    assert diag(0, 1, ws_need) == 1
     assert abl(A, 16, 3, ws_need) == 1                                    # dense arm without its buffer
     aux_need = lib.moe_prefill_ablation_aux_bytes(ctypes.byref(dims), 3)
     assert aux_need == 257 * 3 * 512 * 2048 * 2                           # every expert's weights in fp16

@@ -93,7 +93,7 @@ def test_route_given_logits_bit_exact(m, shape, T, kind):
     logits = crafted_logits(T, shape.n_experts, kind, seed=T)
     gpu = run_route(m, layer, T, logits=logits)
     np.testing.assert_array_equal(gpu["logits"], logits)
-    C.check_routing_exact(gpu, logits, shape.n_experts, shape.top_k, m.tile_rows())
+    C.check_routing_exact(gpu, logits, shape.n_experts, shape.top_k, m.prefill_tile_rows(layer.dims, T))
 
 
 @pytest.mark.parametrize("shape", [MID, WIDE], ids=["E300k9", "E1024k16"])
@@ -113,7 +113,7 @@ def test_route_router_gemm(m, name):
     ref_logits = O.router_logits(x, npl["router_w"], npl["router_bias"])
     tol = C.logit_tolerance(x, npl["router_w"]) + 1e-6 * np.abs(ref_logits)
     assert np.all(np.abs(gpu["logits"].astype(np.float64) - ref_logits) <= tol)
-    C.check_routing_exact(gpu, gpu["logits"], shape.n_experts, shape.top_k, m.tile_rows())
+    C.check_routing_exact(gpu, gpu["logits"], shape.n_experts, shape.top_k, m.prefill_tile_rows(layer.dims, T))
     diff, ok = C.selection_with_near_ties(gpu["logits"], ref_logits, tol, shape.top_k)
     assert ok, f"tokens {diff} select different experts without a near tie"
 
@@ -168,7 +168,8 @@ def prefill_and_check(m, shape, T, seed=0, bias=None, npl=None, layer=None, hidd
     torch.cuda.synchronize()
     assert m.read_device_status(ws) == 0
     g = C.to_np(out)
-    C.check_routing_exact(g, g["logits"], shape.n_experts, shape.top_k, m.tile_rows())
+    R = m.prefill_tile_rows(layer.dims, T)
+    C.check_routing_exact(g, g["logits"], shape.n_experts, shape.top_k, R)
     ref_logits = O.router_logits(x, npl["router_w"], npl["router_bias"])
     tol = C.logit_tolerance(x, npl["router_w"]) + 1e-6 * np.abs(ref_logits)
     diff, ok = C.selection_with_near_ties(g["logits"], ref_logits, tol, shape.top_k)
@@ -179,7 +180,7 @@ def prefill_and_check(m, shape, T, seed=0, bias=None, npl=None, layer=None, hidd
         sel = np.take_along_axis(ref_logits.astype(np.float64), idx.astype(np.int64), axis=1)
         w = np.exp(sel - sel.max(1, keepdims=True))
         routing = (idx, w / w.sum(1, keepdims=True))
-    ref = O.moe_forward(x, npl, tile_rows=m.tile_rows(), routing=routing)
+    ref = O.moe_forward(x, npl, tile_rows=R, routing=routing)
     stats = C.check_y(y, ref["y"])
     print(f"prefill T={T}: {stats}")
     if hidden:
@@ -216,16 +217,20 @@ def test_prefill_full_skew_2048(m):
 
 
 def test_prefill_forced_tile_edges(m):
-    """Every token picks experts 0..k-1: each gets T rows (whole tiles, then a ragged tail)."""
+    """Every token picks experts 0..k-1: each gets T rows (whole tiles, then a ragged tail), in
+    the narrow configuration (384 and 385 tokens: 12 tiles of 32 rows, then one of 1) and in the
+    wide one (576 and 577 tokens: 3 tiles of 192 rows, then one of 1)."""
     shape = FULL
     npl = dict(_np_layer(shape, 3, None))
     rb = np.zeros(shape.n_experts, dtype=np.float32)
     rb[: shape.top_k] = 100.0
     npl["router_bias"] = rb
     layer = m.upload_layer(npl)
-    for T in (2 * m.tile_rows(), 2 * m.tile_rows() + 1):
+    for T, R in ((384, 32), (385, 32), (576, m.tile_rows()), (577, m.tile_rows())):
+        assert m.prefill_tile_rows(layer.dims, T) == R
         _, g = prefill_and_check(m, shape, T, seed=3, npl=npl, layer=layer)
         assert np.all(g["counts"][: shape.top_k] == T)
+        assert int(g["n_tiles"][0]) == shape.top_k * -(-T // R)
 
 
 def integer_layer(shape, seed, force_top=False):
@@ -256,14 +261,17 @@ def sparse_sign_tokens(T, d, nnz, seed):
     return (x.view(np.uint32) >> 16).astype(np.uint16)
 
 
-@pytest.mark.parametrize("T,force_top", [(600, False), (400, True)], ids=["narrow_tiles", "wide_tiles"])
+@pytest.mark.parametrize("T,force_top", [(600, False), (592, True), (300, False), (400, True)],
+                         ids=["wide_cfg_short_tiles", "wide_cfg_192", "narrow_cfg", "narrow_cfg_forced"])
 def test_prefill_integer_weights_exact_hidden(m, T, force_top):
     """Integer-valued case of the expert GEMMs: g and u are exact integers on both sides whatever
-    the order of the K sums (narrow tiles split K over the two MMA issuers, wide tiles split
-    rows: 600 tokens give ~19 rows per expert; forcing every token onto experts 0..k-1 gives
-    tiles of 192 rows and a ragged 16). The SwiGLU rows must then equal the oracle's up to the
-    rounding of silu and of the fp16 pair: 1e-5 relative + 1e-7 absolute, where one unit of
-    error in g or u moves h by at least ~1/|g| > 1e-3 relative."""
+    the order of the K sums (tiles of at most half an accumulator buffer split K over the two MMA
+    issuers, taller tiles split rows). Wide configuration: 600 tokens give ~19 rows per expert;
+    592 tokens forced onto experts 0..k-1 give tiles of 192 rows and a ragged 16. Narrow
+    configuration (32-row tiles): 300 tokens (~9 rows per expert), and 400 tokens forced onto
+    experts 0..k-1 (12 tiles of 32 and a ragged 16). The SwiGLU rows must then equal the oracle's
+    up to the rounding of silu and of the fp16 pair: 1e-5 relative + 1e-7 absolute, where one unit
+    of error in g or u moves h by at least ~1/|g| > 1e-3 relative."""
     shape = FULL
     npl = integer_layer(shape, 21, force_top)
     layer = m.upload_layer(npl)
@@ -274,10 +282,12 @@ def test_prefill_integer_weights_exact_hidden(m, T, force_top):
     torch.cuda.synchronize()
     assert m.read_device_status(ws) == 0
     g = C.to_np({k: v for k, v in out.items() if k != "hidden"})
-    C.check_routing_exact(g, g["logits"], shape.n_experts, shape.top_k, m.tile_rows())
+    R = m.prefill_tile_rows(layer.dims, T)
+    assert R == (32 if T * shape.top_k <= 16 * shape.n_experts else m.tile_rows())
+    C.check_routing_exact(g, g["logits"], shape.n_experts, shape.top_k, R)
     if force_top:
         assert np.all(g["counts"][: shape.top_k] == T)
-    grouping = O.group_assignments(g["topk_idx"], shape.n_experts, m.tile_rows())
+    grouping = O.group_assignments(g["topk_idx"], shape.n_experts, R)
     H = O.hidden_sorted(x, npl, grouping)
     planes = out["hidden"].cpu().numpy().view(np.float16).astype(np.float64)
     err = np.abs(planes[0] + planes[1] - H)
@@ -362,7 +372,7 @@ def test_prefill_full_replays_identical(m):
     assert m.read_device_status(ws) == 0
 
 # ------------------------------------------------------------------------------ prefill ablation arms
-@pytest.mark.parametrize("arm", [1, 2, 3], ids=["host_routing", "tile32", "dense"])
+@pytest.mark.parametrize("arm", [1, 2, 3, 4, 5], ids=["host_routing", "tile32", "dense", "wide_cfg", "narrow_cfg"])
 @pytest.mark.parametrize("shape,T,bias", [(TINY, 300, None), (FULL, 512, None), (FULL, 2048, "zipf")],
                          ids=["tiny300", "full512", "skew2048"])
 def test_prefill_ablation_arms(m, arm, shape, T, bias):
