@@ -526,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int t = 0; t < kAK; ++t) {
               __half2 s2, b2;
-              sb_bad |= sb_out_of_range(sbw[t]);
+              if (part == 0) sb_bad |= sb_out_of_range(sbw[t]);  // each word once: both K halves read it
               scale_bias(sbw[t], s2, b2);
               const uint32_t words[4] = {cw[t].x, cw[t].y, cw[t].z, cw[t].w};
               uint32_t v[16];
