@@ -180,7 +180,7 @@ MOE_API int moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream);
 MOE_API int32_t moe_tile_rows(void);
 
 /* Block-map tile height of a T-token moe_route / moe_prefill call, so a checker can rebuild
- * tile_map: 32 while T * top_k <= 16 * n_experts (few rows per expert: the grouped GEMMs run
+ * tile_map: 32 while T * top_k <= 24 * n_experts (few rows per expert: the grouped GEMMs run
  * their narrow configuration, with deeper copy rings), else moe_tile_rows(). 0 for unsupported
  * dims or T < 1. */
 MOE_API int32_t moe_prefill_tile_rows(const moe_dims* dims, int32_t T);

@@ -63,8 +63,8 @@ constexpr int kATileBytes = kBlockRows * 128;              // 128 rows x 64 16-b
 
 // kIssuers: MMA-issuing warps (each takes a column range of the one accumulator); kSW / kSB: K
 // blocks per weight / activation stage; kStagesW / kStagesB: stages of the weight and activation
-// rings; kStagesA: TMEM A stages (kAK = 2 K blocks each, matching the activation stages, so the
-// MMA warps wait and commit once per 2 K blocks); kWStage: bytes of one weight stage;
+// rings; kStagesA: TMEM A stages (kAK K blocks each, matching the activation stages, so the MMA
+// warps wait and commit once per kAK K blocks); kWStage: bytes of one weight stage;
 // kPlanes: B operand planes per K block (down: leading and remainder fp16 parts of the hidden
 // rows); kRows: maximum tile rows (MMA N); kMRows: output rows of one work item; kAcc: TMEM
 // columns of one accumulator buffer.
@@ -76,7 +76,7 @@ struct Cfg;
 template <>
 struct Cfg<kModeGateUp> {
   static constexpr int kIssuers = 2, kSW = 4, kSB = 2, kStagesW = 3, kStagesB = 3, kStagesA = 2, kPlanes = 1;
-  static constexpr int kRows = kTileRows, kMRows = 64, kAcc = kRows;  // 64 features: gate rows over up rows
+  static constexpr int kRows = kTileRows, kMRows = 64, kAcc = kRows, kAK = 2;  // 64 features: gate over up rows
   static constexpr int kWStage = 2 * kSW * kGUQuarter;               // two row quarters x kSW blocks
   static constexpr bool kFp16 = true, kQ4 = true;
   static constexpr int kEpi = kModeGateUp, kW = kModeGateUp;
@@ -84,27 +84,28 @@ struct Cfg<kModeGateUp> {
 template <>
 struct Cfg<kModeDown> {
   static constexpr int kIssuers = 2, kSW = 2, kSB = 2, kStagesW = 3, kStagesB = 2, kStagesA = 2, kPlanes = 2;
-  static constexpr int kRows = kTileRows, kMRows = kBlockRows, kAcc = kRows;
+  static constexpr int kRows = kTileRows, kMRows = kBlockRows, kAcc = kRows, kAK = 2;
   static constexpr int kWStage = kSW * kBlockBytes;                // codes (2 kSW halves), then kSW sb
   static constexpr bool kFp16 = true, kQ4 = true;
   static constexpr int kEpi = kModeDown, kW = kModeDown;
 };
 // Narrow tiles (at most 32 rows: a short prompt spread over many experts): accumulator buffers of
 // 64 columns, so every tile splits its K blocks over the two issuers, and the room the 192-row
-// operands took goes to deeper rings: 8 (gate/up) or 7 (down) weight stages of 18 KB in flight
-// per SM instead of 3 x 18 KB / 3 x 9 KB, and 6 dequantized A stages instead of 2.
+// operands took goes to deeper rings and larger stages: 7 (gate/up) or 6 (down) weight stages of
+// 18 KB in flight per SM instead of 3 x 18 KB / 3 x 9 KB, and dequantized A stages of 4 K blocks
+// (half the barrier round trips per K block).
 template <>
 struct Cfg<kModeGateUpNarrow> {
-  static constexpr int kIssuers = 2, kSW = 4, kSB = 2, kStagesW = 8, kStagesB = 6, kStagesA = 6, kPlanes = 1;
-  static constexpr int kRows = kNarrowTileRows, kMRows = 64, kAcc = 2 * kRows;
+  static constexpr int kIssuers = 2, kSW = 4, kSB = 4, kStagesW = 7, kStagesB = 4, kStagesA = 3, kPlanes = 1;
+  static constexpr int kRows = kNarrowTileRows, kMRows = 64, kAcc = 2 * kRows, kAK = 4;
   static constexpr int kWStage = 2 * kSW * kGUQuarter;
   static constexpr bool kFp16 = true, kQ4 = true;
   static constexpr int kEpi = kModeGateUp, kW = kModeGateUp;
 };
 template <>
 struct Cfg<kModeDownNarrow> {
-  static constexpr int kIssuers = 2, kSW = 4, kSB = 2, kStagesW = 7, kStagesB = 6, kStagesA = 6, kPlanes = 2;
-  static constexpr int kRows = kNarrowTileRows, kMRows = kBlockRows, kAcc = 2 * kRows;
+  static constexpr int kIssuers = 2, kSW = 4, kSB = 4, kStagesW = 6, kStagesB = 3, kStagesA = 3, kPlanes = 2;
+  static constexpr int kRows = kNarrowTileRows, kMRows = kBlockRows, kAcc = 2 * kRows, kAK = 4;
   static constexpr int kWStage = kSW * kBlockBytes;
   static constexpr bool kFp16 = true, kQ4 = true;
   static constexpr int kEpi = kModeDown, kW = kModeDown;
@@ -112,7 +113,7 @@ struct Cfg<kModeDownNarrow> {
 template <>
 struct Cfg<kModeRouter> {
   static constexpr int kIssuers = 1, kSW = 4, kSB = 4, kStagesW = 2, kStagesB = 2, kStagesA = 0, kPlanes = 1;
-  static constexpr int kRows = kRouterRows, kMRows = kBlockRows, kAcc = kRows;
+  static constexpr int kRows = kRouterRows, kMRows = kBlockRows, kAcc = kRows, kAK = 2;
   static constexpr int kWStage = kSW * kATileBytes;                // bf16 A tiles, read by the MMA
   static constexpr bool kFp16 = false, kQ4 = false;
   static constexpr int kEpi = kModeRouter, kW = kModeRouter;
@@ -122,7 +123,7 @@ struct Cfg<kModeRouter> {
 template <>
 struct Cfg<kModeGateUpDense> {
   static constexpr int kIssuers = 2, kSW = 2, kSB = 2, kStagesW = 3, kStagesB = 2, kStagesA = 0, kPlanes = 1;
-  static constexpr int kRows = kTileRows, kMRows = 64, kAcc = kRows;
+  static constexpr int kRows = kTileRows, kMRows = 64, kAcc = kRows, kAK = 2;
   static constexpr int kWStage = kSW * kATileBytes;
   static constexpr bool kFp16 = true, kQ4 = false;
   static constexpr int kEpi = kModeGateUp, kW = kModeGateUpDense;
@@ -130,7 +131,7 @@ struct Cfg<kModeGateUpDense> {
 template <>
 struct Cfg<kModeDownDense> {
   static constexpr int kIssuers = 2, kSW = 2, kSB = 1, kStagesW = 3, kStagesB = 2, kStagesA = 0, kPlanes = 2;
-  static constexpr int kRows = kTileRows, kMRows = kBlockRows, kAcc = kRows;
+  static constexpr int kRows = kTileRows, kMRows = kBlockRows, kAcc = kRows, kAK = 2;
   static constexpr int kWStage = kSW * kATileBytes;
   static constexpr bool kFp16 = true, kQ4 = false;
   static constexpr int kEpi = kModeDown, kW = kModeDownDense;
@@ -141,7 +142,6 @@ constexpr int tmem_cols_for(int cols) {
 }
 
 constexpr int kXPairs = 4, kXSlots = 2;  // gate/up epilogue exchange: warp pairs x buffered chunks
-constexpr int kAK = 2;                   // K blocks per TMEM A stage (32 columns each)
 
 template <int MODE>
 struct Smem {
@@ -150,8 +150,9 @@ struct Smem {
   static constexpr int kAccCols = C::kAcc;                              // one accumulator buffer
   // TMEM columns: two accumulator buffers, then (Q4 modes) the A tiles, 32 columns per 128x64 tile
   static constexpr int kACol = 2 * kAccCols;
-  static constexpr int kTmemNeed = kACol + C::kStagesA * kAK * 32;
-  static_assert(!C::kQ4 || (C::kSB == kAK && C::kSW % kAK == 0), "A stages follow the activation stages");
+  static constexpr int kTmemNeed = kACol + C::kStagesA * C::kAK * 32;
+  static_assert(!C::kQ4 || (C::kSB == C::kAK && C::kSW % C::kAK == 0 && C::kStagesB >= C::kStagesA),
+                "A stages follow the activation stages");
   static constexpr int kTmemCols = tmem_cols_for(kTmemNeed);
   static_assert(kTmemNeed <= 512, "tensor memory budget");
   // down: each epilogue warp keeps the (token, weight) list of its own chunks (half the rows)
@@ -278,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + S::misc_off + 4);
   auto w_stage = [&](int s) { return smem + S::w_off + s * C::kWStage; };
   auto b_stage = [&](int s) { return base + S::b_off + s * S::kBStage; };
-  auto a_tmem = [&](uint32_t tbase, int stage) { return tbase + S::kACol + stage * kAK * 32; };
+  auto a_tmem = [&](uint32_t tbase, int stage) { return tbase + S::kACol + stage * C::kAK * 32; };
 
   // ---------------------------------------------------------------- set-up
   if (threadIdx.x == 0) {
@@ -427,12 +428,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int buf = n & 1;
         if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(acc_empty(buf), ((n >> 1) & 1) ^ 1, s_abort)))) break;
         tc_fence_after();
-        // A tile of at most half a buffer (96 rows) splits the K blocks instead of the rows:
-        // issuer i takes K block i of every stage over all of the tile's rows, into its own half of
-        // the buffer, and the epilogue adds the halves. Each tcgen05.mma costs its issuing thread
-        // tens of cycles however narrow the tile, so a narrow tile left to one issuer would bound
-        // the kernel (K blocks per stage: kSB = 2, and every K extent here is a multiple of 128).
-        const bool split_k = C::kIssuers == 2 && C::kSB == 2 && it.n16 <= S::kAccCols / 2;
+        // A tile of at most half a buffer splits the K blocks instead of the rows: issuer i takes
+        // the K blocks j of every stage with j % 2 == i over all of the tile's rows, into its own
+        // half of the buffer, and the epilogue adds the halves. Each tcgen05.mma costs its issuing
+        // thread tens of cycles however narrow the tile, so a narrow tile left to one issuer would
+        // bound the kernel (K blocks per stage: an even kSB; every K extent is a multiple of 128).
+        const bool split_k = C::kIssuers == 2 && C::kSB % 2 == 0 && it.n16 <= S::kAccCols / 2;
         const int half16 = C::kIssuers == 2 ? 16 * ((it.n16 / 16 + 1) / 2) : it.n16;
         const int c0 = split_k || issuer == 0 ? 0 : half16;
         const int ncols = split_k ? it.n16 : issuer == 0 ? half16 : it.n16 - half16;
@@ -457,8 +458,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            if (ncols > 0 && (!split_k || j == issuer)) {
-              const int kfirst = split_k ? s0 : kb;  // 0 on this issuer's first K block of the item
+            if (ncols > 0 && (!split_k || (j & 1) == issuer)) {
+              const int kfirst = split_k ? s0 + j - issuer : kb;  // 0 on this issuer's first K block
 #pragma unroll
               for (int ks = 0; ks < kGroup / 16; ++ks) {
 #pragma unroll
@@ -505,12 +506,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           // tcgen05.st is warp-collective: every lane takes the same exit on an abort
           if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(full_w(sw), (gw / C::kStagesW) & 1, s_abort)))) break;
           const uint8_t* ws = w_stage(sw);
-          for (int j0 = 0; j0 < nk; j0 += kAK, ++ga) {
+          for (int j0 = 0; j0 < nk; j0 += C::kAK, ++ga) {
             const int sa = ga % C::kStagesA;
-            uint4 cw[kAK];
-            uint32_t sbw[kAK];
+            uint4 cw[C::kAK];
+            uint32_t sbw[C::kAK];
 #pragma unroll
-            for (int t = 0; t < kAK; ++t) {
+            for (int t = 0; t < C::kAK; ++t) {  // a ragged last stage reads stale, unused blocks
               const int j = j0 + t;
               if constexpr (C::kW == kModeGateUp) {
                 const uint8_t* src = ws + ((quad & 1) * C::kSW + j) * kGUQuarter + (quad >> 1) * kGUMat;
@@ -524,9 +525,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(empty_a(sa), ((ga / C::kStagesA) & 1) ^ 1, s_abort)))) break;
             tc_fence_after();
 #pragma unroll
-            for (int t = 0; t < kAK; ++t) {
+            for (int t = 0; t < C::kAK; ++t) {
               __half2 s2, b2;
-              if (part == 0) sb_bad |= sb_out_of_range(sbw[t]);  // each word once: both K halves read it
+              if (part == 0 && j0 + t < nk) sb_bad |= sb_out_of_range(sbw[t]);  // once per word
               scale_bias(sbw[t], s2, b2);
               const uint32_t words[4] = {cw[t].x, cw[t].y, cw[t].z, cw[t].w};
               uint32_t v[16];
@@ -543,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // an async-proxy write, which the barrier's release does not order after generic
             // reads. Barriers count warps: lane 0 arrives after the warp has synchronised (one
             // arrival instead of 32 on the same shared-memory word).
-            if (j0 + kAK >= nk) {
+            if (j0 + C::kAK >= nk) {
               __syncwarp();
               if (lane == 0) mbar_arrive(empty_w(sw));
             }
@@ -608,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(acc_full(buf), (n >> 1) & 1, s_abort)))) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + lane_addr + buf * S::kAccCols;
-      const bool split_k = C::kIssuers == 2 && C::kSB == 2 && it.n16 <= S::kAccCols / 2;  // the MMA issuers' K split
+      const bool split_k = C::kIssuers == 2 && C::kSB % 2 == 0 && it.n16 <= S::kAccCols / 2;  // the issuers' K split
       for (int j0 = 16 * half; j0 < it.n16 && ok; j0 += 32) {
         uint32_t acc[16];
         tmem_ld16(taddr + j0, acc);

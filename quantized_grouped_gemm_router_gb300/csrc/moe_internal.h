@@ -45,7 +45,7 @@ constexpr int kSBBytes = kBlockRows * 4;                           // 512
 constexpr int kTileRows = 192;      // block-map tile height (max MMA N of the prefill GEMMs)
 constexpr int kMinTileRows = 32;    // smallest tile height a call may ask for (fixed-tile ablation)
 constexpr int kNarrowTileRows = 32; // tile height of the narrow GEMM configuration (few rows per expert)
-constexpr int kNarrowMaxAvgRows = 16;  // narrow configuration while T * k <= this * E
+constexpr int kNarrowMaxAvgRows = 24;  // narrow configuration while T * k <= this * E
 constexpr int kMaxTopK = 16;
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTokens = 65536;
