@@ -173,7 +173,7 @@ RouteParams route_params(const moe_dims& d, const float* logits, int T, const Ws
   p.topk_idx = w.at<int32_t>(w.L.topk_idx);
   p.topk_w = w.at<float>(w.L.topk_w);
   p.chunk_counts = w.at<int32_t>(w.L.chunk_counts);
-  p.chunk_base = w.at<int32_t>(w.L.chunk_base);
+  p.totals = w.at<int32_t>(w.L.totals);
   p.counts = w.at<int32_t>(w.L.counts);
   p.offsets = w.at<int32_t>(w.L.offsets);
   p.perm = w.at<int32_t>(w.L.perm);
@@ -192,6 +192,7 @@ RouteParams route_params(const moe_dims& d, const float* logits, int T, const Ws
   p.k = d.top_k;
   p.d = d.d;
   p.n_chunks = w.L.n_chunks;
+  p.chunk = w.L.chunk;
   return p;
 }
 

@@ -81,7 +81,15 @@ inline PackedLayout packed_layout(const moe_dims& d) {
 // The header words must be zero before the first use of a workspace; the kernels return the
 // counters to zero at the end of every call, and the status word is sticky until read.
 // ------------------------------------------------------------------------------------------
-constexpr int kRouteChunk = 64;     // tokens per routing chunk (one CTA of the top-k kernel)
+constexpr int kRouteChunk = 64;     // tokens per routing chunk (histogram / scatter CTA), at least
+constexpr int kMaxRouteChunks = 64; // chunks per call at most (a scatter CTA sums its predecessors' counts)
+
+// Tokens per routing chunk of a T-token call: 64, or more (a multiple of 64) so that a call has at
+// most kMaxRouteChunks chunks. Non-decreasing in T, so the workspace grows with the token count.
+inline int route_chunk_tokens(int T) {
+  const int per = (T + kMaxRouteChunks - 1) / kMaxRouteChunks;
+  return per <= kRouteChunk ? kRouteChunk : (per + kRouteChunk - 1) / kRouteChunk * kRouteChunk;
+}
 
 struct WsHeader {
   int status;        // sticky device status (moe_status codes ORed as bits 1 << code)
@@ -91,9 +99,9 @@ struct WsHeader {
 static_assert(sizeof(WsHeader) == 256, "header size");
 
 struct WsLayout {
-  size_t header, logits, topk_idx, topk_w, chunk_counts, chunk_base, counts, offsets, perm,
+  size_t header, logits, topk_idx, topk_w, chunk_counts, totals, counts, offsets, perm,
       inv_perm, row_tw, tile_map, tile_row0, n_tiles, x16, hidden, yacc, dec_part, total;
-  int n_chunks, max_tiles;
+  int n_chunks, chunk, max_tiles;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -127,7 +135,8 @@ inline int prefill_tile_rows(const moe_dims& d, int T) {
 inline WsLayout ws_layout(const moe_dims& d, int T) {
   WsLayout L;
   const size_t A = (size_t)T * d.top_k, E = (size_t)d.n_experts;
-  L.n_chunks = (T + kRouteChunk - 1) / kRouteChunk;
+  L.chunk = route_chunk_tokens(T);
+  L.n_chunks = (T + L.chunk - 1) / L.chunk;
   L.max_tiles = max_routed_tiles(T, d.top_k, d.n_experts, kMinTileRows);  // room for any tile height
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t r = o; o = align256(o + bytes); return r; };
@@ -136,7 +145,7 @@ inline WsLayout ws_layout(const moe_dims& d, int T) {
   L.topk_idx = take(A * 4);
   L.topk_w = take(A * 4 + (A + 1) * 4);  // + the batch decode's distinct-expert list
   L.chunk_counts = take((size_t)L.n_chunks * E * 4);
-  L.chunk_base = take((size_t)L.n_chunks * E * 4);
+  L.totals = take(E * 4);
   L.counts = take(E * 4);
   L.offsets = take((E + 1) * 4);
   L.perm = take(A * 4);
@@ -164,7 +173,7 @@ struct RouteParams {
   int32_t* topk_idx;     // [T, k]
   float* topk_w;         // [T, k]
   int32_t* chunk_counts; // [n_chunks, E]
-  int32_t* chunk_base;   // [n_chunks, E]
+  int32_t* totals;       // [E] assignments per expert, summed over the chunks (zeroed by the top-k kernel)
   int32_t* counts;       // [E]
   int32_t* offsets;      // [E + 1]
   int32_t* perm;         // [A]
@@ -179,7 +188,7 @@ struct RouteParams {
   uint16_t* x16;         // [A + T, d] fp16 x: rows A.. in token order (top-k kernel), rows 0..A-1 in
                          // expert-sorted order (row gather after the scatter)
   WsHeader* hdr;
-  int T, E, k, d, n_chunks;
+  int T, E, k, d, n_chunks, chunk;  // chunk: tokens per routing chunk
 };
 
 // kModeGateUpDense / kModeDownDense: the materialised-dequantization ablation, the same GEMMs on

@@ -5,10 +5,11 @@
 //   route_topk_kernel    16 tokens per CTA: warp top-k on order-preserving logit keys (ties to
 //                        the lower index), renormalised softmax weights; the fp16 copy of x and
 //                        the zeroing of the combine accumulator rows
-//   route_hist_kernel    one CTA per 64-token chunk: histogram in shared memory; the last CTA to
-//                        finish (ticket) scans the chunk histograms into counts, offsets,
-//                        per-chunk bases and the tile block map
-//   route_scatter_kernel one CTA per chunk: stable placement of the chunk's assignments (per-warp
+//   route_hist_kernel    one CTA per chunk (64 tokens, more above 4096 tokens): histogram in shared
+//                        memory, added into the per-expert totals; the last CTA to finish (ticket)
+//                        scans the totals into counts, offsets and the tile block map
+//   route_scatter_kernel one CTA per chunk: the chunk's base inside each expert (the earlier chunks'
+//                        counts summed), then stable placement of its assignments (per-warp
 //                        histograms and a prefix in warp order, then in-warp ranks by
 //                        __match_any_sync; no global atomics)
 //   route_rows_kernel    (prefill) copies each assignment's fp16 token row to its sorted
@@ -24,7 +25,7 @@ namespace moe {
 namespace {
 
 constexpr int kTopkThreads = 256;
-constexpr int kTopkTokens = 16;   // tokens per CTA of the top-k kernel
+constexpr int kTopkTokens = 8;    // tokens per CTA of the top-k kernel: one per warp
 
 // Exclusive scan of up to 4*blockDim values held 4 per thread (v[0..3] are items 4t..4t+3).
 // Returns the exclusive prefix of item 4t; *total receives the sum of all items.
@@ -56,9 +57,10 @@ __device__ int block_exclusive_scan4(const int (&v)[4], int* s_warp, int* total)
 }
 
 // The CTA's share of the fp16 copy of x and of the zeroing of the combine accumulator (wide grid:
-// this is the launch that moves the bytes), then the top-k of its kTopkTokens tokens (two per
-// warp). The copy goes first and keeps 8 loads in flight per thread, so the memory stream does not
-// wait for the (latency-bound) selections.
+// this is the launch that moves the bytes), then the top-k of its kTopkTokens tokens (one per
+// warp: a selection is a latency-bound chain, so every token gets its own warp and they all run
+// at once). The copy goes first and keeps 8 loads in flight per thread, so the memory stream does
+// not wait for the selections.
 __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const RouteParams p) {
   pdl_wait();
   pdl_launch_dependents();
@@ -96,6 +98,8 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const RoutePar
     }
     if (__any_sync(0xFFFFFFFFu, over) && lane == 0) set_device_status(p.hdr, MOE_ERR_OUT_OF_RANGE);
   }
+  if (blockIdx.x == 0)  // the histogram kernel adds every chunk into these
+    for (int e = tid; e < E; e += kTopkThreads) p.totals[e] = 0;
   if (p.yacc) {
     float4* yrow = reinterpret_cast<float4*>(p.yacc + (size_t)t_begin * p.d);
     for (int i = tid; i < 2 * n8; i += kTopkThreads) yrow[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -112,8 +116,9 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const RoutePar
   }
 }
 
-// Histogram of one kRouteChunk-token chunk in shared memory. The last CTA to finish (ticket)
-// turns the chunk histograms into counts, offsets, chunk bases and the tile block map.
+// Histogram of one p.chunk-token chunk in shared memory, kept per chunk (the scatter's bases) and
+// added into the per-expert totals. The last CTA to finish (ticket) turns the totals into counts,
+// offsets and the tile block map.
 __global__ void __launch_bounds__(kTopkThreads) route_hist_kernel(const RouteParams p) {
   __shared__ int s_counts[kMaxExperts];
   __shared__ int s_warp[32];
@@ -125,10 +130,14 @@ __global__ void __launch_bounds__(kTopkThreads) route_hist_kernel(const RoutePar
   const int E = p.E, k = p.k;
   for (int e = tid; e < E; e += blockDim.x) s_counts[e] = 0;
   __syncthreads();
-  const int a_begin = c * kRouteChunk * k, a_end = min(p.T, (c + 1) * kRouteChunk) * k;
+  const int a_begin = c * p.chunk * k, a_end = min(p.T, (c + 1) * p.chunk) * k;
   for (int a = a_begin + tid; a < a_end; a += blockDim.x) atomicAdd(&s_counts[p.topk_idx[a]], 1);
   __syncthreads();
-  for (int e = tid; e < E; e += blockDim.x) p.chunk_counts[(size_t)c * E + e] = s_counts[e];
+  for (int e = tid; e < E; e += blockDim.x) {
+    const int n = s_counts[e];
+    p.chunk_counts[(size_t)c * E + e] = n;
+    if (n) atomicAdd(p.totals + e, n);  // integer adds: the totals do not depend on their order
+  }
   __threadfence();
   __syncthreads();
   if (tid == 0) s_last = (atomicAdd(&p.hdr->ticket, 1u) == gridDim.x - 1);
@@ -136,23 +145,7 @@ __global__ void __launch_bounds__(kTopkThreads) route_hist_kernel(const RoutePar
   if (!s_last) return;
   __threadfence();
 
-  // Per expert, the running sum over the chunks (chunk bases) and the total. Thread t takes
-  // experts t, t + blockDim, ...; the chunk counts are read 16 at a time so their loads overlap.
-  for (int e = tid; e < E; e += blockDim.x) {
-    int run = 0;
-    for (int cc0 = 0; cc0 < p.n_chunks; cc0 += 16) {
-      int v[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) v[j] = cc0 + j < p.n_chunks ? __ldcg(p.chunk_counts + (size_t)(cc0 + j) * E + e) : 0;
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        if (cc0 + j < p.n_chunks) {
-          p.chunk_base[(size_t)(cc0 + j) * E + e] = run;  // position of chunk cc's first row inside expert e
-          run += v[j];
-        }
-    }
-    s_counts[e] = run;  // this CTA's own histogram is no longer needed
-  }
+  for (int e = tid; e < E; e += blockDim.x) s_counts[e] = __ldcg(p.totals + e);  // own histogram done
   __syncthreads();
   int cnt[4], tiles[4];
 #pragma unroll
@@ -204,8 +197,8 @@ __global__ void __launch_bounds__(kScatterWarps * 32) route_scatter_kernel(const
   const int E = p.E;
   for (int i = threadIdx.x; i < kScatterWarps * E; i += blockDim.x) s_run[i / E][i % E] = 0;
   __syncthreads();
-  const int a_begin = c * kRouteChunk * p.k;
-  const int a_end = min(p.T, (c + 1) * kRouteChunk) * p.k;
+  const int a_begin = c * p.chunk * p.k;
+  const int a_end = min(p.T, (c + 1) * p.chunk) * p.k;
   const int per = (a_end - a_begin + kScatterWarps - 1) / kScatterWarps;
   const int w_begin = min(a_end, a_begin + w * per), w_end = min(a_end, w_begin + per);
   const unsigned lt_mask = (1u << lane) - 1u;
@@ -221,7 +214,16 @@ __global__ void __launch_bounds__(kScatterWarps * 32) route_scatter_kernel(const
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int pos = p.offsets[e] + p.chunk_base[(size_t)c * E + e];
+    // the chunk's first position inside expert e: the earlier chunks' counts, 16 loads in flight
+    int base = 0;
+    for (int c0 = 0; c0 < c; c0 += 16) {
+      int v[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = c0 + j < c ? __ldcg(p.chunk_counts + (size_t)(c0 + j) * E + e) : 0;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) base += v[j];
+    }
+    int pos = p.offsets[e] + base;
 #pragma unroll
     for (int v = 0; v < kScatterWarps; ++v) {
       const int n = s_run[v][e];
