@@ -167,7 +167,7 @@ int copy_out(void* dst, const void* src, size_t bytes, cudaStream_t s) {
 }
 
 RouteParams route_params(const moe_dims& d, const float* logits, int T, const Ws& w, float* yacc, const uint16_t* x,
-                         int tile_rows) {
+                         int tile_rows, int ksplit) {
   RouteParams p;
   p.logits = logits;
   p.topk_idx = w.at<int32_t>(w.L.topk_idx);
@@ -183,6 +183,7 @@ RouteParams route_params(const moe_dims& d, const float* logits, int T, const Ws
   p.tile_row0 = w.at<int32_t>(w.L.tile_row0);
   p.n_tiles = w.at<int32_t>(w.L.n_tiles);
   p.tile_rows = tile_rows;
+  p.ksplit = ksplit;
   p.yacc = yacc;
   p.x = x;
   p.x16 = w.at<uint16_t>(w.L.x16);
@@ -199,9 +200,11 @@ RouteParams route_params(const moe_dims& d, const float* logits, int T, const Ws
 // Routing on top of logits already in the workspace (or caller-given): top-k, histogram, scan,
 // scatter and block map. `yacc` non-NULL also zeroes the combine accumulator rows.
 // `x` non-NULL also writes its fp16 copy (the expert GEMMs' operand) into the workspace.
+// ksplit: the router GEMM's K slices whose partial logits the top-k kernel sums (1: final logits).
 int run_route(const moe_dims& d, const float* logits, int T, const Ws& w, float* yacc, const uint16_t* x,
-              cudaStream_t s, int tile_rows) {
-  return launch_route(route_params(d, logits, T, w, yacc, x, tile_rows), s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+              cudaStream_t s, int tile_rows, int ksplit) {
+  return launch_route(route_params(d, logits, T, w, yacc, x, tile_rows, ksplit), s) == cudaSuccess ? MOE_OK
+                                                                                                  : MOE_ERR_CUDA;
 }
 
 // The host round trip the GPU-resident routing removes (ablation): after the top-k kernel, the
@@ -209,8 +212,8 @@ int run_route(const moe_dims& d, const float* logits, int T, const Ws& w, float*
 // the exclusive scan, the stable scatter and the block map exactly as the device kernels define
 // them and copies them back; then the fp16 rows are placed as usual.
 int run_route_host(const moe_dims& d, const float* logits, int T, const Ws& w, float* yacc, const uint16_t* x,
-                   cudaStream_t s, int tile_rows) {
-  const RouteParams p = route_params(d, logits, T, w, yacc, x, tile_rows);
+                   cudaStream_t s, int tile_rows, int ksplit) {
+  const RouteParams p = route_params(d, logits, T, w, yacc, x, tile_rows, ksplit);
   if (launch_route_topk(p, s) != cudaSuccess) return MOE_ERR_CUDA;
   const int E = d.n_experts, k = d.top_k, A = T * k;
   std::vector<int32_t> idx(A), counts(E, 0), offsets(E + 1, 0), perm(A), inv(A), tile_map, tile_row0;
@@ -259,7 +262,8 @@ int run_router_gemm(const moe_layer* L, const uint16_t* x, int T, const Ws& w, c
       !make_rows_map(&maps.a, L->router_w, d.n_experts, d.d, kBlockRows, gemm_kw_per_stage(kModeRouter), false))
     return MOE_ERR_CUDA;
   GemmParams p = {};
-  p.k_blocks = d.d / kGroup;
+  p.ksplit = router_split(d, T);
+  p.k_blocks = d.d / kGroup / p.ksplit;
   p.m_tiles = (d.n_experts + kBlockRows - 1) / kBlockRows;
   p.logits = w.at<float>(w.L.logits);
   p.router_bias = L->router_bias;
@@ -270,7 +274,7 @@ int run_router_gemm(const moe_layer* L, const uint16_t* x, int T, const Ws& w, c
   p.d = d.d;
   p.inter = d.inter;
   const int rt = router_tile_rows();
-  const int grid = ((T + rt - 1) / rt) * p.m_tiles;
+  const int grid = ((T + rt - 1) / rt) * p.m_tiles * p.ksplit;
   return launch_gemm(kModeRouter, p, &maps, grid, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -390,7 +394,9 @@ int moe_route(const moe_layer* layer, const uint16_t* x, const float* logits_in,
   } else if ((st = run_router_gemm(layer, x, T, w, stream))) {
     return st;
   }
-  if ((st = run_route(d, logits, T, w, nullptr, nullptr, stream, prefill_tile_rows(d, T)))) return st;
+  if ((st = run_route(d, logits, T, w, nullptr, nullptr, stream, prefill_tile_rows(d, T),
+                       logits_in ? 1 : router_split(d, T))))
+    return st;
   return copy_route_out(d, T, w, out, stream);
 }
 
@@ -429,8 +435,9 @@ static int prefill_impl(const moe_layer* layer, const uint16_t* x, int32_t T, ui
                                                               : prefill_tile_rows(d, T);
   const bool narrow = tile_rows == kNarrowTileRows && arm != MOE_PREFILL_ARM_TILE32 && arm != MOE_PREFILL_ARM_DENSE;
   if (arm == MOE_PREFILL_ARM_HOST_ROUTING) {
-    if ((st = run_route_host(d, w.at<float>(w.L.logits), T, w, yacc, x, stream, tile_rows))) return st;
-  } else if ((st = run_route(d, w.at<float>(w.L.logits), T, w, yacc, x, stream, tile_rows))) {
+    if ((st = run_route_host(d, w.at<float>(w.L.logits), T, w, yacc, x, stream, tile_rows, router_split(d, T))))
+      return st;
+  } else if ((st = run_route(d, w.at<float>(w.L.logits), T, w, yacc, x, stream, tile_rows, router_split(d, T)))) {
     return st;
   }
 

@@ -217,6 +217,7 @@ __device__ __forceinline__ void scale_bias(uint32_t sbw, __half2& s2, __half2& b
 // rows (gate/up: 64 features, stacked gate over up; down / router: 128 rows).
 struct Item {
   int expert, r0, nrows, row0, m, n16;
+  int ks, kbo;  // router: K slice and its first K block (0 otherwise)
   bool shared;
 };
 
@@ -227,8 +228,13 @@ __device__ __forceinline__ Item decode_item(const GemmParams& p, int item, int n
   it.m = item % p.m_tiles;
   it.shared = false;
   it.expert = 0;
-  if (MODE == kModeRouter) {
-    it.r0 = tile * kRouterRows;
+  it.ks = it.kbo = 0;
+  if (MODE == kModeRouter) {  // item = (token tile, m block, K slice), the slice fastest
+    const int rest = item / p.ksplit;
+    it.ks = item % p.ksplit;
+    it.kbo = it.ks * p.k_blocks;
+    it.m = rest % p.m_tiles;
+    it.r0 = rest / p.m_tiles * kRouterRows;
     it.nrows = min(kRouterRows, p.T - it.r0);
     it.row0 = it.r0;
   } else if (tile < n_routed) {
@@ -332,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     n_routed = *p.n_tiles;
     n_tile_total = n_routed + (p.T + p.tile_rows - 1) / p.tile_rows;  // routed tiles, then shared
   }
-  const int n_items = n_tile_total * p.m_tiles;
+  const int n_items = n_tile_total * p.m_tiles * (MODE == kModeRouter ? p.ksplit : 1);
 
   if (warp == kWarpW) {
     // ------------------------------------------------------------ weight producer
@@ -368,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                              : MODE == kModeGateUpDense ? (it.expert * p.m_tiles + it.m) * kBlockRows
                                                         : it.expert * p.d + it.m * kBlockRows;
             mbar_arrive_expect_tx(full_w(s), (uint32_t)C::kWStage);
-            tma_load_3d(dst, &maps.a, 0, row0, kb0, full_w(s));
+            tma_load_3d(dst, &maps.a, 0, row0, kb0 + it.kbo, full_w(s));
           }
         }
       }
@@ -393,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (C::kPlanes == 2)
             tma_load_4d(b_stage(s), map, 0, it.row0, 0, kb0, full_b(s));
           else
-            tma_load_3d(b_stage(s), map, 0, it.row0, kb0, full_b(s));
+            tma_load_3d(b_stage(s), map, 0, it.row0, kb0 + it.kbo, full_b(s));
         }
       }
     }
@@ -678,9 +684,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) {
             const int j = j0 + jj;
-            if (j < it.nrows && orow < p.E)
-              p.logits[(size_t)(it.r0 + j) * p.E + orow] =
-                  __uint_as_float(acc[jj]) + (p.router_bias ? p.router_bias[orow] : 0.f);
+            if (j < it.nrows && orow < p.E)  // K slice ks: its partial logits (the bias in slice 0)
+              p.logits[((size_t)it.ks * p.T + it.r0 + j) * p.E + orow] =
+                  __uint_as_float(acc[jj]) + (p.router_bias && it.ks == 0 ? p.router_bias[orow] : 0.f);
           }
         }
       }
@@ -773,5 +779,13 @@ int gemm_kw_per_stage(int mode) { return cfg_value<1>(mode); }
 int gemm_out_rows(int mode) { return cfg_value<2>(mode); }
 
 int router_tile_rows() { return kRouterRows; }
+
+int router_split(const moe_dims& d, int T) {
+  const int items = ((T + kRouterRows - 1) / kRouterRows) * ((d.n_experts + kBlockRows - 1) / kBlockRows);
+  const int kb = d.d / kGroup;
+  int s = 1;
+  while (s < kMaxRouterSplit && 2 * s * items <= num_sms() && kb % (2 * s * Cfg<kModeRouter>::kSW) == 0) s *= 2;
+  return s;
+}
 
 }  // namespace moe

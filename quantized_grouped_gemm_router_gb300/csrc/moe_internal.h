@@ -81,6 +81,7 @@ inline PackedLayout packed_layout(const moe_dims& d) {
 // The header words must be zero before the first use of a workspace; the kernels return the
 // counters to zero at the end of every call, and the status word is sticky until read.
 // ------------------------------------------------------------------------------------------
+constexpr int kMaxRouterSplit = 4;  // K slices of the prefill router GEMM at most (partial logits)
 constexpr int kRouteChunk = 64;     // tokens per routing chunk (histogram / scatter CTA), at least
 constexpr int kMaxRouteChunks = 64; // chunks per call at most (a scatter CTA sums its predecessors' counts)
 
@@ -141,7 +142,7 @@ inline WsLayout ws_layout(const moe_dims& d, int T) {
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t r = o; o = align256(o + bytes); return r; };
   L.header = take(sizeof(WsHeader));
-  L.logits = take((size_t)T * E * 4);
+  L.logits = take((size_t)kMaxRouterSplit * T * E * 4);  // [K slice][T][E]: slice 0 the logits
   L.topk_idx = take(A * 4);
   L.topk_w = take(A * 4 + (A + 1) * 4);  // + the batch decode's distinct-expert list
   L.chunk_counts = take((size_t)L.n_chunks * E * 4);
@@ -169,7 +170,8 @@ __host__ __device__ inline int status_bit(int code) { return 1 << code; }
 // Kernel parameter blocks
 // ------------------------------------------------------------------------------------------
 struct RouteParams {
-  const float* logits;   // [T, E] fp32 (computed or caller-given)
+  const float* logits;   // [T, E] fp32 (computed or caller-given); with ksplit > 1 the router's
+                         // K slices [ksplit][T][E], summed by the top-k kernel into slice 0
   int32_t* topk_idx;     // [T, k]
   float* topk_w;         // [T, k]
   int32_t* chunk_counts; // [n_chunks, E]
@@ -189,6 +191,7 @@ struct RouteParams {
                          // expert-sorted order (row gather after the scatter)
   WsHeader* hdr;
   int T, E, k, d, n_chunks, chunk;  // chunk: tokens per routing chunk
+  int ksplit;                        // router K slices: the top-k kernel sums their partial logits
 };
 
 // kModeGateUpDense / kModeDownDense: the materialised-dequantization ablation, the same GEMMs on
@@ -223,11 +226,12 @@ struct GemmParams {
   uint16_t* hidden;           // [2, A + T, I] fp16: leading part, then remainder (gate/up writes,
                               // down reads both planes via TMA)
   float* yacc;                // [T, d] fp32 combine accumulator (down)
-  float* logits;              // [T, E] (router)
+  float* logits;              // [ksplit][T][E] (router): partial logits per K slice
   const float* router_bias;   // [E] or NULL (router)
   WsHeader* hdr;
   int T, k, E, d, inter;
   int tile_rows;              // block-map tile height (shared-expert tiles use the same)
+  int ksplit;                 // router: K slices (k_blocks each); slice s writes logits + s * T * E
   int hidden_rows;            // A + T: row offset of the remainder plane of `hidden`
 };
 
@@ -289,6 +293,9 @@ cudaError_t launch_gemm_read_probe(int mode, const GemmParams& p, const GemmMaps
 int gemm_kb_per_stage(int mode);  // K blocks that one activation copy covers
 int gemm_kw_per_stage(int mode);  // K blocks that one weight stage covers
 int gemm_out_rows(int mode);      // output rows of one work item (gate/up: 64 features)
+// K slices of the prefill router GEMM for T tokens: more than one only while the token tiles
+// leave SMs idle (each slice a CTA of its own; the top-k kernel sums the partial logits).
+int router_split(const moe_dims& d, int T);
 cudaError_t launch_cast(const float* yacc, uint16_t* y, size_t n, cudaStream_t s);
 // mode: 0 the decode path; kDecodeDiagNoMath the same chain with the GEMV arithmetic deleted
 // (y = 0); kDecodeDiagReadOnly one kernel that copies every weight the layer reads, alone.

@@ -105,6 +105,28 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const RoutePar
     for (int i = tid; i < 2 * n8; i += kTopkThreads) yrow[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   for (int t = t_begin + warp; t < t_end; t += kTopkThreads / 32) {
+    if (p.ksplit > 1) {  // the router GEMM's K slices: their partial logits summed in slice order
+      float* row = const_cast<float*>(p.logits) + (size_t)t * E;
+      const size_t slice = (size_t)p.T * E;
+      for (int e0 = 0; e0 < E; e0 += 8 * 32) {  // 8 experts per lane, every slice's loads in flight
+        float v[kMaxRouterSplit][8];
+#pragma unroll
+        for (int s = 0; s < kMaxRouterSplit; ++s)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int e = e0 + lane + 32 * i;
+            v[s][i] = s < p.ksplit && e < E ? __ldcg(row + s * slice + e) : 0.f;
+          }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float a = v[0][i];
+#pragma unroll
+          for (int s = 1; s < kMaxRouterSplit; ++s) a += v[s][i];  // zero beyond ksplit: exact
+          if (e0 + lane + 32 * i < E) row[e0 + lane + 32 * i] = a;
+        }
+      }
+      __syncwarp();
+    }
     int my_e;
     float my_w;
     const bool bad = warp_topk_softmax(p.logits + (size_t)t * E, E, k, &my_e, &my_w);
