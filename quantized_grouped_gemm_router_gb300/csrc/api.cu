@@ -214,7 +214,7 @@ int run_route(const moe_dims& d, const float* logits, int T, const Ws& w, float*
 int run_route_host(const moe_dims& d, const float* logits, int T, const Ws& w, float* yacc, const uint16_t* x,
                    cudaStream_t s, int tile_rows, int ksplit) {
   const RouteParams p = route_params(d, logits, T, w, yacc, x, tile_rows, ksplit);
-  if (launch_route_topk(p, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_route_topk(p, s) != cudaSuccess || launch_route_streams(p, s) != cudaSuccess) return MOE_ERR_CUDA;
   const int E = d.n_experts, k = d.top_k, A = T * k;
   std::vector<int32_t> idx(A), counts(E, 0), offsets(E + 1, 0), perm(A), inv(A), tile_map, tile_row0;
   std::vector<float> wt(A);

@@ -268,8 +268,10 @@ size_t dense_dn_bytes(const moe_dims& d);
 cudaError_t launch_dense_dequant(const moe_dims& d, const uint8_t* packed, const int32_t* counts, uint16_t* dense_gu,
                                  uint16_t* dense_dn, cudaStream_t s);
 cudaError_t launch_route(const RouteParams& p, cudaStream_t s);        // all of the routing below
-cudaError_t launch_route_topk(const RouteParams& p, cudaStream_t s);   // top-k (+ fp16 x, zero Yacc)
+cudaError_t launch_route_topk(const RouteParams& p, cudaStream_t s);   // top-k
 cudaError_t launch_route_group(const RouteParams& p, cudaStream_t s);  // histogram, scan, block map, scatter
+                                                                       // (+ fp16 x, zero Yacc)
+cudaError_t launch_route_streams(const RouteParams& p, cudaStream_t s);  // fp16 x, zero Yacc alone
 cudaError_t launch_route_rows(const RouteParams& p, cudaStream_t s);   // expert-sorted fp16 x rows
 // Tensor maps of the prefill GEMMs.
 //   rows[i]: the activation operand for tiles of 16 (i + 1) rows, box = 64 columns x 16 (i + 1)

@@ -2,16 +2,18 @@
 // one model", section "Prefill: keep routing on the GPU, dequantize in flight": after the top-8
 // selection, histogram, prefix scan, scatter and block map run on the GPU with no host round
 // trip). Three launches (four in prefill):
-//   route_topk_kernel    16 tokens per CTA: warp top-k on order-preserving logit keys (ties to
-//                        the lower index), renormalised softmax weights; the fp16 copy of x and
-//                        the zeroing of the combine accumulator rows
+//   route_topk_kernel    8 tokens per CTA, one per warp: top-k on order-preserving logit keys
+//                        (ties to the lower index), renormalised softmax weights (after summing
+//                        the router GEMM's K slices when it was split)
 //   route_hist_kernel    one CTA per chunk (64 tokens, more above 4096 tokens): histogram in shared
 //                        memory, added into the per-expert totals; the last CTA to finish (ticket)
-//                        scans the totals into counts, offsets and the tile block map
+//                        scans the totals into counts, offsets and the tile block map. In prefill
+//                        its extra CTAs make the fp16 copy of x meanwhile.
 //   route_scatter_kernel one CTA per chunk: the chunk's base inside each expert (the earlier chunks'
 //                        counts summed), then stable placement of its assignments (per-warp
 //                        histograms and a prefix in warp order, then in-warp ranks by
-//                        __match_any_sync; no global atomics)
+//                        __match_any_sync; no global atomics). In prefill its extra CTAs zero the
+//                        combine accumulator rows meanwhile.
 //   route_rows_kernel    (prefill) copies each assignment's fp16 token row to its sorted
 //                        position, so the grouped GEMM reads every tile as contiguous rows.
 #include <cuda_bf16.h>
@@ -56,11 +58,58 @@ __device__ int block_exclusive_scan4(const int (&v)[4], int* s_warp, int* total)
   return before_warp + incl - mine;
 }
 
-// The CTA's share of the fp16 copy of x and of the zeroing of the combine accumulator (wide grid:
-// this is the launch that moves the bytes), then the top-k of its kTopkTokens tokens (one per
-// warp: a selection is a latency-bound chain, so every token gets its own warp and they all run
-// at once). The copy goes first and keeps 8 loads in flight per thread, so the memory stream does
-// not wait for the selections.
+// Share `part` of `parts` of the fp16 copy of x (token order, the expert GEMMs' operand; exact
+// inside the fp16 range, anything beyond it is reported): 8 loads in flight per thread.
+__device__ void copy_x16_share(const RouteParams& p, int part, int parts) {
+  constexpr int kU = 8;
+  const int lane = threadIdx.x & 31;
+  const size_t n8 = (size_t)p.T * p.d / 8, step = (size_t)parts * blockDim.x;
+  const uint4* xs = reinterpret_cast<const uint4*>(p.x);
+  uint4* xd = reinterpret_cast<uint4*>(p.x16 + (size_t)p.T * p.k * p.d);
+  bool over = false;
+  for (size_t i0 = (size_t)part * blockDim.x + threadIdx.x; i0 < n8; i0 += kU * step) {
+    uint4 v[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const size_t i = i0 + u * step;
+      v[u] = i < n8 ? xs[i] : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const size_t i = i0 + u * step;
+      const uint32_t in[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float lo = __uint_as_float(in[j] << 16), hi = __uint_as_float(in[j] & 0xFFFF0000u);
+        over |= !(fabsf(lo) <= 65504.f) || !(fabsf(hi) <= 65504.f);
+        const __half2 h = __floats2half2_rn(lo, hi);
+        o[j] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      if (i < n8) xd[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+  if (__any_sync(0xFFFFFFFFu, over) && lane == 0) set_device_status(p.hdr, MOE_ERR_OUT_OF_RANGE);
+}
+
+// Share `part` of `parts` of the zeroing of the combine accumulator rows [T, d].
+__device__ void zero_yacc_share(const RouteParams& p, int part, int parts) {
+  const size_t n4 = (size_t)p.T * p.d / 4, step = (size_t)parts * blockDim.x;
+  float4* y = reinterpret_cast<float4*>(p.yacc);
+  for (size_t i = (size_t)part * blockDim.x + threadIdx.x; i < n4; i += step) y[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// Extra CTAs the histogram (fp16 copy of x) and scatter (accumulator zeroing) launches carry: the
+// two byte streams run beside those latency-bound kernels instead of in front of the selections.
+// One CTA per 64 KB written, two per SM at most.
+constexpr int kStreamCtas = 304;
+inline int stream_ctas(size_t bytes) {
+  const size_t n = (bytes + 65535) / 65536;
+  return (int)(n < 8 ? 8 : n > (size_t)kStreamCtas ? kStreamCtas : n);
+}
+
+// The top-k of the CTA's kTopkTokens tokens, one per warp: a selection is a latency-bound chain,
+// so every token gets its own warp and they all run at once.
 __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const RouteParams p) {
   pdl_wait();
   pdl_launch_dependents();
@@ -68,42 +117,8 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const RoutePar
   const int E = p.E, k = p.k;
   const int t_begin = blockIdx.x * kTopkTokens;
   const int t_end = min(p.T, t_begin + kTopkTokens);
-  const int n8 = (t_end - t_begin) * p.d / 8;  // 8-element chunks of this CTA's rows
-  if (p.x) {  // fp16 operand copy of x for the expert GEMMs (exact inside the fp16 range)
-    constexpr int kU = 8;
-    const uint4* xs = reinterpret_cast<const uint4*>(p.x + (size_t)t_begin * p.d);
-    uint4* xd = reinterpret_cast<uint4*>(p.x16 + ((size_t)p.T * p.k + t_begin) * p.d);
-    bool over = false;
-    for (int i0 = tid; i0 < n8; i0 += kU * kTopkThreads) {
-      uint4 v[kU];
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int i = i0 + u * kTopkThreads;
-        v[u] = i < n8 ? xs[i] : make_uint4(0u, 0u, 0u, 0u);
-      }
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int i = i0 + u * kTopkThreads;
-        const uint32_t in[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-        uint32_t o[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float lo = __uint_as_float(in[j] << 16), hi = __uint_as_float(in[j] & 0xFFFF0000u);
-          over |= !(fabsf(lo) <= 65504.f) || !(fabsf(hi) <= 65504.f);
-          const __half2 h = __floats2half2_rn(lo, hi);
-          o[j] = *reinterpret_cast<const uint32_t*>(&h);
-        }
-        if (i < n8) xd[i] = make_uint4(o[0], o[1], o[2], o[3]);
-      }
-    }
-    if (__any_sync(0xFFFFFFFFu, over) && lane == 0) set_device_status(p.hdr, MOE_ERR_OUT_OF_RANGE);
-  }
   if (blockIdx.x == 0)  // the histogram kernel adds every chunk into these
     for (int e = tid; e < E; e += kTopkThreads) p.totals[e] = 0;
-  if (p.yacc) {
-    float4* yrow = reinterpret_cast<float4*>(p.yacc + (size_t)t_begin * p.d);
-    for (int i = tid; i < 2 * n8; i += kTopkThreads) yrow[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
   for (int t = t_begin + warp; t < t_end; t += kTopkThreads / 32) {
     if (p.ksplit > 1) {  // the router GEMM's K slices: their partial logits summed in slice order
       float* row = const_cast<float*>(p.logits) + (size_t)t * E;
@@ -147,6 +162,10 @@ __global__ void __launch_bounds__(kTopkThreads) route_hist_kernel(const RoutePar
   __shared__ int s_last;
   pdl_wait();
   pdl_launch_dependents();
+  if ((int)blockIdx.x >= p.n_chunks) {  // a stream CTA: its share of the fp16 copy of x
+    copy_x16_share(p, blockIdx.x - p.n_chunks, gridDim.x - p.n_chunks);
+    return;
+  }
   const int tid = threadIdx.x;
   const int c = blockIdx.x;
   const int E = p.E, k = p.k;
@@ -162,7 +181,7 @@ __global__ void __launch_bounds__(kTopkThreads) route_hist_kernel(const RoutePar
   }
   __threadfence();
   __syncthreads();
-  if (tid == 0) s_last = (atomicAdd(&p.hdr->ticket, 1u) == gridDim.x - 1);
+  if (tid == 0) s_last = (atomicAdd(&p.hdr->ticket, 1u) == (unsigned)p.n_chunks - 1u);
   __syncthreads();
   if (!s_last) return;
   __threadfence();
@@ -214,6 +233,10 @@ __global__ void __launch_bounds__(kScatterWarps * 32) route_scatter_kernel(const
   __shared__ int s_run[kScatterWarps][kMaxExperts];  // counts, then first free positions
   pdl_wait();
   pdl_launch_dependents();
+  if ((int)blockIdx.x >= p.n_chunks) {  // a stream CTA: its share of the accumulator zeroing
+    zero_yacc_share(p, blockIdx.x - p.n_chunks, gridDim.x - p.n_chunks);
+    return;
+  }
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int c = blockIdx.x;
   const int E = p.E;
@@ -322,9 +345,29 @@ cudaError_t launch_route_topk(const RouteParams& p, cudaStream_t s) {
 }
 
 cudaError_t launch_route_group(const RouteParams& p, cudaStream_t s) {
-  cudaError_t err = launch_pdl(route_hist_kernel, p.n_chunks, kTopkThreads, 0, 1, s, p);
+  const size_t rows_bytes = (size_t)p.T * p.d * 2;  // fp16 copy; the accumulator takes twice that
+  cudaError_t err = launch_pdl(route_hist_kernel, p.n_chunks + (p.x ? stream_ctas(rows_bytes) : 0), kTopkThreads, 0, 1,
+                               s, p);
   if (err != cudaSuccess) return err;
-  return launch_pdl(route_scatter_kernel, p.n_chunks, kScatterWarps * 32, 0, 1, s, p);
+  return launch_pdl(route_scatter_kernel, p.n_chunks + (p.yacc ? stream_ctas(2 * rows_bytes) : 0),
+                    kScatterWarps * 32, 0, 1, s, p);
+}
+
+// The fp16 copy of x and the accumulator zeroing on their own (the host-routing ablation, whose
+// histogram and scatter run on the host).
+__global__ void __launch_bounds__(256) route_streams_kernel(const RouteParams p) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int half = gridDim.x / 2;
+  if ((int)blockIdx.x < half) {
+    if (p.x) copy_x16_share(p, blockIdx.x, half);
+  } else if (p.yacc) {
+    zero_yacc_share(p, blockIdx.x - half, gridDim.x - half);
+  }
+}
+
+cudaError_t launch_route_streams(const RouteParams& p, cudaStream_t s) {
+  return launch_pdl(route_streams_kernel, 2 * kStreamCtas, 256, 0, 1, s, p);
 }
 
 cudaError_t launch_route_rows(const RouteParams& p, cudaStream_t s) {
