@@ -516,6 +516,7 @@ def run_ours(args, config: dict) -> None:
         e2e = {"value": world * L * T * args.steps / (red["pre"] / 1e3) if T else None, "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": h2d,
                "decode_us_per_layer": 1e3 * red["dec"] / (args.steps * max(1, S * L)) if S else None,
+               "prefill_ms_per_step": getattr(W, "e2e_prefill_ms_per_step", None),
                "how": "prefill: per layer, pinned host x copied in on a copy stream, an eager moe_prefill call "
                       "through the Python binding on the compute stream once its input has landed, y copied "
                       "back on a second copy stream, so layer l's copies overlap the neighbouring layers' "
@@ -716,13 +717,29 @@ def end_to_end(W, args, e0, e1, e2):
     summed over args.steps steps. Prefill overlaps each layer's host copies with the neighbouring
     layers' compute (copy-in stream, compute stream, copy-out stream); decode copies all inputs in,
     runs the eager calls and copies all outputs back."""
+    import gc
     import torch
     L, T, S = args.layers, args.prefill_tokens, args.decode_steps
     compute = torch.cuda.current_stream()
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    # as timeit does: no garbage-collection pause of the enqueuing thread inside a timed step (the
+    # 10,240 eager decode calls of a step leave garbage behind that a collection would otherwise
+    # sweep while the next step's prefill calls are being enqueued, leaving the GPU idle)
+    gc.collect()
+    gc.disable()
+    try:
+        pre, dec = _end_to_end_steps(W, args, e0, e1, e2, compute, s_in, s_out, L, T, S)
+    finally:
+        gc.enable()
+    return pre, dec
+
+
+def _end_to_end_steps(W, args, e0, e1, e2, compute, s_in, s_out, L, T, S):
+    import torch
     ev_in = [torch.cuda.Event() for _ in range(L)]
     ev_done = [torch.cuda.Event() for _ in range(L)]
     pre = dec = 0.0
+    per_step = []
     for _ in range(args.steps):
         e0.record(compute)
         if T:
@@ -748,6 +765,8 @@ def end_to_end(W, args, e0, e1, e2):
         compute.synchronize()
         pre += e0.elapsed_time(e1)
         dec += e1.elapsed_time(e2)
+        per_step.append(round(e0.elapsed_time(e1), 2))
+    W.e2e_prefill_ms_per_step = per_step
     return pre, dec
 
 
