@@ -262,6 +262,8 @@ int run_router_gemm(const moe_layer* L, const uint16_t* x, int T, const Ws& w, c
       !make_rows_map(&maps.a, L->router_w, d.n_experts, d.d, kBlockRows, gemm_kw_per_stage(kModeRouter), false))
     return MOE_ERR_CUDA;
   GemmParams p = {};
+  p.b_kb = gemm_kb_per_stage(kModeRouter);
+  p.w_kb = gemm_kw_per_stage(kModeRouter);
   p.ksplit = router_split(d, T);
   p.k_blocks = d.d / kGroup / p.ksplit;
   p.m_tiles = (d.n_experts + kBlockRows - 1) / kBlockRows;
@@ -441,12 +443,17 @@ static int prefill_impl(const moe_layer* layer, const uint16_t* x, int32_t T, ui
     return st;
   }
 
-  // 3. gate|up grouped GEMM + SwiGLU -> hidden; 4. down grouped GEMM + weighted combine -> yacc
-  int mode_gu = narrow ? kModeGateUpNarrow : kModeGateUp, mode_dn = narrow ? kModeDownNarrow : kModeDown;
+  // 3. gate|up grouped GEMM + SwiGLU -> hidden; 4. down grouped GEMM + weighted combine -> yacc.
+  // Every tensor map is built with the stage sizes of the configuration that reads it (a box
+  // wider than the kernel's stage would overrun its shared memory; launch_gemm checks the match).
+  const bool dense = arm == MOE_PREFILL_ARM_DENSE;
+  const int mode_gu = dense ? kModeGateUpDense : narrow ? kModeGateUpNarrow : kModeGateUp;
+  const int mode_dn = dense ? kModeDownDense : narrow ? kModeDownNarrow : kModeDown;
   GemmMaps x_maps, h_maps;
   if (!make_gemm_rows(&x_maps, w.at<uint16_t>(w.L.x16), (uint64_t)A + T, d.d, gemm_kb_per_stage(mode_gu), true) ||
       !make_gemm_planes(&h_maps, hidden, (uint64_t)A + T, d.inter, gemm_kb_per_stage(mode_dn)) ||
-      !make_down_weight_maps(&h_maps, static_cast<const uint8_t*>(layer->packed), P, d, gemm_kw_per_stage(mode_dn)))
+      (!dense && !make_down_weight_maps(&h_maps, static_cast<const uint8_t*>(layer->packed), P, d,
+                                        gemm_kw_per_stage(mode_dn))))
     return MOE_ERR_CUDA;
   GemmParams p = {};
   p.packed = static_cast<const uint8_t*>(layer->packed);
@@ -465,15 +472,14 @@ static int prefill_impl(const moe_layer* layer, const uint16_t* x, int32_t T, ui
   p.inter = d.inter;
   p.hidden_rows = A + T;
   p.tile_rows = tile_rows;
+  p.b_kb = gemm_kb_per_stage(mode_gu);
+  p.w_kb = gemm_kw_per_stage(mode_gu);
   const int tiles = max_routed_tiles(T, d.top_k, d.n_experts, tile_rows) + (T + tile_rows - 1) / tile_rows;
 
-  if (arm == MOE_PREFILL_ARM_DENSE) {  // expand the selected experts' weights, then dense GEMMs on them
+  if (dense) {  // expand the selected experts' weights, then dense GEMMs on them
     uint16_t* dgu = static_cast<uint16_t*>(aux);
     uint16_t* ddn = dgu + dense_gu_bytes(d) / 2;
-    mode_gu = kModeGateUpDense;
-    mode_dn = kModeDownDense;
     if (launch_dense_dequant(d, p.packed, w.at<int32_t>(w.L.counts), dgu, ddn, stream) != cudaSuccess ||
-        !make_gemm_planes(&h_maps, hidden, (uint64_t)A + T, d.inter, gemm_kb_per_stage(kModeDownDense)) ||
         !make_rows_map(&x_maps.a, dgu, (uint64_t)(d.n_experts + 1) * 2 * d.inter, d.d, kBlockRows,
                        gemm_kw_per_stage(kModeGateUpDense), true) ||
         !make_rows_map(&h_maps.a, ddn, (uint64_t)(d.n_experts + 1) * d.d, d.inter, kBlockRows,
@@ -492,6 +498,8 @@ static int prefill_impl(const moe_layer* layer, const uint16_t* x, int32_t T, ui
   p.region_offset = P.gu_bytes;
   p.m_tiles = d.d / kBlockRows;
   p.k_blocks = d.inter / kGroup;
+  p.b_kb = gemm_kb_per_stage(mode_dn);
+  p.w_kb = gemm_kw_per_stage(mode_dn);
   if (record_event(events, 3, stream) != cudaSuccess) return MOE_ERR_CUDA;
   if ((probe ? launch_gemm_read_probe(mode_dn, p, &h_maps, tiles * p.m_tiles, stream)
              : launch_gemm(mode_dn, p, &h_maps, tiles * p.m_tiles, stream)) != cudaSuccess)

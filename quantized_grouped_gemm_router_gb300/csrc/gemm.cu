@@ -722,6 +722,8 @@ int num_sms() {
 
 template <int MODE, bool RO = false>
 cudaError_t launch_mode(const GemmParams& p, const GemmMaps* maps, int max_items, cudaStream_t s) {
+  // the maps' boxes must be the stages this configuration's shared memory holds
+  if (p.b_kb != Cfg<MODE>::kSB || p.w_kb != Cfg<MODE>::kSW) return cudaErrorInvalidValue;
   static cudaError_t attr = cudaFuncSetAttribute(moe_gemm_kernel<MODE, RO>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<MODE>::alloc);
   if (attr != cudaSuccess) return attr;

@@ -232,6 +232,8 @@ struct GemmParams {
   int T, k, E, d, inter;
   int tile_rows;              // block-map tile height (shared-expert tiles use the same)
   int ksplit;                 // router: K slices (k_blocks each); slice s writes logits + s * T * E
+  int b_kb, w_kb;             // K blocks per box of the activation / weight tensor maps (launch_gemm
+                              // refuses a launch whose maps do not match the mode's stages)
   int hidden_rows;            // A + T: row offset of the remainder plane of `hidden`
 };
 

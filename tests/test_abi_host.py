@@ -35,13 +35,14 @@ def test_exports_every_declared_symbol(m):
 def test_host_queries(m):
     from synthetic import FULL, TINY
     full = m.dims_of(FULL)
-    assert m.tile_rows() == 192
+    R = m.tile_rows()
+    assert R == 192
     # block-map tile height by token count: 32-row tiles while T * k <= 24 * E
     assert m.prefill_tile_rows(full, 1) == 32 and m.prefill_tile_rows(full, 768) == 32
-    assert m.prefill_tile_rows(full, 769) == 192 and m.prefill_tile_rows(full, 4096) == 192
+    assert m.prefill_tile_rows(full, 769) == R and m.prefill_tile_rows(full, 4096) == R
     tiny = m.dims_of(TINY)
     lim = 24 * tiny.n_experts // tiny.top_k
-    assert m.prefill_tile_rows(tiny, lim) == 32 and m.prefill_tile_rows(tiny, lim + 1) == 192
+    assert m.prefill_tile_rows(tiny, lim) == 32 and m.prefill_tile_rows(tiny, lim + 1) == R
     assert m.prefill_tile_rows(full, 0) == 0
     assert m.packed_bytes(full) == 257 * 1769472          # (E + 1) experts x 3*I*d*(1/2 + 4/64) bytes
     assert m.packed_bytes(m.dims_of(TINY)) == 17 * 3 * 128 * 256 * 9 // 16
