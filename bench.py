@@ -789,8 +789,11 @@ def config_results(W, peaks: dict, reps: int = 8) -> dict:
       skew2048    2048-token prefill with the Zipf router bias (a few experts with hundreds of rows,
                   most with few or none), eight layers rotated: tensor fraction of the grouped
                   gate/up + down GEMMs (the target the pages' design is held to) and of the layer.
-    Kernel times come from events recorded by the library at its kernel boundaries inside a CUDA
-    graph (the timed launch configuration). Peaks: the burst figures (kernels timed alone)."""
+    Layer times come from a CUDA graph of the plain calls (the timed launch configuration, best of
+    3 replays); kernel times from events recorded by the library at its kernel boundaries in a
+    second graph, where each event node also stops the PDL overlap of the kernels around it (so
+    the kernel times and their sum, `layer_with_events`, are upper bounds). Peaks: the burst
+    figures (kernels timed alone)."""
     import numpy as np
     import torch
     from synthetic import make_tokens, zipf_router_bias
@@ -832,13 +835,20 @@ def config_results(W, peaks: dict, reps: int = 8) -> dict:
                 for i, layer in enumerate(layers):
                     m.prefill(layer, xs[i], ws, y=ys[i], events=evs[r][i])
         _graph_time_ms(body, reps=1, eager=False)
+
+        def plain():
+            for _ in range(reps):
+                for i, layer in enumerate(layers):
+                    m.prefill(layer, xs[i], ws, y=ys[i])
+        # the layer time without events: an event node between two kernels stops the PDL overlap
+        layer_us = 1e3 * _graph_time_ms(plain) / (reps * len(layers))
         abl = {}
         for arm in arms:
             abl[arm] = prefill_ablation_arm(m, arm, layers, xs, ys, ws, reps)
         names = ["router", "route", "gate_up", "down", "cast"]
         per = {n: statistics.mean(1e3 * e[j].elapsed_time(e[j + 1]) for row in evs for e in row)
                for j, n in enumerate(names)}
-        layer_us = statistics.mean(1e3 * e[0].elapsed_time(e[5]) for row in evs for e in row)
+        per["layer_with_events"] = statistics.mean(1e3 * e[0].elapsed_time(e[5]) for row in evs for e in row)
         hit = []
         for i, layer in enumerate(layers):
             o = m.route(layer, xs[i], T, ws, out=m.route_out_tensors(W.dims, T, dev, want=("counts",)))
@@ -879,8 +889,11 @@ def config_results(W, peaks: dict, reps: int = 8) -> dict:
                      "per_launch_flop": gemm_flop(T)},
         "layer_tensor_frac": (gemm_flop(T) + 2.0 * T * E * d) / (layer_us * 1e-6) / 1e12 / tf, "ablations": abl,
         "read_probe": probe}
-    out["how"] = (f"CUDA graphs of {reps} repetitions; events recorded by moe_decode_timed / moe_prefill_timed "
-                  f"at the kernel boundaries; peaks: {peaks['source']} burst (HBM copy, bf16 dense = fp16 dense)")
+    out["how"] = (f"CUDA graphs of {reps} repetitions; prefill layer times from the plain calls (best of 3 "
+                  f"replays), kernel times from events recorded by moe_prefill_timed at the kernel boundaries "
+                  f"in a second graph (an event node stops the PDL overlap: upper bounds); decode: events "
+                  f"around each moe_decode_timed call; peaks: {peaks['source']} burst (HBM copy, bf16 dense = "
+                  f"fp16 dense)")
     return out
 
 
