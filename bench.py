@@ -521,7 +521,7 @@ def run_ours(args, config: dict) -> None:
                       "through the Python binding on the compute stream once its input has landed, y copied "
                       "back on a second copy stream, so layer l's copies overlap the neighbouring layers' "
                       "compute; decode: all inputs copied in, 256x40 eager moe_decode calls, outputs copied "
-                      "back, per step"}
+                      f"back, per step; {args.warmup} untimed steps first"}
 
     diag = decode_diagnostics(W) if S and not args.skip_diag else None
     probe = None
@@ -714,7 +714,7 @@ def chunked_prefill_diagnostics(W, prompt_chunks: int = 4, chunks=(512, 1024, 20
 
 def end_to_end(W, args, e0, e1, e2):
     """The same workload through the public binding with host buffers: (prefill ms, decode ms)
-    summed over args.steps steps. Prefill overlaps each layer's host copies with the neighbouring
+    summed over args.steps steps, after args.warmup untimed ones. Prefill overlaps each layer's host copies with the neighbouring
     layers' compute (copy-in stream, compute stream, copy-out stream); decode copies all inputs in,
     runs the eager calls and copies all outputs back."""
     import gc
@@ -740,7 +740,7 @@ def _end_to_end_steps(W, args, e0, e1, e2, compute, s_in, s_out, L, T, S):
     ev_done = [torch.cuda.Event() for _ in range(L)]
     pre = dec = 0.0
     per_step = []
-    for _ in range(args.steps):
+    for step in range(args.warmup + args.steps):  # the first `warmup` steps are not counted
         e0.record(compute)
         if T:
             s_in.wait_stream(compute)      # the copies belong to the timed region
@@ -763,6 +763,8 @@ def _end_to_end_steps(W, args, e0, e1, e2, compute, s_in, s_out, L, T, S):
             W.yd_host.copy_(W.yd, non_blocking=True)
         e2.record(compute)
         compute.synchronize()
+        if step < args.warmup:
+            continue
         pre += e0.elapsed_time(e1)
         dec += e1.elapsed_time(e2)
         per_step.append(round(e0.elapsed_time(e1), 2))
