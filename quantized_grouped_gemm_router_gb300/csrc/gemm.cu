@@ -197,6 +197,26 @@ __device__ __forceinline__ uint4 dequant8(uint32_t w, __half2 s2, __half2 b2) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// The same 8 weights without the base subtraction for the pairs of nibbles 1/5 and 3/7: masked
+// to mantissa bits [7:4] with a zero exponent field, such a pair is the fp16 subnormal q * 2^-20
+// exactly, so w = (q * 2^-20) * (scale * 2^20) + bias is one fused multiply-add with the exact
+// product q * scale, the result the base path rounds once too (bit-identical). Valid while
+// scale * 2^20 is an fp16 number (|scale| <= 0.0624); the caller picks the path per warp.
+__device__ __forceinline__ uint4 dequant8_sub(uint32_t w, __half2 s2, __half2 s2x, __half2 b2) {
+  const __half2 k1024 = __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400));
+  const uint32_t sw = __byte_perm(w, 0, 0x2301);
+  uint32_t t[4] = {(w & 0x000F000Fu) | 0x64006400u, w & 0x00F000F0u, (sw & 0x000F000Fu) | 0x64006400u,
+                   sw & 0x00F000F0u};
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __half2 v = *reinterpret_cast<__half2*>(&t[i]);
+    v = (i & 1) ? __hfma2(v, s2x, b2) : __hfma2(__hsub2(v, k1024), s2, b2);
+    o[i] = *reinterpret_cast<uint32_t*>(&v);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // A (scale, bias) pair the fp16 dequantization cannot carry exactly: a nonzero scale or bias below
 // the normal fp16 range (2^-14, where fp16 starts losing significant bits), or a weight
 // scale * q + bias that could exceed 65504 (q <= 15); NaN and infinity included.
@@ -553,14 +573,37 @@ __global__ void __launch_bounds__(kThreads, 1)
               if ((kWhole || part == 0) && j0 + t < nk) sb_bad |= sb_out_of_range(sbw[u]);  // once per word
               scale_bias(sbw[u], s2, b2);
               uint32_t v[16 * kHalves];
+              // whole blocks: the subnormal path when every lane's scale allows it (a uniform branch;
+              // measured 3.3% faster at 512 tokens, 1% slower with the wide configuration's half blocks)
+              bool sub = false;
+              __half2 s2x;
+              if constexpr (kWhole) {
+                const float sf = __uint_as_float(sbw[u] << 16);
+                const __half sxh = __float2half_rn(sf * 1048576.f);  // scale * 2^20, exact while sub
+                s2x = __halves2half2(sxh, sxh);
+                sub = __all_sync(0xFFFFFFFFu, fabsf(sf) <= 0.0624f);
+              }
+              if (sub) {
 #pragma unroll
-              for (int h = 0; h < kHalves; ++h) {
-                const uint32_t words[4] = {cw[u][h].x, cw[u][h].y, cw[u][h].z, cw[u][h].w};
+                for (int h = 0; h < kHalves; ++h) {
+                  const uint32_t words[4] = {cw[u][h].x, cw[u][h].y, cw[u][h].z, cw[u][h].w};
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                  const uint4 o = dequant8(words[c], s2, b2);
-                  v[16 * h + 4 * c] = o.x, v[16 * h + 4 * c + 1] = o.y, v[16 * h + 4 * c + 2] = o.z;
-                  v[16 * h + 4 * c + 3] = o.w;
+                  for (int c = 0; c < 4; ++c) {
+                    const uint4 o = dequant8_sub(words[c], s2, s2x, b2);
+                    v[16 * h + 4 * c] = o.x, v[16 * h + 4 * c + 1] = o.y, v[16 * h + 4 * c + 2] = o.z;
+                    v[16 * h + 4 * c + 3] = o.w;
+                  }
+                }
+              } else {
+#pragma unroll
+                for (int h = 0; h < kHalves; ++h) {
+                  const uint32_t words[4] = {cw[u][h].x, cw[u][h].y, cw[u][h].z, cw[u][h].w};
+#pragma unroll
+                  for (int c = 0; c < 4; ++c) {
+                    const uint4 o = dequant8(words[c], s2, b2);
+                    v[16 * h + 4 * c] = o.x, v[16 * h + 4 * c + 1] = o.y, v[16 * h + 4 * c + 2] = o.z;
+                    v[16 * h + 4 * c + 3] = o.w;
+                  }
                 }
               }
               if constexpr (kWhole)

@@ -338,6 +338,36 @@ def test_prefill_integer_weights_exact_hidden(m, T, force_top):
     assert worst <= 1.0, f"hidden rows off by {worst:.2f} x tolerance"
 
 
+def mixed_scale_layer(shape, seed):
+    """The synthetic layer with a quarter of the (row, group) scales of every matrix raised to
+    0.0625..0.25 (bias -8 * scale, exact in bf16): scales the narrow configuration's subnormal
+    dequantization (|scale| < 2^-4) cannot take, mixed with ones it can inside the same warps."""
+    npl = dict(_np_layer(shape, seed, None))
+    rng = np.random.default_rng(seed + 1)
+    for mat in ("gate", "up", "down", "sh_gate", "sh_up", "sh_down"):
+        q = dict(npl[mat])
+        sc = np.asarray(q["scale"]).view(np.uint16).copy()
+        pick = rng.random(sc.shape) < 0.25
+        big = (np.float32(2.0) ** rng.uniform(-4.0, -2.0, size=sc.shape)).astype(np.float32)
+        big_bits = (big.view(np.uint32) >> 16).astype(np.uint16)  # truncated to bf16: still >= 2^-4
+        sc[pick] = big_bits[pick]
+        f = (sc.astype(np.uint32) << 16).view(np.float32)
+        q["scale"] = sc.view(np.asarray(q["scale"]).dtype)
+        q["bias"] = ((np.float32(-8.0) * f).view(np.uint32) >> 16).astype(np.uint16).view(np.asarray(q["bias"]).dtype)
+        npl[mat] = q
+    return npl
+
+
+@pytest.mark.parametrize("T", [300, 2000], ids=["narrow_cfg", "wide_cfg"])
+def test_prefill_mixed_scales(m, T):
+    """Warps whose rows mix scales below and above 2^-4 take the base-subtracting dequantization,
+    the others the subnormal one (narrow configuration); both must match the oracle."""
+    npl = mixed_scale_layer(FULL, 31)
+    layer = m.upload_layer(npl)
+    assert m.prefill_tile_rows(layer.dims, T) == (32 if T * FULL.top_k <= 24 * FULL.n_experts else m.tile_rows())
+    prefill_and_check(m, FULL, T, seed=31, npl=npl, layer=layer, hidden=True)
+
+
 def test_prefill_out_of_range_sets_status(m):
     """x beyond the fp16 operand range is reported on the device instead of silently saturating."""
     layer = dev_layer(m, TINY)
