@@ -496,17 +496,25 @@ __global__ void __launch_bounds__(kThreads, 1)
               // (16-byte units, 14 bits; every shared-memory address here is below 2^18) advanced
               // from the stage's first row instead of rebuilt per instruction
               const uint64_t bdj = sw128_desc(b_stage(sb) + c0 * 128) + (uint64_t)(j * C::kPlanes * it.n16 * 8);
+              if constexpr (C::kQ4) {
+                // the K block's 4 K steps (x 2 planes for down) under one elected lane: fewer
+                // instructions per MMA on a scheduler the dequant warps share (measured: 512 tokens
+                // 199.4 -> 196.2 us per layer, 4096 tokens 373.9 -> 371.8)
+                if constexpr (C::kPlanes == 1)
+                  umma_f16_ts_k64_elect(acc, a_tmem(tmem_base, sa) + j * 32, bdj, idesc, kfirst != 0);
+                else
+                  umma_f16_ts_k64x2_elect(acc, a_tmem(tmem_base, sa) + j * 32, bdj, bdj + (uint64_t)(it.n16 * 8), idesc,
+                                          kfirst != 0);
+              } else {
 #pragma unroll
-              for (int ks = 0; ks < kGroup / 16; ++ks) {
+                for (int ks = 0; ks < kGroup / 16; ++ks) {
 #pragma unroll
-                for (int b = 0; b < C::kPlanes; ++b) {
-                  const uint64_t bdesc = bdj + (uint64_t)(b * it.n16 * 8 + ks * 2);
-                  const uint32_t accumulate = (kfirst | ks | b) != 0;
-                  if constexpr (C::kQ4)
-                    umma_f16_ts_elect(acc, a_tmem(tmem_base, sa) + j * 32 + ks * 8, bdesc, idesc, accumulate);
-                  else
+                  for (int b = 0; b < C::kPlanes; ++b) {
+                    const uint64_t bdesc = bdj + (uint64_t)(b * it.n16 * 8 + ks * 2);
+                    const uint32_t accumulate = (kfirst | ks | b) != 0;
                     umma_f16_ss_elect(acc, sw128_desc(smem_u32(w_stage(sw)) + jw * kATileBytes + ks * 32), bdesc, idesc,
                                       accumulate);
+                  }
                 }
               }
             }

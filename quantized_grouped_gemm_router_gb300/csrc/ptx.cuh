@@ -102,14 +102,47 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
 // Warp-collective forms: every lane of a converged warp executes them with the same (uniform)
 // operands and one elected lane issues the instruction. Issuing from a whole warp keeps the
 // operands in uniform registers; a one-lane branch around the issue costs far more per MMA.
-__device__ __forceinline__ void umma_f16_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                                   uint32_t accumulate) {
+// One K block (64 values = 4 K steps of 16) with A in tensor memory: four MMAs under one elected
+// lane; A advances 8 columns and the B descriptor 2 (32 bytes) per step; only the first may
+// start a fresh accumulator.
+__device__ __forceinline__ void umma_f16_ts_k64_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                      uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "{\n\t.reg .pred p, t, e;\n\t.reg .b32 a1, a2, a3;\n\t.reg .b64 b1, b2, b3;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+      "add.u32 a1, %1, 8;\n\tadd.u32 a2, %1, 16;\n\tadd.u32 a3, %1, 24;\n\t"
+      "add.s64 b1, %2, 2;\n\tadd.s64 b2, %2, 4;\n\tadd.s64 b3, %2, 6;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, t;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// The same for two B planes (leading part and remainder) per K step: eight MMAs, plane order
+// within each step.
+__device__ __forceinline__ void umma_f16_ts_k64x2_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b0, uint64_t b1,
+                                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, t, e;\n\t.reg .b32 a1, a2, a3;\n\t.reg .b64 c1, c2, c3, d1, d2, d3;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+      "add.u32 a1, %1, 8;\n\tadd.u32 a2, %1, 16;\n\tadd.u32 a3, %1, 24;\n\t"
+      "add.s64 c1, %2, 2;\n\tadd.s64 c2, %2, 4;\n\tadd.s64 c3, %2, 6;\n\t"
+      "add.s64 d1, %3, 2;\n\tadd.s64 d2, %3, 4;\n\tadd.s64 d3, %3, 6;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %4, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %3, %4, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], c1, %4, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], d1, %4, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], c2, %4, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], d2, %4, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], c3, %4, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], d3, %4, t;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b0), "l"(b1), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// One MMA with both operands in shared memory (router weights, the dense ablation's weights).
 __device__ __forceinline__ void umma_f16_ss_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                                    uint32_t accumulate) {
   asm volatile(
